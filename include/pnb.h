@@ -1,0 +1,206 @@
+/*
+ * pnb.h - C ABI of the GB300 (sm_103a) transformer decode step.
+ *
+ * One call advances a sequence by one token through a Llama-family decoder
+ * (Llama, Qwen2-style, Mistral sliding window, Mixtral top-k MoE) and returns
+ * fp32 logits and/or the greedy token.  It is the decode seam of the Pantheon
+ * engine pages: a forward function of type tm_tensor* (*)(pn_model*, uint32_t
+ * token, pn_state*) that reads the token, appends to the state's KV cache,
+ * advances state->pos and returns logits ("Core Engine API", section
+ * "pn_model struct"), plus its batched form, in which several sequences with
+ * their own states advance one token each ("Engine Architecture", section
+ * "Continuous-Batch VLM Decoder": one M=B decode over all slots).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev are device pointers of the calling thread's current
+ *    device, which must be the device current when the model was created.
+ *    Weights, KV buffers, logits and token buffers are owned by the caller and
+ *    must outlive the model / state that uses them.  Device pointers must be
+ *    16-byte aligned (PNB_E_ALIGN otherwise).
+ *  - Calls that take a stream are stream-ordered: they validate arguments on
+ *    the host, enqueue work and return without waiting.  The caller
+ *    synchronises (or records an event) to read results.  This replaces the
+ *    pages' begin / poll pair ("Core Engine API", section "Async forward-step
+ *    seam"), where begin returns at once and poll reports running / done / error.
+ *  - At most one step may be in flight per state, and one batched step per
+ *    model (the pages' per-model gen_lock gives the same guarantee).
+ *  - Return value: PNB_OK (0) or a negative PNB_E_* code; nothing is enqueued
+ *    when a call fails its host-side checks.  A step whose device-side checks
+ *    fail (a token id out of range arriving through device memory, a bounded
+ *    wait that expired) records an error word in the state, read with
+ *    pnb_state_check().
+ */
+#ifndef PNB_H
+#define PNB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *pnb_stream;
+
+/* storage type of weights and of the KV cache */
+enum { PNB_F32 = 0, PNB_BF16 = 1 };
+
+enum {
+  PNB_OK = 0,
+  PNB_E_INVAL = -1,       /* invalid configuration or argument */
+  PNB_E_NULL = -2,        /* a required pointer is NULL */
+  PNB_E_ALIGN = -3,       /* a device pointer is not 16-byte aligned */
+  PNB_E_CTX_FULL = -4,    /* pos would reach n_ctx */
+  PNB_E_UNSUPPORTED = -5, /* valid but not supported by this build (cf. the pages' -1) */
+  PNB_E_CUDA = -6,        /* a CUDA runtime call failed */
+  PNB_E_TOKEN = -7,       /* token id outside [0, n_vocab) */
+  PNB_E_DEVICE = -8,      /* a device-side check failed (see pnb_state_check) */
+  PNB_E_NOMEM = -9,       /* host or device allocation failed */
+  PNB_E_WRONG_DEVICE = -10 /* current device differs from the model's */
+};
+
+/* device-side error bits (pnb_state_check) */
+enum {
+  PNB_DEV_ERR_TOKEN = 1,   /* a token from device memory was out of range; id 0 was used */
+  PNB_DEV_ERR_TIMEOUT = 2  /* a bounded wait inside a kernel expired; results are invalid */
+};
+
+/* Model dimensions: the config fields of the pages ("Engine Architecture",
+   section "Config Parsing": n_vocab, n_embd, n_head, n_kv_head (default
+   n_head), n_layer, n_ff, n_ctx (default 2048), rope_theta (default 10000),
+   rms_norm_eps (default 1e-5), sliding_window (default 0 = disabled)) plus the
+   MoE fields (expert_count > 0 selects the Mixtral FFN, "Architecture
+   Detection"; the arena reserves n_experts + 2*n_experts_used floats for the
+   router, "Core Engine API", section "Scratch (arena) estimation").
+   The library applies no defaults: every field is used as given.
+   head_dim = n_embd / n_head. */
+typedef struct {
+  int32_t n_vocab, n_embd, n_head, n_kv_head, n_layer, n_ff, n_ctx;
+  double rope_theta, rms_norm_eps;
+  int32_t sliding_window; /* 0 = attend to every position */
+  int32_t expert_count;   /* 0 = dense SwiGLU FFN */
+  int32_t expert_used;    /* top-k experts per token when expert_count > 0 */
+  int32_t dtype;          /* PNB_F32 or PNB_BF16: weights and KV cache */
+} pnb_config;
+
+/* Device weights, caller-owned, in the library's layout (row-major; "dtype" =
+   the config's storage type; norm vectors are always fp32, as the pages keep
+   layer norms in F32: "Engine Architecture", section "Weight Loading Modes").
+   Per-layer entries are HOST arrays of device pointers, read once by
+   pnb_model_create.  With S = max(1, expert_count), E = n_embd, hd = head_dim:
+     tok_embd            [n_vocab][E]                          dtype
+     out_norm            [E]                                   fp32
+     output              [n_vocab][E]                          dtype  (LM head)
+     attn_norm[l]        [E]                                   fp32
+     wqkv[l]             [(n_head + 2 n_kv_head) hd][E]        dtype  rows: Wq, then Wk, then Wv
+     wo[l]               [E][n_head hd]                        dtype
+     ffn_norm[l]         [E]                                   fp32
+     w_router[l]         [expert_count][E]                     dtype  (NULL array when dense)
+     w_gate_up[l*S + e]  [2 n_ff][E]                           dtype  row 2i = gate row i, 2i+1 = up row i
+     w_down[l*S + e]     [E][n_ff]                             dtype                                     */
+typedef struct {
+  const void *tok_embd;
+  const float *out_norm;
+  const void *output;
+  const float *const *attn_norm;
+  const void *const *wqkv;
+  const void *const *wo;
+  const float *const *ffn_norm;
+  const void *const *w_router;
+  const void *const *w_gate_up;
+  const void *const *w_down;
+} pnb_weights;
+
+typedef struct pnb_model pnb_model;
+typedef struct pnb_state pnb_state;
+
+/* Create a model on the current device from a config and device weights
+   (the pages' pn_model: config + weights + forward, "Core Engine API",
+   section "pn_model struct"; Llama, Qwen2, Mistral and Mixtral share one
+   forward, "Architecture registry").  Checks: n_embd = n_head * head_dim,
+   head_dim even and in {32, 64, 128}, n_head % n_kv_head == 0, n_embd and
+   n_ff multiples of 8, 0 < expert_used <= expert_count <= 64 when MoE,
+   pointer non-NULL and 16-byte aligned.  *out is set on success. */
+int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **out);
+void pnb_model_free(pnb_model *m);
+
+/* Bytes of the KV buffer a state needs: n_layer * 2 * n_kv_head * cap *
+   head_dim * sizeof(dtype), with cap = min(n_ctx, sliding_window) when the
+   window is set, else n_ctx.  Layout, row-major:
+     [n_layer][2 (K, V)][n_kv_head][cap][head_dim]
+   Position j lives in slot j % cap (a ring when the window is set: the last
+   `sliding_window` positions are all a step can attend).  Cache contents are
+   raw, i.e. keys are stored after RoPE. */
+size_t pnb_state_kv_bytes(const pnb_model *m);
+
+/* Create a state over a caller-owned KV buffer (the pages' pn_state: KV cache
+   and pos, "Core Engine API", section "pn_state struct").  The library
+   allocates the state's device workspace (activations, split-KV partials,
+   counters: the role of the pages' per-state arena, "Scratch (arena)
+   estimation").  The new state has pos = 0; the KV buffer is not touched. */
+int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out);
+void pnb_state_free(pnb_state *s);
+
+/* Zero every K and V entry and set pos = 0 (pn_state_reset, "Core Engine
+   API", section "State lifecycle"); also clears the device error word. */
+int pnb_state_reset(pnb_state *s, pnb_stream stream);
+
+/* Set pos, e.g. after the caller has filled cache positions [0, pos) itself.
+   Requires 0 <= pos < n_ctx. */
+int pnb_state_set_pos(pnb_state *s, int32_t pos, pnb_stream stream);
+
+/* pos as of the last enqueued call (host bookkeeping, no device access). */
+int pnb_state_get_pos(const pnb_state *s, int32_t *pos);
+
+/* Synchronise the state's last stream work and read its device error word
+   (PNB_DEV_ERR_* bits, 0 = none).  Returns PNB_E_DEVICE when it is nonzero. */
+int pnb_state_check(pnb_state *s, int32_t *device_error);
+
+/* Token value meaning "the greedy token of this state's previous step". */
+#define PNB_TOKEN_PREV (-1)
+
+/* One decode step of one sequence (model->forward(model, token, state)).
+   token: an id in [0, n_vocab), or PNB_TOKEN_PREV to feed back the argmax
+   of this state's previous step without a host round trip.
+   logits_dev: [n_vocab] fp32 output or NULL.  argmax_dev: [1] int32 output
+   (greedy token, lowest id on ties; "Engine Architecture", section
+   "Sampling": temperature 0 is argmax) or NULL.  Advances pos by one.
+   Errors: PNB_E_TOKEN, PNB_E_CTX_FULL (pos = n_ctx - 1 already used). */
+int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, float *logits_dev,
+                int32_t *argmax_dev);
+
+/* One decode step of B sequences together (pn_llama_forward_batch, "Engine
+   Architecture", section "Continuous-Batch VLM Decoder"); slot b reads
+   tokens_dev[b] (or, when tokens_dev is NULL, its own previous argmax) and
+   its own state's KV cache and pos.  Results equal B single-sequence steps up
+   to fp32 summation order.  logits_dev: [B][n_vocab] or NULL; argmax_dev: [B]
+   or NULL.  Distinct states only; 1 <= B <= 64.  MoE models return
+   PNB_E_UNSUPPORTED (as the pages' batched decoder returns -1 for MoE). */
+int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const int32_t *tokens_dev,
+                      pnb_stream stream, float *logits_dev, int32_t *argmax_dev);
+
+/* Capture each step into a CUDA graph and replay it (default 1), or launch
+   the kernels one by one (0).  Results are identical either way. */
+int pnb_model_set_graphs(pnb_model *m, int enable);
+
+/* Number of this library's kernels one step launches (single sequence when
+   B == 0, batched otherwise). */
+int pnb_step_kernel_count(const pnb_model *m, int32_t B);
+
+/* Device pointers of a state's fp32 activation buffers after its last step
+   (x: residual [n_embd]; q: rotated queries [n_head*hd]; attn: attention
+   output [n_head*hd]; h: SwiGLU activations [max(1,expert_used)][n_ff]);
+   meant for layer-level checks in tests. */
+typedef struct {
+  float *x, *q, *attn, *h;
+} pnb_activations;
+int pnb_state_activations(const pnb_state *s, pnb_activations *out);
+
+const char *pnb_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PNB_H */

@@ -1,1 +1,209 @@
-"""GB300-native transformer decode step (binding filled in with the library)."""
+"""GB300 (sm_103a) transformer decode step: Python binding of libpnb.so.
+
+The binding only marshals arguments to the C ABI declared in include/pnb.h;
+every step of the decode path runs in the library's CUDA kernels.  PyTorch is
+used by callers for device memory and streams only.  Importing this package
+fails loudly when the library has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+from ._build import LIB
+
+if not os.path.exists(LIB):
+    raise ImportError(f"{LIB} is missing: build it with __graft_entry__.build() "
+                      "(the decode step has no non-CUDA implementation)")
+
+_lib = ctypes.CDLL(LIB)
+
+PNB_F32, PNB_BF16 = 0, 1
+PNB_TOKEN_PREV = -1
+PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT = 1, 2
+ERRORS = {0: "PNB_OK", -1: "PNB_E_INVAL", -2: "PNB_E_NULL", -3: "PNB_E_ALIGN",
+          -4: "PNB_E_CTX_FULL", -5: "PNB_E_UNSUPPORTED", -6: "PNB_E_CUDA", -7: "PNB_E_TOKEN",
+          -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE"}
+
+
+class pnb_config(ctypes.Structure):
+    _fields_ = [("n_vocab", ctypes.c_int32), ("n_embd", ctypes.c_int32),
+                ("n_head", ctypes.c_int32), ("n_kv_head", ctypes.c_int32),
+                ("n_layer", ctypes.c_int32), ("n_ff", ctypes.c_int32), ("n_ctx", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double), ("rms_norm_eps", ctypes.c_double),
+                ("sliding_window", ctypes.c_int32), ("expert_count", ctypes.c_int32),
+                ("expert_used", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class pnb_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("tok_embd", "out_norm", "output", "attn_norm", "wqkv", "wo", "ffn_norm",
+                 "w_router", "w_gate_up", "w_down")]
+
+
+class pnb_activations(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "q", "attn", "h")]
+
+
+_p, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_SIGS = {
+    "pnb_model_create": (_i32, [_p, _p, _p]),
+    "pnb_model_free": (None, [_p]),
+    "pnb_state_kv_bytes": (_sz, [_p]),
+    "pnb_state_new": (_i32, [_p, _p, _sz, _p]),
+    "pnb_state_free": (None, [_p]),
+    "pnb_state_reset": (_i32, [_p, _p]),
+    "pnb_state_set_pos": (_i32, [_p, _i32, _p]),
+    "pnb_state_get_pos": (_i32, [_p, _p]),
+    "pnb_state_check": (_i32, [_p, _p]),
+    "pnb_forward": (_i32, [_p, _p, _i32, _p, _p, _p]),
+    "pnb_forward_batch": (_i32, [_p, _p, _i32, _p, _p, _p, _p]),
+    "pnb_model_set_graphs": (_i32, [_p, _i32]),
+    "pnb_step_kernel_count": (_i32, [_p, _i32]),
+    "pnb_state_activations": (_i32, [_p, _p]),
+    "pnb_strerror": (ctypes.c_char_p, [_i32]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+    globals()[_name] = _fn
+
+EXPORTED = tuple(_SIGS)
+
+
+class PnbError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({pnb_strerror(code).decode()})")
+        self.code = code
+
+
+def check(code: int, what: str):
+    if code != 0:
+        raise PnbError(code, what)
+
+
+def _ptr(t) -> Optional[int]:
+    """Device pointer of a torch tensor (or an int), None for None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Model:
+    """A pnb_model over caller-owned device weights.
+
+    cfg: pnb_config.  Pointers (ints): tok_embd, out_norm, output; per-layer
+    lists attn_norm, wqkv, wo, ffn_norm, w_router (MoE) and w_gate_up, w_down
+    with n_layer * max(1, expert_count) entries (layout: include/pnb.h)."""
+
+    def __init__(self, cfg: pnb_config, *, tok_embd, out_norm, output, attn_norm, wqkv, wo,
+                 ffn_norm, w_gate_up, w_down, w_router=None, keepalive=None):
+        self.cfg = cfg
+        self._keep = [keepalive]
+        arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs) if xs else None
+        self._arrays = [arr(attn_norm), arr(wqkv), arr(wo), arr(ffn_norm), arr(w_router),
+                        arr(w_gate_up), arr(w_down)]
+        w = pnb_weights()
+        w.tok_embd, w.out_norm, w.output = tok_embd, out_norm, output
+        (an, qkv, o, fn, rt, gu, dn) = self._arrays
+        cast = lambda a: ctypes.cast(a, ctypes.c_void_p) if a is not None else None
+        w.attn_norm, w.wqkv, w.wo, w.ffn_norm = cast(an), cast(qkv), cast(o), cast(fn)
+        w.w_router, w.w_gate_up, w.w_down = cast(rt), cast(gu), cast(dn)
+        h = ctypes.c_void_p()
+        check(pnb_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)),
+              "pnb_model_create")
+        self._h = h.value
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            pnb_model_free(self._h)
+            self._h = None
+
+    @property
+    def handle(self) -> int:
+        return self._h
+
+    def kv_bytes(self) -> int:
+        return int(pnb_state_kv_bytes(self._h))
+
+    def set_graphs(self, enable: bool):
+        check(pnb_model_set_graphs(self._h, 1 if enable else 0), "pnb_model_set_graphs")
+
+    def step_kernel_count(self, batch: int = 0) -> int:
+        return int(pnb_step_kernel_count(self._h, batch))
+
+    def new_state(self, kv=None) -> "State":
+        """A state over `kv` (a device tensor of at least kv_bytes()), allocated if None."""
+        if kv is None:
+            import torch
+            kv = torch.zeros(self.kv_bytes(), dtype=torch.uint8, device="cuda")
+        return State(self, kv)
+
+    def forward_batch(self, states: Sequence["State"], tokens=None, logits=None, argmax=None,
+                      stream=None):
+        arr = (ctypes.c_void_p * len(states))(*[s.handle for s in states])
+        check(pnb_forward_batch(self._h, arr, len(states), _ptr(tokens), _stream(stream),
+                                _ptr(logits), _ptr(argmax)), "pnb_forward_batch")
+
+
+class State:
+    def __init__(self, model: Model, kv):
+        self.model = model
+        self.kv = kv
+        h = ctypes.c_void_p()
+        check(pnb_state_new(model.handle, _ptr(kv), kv.numel() * kv.element_size(),
+                            ctypes.byref(h)), "pnb_state_new")
+        self._h = h.value
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            pnb_state_free(self._h)
+            self._h = None
+
+    @property
+    def handle(self) -> int:
+        return self._h
+
+    def forward(self, token: int, logits=None, argmax=None, stream=None):
+        check(pnb_forward(self.model.handle, self._h, token, _stream(stream), _ptr(logits),
+                          _ptr(argmax)), "pnb_forward")
+
+    def reset(self, stream=None):
+        check(pnb_state_reset(self._h, _stream(stream)), "pnb_state_reset")
+
+    def set_pos(self, pos: int, stream=None):
+        check(pnb_state_set_pos(self._h, pos, _stream(stream)), "pnb_state_set_pos")
+
+    @property
+    def pos(self) -> int:
+        p = ctypes.c_int32()
+        check(pnb_state_get_pos(self._h, ctypes.byref(p)), "pnb_state_get_pos")
+        return p.value
+
+    def device_error(self) -> int:
+        e = ctypes.c_int32()
+        rc = pnb_state_check(self._h, ctypes.byref(e))
+        if rc not in (0, -8):
+            check(rc, "pnb_state_check")
+        return e.value
+
+    def activations(self) -> dict:
+        a = pnb_activations()
+        check(pnb_state_activations(self._h, ctypes.byref(a)), "pnb_state_activations")
+        return {"x": a.x, "q": a.q, "attn": a.attn, "h": a.h}
+
+
+from .synthetic import SynthModel  # noqa: E402  (generated-weight models for tests / bench)

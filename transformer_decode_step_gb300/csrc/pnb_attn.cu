@@ -1,0 +1,387 @@
+// pnb_attn.cu - split-KV flash-decode attention for one query token (GQA,
+// optional sliding window, ring KV cache).
+//
+// Grid (n_split, n_kv, zgroups).  A CTA takes one KV head g, a block of
+// `heads_per_cta` of the query heads that share it, and one contiguous chunk
+// of the attended positions [lo, pos].  Warp 8 streams the chunk's K and V
+// rows through a shared-memory ring with 1-D bulk copies; rows of positions
+// before `pos` are issued before griddepcontrol.wait (earlier steps wrote
+// them), the current position only after it.  Eight consumer warps score four
+// positions at a time (eight lanes per position), keep a running max / sum /
+// weighted V per head in the log2 domain, and merge across warps.  Each CTA
+// writes (max, sum, unnormalised output) for its chunk; the last CTA of a KV
+// head (atomic arrival counter, no waiting) merges all chunks.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pnb_kernels.cuh"
+
+namespace pnb {
+namespace {
+
+extern __shared__ __align__(128) uint8_t a_smem[];
+
+template <typename T, int N>
+__device__ __forceinline__ void load_vals(const T *p, float (&f)[N]) {
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (N == 8) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(p);
+      f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+      f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+    } else if constexpr (N == 4) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(p);
+      f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+    } else if constexpr (N == 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+      f[0] = bf16lo(u); f[1] = bf16hi(u);
+    } else {
+      f[0] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
+    }
+  } else {
+    if constexpr (N == 4) {
+      const float4 u = *reinterpret_cast<const float4 *>(p);
+      f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+    } else if constexpr (N == 2) {
+      const float2 u = *reinterpret_cast<const float2 *>(p);
+      f[0] = u.x; f[1] = u.y;
+    } else {
+      f[0] = *p;
+    }
+  }
+}
+
+struct AttnSmem {
+  int ring, mo, mm, ml, flag, bars, total;
+};
+
+__host__ __device__ inline AttnSmem attn_smem(int stage_pos, int nstages, int hd, int gb, int es) {
+  AttnSmem L;
+  L.ring = 0;
+  L.mo = align_up(nstages * 2 * stage_pos * hd * es, 16);
+  L.mm = L.mo + kConsumerWarps * gb * hd * 4;
+  L.ml = L.mm + kConsumerWarps * gb * 4;
+  L.flag = L.ml + kConsumerWarps * gb * 4;
+  L.bars = align_up(L.flag + 16, 16);
+  L.total = L.bars + 2 * nstages * 8;
+  return L;
+}
+
+template <typename T, int HD, int GB>
+__global__ void __launch_bounds__(kThreads, 1) k_attn(const AttnArgs a) {
+  constexpr int ES = (int)sizeof(T);
+  constexpr int DPL = HD / 8;                             // dims per lane when scoring
+  constexpr int UNIT = (DPL * ES < 16) ? DPL * ES : 16;   // bytes per shared-memory load
+  constexpr int EPU = UNIT / ES;
+  constexpr int C = DPL / EPU;                            // loads per lane per key row
+  constexpr int VPL = HD / 32;                            // dims per lane when accumulating V
+  constexpr int ROTDIV = 8 / C;                           // lanes sharing a load order
+  const int SP = a.stage_pos, NS = a.nstages;
+  const int split = blockIdx.x, g = blockIdx.y, z = blockIdx.z;
+  const int G = a.n_head / a.n_kv;
+  const int h0 = g * G + z * GB;
+
+  // positions of this CTA (pos was written by an earlier step: readable before the wait)
+  const int pos = a.io->pos;
+  const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+  const int n = pos - lo + 1;
+  const int chunk = (n + a.n_split - 1) / a.n_split;
+  const int c0 = lo + split * chunk;
+  const int npos = max(0, min(pos + 1, c0 + chunk) - c0);
+  const int nst = (npos + SP - 1) / SP;
+
+  const AttnSmem L = attn_smem(SP, NS, HD, GB, ES);
+  T *ring = reinterpret_cast<T *>(a_smem + L.ring);
+  float *mo = reinterpret_cast<float *>(a_smem + L.mo);
+  float *mm = reinterpret_cast<float *>(a_smem + L.mm);
+  float *ml = reinterpret_cast<float *>(a_smem + L.ml);
+  int *flag = reinterpret_cast<int *>(a_smem + L.flag);
+  uint64_t *full = reinterpret_cast<uint64_t *>(a_smem + L.bars);
+  uint64_t *empty = full + NS;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      const T *kb = static_cast<const T *>(a.k_cache) + (int64_t)g * a.cap * HD;
+      const T *vb = static_cast<const T *>(a.v_cache) + (int64_t)g * a.cap * HD;
+      bool waited = false, ok = true;
+      int st = 0;
+      for (; st < nst; ++st) {
+        const int a0 = c0 + st * SP, np = min(SP, npos - st * SP);
+        const int slot = st % NS, round = st / NS;
+        if (!waited && (a0 + np > pos || st == NS)) {
+          pdl_wait();
+          pdl_trigger();
+          waited = true;
+        }
+        if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[slot], 2u * np * HD * ES);
+        T *ks = ring + (size_t)slot * 2 * SP * HD, *vs = ks + SP * HD;
+        const int s0 = a0 % a.cap, n1 = min(np, a.cap - s0);
+        bulk_g2s(ks, kb + (int64_t)s0 * HD, n1 * HD * ES, &full[slot]);
+        bulk_g2s(vs, vb + (int64_t)s0 * HD, n1 * HD * ES, &full[slot]);
+        if (n1 < np) {
+          bulk_g2s(ks + n1 * HD, kb, (np - n1) * HD * ES, &full[slot]);
+          bulk_g2s(vs + n1 * HD, vb, (np - n1) * HD * ES, &full[slot]);
+        }
+      }
+      if (!waited) {
+        pdl_wait();
+        pdl_trigger();
+      }
+      if (!ok) set_error(&a.io->error, kErrTimeout);
+      for (int j = st > NS ? st - NS : 0; j < st; ++j)
+        if (!mbar_wait(&full[j % NS], (j / NS) & 1)) set_error(&a.io->error, kErrTimeout);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  pdl_wait();
+  const int sub = lane & 7, t = lane >> 3;
+  const int rot = sub / ROTDIV;
+  float qr[GB][C][EPU];
+#pragma unroll
+  for (int gh = 0; gh < GB; ++gh)
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      const int u = (c + rot) % C;
+#pragma unroll
+      for (int e = 0; e < EPU; ++e)
+        qr[gh][c][e] = a.q[(int64_t)(h0 + gh) * HD + sub * DPL + u * EPU + e] * a.qscale;
+    }
+  float m[GB], l[GB], o[GB][VPL];
+#pragma unroll
+  for (int gh = 0; gh < GB; ++gh) {
+    m[gh] = -INFINITY;
+    l[gh] = 0.f;
+#pragma unroll
+    for (int d = 0; d < VPL; ++d) o[gh][d] = 0.f;
+  }
+  const int PPW = SP / kConsumerWarps;
+  bool ok = true;
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % NS, round = st / NS;
+    if (ok && !mbar_wait(&full[slot], round & 1)) {
+      ok = false;
+      if (lane == 0) set_error(&a.io->error, kErrTimeout);
+    }
+    if (!ok) continue;
+    const T *ks = ring + (size_t)slot * 2 * SP * HD, *vs = ks + SP * HD;
+    const int np = min(SP, npos - st * SP);
+    for (int it = 0; it < PPW; it += 4) {
+      const int pbase = warp * PPW + it;
+      if (pbase >= np) break;
+      const int pi = pbase + t;
+      const bool valid = pi < np;
+      float s[GB];
+#pragma unroll
+      for (int gh = 0; gh < GB; ++gh) s[gh] = 0.f;
+      if (valid) {
+        const T *kr = ks + pi * HD + sub * DPL;
+        float kf[C][EPU];
+#pragma unroll
+        for (int c = 0; c < C; ++c) load_vals<T, EPU>(kr + ((c + rot) % C) * EPU, kf[c]);
+#pragma unroll
+        for (int gh = 0; gh < GB; ++gh) {
+          float acc = 0.f;
+#pragma unroll
+          for (int c = 0; c < C; ++c)
+#pragma unroll
+            for (int e = 0; e < EPU; ++e) acc = fmaf(qr[gh][c][e], kf[c][e], acc);
+          s[gh] = acc;
+        }
+      }
+#pragma unroll
+      for (int gh = 0; gh < GB; ++gh) {
+        s[gh] += __shfl_xor_sync(0xffffffffu, s[gh], 4);
+        s[gh] += __shfl_xor_sync(0xffffffffu, s[gh], 2);
+        s[gh] += __shfl_xor_sync(0xffffffffu, s[gh], 1);
+        if (!valid) s[gh] = -INFINITY;
+      }
+      float sc[4][GB];
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+        for (int gh = 0; gh < GB; ++gh) sc[tt][gh] = __shfl_sync(0xffffffffu, s[gh], tt * 8);
+      float vv[4][VPL];
+#pragma unroll
+      for (int tt = 0; tt < 4; ++tt) {
+        if (pbase + tt < np) {
+          load_vals<T, VPL>(vs + (pbase + tt) * HD + lane * VPL, vv[tt]);
+        } else {
+#pragma unroll
+          for (int d = 0; d < VPL; ++d) vv[tt][d] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int gh = 0; gh < GB; ++gh) {
+        float mx = m[gh];
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) mx = fmaxf(mx, sc[tt][gh]);
+        if (mx == -INFINITY) continue;
+        const float alpha = exp2f(m[gh] - mx);
+        l[gh] *= alpha;
+#pragma unroll
+        for (int d = 0; d < VPL; ++d) o[gh][d] *= alpha;
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+          if (pbase + tt < np) {
+            const float p = exp2f(sc[tt][gh] - mx);
+            l[gh] += p;
+#pragma unroll
+            for (int d = 0; d < VPL; ++d) o[gh][d] = fmaf(p, vv[tt][d], o[gh][d]);
+          }
+        }
+        m[gh] = mx;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+
+  // merge the eight warps of this CTA
+#pragma unroll
+  for (int gh = 0; gh < GB; ++gh) {
+    if (lane == 0) {
+      mm[warp * GB + gh] = m[gh];
+      ml[warp * GB + gh] = l[gh];
+    }
+#pragma unroll
+    for (int d = 0; d < VPL; ++d) mo[(warp * GB + gh) * HD + lane * VPL + d] = o[gh][d];
+  }
+  consumer_sync();
+  for (int idx = tid; idx < GB * HD; idx += kConsumerThreads) {
+    const int gh = idx / HD, d = idx - gh * HD;
+    float M = -INFINITY;
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * GB + gh]);
+    float Ls = 0.f, Os = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = exp2f(mm[w * GB + gh] - M);
+        Ls = fmaf(ml[w * GB + gh], f, Ls);
+        Os = fmaf(mo[(w * GB + gh) * HD + d], f, Os);
+      }
+    }
+    float *P = a.part + ((int64_t)(h0 + gh) * a.n_split + split) * (HD + 2);
+    if (d == 0) {
+      P[0] = M;
+      P[1] = Ls;
+    }
+    P[2 + d] = Os;
+  }
+  __threadfence();
+  consumer_sync();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&a.counter[g * gridDim.z + z], 1u);
+    *flag = (prev == (unsigned)a.n_split - 1u);
+  }
+  consumer_sync();
+  if (*flag) {
+    __threadfence();
+    for (int idx = tid; idx < GB * HD; idx += kConsumerThreads) {
+      const int gh = idx / HD, d = idx - gh * HD;
+      const float *P0 = a.part + (int64_t)(h0 + gh) * a.n_split * (HD + 2);
+      float M = -INFINITY;
+      for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, __ldcg(P0 + s * (HD + 2)));
+      float Ls = 0.f, Os = 0.f;
+      for (int s = 0; s < a.n_split; ++s) {
+        const float ms = __ldcg(P0 + s * (HD + 2));
+        if (ms == -INFINITY) continue;
+        const float f = exp2f(ms - M);
+        Ls = fmaf(__ldcg(P0 + s * (HD + 2) + 1), f, Ls);
+        Os = fmaf(__ldcg(P0 + s * (HD + 2) + 2 + d), f, Os);
+      }
+      a.out[(int64_t)(h0 + gh) * HD + d] = Os / Ls;
+    }
+    if (tid == 0) a.counter[g * gridDim.z + z] = 0u;
+  }
+}
+
+template <typename T, int HD, int GB>
+cudaError_t launch_one(const AttnArgs &a, const AttnGeom &ag, cudaStream_t st, bool pdl,
+                       bool prepare_only) {
+  auto kern = k_attn<T, HD, GB>;
+  if (prepare_only) {
+    if (ag.smem <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ag.smem);
+  }
+  const int G = a.n_head / a.n_kv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_split, a.n_kv, G / GB);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = ag.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <typename T, int HD>
+cudaError_t launch_hd(const AttnArgs &a, const AttnGeom &ag, cudaStream_t st, bool pdl,
+                      bool prep) {
+  switch (ag.heads_per_cta) {
+    case 1: return launch_one<T, HD, 1>(a, ag, st, pdl, prep);
+    case 2: return launch_one<T, HD, 2>(a, ag, st, pdl, prep);
+    case 4: return launch_one<T, HD, 4>(a, ag, st, pdl, prep);
+    case 8:
+      if constexpr (HD <= 64) return launch_one<T, HD, 8>(a, ag, st, pdl, prep);
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_t(int hd, const AttnArgs &a, const AttnGeom &ag, cudaStream_t st, bool pdl,
+                     bool prep) {
+  switch (hd) {
+    case 32: return launch_hd<T, 32>(a, ag, st, pdl, prep);
+    case 64: return launch_hd<T, 64>(a, ag, st, pdl, prep);
+    case 128: return launch_hd<T, 128>(a, ag, st, pdl, prep);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+AttnGeom attn_geom(int dtype, int head_dim, int group) {
+  AttnGeom ag;
+  const int es = dtype ? 2 : 4;
+  int gb = 1;
+  while (gb * 2 <= 8 && group % (gb * 2) == 0 && gb * 2 * head_dim <= 512) gb *= 2;
+  ag.heads_per_cta = gb;
+  int sp = 8192 / (head_dim * es);
+  sp = sp < 32 ? 32 : sp - sp % 32;
+  ag.stage_pos = sp;
+  int ns = (96 * 1024) / (2 * sp * head_dim * es);
+  ag.nstages = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+  ag.smem = attn_smem(sp, ag.nstages, head_dim, gb, es).total;
+  return ag;
+}
+
+cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGeom &ag,
+                        cudaStream_t st, bool pdl) {
+  return dtype ? launch_t<__nv_bfloat16>(head_dim, a, ag, st, pdl, false)
+               : launch_t<float>(head_dim, a, ag, st, pdl, false);
+}
+
+cudaError_t prepare_attn_kernel(int dtype, int head_dim, const AttnGeom &ag) {
+  AttnArgs a{};
+  return dtype ? launch_t<__nv_bfloat16>(head_dim, a, ag, nullptr, false, true)
+               : launch_t<float>(head_dim, a, ag, nullptr, false, true);
+}
+
+}  // namespace pnb

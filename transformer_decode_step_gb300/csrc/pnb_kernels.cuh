@@ -1,0 +1,190 @@
+// pnb_kernels.cuh - argument blocks and launchers of the decode-step kernels.
+//
+// Every weight-streaming kernel is a row-split GEMV over one or more matrices
+// that share a column count K: each CTA owns a contiguous range of output rows
+// and streams those rows whole through a ring of shared-memory stages filled
+// by 1-D bulk copies (one elected producer thread, mbarrier completion).  The
+// first ring's worth is issued before griddepcontrol.wait, so a kernel's
+// weight traffic overlaps the tail of the kernel before it.  Eight consumer
+// warps multiply the staged rows by an fp32 activation vector held in shared
+// memory and fold the result into a fused epilogue.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pnb_device.cuh"
+
+namespace pnb {
+
+// Geometry of one streaming GEMV launch (host-computed).
+struct Geom {
+  int K;              // columns (elements)
+  int es;             // element bytes (2 bf16, 4 fp32)
+  int row_bytes;      // K * es
+  int rows_per_stage; // power of two <= 64: whole rows per ring slot
+  int stage_bytes;    // ring slot size = rows_per_stage * row_bytes
+  int nstages;        // ring slots
+  int wpr;            // partial sums per row = max(1, consumer warps / rows_per_stage)
+  int chunk;          // vectors per warp when several warps share a row (multiple of 8)
+  int row_align;      // CTA row ranges are multiples of this
+  int rows_cta_max;   // most rows any CTA owns
+  int xs_floats;      // padded activation vector length in shared memory
+  int nsum;           // matrices summed into the same rows (1 = concatenated rows)
+};
+
+// The matrices of one launch.  Rows of segment i are virtual rows
+// [i*rows, (i+1)*rows) (concatenated) or the same output rows (summed).
+struct Segs {
+  int n;
+  int64_t rows;
+  const void *w[kMaxSegments];
+  // MoE: segment i is expert expert_idx[i] of `table` (device pointers), known
+  // only after the router kernel has run
+  const void *const *table;
+  const int32_t *expert_idx;
+};
+
+struct SmemLayout {
+  int ring, xs, part, red, bars, total;
+};
+
+__host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout smem_layout(const Geom &g) {
+  SmemLayout L;
+  L.ring = 0;
+  L.xs = align_up(g.nstages * g.stage_bytes, 128);
+  L.part = align_up(L.xs + g.xs_floats * 4, 16);
+  L.red = align_up(L.part + g.rows_cta_max * g.wpr * g.nsum * 4, 16);
+  L.bars = align_up(L.red + 64 * 4, 16);
+  L.total = L.bars + 2 * g.nstages * 8;
+  return L;
+}
+
+// ---------------------------------------------------------------- kernels
+
+// layer input: RMSNorm(x) (or of the embedding row of io->token when emb is
+// set) -> [Wq; Wk; Wv] -> RoPE on q and k -> q buffer, K/V cache slot of pos
+struct QkvArgs {
+  Geom g;
+  Segs s;
+  const float *x;
+  const void *emb;     // token embedding table (first layer) or nullptr
+  float *x_out;        // residual stream, written from the embedding row
+  int n_vocab;
+  const float *norm_w;
+  float eps;
+  int n_head, n_kv, head_dim;
+  const double *inv_freq;  // [head_dim / 2] = rope_theta^(-2i/head_dim)
+  float *q;
+  void *k_cache, *v_cache; // this layer's [n_kv][cap][head_dim]
+  int cap, window;
+  StepIO *io;
+};
+
+// x[r] += (W v)[r]  (output projection, dense down projection)
+struct ResidArgs {
+  Geom g;
+  Segs s;
+  const float *vec;
+  float *x;
+  StepIO *io;
+};
+
+// h[s][i] = silu((Wg xn)_i) * (Wu xn)_i with xn = RMSNorm(x); rows of W are
+// gate/up interleaved; s runs over the segments (experts)
+struct GateUpArgs {
+  Geom g;
+  Segs s;
+  const float *x;
+  const float *norm_w;
+  float eps;
+  float *h;  // [nseg][n_ff]
+  int n_ff;
+  StepIO *io;
+};
+
+// x[r] += sum_s gate[s] * (W_s h_s)[r]  (MoE down projections, summed)
+struct DownMoeArgs {
+  Geom g;
+  Segs s;
+  const float *h;  // [nseg][n_ff]
+  int n_ff;
+  const float *gate;
+  float *x;
+  StepIO *io;
+};
+
+// logits = W RMSNorm(x); greedy token; pos += 1
+struct LmArgs {
+  Geom g;
+  Segs s;
+  const float *x;
+  const float *norm_w;
+  float eps;
+  float *logits;       // optional
+  int32_t *argmax_out; // optional
+  float *part_val;     // [gridDim.x]
+  int32_t *part_idx;   // [gridDim.x]
+  unsigned int *counter;
+  StepIO *io;
+};
+
+// router logits, top-k, softmax over the chosen logits
+struct RouterArgs {
+  const void *w;  // [n_expert][E]
+  int n_expert, k, E;
+  const float *x;
+  const float *norm_w;
+  float eps;
+  int32_t *idx;
+  float *gate;
+  StepIO *io;
+};
+
+// split-KV decode attention of the token at io->pos (grid: n_split x n_kv x zgroups)
+struct AttnArgs {
+  const float *q;        // [n_head][hd]
+  const void *k_cache;   // this layer's [n_kv][cap][hd]
+  const void *v_cache;
+  int n_head, n_kv, cap, window;
+  int n_split;
+  float *part;           // [n_head][n_split][hd + 2]
+  unsigned int *counter; // [n_kv * zgroups]
+  float *out;            // [n_head][hd]
+  float qscale;          // log2(e) / sqrt(hd)
+  int stage_pos;         // positions per ring slot
+  int nstages;           // ring slots
+  StepIO *io;
+};
+
+struct AttnGeom {
+  int stage_pos;  // positions per ring slot
+  int nstages;
+  int heads_per_cta;
+  int smem;       // dynamic shared memory bytes
+};
+
+// Launchers (dtype: 0 fp32, 1 bf16).  pdl = launch with programmatic stream
+// serialization.  Return the CUDA error of the launch.
+cudaError_t launch_qkv(int dtype, const QkvArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_resid(int dtype, const ResidArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_gateup(int dtype, const GateUpArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_down_moe(int dtype, const DownMoeArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_lmhead(int dtype, const LmArgs &a, int grid, cudaStream_t st, bool pdl);
+cudaError_t launch_router(int dtype, const RouterArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGeom &ag,
+                        cudaStream_t st, bool pdl);
+cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st);
+cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st);
+
+// raise the dynamic shared-memory limit of the kernels a model will launch
+// (outside any stream capture)
+cudaError_t prepare_gemv_kernels(int dtype, int smem_bytes);
+cudaError_t prepare_attn_kernel(int dtype, int head_dim, const AttnGeom &ag);
+
+// attention geometry for a head_dim / group size (host)
+AttnGeom attn_geom(int dtype, int head_dim, int group);
+
+}  // namespace pnb
