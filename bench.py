@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: tokens/s and achieved HBM GB/s per step on one GB300.
+
+Default workload: the Llama-7B-shaped dense decoder in bf16 (E4096, H32,
+Hkv32, L32, F11008, V32000), KV cache pre-filled to position 2048 with
+generated N(0,1) bf16 entries, greedy decode of 128 tokens at batch 1.  A
+step is one token through the whole decode path (embedding, 32 layers, LM head,
+argmax), replayed from its CUDA graph.  Every 128 steps the position rewinds
+to 2048 (a new 128-token decode of the same workload).  The weights (13.2 GB)
+and KV cache are far larger than L2, so nothing stays cached between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
+only reference this project has) on the same workload, per-layer units.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and achieved HBM GB/s per step vs ~8 TB/s peak, 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SOURCES = ["transformer_decode_step_gb300/csrc/pnb_gemv.cu",
+                  "transformer_decode_step_gb300/csrc/pnb_device.cuh",
+                  "transformer_decode_step_gb300/csrc/pnb_kernels.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama7b_bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="use only the first N layers (small cases for ncu captures)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ accounting
+
+def step_bytes(shape, pos: int) -> int:
+    """Algorithmic HBM bytes of one decode step at position pos: weights read
+    (one embedding row, all projections of the chosen experts, router, norms,
+    LM head), KV entries attended (window-limited) and the new KV entry."""
+    es = shape.elem_bytes
+    weights = shape.params_read_per_token() * es + (2 * shape.n_layer + 1) * shape.n_embd * 4
+    n_att = pos + 1 if shape.sliding_window <= 0 else min(pos + 1, shape.sliding_window)
+    per_pos = shape.n_layer * 2 * shape.n_kv_head * shape.head_dim * es
+    return weights + n_att * per_pos + per_pos
+
+
+def gateup_bytes(shape) -> int:
+    """Algorithmic bytes of one gate/up launch: the chosen experts' [2F][E]
+    weights, the residual and norm vectors read, the SwiGLU output written."""
+    k = shape.expert_used if shape.expert_count > 0 else 1
+    return k * 2 * shape.n_ff * shape.n_embd * shape.elem_bytes + 2 * shape.n_embd * 4 + \
+        k * shape.n_ff * 4
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per gate/up launch from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"gateup_{workload}_ncu.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources_sha256_16") != kernel_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError as e:
+            self.error = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line.strip()))
+
+    def start(self):
+        self.t0 = time.monotonic()
+
+    def stop(self):
+        self.t1 = time.monotonic()
+
+    def summary(self):
+        if self.proc is None:
+            return {"error": getattr(self, "error", "nvidia-smi unavailable")}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [p for t, p in rows if self.t0 is not None and self.t0 <= t <= self.t1]
+        use = inside or [p for _, p in rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in use if num(p[1]) is not None]
+        mx = [num(p[2]) for p in use if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "power_w_max": max((num(p[3]) or 0) for p in use) if use else None}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(n_gpus: int):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0):
+    """Time the oracle on the workload in per-token units (layer 0 with the
+    embedding, layers 1..L-1, final norm + LM head), rotating through them.
+    Returns (tokens/s, units run, seconds, threads)."""
+    import oracle
+    import synth.workloads as wl
+
+    m = oracle.Model(w.shape, seed=w.seed)
+    st = m.new_state()
+    lo, hi = wl.kv_prefill_range(w.shape, w.prefill)
+    st.prefill_synth(w.seed, 0, lo, hi)
+    tok = wl.prompt_tokens(w)[0]
+    L = w.shape.n_layer
+    x = None
+
+    def run_unit(u):
+        nonlocal x
+        if u == 0:
+            x = st.embed(tok)
+        if u < L:
+            st.layer(u, x)
+        else:
+            st.head(x, want_logits=False)
+
+    for u in range(warmup):
+        run_unit(u % (L + 1))
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_units:
+        run_unit(n % (L + 1))
+        n += 1
+        if time.perf_counter() - t0 > seconds_budget and n % (L + 1) == 0:
+            break
+    dt = time.perf_counter() - t0
+    return (n / (L + 1)) / dt, n, dt, oracle.max_threads()
+
+
+# ------------------------------------------------------------------ main arms
+
+def workload_config(w, extra=None):
+    s = w.shape
+    cfg = {"workload": f"{w.name}: E{s.n_embd} H{s.n_head} Hkv{s.n_kv_head} L{s.n_layer} "
+                       f"F{s.n_ff} V{s.n_vocab} theta{s.rope_theta:g}"
+                       + (f" window{s.sliding_window}" if s.sliding_window else "")
+                       + (f" experts{s.expert_count}top{s.expert_used}" if s.expert_count else "")
+                       + f", KV pre-filled to {w.prefill}, greedy decode of {w.steps} tokens, batch {w.batch if w.batch else 1}",
+           "batch": 1, "weights_dtype": "bf16" if s.dtype == 1 else "f32",
+           "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_reference(args, w):
+    rank, world, local = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    budget = 200.0
+    tps, n, dt, threads = oracle_units(w, budget, max_units=args.steps, warmup=min(args.warmup, 2))
+    L = w.shape.n_layer
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n} per-token units ({L} layers + LM head, rotated) of the "
+                                       f"workload's first decode step, {dt:.1f} s"},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+
+    import transformer_decode_step_gb300 as pnb
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    s = w.shape
+    P = w.prefill
+    budget = s.n_ctx - P                       # decode steps one pass can take
+    sm = pnb.SynthModel(s, w.seed)
+    st = sm.new_state(start_pos=P, slot=rank)
+    import synth.workloads as wl
+    tok0 = wl.prompt_tokens(w, rank)[0]
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one_pass_step(i):
+        if i % budget == 0:
+            st.set_pos(P)
+            st.forward(tok0, argmax=am)
+        else:
+            st.forward(pnb.PNB_TOKEN_PREV, argmax=am)
+
+    # warm-up (captures the graph)
+    for i in range(max(3, args.warmup)):
+        one_pass_step(i)
+    torch.cuda.synchronize()
+    if st.device_error():
+        raise SystemExit("device error during warm-up")
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    e0.record(stream)
+    for i in range(args.steps):
+        one_pass_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    err = st.device_error()
+    clk = clocks.summary()
+    passes = (args.steps + budget - 1) // budget
+    launches = args.steps * sm.step_kernel_count() + 2 * passes
+    ms_step = ms / args.steps
+    tokens_per_s = world * args.steps / (ms / 1000.0)
+    mean_bytes = sum(step_bytes(s, P + (i % budget)) for i in range(args.steps)) / args.steps
+    step_gbs = mean_bytes / (ms_step / 1000.0) / 1e9
+
+    # dominant kernel (SwiGLU gate/up: the largest weight stream of the step) timed alone
+    L = s.n_layer
+    for l in range(3):
+        st.run_kernel(pnb.PNB_KERNEL_GATE_UP, l % L)
+    reps = 3 * L
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for i in range(reps):
+        st.run_kernel(pnb.PNB_KERNEL_GATE_UP, i % L)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    k_ms = k0.elapsed_time(k1) / reps
+    kb = gateup_bytes(s)
+    peaks, peak_kind = measured_peaks()
+    k_gbs = kb / (k_ms / 1000.0) / 1e9
+    traffic = recorded_traffic(w.name)
+
+    # end to end through the C ABI: the host feeds each token by value and reads
+    # the greedy token back (pinned host memory) before the next step
+    pinned = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    e2e_steps = min(args.steps, budget)
+    st.set_pos(P)
+    torch.cuda.synchronize()
+    tok = tok0
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        st.forward(tok, argmax=am)
+        pinned.copy_(am, non_blocking=True)
+        stream.synchronize()
+        tok = int(pinned[0])
+    e2e_s = time.perf_counter() - t0
+    e2e_tps = world * e2e_steps / e2e_s   # every rank runs the same loop
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, n, dt, threads = oracle_units(w, 15.0, max_units=10 * (L + 1))
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} per-token units ({L} layers + LM head) = {n / (L + 1):.2f} decode "
+                         f"steps of the workload at position {P}, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded generated weights and KV cache)",
+                "config": workload_config(w, {"parallelism": f"replicas x{world}",
+                                              "positions": f"{P}..{P + budget - 1}"}),
+                "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"],
+                "bytes_per_step": mean_bytes,
+                "roofline": {"bound": "hbm", "kernel": "k_gateup (RMSNorm + gate/up GEMV + SwiGLU)",
+                             "achieved": k_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": k_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                             "bytes_per_launch": kb, "launch_us": k_ms * 1000.0,
+                             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                             "timing": "CUDA events over 96 launches of the kernel alone, "
+                                       "rotating over the 32 layers' weights"},
+                "clocks": clk, "gpu_launches": launches, "device_error": err,
+                "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                        "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                        "how": "pnb_forward with the token passed by value from the host, "
+                               "argmax copied to pinned host memory and synchronised every step"},
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    import dataclasses
+
+    import synth.workloads as wl
+    w = wl.BY_NAME[args.workload]
+    if args.layers:
+        w = w.with_(shape=dataclasses.replace(w.shape, n_layer=args.layers),
+                    name=f"{w.name}_L{args.layers}")
+    import __graft_entry__
+    __graft_entry__.build(import_package=args.impl == "ours")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -184,9 +184,35 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
    the kernels one by one (0).  Results are identical either way. */
 int pnb_model_set_graphs(pnb_model *m, int enable);
 
+/* Run each single-sequence step as one persistent cooperative kernel (the
+   default whenever the shape allows it: head_dim in {32, 64, 128}, n_head /
+   n_kv_head in {1, 2, 4, 8} with (n_head / n_kv_head) * head_dim <= 512), or
+   as one kernel per phase (enable = 0).  Results agree to fp32 rounding.
+   Returns PNB_E_UNSUPPORTED when enabling is not possible for this model. */
+int pnb_model_set_persistent(pnb_model *m, int enable);
+int pnb_model_is_persistent(const pnb_model *m);
+
 /* Number of this library's kernels one step launches (single sequence when
    B == 0, batched otherwise). */
 int pnb_step_kernel_count(const pnb_model *m, int32_t B);
+
+/* The kernels of one decode step, in launch order within a layer. */
+enum {
+  PNB_KERNEL_QKV = 0,     /* RMSNorm (+ embedding in layer 0), Wqkv, RoPE, KV append */
+  PNB_KERNEL_ATTN = 1,    /* split-KV attention with window, log-sum-exp merge */
+  PNB_KERNEL_OPROJ = 2,   /* Wo + residual */
+  PNB_KERNEL_ROUTER = 3,  /* MoE only: router logits, top-k, softmax */
+  PNB_KERNEL_GATE_UP = 4, /* RMSNorm, gate/up (chosen experts), SwiGLU */
+  PNB_KERNEL_DOWN = 5,    /* down projection(s) + residual */
+  PNB_KERNEL_LM_HEAD = 6  /* final RMSNorm, LM head, argmax, pos += 1 */
+};
+
+/* Launch one kernel of the single-sequence step for `layer` in isolation
+   (stream-ordered, no overlap with the previous kernel), reading and writing
+   the state's workspace and KV cache exactly as inside a step: meant for
+   per-kernel timing and checks.  The host position is not changed (the LM
+   head kernel still advances the device position, as in a step). */
+int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb_stream stream);
 
 /* Device pointers of a state's fp32 activation buffers after its last step
    (x: residual [n_embd]; q: rotated queries [n_head*hd]; attn: attention
@@ -196,6 +222,16 @@ typedef struct {
   float *x, *q, *attn, *h;
 } pnb_activations;
 int pnb_state_activations(const pnb_state *s, pnb_activations *out);
+
+/* Diagnostics: have the persistent kernel record globaltimer stamps (ns) into
+   trace_dev, laid out [CTA][phase][6] with CTA < number of SMs, phase < 5 *
+   n_layer + 1 (per layer: QKV, attention, output projection, gate/up, down;
+   then the LM head) and slots 0 = compute finished the phase, 1 = passed the
+   phase's grid barrier (for the LM-head phase: kernel start), 2 = ns the first compute warp spent on staged GEMV slots after their data
+   arrived, 3 = ns it spent waiting for ring data (accumulated: zero the buffer
+   first), 4 / 5 = when its last GEMV slot loop of the phase started / ended.
+   NULL turns it off.  bytes must cover the layout. */
+int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes);
 
 const char *pnb_strerror(int code);
 

@@ -89,6 +89,11 @@ def lib():
         L.orc_state_prefill_synth.argtypes = [p, ctypes.c_uint64, ctypes.c_uint32, i64, i64, f]
         L.orc_forward.restype = i32
         L.orc_forward.argtypes = [p, p, ctypes.c_int32, p, p]
+        L.orc_embed.restype = i32
+        L.orc_embed.argtypes = [p, ctypes.c_int32, p]
+        L.orc_layer.restype = i32
+        L.orc_layer.argtypes = [p, p, i32, p]
+        L.orc_head.argtypes = [p, p, p, p]
         L.orc_set_threads.argtypes = [i32]
         L.orc_max_threads.restype = i32
         _lib = L
@@ -281,4 +286,25 @@ class State:
             raise ValueError(f"token {token} out of range")
         if rc == -2:
             raise ValueError("KV cache full")
+        return logits, int(am.value)
+
+    # The step in parts (same arithmetic as forward): embed, each layer, head.
+    def embed(self, token: int) -> np.ndarray:
+        x = np.empty(self.model.shape.n_embd, dtype=np.float32)
+        if lib().orc_embed(self.model._h, token, x.ctypes.data) != 0:
+            raise ValueError(f"token {token} out of range")
+        return x
+
+    def layer(self, l: int, x: np.ndarray) -> np.ndarray:
+        """Layer l for the token at the current pos (pos is not advanced); x in place."""
+        if lib().orc_layer(self.model._h, self._h, l, x.ctypes.data) != 0:
+            raise ValueError("KV cache full")
+        return x
+
+    def head(self, x: np.ndarray, want_logits: bool = True):
+        V = self.model.shape.n_vocab
+        logits = np.empty(V, dtype=np.float32) if want_logits else None
+        am = ctypes.c_int32(-1)
+        lib().orc_head(self.model._h, x.ctypes.data,
+                       logits.ctypes.data if logits is not None else None, ctypes.byref(am))
         return logits, int(am.value)

@@ -370,19 +370,27 @@ int orc_state_prefill_synth(orc_state *s, uint64_t seed, uint32_t sub, int64_t j
 
 /* ------------------------------------------------------------ forward */
 
-/* One decode step for `token` at position state->pos.  Writes fp32 logits
-   [n_vocab] (if logits != NULL) and the greedy token (if argmax != NULL),
-   then advances pos.  Returns 0, -1 for a bad token, -2 when the cache is full. */
-int orc_forward(const orc_model *m, orc_state *s, int32_t token, float *logits, int32_t *argmax) {
+/* Token embedding: x = row `token` of tok_embd (storage values as fp32).
+   Returns 0, or -1 for a token outside [0, n_vocab). */
+int orc_embed(const orc_model *m, int32_t token, float *x) {
+  if (token < 0 || token >= m->cfg.n_vocab) return -1;
+  get_row(&m->glob[ORC_G_TOK_EMBD], token, m->cfg.n_embd, m->cfg.dtype, x);
+  return 0;
+}
+
+/* One transformer layer l for the token at position state->pos: attention
+   block (RMSNorm, Q/K/V, RoPE, cache append, attention, output projection,
+   residual) then feed-forward block (RMSNorm, SwiGLU or top-k MoE, residual),
+   updating x [n_embd] in place.  Does not advance pos.  Returns -2 when the
+   cache is full. */
+int orc_layer(const orc_model *m, orc_state *s, int l, float *x) {
   const orc_config *c = &m->cfg;
   const int64_t E = c->n_embd, H = c->n_head, Hkv = c->n_kv_head, hd = m->head_dim;
-  const int64_t F = c->n_ff, V = c->n_vocab;
+  const int64_t F = c->n_ff;
   const int dt = c->dtype;
   const int64_t p = s->pos;
-  if (token < 0 || token >= V) return -1;
   if (p >= c->n_ctx) return -2;
 
-  float *x = (float *)malloc((size_t)E * sizeof(float));
   float *xn = (float *)malloc((size_t)E * sizeof(float));
   float *wbuf = (float *)malloc((size_t)E * sizeof(float));
   float *q = (float *)malloc((size_t)(H * hd) * sizeof(float));
@@ -391,64 +399,49 @@ int orc_forward(const orc_model *m, orc_state *s, int32_t token, float *logits, 
   float *o = (float *)malloc((size_t)(H * hd) * sizeof(float));
   float *t = (float *)malloc((size_t)E * sizeof(float));
   float *t2 = (float *)malloc((size_t)E * sizeof(float));
-  float *lg = (float *)malloc((size_t)V * sizeof(float));
 
-  /* token embedding: row `token` of tok_embd */
-  get_row(&m->glob[ORC_G_TOK_EMBD], token, E, dt, x);
-
-  for (int l = 0; l < c->n_layer; ++l) {
-    /* attention block */
-    get_row(ltensor(m, l, ORC_L_ATTN_NORM), 0, E, 0, wbuf);
-    orc_rmsnorm(x, wbuf, E, c->rms_norm_eps, xn);
-    orc_matvec(ltensor(m, l, ORC_L_WQ), H * hd, E, dt, xn, q);
-    orc_matvec(ltensor(m, l, ORC_L_WK), Hkv * hd, E, dt, xn, kn);
-    orc_matvec(ltensor(m, l, ORC_L_WV), Hkv * hd, E, dt, xn, vn);
-    for (int64_t h = 0; h < H; ++h) orc_rope(q + h * hd, (int)hd, p, c->rope_theta);
-    for (int64_t g = 0; g < Hkv; ++g) orc_rope(kn + g * hd, (int)hd, p, c->rope_theta);
-    float *Kl = orc_state_kv(s, l, 0), *Vl = orc_state_kv(s, l, 1);
-    for (int64_t e = 0; e < Hkv * hd; ++e) {
-      Kl[p * Hkv * hd + e] = dt ? orc_round_bf16(kn[e]) : kn[e];
-      Vl[p * Hkv * hd + e] = dt ? orc_round_bf16(vn[e]) : vn[e];
-    }
-    orc_attention(q, Kl, Vl, (int)H, (int)Hkv, (int)hd, p, c->sliding_window, o);
-    orc_matvec(ltensor(m, l, ORC_L_WO), E, H * hd, dt, o, t);
-    for (int64_t i = 0; i < E; ++i) x[i] = x[i] + t[i];
-
-    /* feed-forward block */
-    get_row(ltensor(m, l, ORC_L_FFN_NORM), 0, E, 0, wbuf);
-    orc_rmsnorm(x, wbuf, E, c->rms_norm_eps, xn);
-    if (c->expert_count <= 0) {
-      orc_ffn(ltensor(m, l, ORC_L_EXPERT0), ltensor(m, l, ORC_L_EXPERT0 + 1),
-              ltensor(m, l, ORC_L_EXPERT0 + 2), E, F, dt, xn, t);
-    } else {
-      const int X = c->expert_count, k = c->expert_used;
-      float r[256];
-      int32_t idx[256];
-      double g[256];
-      orc_matvec(ltensor(m, l, ORC_L_WROUTER), X, E, dt, xn, r);
-      orc_topk_softmax(r, X, k, idx, g);
-      double *acc = (double *)calloc((size_t)E, sizeof(double));
-      for (int i = 0; i < k; ++i) {
-        const int base = ORC_L_EXPERT0 + 3 * idx[i];
-        orc_ffn(ltensor(m, l, base), ltensor(m, l, base + 1), ltensor(m, l, base + 2), E, F, dt, xn,
-                t2);
-        for (int64_t e = 0; e < E; ++e) acc[e] += g[i] * (double)t2[e];
-      }
-      for (int64_t e = 0; e < E; ++e) t[e] = (float)acc[e];
-      free(acc);
-    }
-    for (int64_t i = 0; i < E; ++i) x[i] = x[i] + t[i];
-  }
-
-  /* final norm, LM head, greedy pick */
-  get_row(&m->glob[ORC_G_OUT_NORM], 0, E, 0, wbuf);
+  /* attention block */
+  get_row(ltensor(m, l, ORC_L_ATTN_NORM), 0, E, 0, wbuf);
   orc_rmsnorm(x, wbuf, E, c->rms_norm_eps, xn);
-  orc_matvec(&m->glob[ORC_G_OUTPUT], V, E, dt, xn, lg);
-  if (logits) memcpy(logits, lg, (size_t)V * sizeof(float));
-  if (argmax) *argmax = orc_argmax(lg, V);
-  s->pos = p + 1;
+  orc_matvec(ltensor(m, l, ORC_L_WQ), H * hd, E, dt, xn, q);
+  orc_matvec(ltensor(m, l, ORC_L_WK), Hkv * hd, E, dt, xn, kn);
+  orc_matvec(ltensor(m, l, ORC_L_WV), Hkv * hd, E, dt, xn, vn);
+  for (int64_t h = 0; h < H; ++h) orc_rope(q + h * hd, (int)hd, p, c->rope_theta);
+  for (int64_t g = 0; g < Hkv; ++g) orc_rope(kn + g * hd, (int)hd, p, c->rope_theta);
+  float *Kl = orc_state_kv(s, l, 0), *Vl = orc_state_kv(s, l, 1);
+  for (int64_t e = 0; e < Hkv * hd; ++e) {
+    Kl[p * Hkv * hd + e] = dt ? orc_round_bf16(kn[e]) : kn[e];
+    Vl[p * Hkv * hd + e] = dt ? orc_round_bf16(vn[e]) : vn[e];
+  }
+  orc_attention(q, Kl, Vl, (int)H, (int)Hkv, (int)hd, p, c->sliding_window, o);
+  orc_matvec(ltensor(m, l, ORC_L_WO), E, H * hd, dt, o, t);
+  for (int64_t i = 0; i < E; ++i) x[i] = x[i] + t[i];
 
-  free(x);
+  /* feed-forward block */
+  get_row(ltensor(m, l, ORC_L_FFN_NORM), 0, E, 0, wbuf);
+  orc_rmsnorm(x, wbuf, E, c->rms_norm_eps, xn);
+  if (c->expert_count <= 0) {
+    orc_ffn(ltensor(m, l, ORC_L_EXPERT0), ltensor(m, l, ORC_L_EXPERT0 + 1),
+            ltensor(m, l, ORC_L_EXPERT0 + 2), E, F, dt, xn, t);
+  } else {
+    const int X = c->expert_count, k = c->expert_used;
+    float r[256];
+    int32_t idx[256];
+    double g[256];
+    orc_matvec(ltensor(m, l, ORC_L_WROUTER), X, E, dt, xn, r);
+    orc_topk_softmax(r, X, k, idx, g);
+    double *acc = (double *)calloc((size_t)E, sizeof(double));
+    for (int i = 0; i < k; ++i) {
+      const int base = ORC_L_EXPERT0 + 3 * idx[i];
+      orc_ffn(ltensor(m, l, base), ltensor(m, l, base + 1), ltensor(m, l, base + 2), E, F, dt, xn,
+              t2);
+      for (int64_t e = 0; e < E; ++e) acc[e] += g[i] * (double)t2[e];
+    }
+    for (int64_t e = 0; e < E; ++e) t[e] = (float)acc[e];
+    free(acc);
+  }
+  for (int64_t i = 0; i < E; ++i) x[i] = x[i] + t[i];
+
   free(xn);
   free(wbuf);
   free(q);
@@ -457,6 +450,37 @@ int orc_forward(const orc_model *m, orc_state *s, int32_t token, float *logits, 
   free(o);
   free(t);
   free(t2);
+  return 0;
+}
+
+/* Final RMSNorm, LM head and greedy pick from the residual x [n_embd]. */
+void orc_head(const orc_model *m, const float *x, float *logits, int32_t *argmax) {
+  const int64_t E = m->cfg.n_embd, V = m->cfg.n_vocab;
+  float *xn = (float *)malloc((size_t)E * sizeof(float));
+  float *wbuf = (float *)malloc((size_t)E * sizeof(float));
+  float *lg = (float *)malloc((size_t)V * sizeof(float));
+  get_row(&m->glob[ORC_G_OUT_NORM], 0, E, 0, wbuf);
+  orc_rmsnorm(x, wbuf, E, m->cfg.rms_norm_eps, xn);
+  orc_matvec(&m->glob[ORC_G_OUTPUT], V, E, m->cfg.dtype, xn, lg);
+  if (logits) memcpy(logits, lg, (size_t)V * sizeof(float));
+  if (argmax) *argmax = orc_argmax(lg, V);
+  free(xn);
+  free(wbuf);
   free(lg);
+}
+
+/* One decode step for `token` at position state->pos: embedding, every
+   layer, final norm + LM head; writes fp32 logits [n_vocab] (if logits !=
+   NULL) and the greedy token (if argmax != NULL), then advances pos.
+   Returns 0, -1 for a bad token, -2 when the cache is full. */
+int orc_forward(const orc_model *m, orc_state *s, int32_t token, float *logits, int32_t *argmax) {
+  if (token < 0 || token >= m->cfg.n_vocab) return -1;
+  if (s->pos >= m->cfg.n_ctx) return -2;
+  float *x = (float *)malloc((size_t)m->cfg.n_embd * sizeof(float));
+  orc_embed(m, token, x);
+  for (int l = 0; l < m->cfg.n_layer; ++l) orc_layer(m, s, l, x);
+  orc_head(m, x, logits, argmax);
+  s->pos += 1;
+  free(x);
   return 0;
 }

@@ -33,6 +33,21 @@ def tol(shape):
     return 1e-3 if shape.dtype == F32 else 2e-2
 
 
+def set_mode(sm, mode):
+    """'persistent': one cooperative kernel per step; 'kernels': one kernel per phase."""
+    if mode == "persistent":
+        try:
+            sm.model.set_persistent(True)
+        except pnb.PnbError as e:
+            if e.code == -5:
+                pytest.skip("the persistent kernel does not cover this shape")
+            raise
+        assert sm.model.persistent and sm.model.step_kernel_count() == 1
+    else:
+        sm.model.set_persistent(False)
+        assert not sm.model.persistent
+
+
 def gpu_run(sm, state, tokens, graphs=True):
     sm.model.set_graphs(graphs)
     V = sm.shape.n_vocab
@@ -117,21 +132,25 @@ def _tiny_tokens():
     return prompt, gen
 
 
-def test_tiny_teacher_forced_matches_oracle():
+@pytest.mark.parametrize("mode", ["persistent", "kernels"])
+def test_tiny_teacher_forced_matches_oracle(mode):
     w = wl.TINY
     prompt, gen = _tiny_tokens()
     tokens = prompt + gen[:-1]
     sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
+    set_mode(sm, mode)
     got, gam = gpu_run(sm, sm.new_state(), tokens)
     ref, ram = oracle_run(w.shape, w.seed, tokens)
     assert compare(w.shape, got, gam, ref, ram, "tiny") == 0
     assert gam[len(prompt) - 1:] == gen
 
 
-def test_tiny_free_running_greedy_matches_stored_oracle_run():
+@pytest.mark.parametrize("mode", ["persistent", "kernels"])
+def test_tiny_free_running_greedy_matches_stored_oracle_run(mode):
     w = wl.TINY
     prompt, gen = _tiny_tokens()
     sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
+    set_mode(sm, mode)
     st = sm.new_state()
     a = torch.empty(len(gen), dtype=torch.int32, device=DEV)
     for t in prompt[:-1]:
@@ -144,11 +163,13 @@ def test_tiny_free_running_greedy_matches_stored_oracle_run():
     assert st.pos == len(prompt) + len(gen) - 1
 
 
-def test_graph_replay_equals_eager_launches_bitwise():
+@pytest.mark.parametrize("mode", ["persistent", "kernels"])
+def test_graph_replay_equals_eager_launches_bitwise(mode):
     w = wl.TINY
     prompt, gen = _tiny_tokens()
     tokens = prompt + gen[:8]
     sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
+    set_mode(sm, mode)
     a, _ = gpu_run(sm, sm.new_state(), tokens, graphs=True)
     b, _ = gpu_run(sm, sm.new_state(), tokens, graphs=False)
     for x, y in zip(a, b):
@@ -192,20 +213,25 @@ SMALL_MHA = dataclasses.replace(SMALL_WIN, n_kv_head=8, sliding_window=0, n_ff=1
 SMALL_MOE = wl.Shape(n_vocab=777, n_embd=256, n_head=4, n_kv_head=2, n_layer=2, n_ff=512,
                      n_ctx=64, rope_theta=1e6, rms_norm_eps=1e-5, expert_count=4, expert_used=2,
                      dtype=BF16)
+SMALL_G8 = wl.Shape(n_vocab=512, n_embd=2048, n_head=16, n_kv_head=2, n_layer=1, n_ff=1024,
+                    n_ctx=64, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
 SMALL_HD128 = wl.Shape(n_vocab=1000, n_embd=1024, n_head=8, n_kv_head=2, n_layer=1, n_ff=2816,
                        n_ctx=300, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
 
 
+@pytest.mark.parametrize("mode", ["persistent", "kernels"])
 @pytest.mark.parametrize("name,shape,start,steps", [
     ("window_ring", SMALL_WIN, 40, 24),       # ring of 24 slots, pre-fill wraps it
     ("window_short", SMALL_WIN, 0, 30),       # empty cache, window fills then slides
     ("mha", SMALL_MHA, 17, 12),
     ("moe", SMALL_MOE, 9, 12),
     ("hd128", SMALL_HD128, 250, 8),
+    ("hd128_gqa8", SMALL_G8, 40, 6),           # 8 query heads per KV head at head_dim 128
 ])
-def test_small_bf16_models_match_oracle(name, shape, start, steps):
+def test_small_bf16_models_match_oracle(name, shape, start, steps, mode):
     seed = 77
     sm = pnb.SynthModel(shape, seed, device=DEV)
+    set_mode(sm, mode)
     st = sm.new_state(start_pos=start)
     rng = np.random.default_rng(5)
     tokens = [int(t) for t in rng.integers(0, shape.n_vocab, size=steps)]
@@ -213,6 +239,19 @@ def test_small_bf16_models_match_oracle(name, shape, start, steps):
     ref, ram = oracle_run(shape, seed, tokens, start_pos=start)
     ties = compare(shape, got, gam, ref, ram, name)
     assert ties <= 1
+
+
+def test_persistent_and_per_kernel_steps_agree():
+    """Same model and tokens through both execution modes: logits agree to fp32 rounding."""
+    shape, seed = SMALL_WIN, 13
+    tokens = [5, 17, 400, 3000, 9, 9, 1]
+    outs = []
+    for mode in ("persistent", "kernels"):
+        sm = pnb.SynthModel(shape, seed, device=DEV)
+        set_mode(sm, mode)
+        outs.append(gpu_run(sm, sm.new_state(start_pos=30), tokens))
+    for a, b in zip(outs[0][0], outs[1][0]):
+        assert np.max(np.abs(a - b)) <= 1e-4 * np.max(np.abs(a))
 
 
 # ------------------------------------------------- full-size workloads, sampled steps

@@ -504,3 +504,19 @@ def test_tiny_workload_matches_stored_oracle_run():
     for (i, v), s in zip(top, stored["top5"]):
         si, sv = s.split(":")
         assert i == int(si) and math.isclose(v, float(sv), rel_tol=1e-6)
+
+
+def test_step_in_parts_equals_forward():
+    """embed + every layer + head (pos advanced by hand) reproduces forward bit for bit."""
+    shape = dataclasses.replace(TS, dtype=BF16, sliding_window=4)
+    arrays = _rand_arrays(shape)
+    m = oracle.Model(shape, arrays=arrays)
+    a, b = m.new_state(), m.new_state()
+    for t in [3, 1, 4, 1, 5, 9, 2]:
+        la, ama = a.forward(t)
+        x = b.embed(t)
+        for l in range(shape.n_layer):
+            b.layer(l, x)
+        lb, amb = b.head(x)
+        b.pos = b.pos + 1
+        assert np.array_equal(la, lb) and ama == amb

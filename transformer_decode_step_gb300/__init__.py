@@ -22,6 +22,8 @@ _lib = ctypes.CDLL(LIB)
 PNB_F32, PNB_BF16 = 0, 1
 PNB_TOKEN_PREV = -1
 PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT = 1, 2
+(PNB_KERNEL_QKV, PNB_KERNEL_ATTN, PNB_KERNEL_OPROJ, PNB_KERNEL_ROUTER, PNB_KERNEL_GATE_UP,
+ PNB_KERNEL_DOWN, PNB_KERNEL_LM_HEAD) = range(7)
 ERRORS = {0: "PNB_OK", -1: "PNB_E_INVAL", -2: "PNB_E_NULL", -3: "PNB_E_ALIGN",
           -4: "PNB_E_CTX_FULL", -5: "PNB_E_UNSUPPORTED", -6: "PNB_E_CUDA", -7: "PNB_E_TOKEN",
           -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE"}
@@ -60,8 +62,12 @@ _SIGS = {
     "pnb_forward": (_i32, [_p, _p, _i32, _p, _p, _p]),
     "pnb_forward_batch": (_i32, [_p, _p, _i32, _p, _p, _p, _p]),
     "pnb_model_set_graphs": (_i32, [_p, _i32]),
+    "pnb_model_set_persistent": (_i32, [_p, _i32]),
+    "pnb_model_is_persistent": (_i32, [_p]),
     "pnb_step_kernel_count": (_i32, [_p, _i32]),
     "pnb_state_activations": (_i32, [_p, _p]),
+    "pnb_step_kernel": (_i32, [_p, _p, _i32, _i32, _p]),
+    "pnb_state_set_trace": (_i32, [_p, _p, _sz]),
     "pnb_strerror": (ctypes.c_char_p, [_i32]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -142,6 +148,13 @@ class Model:
     def set_graphs(self, enable: bool):
         check(pnb_model_set_graphs(self._h, 1 if enable else 0), "pnb_model_set_graphs")
 
+    def set_persistent(self, enable: bool):
+        check(pnb_model_set_persistent(self._h, 1 if enable else 0), "pnb_model_set_persistent")
+
+    @property
+    def persistent(self) -> bool:
+        return bool(pnb_model_is_persistent(self._h))
+
     def step_kernel_count(self, batch: int = 0) -> int:
         return int(pnb_step_kernel_count(self._h, batch))
 
@@ -199,6 +212,16 @@ class State:
         if rc not in (0, -8):
             check(rc, "pnb_state_check")
         return e.value
+
+    def run_kernel(self, kind: int, layer: int, stream=None):
+        """One kernel of the step in isolation (pnb_step_kernel)."""
+        check(pnb_step_kernel(self.model.handle, self._h, kind, layer, _stream(stream)),
+              "pnb_step_kernel")
+
+    def set_trace(self, buf):
+        """Phase timestamps of the persistent kernel into `buf` (device int64 tensor) or off."""
+        nbytes = buf.numel() * buf.element_size() if buf is not None else 0
+        check(pnb_state_set_trace(self._h, _ptr(buf), nbytes), "pnb_state_set_trace")
 
     def activations(self) -> dict:
         a = pnb_activations()

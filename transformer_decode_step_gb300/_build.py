@@ -19,12 +19,24 @@ def headers():
     return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
+OBJ = os.path.join(PKG, "_objs")
+FLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-lineinfo",
+         f"-gencode=arch=compute_{ARCH},code=sm_{ARCH}"]
+
+
 def build_jobs():
-    """(output, inputs, command) triples; empty until the CUDA sources exist."""
+    """Build stages: a list of parallel (output, inputs, command) jobs per stage -
+    one object per CUDA source, then the shared-library link."""
     srcs = sources()
     if not srcs:
         return []
-    cmd = ["nvcc", "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-lineinfo",
-           f"-gencode=arch=compute_{ARCH},code=sm_{ARCH}", "-I", os.path.join(ROOT, "include"),
-           "-I", CSRC, "-o", LIB] + srcs
-    return [(LIB, srcs + headers(), cmd)]
+    objs, compile_jobs = [], []
+    for src in srcs:
+        obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+        objs.append(obj)
+        compile_jobs.append((obj, [src] + headers(),
+                             ["nvcc"] + FLAGS + ["-I", os.path.join(ROOT, "include"), "-I", CSRC,
+                                                 "-c", src, "-o", obj]))
+    link = (LIB, objs, ["nvcc", "-shared", f"-gencode=arch=compute_{ARCH},code=sm_{ARCH}",
+                        "-o", LIB] + objs)
+    return [compile_jobs, [link]]

@@ -11,13 +11,14 @@
 
 #include "pnb.h"
 #include "pnb_kernels.cuh"
+#include "pnb_step.cuh"
 
 using namespace pnb;
 
 namespace {
 
 constexpr int kStageTarget = 32 * 1024;   // bytes of whole rows per GEMV ring slot
-constexpr int kRingBudget = 128 * 1024;   // bytes of GEMV ring per CTA
+constexpr int kRingBudget = 192 * 1024;   // bytes of GEMV ring per CTA
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxBatch = 64;
 
@@ -32,15 +33,22 @@ Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int g
   while (rps * 2 <= 64 && rps * 2 * g.row_bytes <= kStageTarget) rps *= 2;
   g.rows_per_stage = rps;
   g.stage_bytes = rps * g.row_bytes;
-  g.nstages = std::min(8, std::max(2, kRingBudget / g.stage_bytes));
-  g.wpr = std::max(1, kConsumerWarps / rps);
+  // warps per row: enough that a lane holds at most 4 column vectors, and no
+  // more row groups than rows per ring slot
   const int vpr = g.row_bytes / 16;
-  g.chunk = (ceil_div(vpr, g.wpr) + 7) / 8 * 8;
+  int cw = 1;
+  while (cw < kGemvWarps && (cw * 32 * 4 < vpr || kGemvWarps / cw > rps)) cw *= 2;
+  g.cw = cw;
+  const int nv = ceil_div(vpr, 32 * cw);
+  g.nv = nv <= 1 ? 1 : (nv <= 2 ? 2 : (nv <= 4 ? 4 : 8));  // 8 = unsupported
   g.row_align = row_align;
   const int64_t units = rows_total / row_align;
   g.rows_cta_max = ceil_div(units, grid) * row_align;
-  g.xs_floats = xpad_size(K);
   g.nsum = nsum;
+  g.nstages = 2;
+  const int fixed = smem_layout(g).total - 2 * g.stage_bytes - 2 * 16;  // everything but the ring
+  const int ring = std::min(kRingBudget, kMaxSmem - fixed - 1024);
+  g.nstages = std::min(8, std::max(2, ring / g.stage_bytes));
   return g;
 }
 
@@ -66,6 +74,9 @@ struct pnb_model {
   AttnGeom ag{};
   int n_split = 1, zgroups = 1;
   bool graphs = true;
+  // persistent step kernel
+  bool persistent = false;
+  int st_nslots = 0, st_slot_bytes = 0, st_sp = 0, st_union = 0, st_smem = 0;
   cudaStream_t cap_stream = nullptr;     // stream used for graph capture
 };
 
@@ -81,6 +92,12 @@ struct pnb_state {
   int32_t *idx = nullptr, *lm_idx = nullptr;
   unsigned *attn_cnt = nullptr, *lm_cnt = nullptr;
   size_t counters_off = 0, counters_bytes = 0;
+  unsigned *bar_count = nullptr, *bar_gen = nullptr;
+  int32_t *abort_flag = nullptr;
+  float *step_part = nullptr;            // attention partials of the persistent kernel
+  float *ss_part = nullptr;              // per-CTA sums of squares [2][grid]
+  StepLayer *layers = nullptr;           // device [n_layer]
+  unsigned long long *trace = nullptr;   // optional phase timestamps (persistent kernel)
   cudaGraphExec_t exec = nullptr;
   float *g_logits = nullptr;
   int32_t *g_argmax = nullptr;
@@ -124,8 +141,46 @@ void plan(pnb_model *m) {
   const int G = c.n_head / c.n_kv_head;
   m->ag = attn_geom(c.dtype, m->hd, G);
   m->zgroups = G / m->ag.heads_per_cta;
-  const int want = std::max(1, 2 * m->num_sms / (c.n_kv_head * m->zgroups));
+  // one wave: at most one CTA per SM (the attention CTA's registers allow one)
+  const int want = std::max(1, m->num_sms / (c.n_kv_head * m->zgroups));
   m->n_split = std::max(1, std::min(want, std::max(1, m->cap / 16)));
+}
+
+bool geoms_supported(const pnb_model *m);
+
+// Persistent-kernel geometry: one ring slot holds the largest GEMV stage or a
+// 2 x sp x head_dim KV stage; the scratch union holds the largest per-CTA
+// partial array or the attention merge area.
+void plan_step(pnb_model *m) {
+  const pnb_config &c = m->cfg;
+  const int G = c.n_head / c.n_kv_head, hd = m->hd, es = m->es;
+  m->persistent = false;
+  if (!(hd == 32 || hd == 64 || hd == 128) || !(G == 1 || G == 2 || G == 4 || G == 8) ||
+      G * hd > 512)
+    return;
+  int slot = 0, uni = 0;
+  for (const Geom *g : {&m->g_qkv, &m->g_o, &m->g_gateup, &m->g_down, &m->g_lm}) {
+    slot = std::max(slot, g->stage_bytes);
+    uni = std::max(uni, g->rows_cta_max * g->cw * g->nsum);
+  }
+  slot = std::max(slot, 2 * 32 * hd * es);
+  int sp = slot / (2 * hd * es);
+  sp = std::min(256, sp - sp % 32);
+  uni = std::max(uni, kGemvWarps * G * (hd + 2));
+  const int fixed = step_smem(1, slot, uni).total - slot;
+  int ns = std::min(kRingBudget / slot, (kMaxSmem - fixed - 1024) / slot);
+  if (ns < 2) return;
+  ns = std::min(ns, 8);
+  m->st_nslots = ns;
+  m->st_slot_bytes = slot;
+  m->st_sp = sp;
+  m->st_union = uni;
+  m->st_smem = step_smem(ns, slot, uni).total;
+  if (m->st_smem > kMaxSmem || !geoms_supported(m)) return;
+  StepArgs dummy{};
+  int bps = 0;
+  cudaError_t e = (c.dtype ? step_bf16 : step_f32)(hd, G, dummy, m->grid, m->st_smem, nullptr, true, &bps);
+  m->persistent = e == cudaSuccess && bps >= 1;
 }
 
 int max_smem(const pnb_model *m) {
@@ -135,92 +190,80 @@ int max_smem(const pnb_model *m) {
   return s;
 }
 
-// Enqueue one single-sequence step (everything after the token write).
-cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *logits,
-                         int32_t *argmax) {
+// every streaming GEMV fits the kernels' register slices (at most 4 vectors per lane)
+bool geoms_supported(const pnb_model *m) {
+  for (const Geom *g : {&m->g_qkv, &m->g_o, &m->g_gateup, &m->g_down, &m->g_lm})
+    if (g->nv > 4) return false;
+  return true;
+}
+
+// Enqueue one kernel of the single-sequence step.
+cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStream_t st, bool pdl,
+                           float *logits, int32_t *argmax) {
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, hd = m->hd, F = c.n_ff;
   const size_t layer_kv = (size_t)Hkv * m->cap * hd * m->es;
+  uint8_t *kc = s->kv + (size_t)(2 * l) * layer_kv, *vc = kc + layer_kv;
   const float eps = (float)c.rms_norm_eps;
   const bool moe = c.expert_count > 0;
   const int k = moe ? c.expert_used : 1;
-  cudaError_t e;
-  for (int l = 0; l < c.n_layer; ++l) {
-    uint8_t *kc = s->kv + (size_t)(2 * l) * layer_kv, *vc = kc + layer_kv;
-    QkvArgs qa{};
-    qa.g = m->g_qkv;
-    qa.s.n = 1;
-    qa.s.rows = m->qkv_rows;
-    qa.s.w[0] = m->wqkv[l];
-    qa.x = s->x;
-    qa.emb = l == 0 ? m->tok_embd : nullptr;
-    qa.x_out = s->x;
-    qa.n_vocab = c.n_vocab;
-    qa.norm_w = m->attn_norm[l];
-    qa.eps = eps;
-    qa.n_head = H;
-    qa.n_kv = Hkv;
-    qa.head_dim = hd;
-    qa.inv_freq = m->inv_freq;
-    qa.q = s->q;
-    qa.k_cache = kc;
-    qa.v_cache = vc;
-    qa.cap = m->cap;
-    qa.window = c.sliding_window;
-    qa.io = s->io;
-    if ((e = launch_qkv(c.dtype, qa, m->grid, st, l > 0)) != cudaSuccess) return e;
-
-    AttnArgs aa{};
-    aa.q = s->q;
-    aa.k_cache = kc;
-    aa.v_cache = vc;
-    aa.n_head = H;
-    aa.n_kv = Hkv;
-    aa.cap = m->cap;
-    aa.window = c.sliding_window;
-    aa.n_split = m->n_split;
-    aa.part = s->part;
-    aa.counter = s->attn_cnt;
-    aa.out = s->attn;
-    aa.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
-    aa.stage_pos = m->ag.stage_pos;
-    aa.nstages = m->ag.nstages;
-    aa.io = s->io;
-    if ((e = launch_attn(c.dtype, hd, aa, m->ag, st, true)) != cudaSuccess) return e;
-
-    ResidArgs oa{};
-    oa.g = m->g_o;
-    oa.s.n = 1;
-    oa.s.rows = E;
-    oa.s.w[0] = m->wo[l];
-    oa.vec = s->attn;
-    oa.x = s->x;
-    oa.io = s->io;
-    if ((e = launch_resid(c.dtype, oa, m->grid, st, true)) != cudaSuccess) return e;
-
-    GateUpArgs ga{};
-    ga.g = m->g_gateup;
-    ga.s.rows = 2 * (int64_t)F;
-    ga.x = s->x;
-    ga.norm_w = m->ffn_norm[l];
-    ga.eps = eps;
-    ga.h = s->h;
-    ga.n_ff = F;
-    ga.io = s->io;
-    if (!moe) {
-      ga.s.n = 1;
-      ga.s.w[0] = m->w_gate_up[l];
-      if ((e = launch_gateup(c.dtype, ga, m->grid, st, true)) != cudaSuccess) return e;
-      ResidArgs da{};
-      da.g = m->g_down;
-      da.s.n = 1;
-      da.s.rows = E;
-      da.s.w[0] = m->w_down[l];
-      da.vec = s->h;
-      da.x = s->x;
-      da.io = s->io;
-      if ((e = launch_resid(c.dtype, da, m->grid, st, true)) != cudaSuccess) return e;
-    } else {
+  switch (kind) {
+    case PNB_KERNEL_QKV: {
+      QkvArgs qa{};
+      qa.g = m->g_qkv;
+      qa.s.n = 1;
+      qa.s.rows = m->qkv_rows;
+      qa.s.w[0] = m->wqkv[l];
+      qa.x = s->x;
+      qa.emb = l == 0 ? m->tok_embd : nullptr;
+      qa.x_out = s->x;
+      qa.n_vocab = c.n_vocab;
+      qa.norm_w = m->attn_norm[l];
+      qa.eps = eps;
+      qa.n_head = H;
+      qa.n_kv = Hkv;
+      qa.head_dim = hd;
+      qa.inv_freq = m->inv_freq;
+      qa.q = s->q;
+      qa.k_cache = kc;
+      qa.v_cache = vc;
+      qa.cap = m->cap;
+      qa.window = c.sliding_window;
+      qa.io = s->io;
+      return launch_qkv(c.dtype, qa, m->grid, st, pdl);
+    }
+    case PNB_KERNEL_ATTN: {
+      AttnArgs aa{};
+      aa.q = s->q;
+      aa.k_cache = kc;
+      aa.v_cache = vc;
+      aa.n_head = H;
+      aa.n_kv = Hkv;
+      aa.cap = m->cap;
+      aa.window = c.sliding_window;
+      aa.n_split = m->n_split;
+      aa.part = s->part;
+      aa.counter = s->attn_cnt;
+      aa.out = s->attn;
+      aa.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
+      aa.stage_pos = m->ag.stage_pos;
+      aa.nstages = m->ag.nstages;
+      aa.io = s->io;
+      return launch_attn(c.dtype, hd, aa, m->ag, st, pdl);
+    }
+    case PNB_KERNEL_OPROJ: {
+      ResidArgs oa{};
+      oa.g = m->g_o;
+      oa.s.n = 1;
+      oa.s.rows = E;
+      oa.s.w[0] = m->wo[l];
+      oa.vec = s->attn;
+      oa.x = s->x;
+      oa.io = s->io;
+      return launch_resid(c.dtype, oa, m->grid, st, pdl);
+    }
+    case PNB_KERNEL_ROUTER: {
+      if (!moe) return cudaErrorInvalidValue;
       RouterArgs ra{};
       ra.w = m->w_router[l];
       ra.n_expert = c.expert_count;
@@ -232,11 +275,39 @@ cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *log
       ra.idx = s->idx;
       ra.gate = s->gate;
       ra.io = s->io;
-      if ((e = launch_router(c.dtype, ra, st, true)) != cudaSuccess) return e;
+      return launch_router(c.dtype, ra, st, pdl);
+    }
+    case PNB_KERNEL_GATE_UP: {
+      GateUpArgs ga{};
+      ga.g = m->g_gateup;
+      ga.s.rows = 2 * (int64_t)F;
+      ga.x = s->x;
+      ga.norm_w = m->ffn_norm[l];
+      ga.eps = eps;
+      ga.h = s->h;
+      ga.n_ff = F;
+      ga.io = s->io;
       ga.s.n = k;
-      ga.s.table = m->tab_gate_up + (size_t)l * c.expert_count;
-      ga.s.expert_idx = s->idx;
-      if ((e = launch_gateup(c.dtype, ga, m->grid, st, true)) != cudaSuccess) return e;
+      if (moe) {
+        ga.s.table = m->tab_gate_up + (size_t)l * c.expert_count;
+        ga.s.expert_idx = s->idx;
+      } else {
+        ga.s.w[0] = m->w_gate_up[l];
+      }
+      return launch_gateup(c.dtype, ga, m->grid, st, pdl);
+    }
+    case PNB_KERNEL_DOWN: {
+      if (!moe) {
+        ResidArgs da{};
+        da.g = m->g_down;
+        da.s.n = 1;
+        da.s.rows = E;
+        da.s.w[0] = m->w_down[l];
+        da.vec = s->h;
+        da.x = s->x;
+        da.io = s->io;
+        return launch_resid(c.dtype, da, m->grid, st, pdl);
+      }
       DownMoeArgs da{};
       da.g = m->g_down;
       da.s.n = k;
@@ -248,24 +319,110 @@ cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *log
       da.gate = s->gate;
       da.x = s->x;
       da.io = s->io;
-      if ((e = launch_down_moe(c.dtype, da, m->grid, st, true)) != cudaSuccess) return e;
+      return launch_down_moe(c.dtype, da, m->grid, st, pdl);
     }
+    case PNB_KERNEL_LM_HEAD: {
+      LmArgs la{};
+      la.g = m->g_lm;
+      la.s.n = 1;
+      la.s.rows = c.n_vocab;
+      la.s.w[0] = m->output;
+      la.x = s->x;
+      la.norm_w = m->out_norm;
+      la.eps = eps;
+      la.logits = logits;
+      la.argmax_out = argmax;
+      la.part_val = s->lm_val;
+      la.part_idx = s->lm_idx;
+      la.counter = s->lm_cnt;
+      la.io = s->io;
+      return launch_lmhead(c.dtype, la, m->grid, st, pdl);
+    }
+    default:
+      return cudaErrorInvalidValue;
   }
-  LmArgs la{};
-  la.g = m->g_lm;
-  la.s.n = 1;
-  la.s.rows = c.n_vocab;
-  la.s.w[0] = m->output;
-  la.x = s->x;
-  la.norm_w = m->out_norm;
-  la.eps = eps;
-  la.logits = logits;
-  la.argmax_out = argmax;
-  la.part_val = s->lm_val;
-  la.part_idx = s->lm_idx;
-  la.counter = s->lm_cnt;
-  la.io = s->io;
-  return launch_lmhead(c.dtype, la, m->grid, st, true);
+}
+
+// The persistent kernel's arguments for state s.
+StepArgs step_args(const pnb_model *m, const pnb_state *s, float *logits, int32_t *argmax) {
+  const pnb_config &c = m->cfg;
+  StepArgs a{};
+  a.E = c.n_embd;
+  a.H = c.n_head;
+  a.Hkv = c.n_kv_head;
+  a.hd = m->hd;
+  a.F = c.n_ff;
+  a.V = c.n_vocab;
+  a.L = c.n_layer;
+  a.X = c.expert_count;
+  a.k = c.expert_count > 0 ? c.expert_used : 1;
+  a.cap = m->cap;
+  a.window = c.sliding_window;
+  a.eps = (float)c.rms_norm_eps;
+  a.qscale = (float)(1.4426950408889634 / std::sqrt((double)m->hd));
+  a.g_qkv = m->g_qkv;
+  a.g_o = m->g_o;
+  a.g_gu = m->g_gateup;
+  a.g_dn = m->g_down;
+  a.g_lm = m->g_lm;
+  a.nslots = m->st_nslots;
+  a.slot_bytes = m->st_slot_bytes;
+  a.sp = m->st_sp;
+  a.union_floats = m->st_union;
+  a.tok_embd = m->tok_embd;
+  a.output = m->output;
+  a.out_norm = m->out_norm;
+  a.inv_freq = m->inv_freq;
+  a.layers = s->layers;
+  a.x = s->x;
+  a.q = s->q;
+  a.o = s->attn;
+  a.h = s->h;
+  a.attn_part = s->step_part;
+  a.lm_val = s->lm_val;
+  a.lm_idx = s->lm_idx;
+  a.attn_cnt = s->attn_cnt;
+  a.lm_cnt = s->lm_cnt;
+  a.bar_count = s->bar_count;
+  a.bar_gen = s->bar_gen;
+  a.abort_flag = s->abort_flag;
+  a.ss_part = s->ss_part;
+  a.logits = logits;
+  a.argmax_out = argmax;
+  a.io = s->io;
+  a.trace = s->trace;
+  return a;
+}
+
+// Enqueue one single-sequence step (everything after the token write): the
+// persistent kernel when the model supports it, else one kernel per phase
+// (the first waits for all earlier stream work; every later one is launched
+// with programmatic stream serialization).
+cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *logits,
+                         int32_t *argmax) {
+  if (m->persistent) {
+    const StepArgs a = step_args(m, s, logits, argmax);
+    const int G = m->cfg.n_head / m->cfg.n_kv_head;
+    return (m->cfg.dtype ? step_bf16 : step_f32)(m->hd, G, a, m->grid, m->st_smem, st, false, nullptr);
+  }
+  const bool moe = m->cfg.expert_count > 0;
+  cudaError_t e;
+  for (int l = 0; l < m->cfg.n_layer; ++l) {
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
+      return e;
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN, l, st, true, nullptr, nullptr)) != cudaSuccess)
+      return e;
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_OPROJ, l, st, true, nullptr, nullptr)) != cudaSuccess)
+      return e;
+    if (moe && (e = enqueue_kernel(m, s, PNB_KERNEL_ROUTER, l, st, true, nullptr, nullptr)) !=
+                   cudaSuccess)
+      return e;
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_GATE_UP, l, st, true, nullptr, nullptr)) != cudaSuccess)
+      return e;
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_DOWN, l, st, true, nullptr, nullptr)) != cudaSuccess)
+      return e;
+  }
+  return enqueue_kernel(m, s, PNB_KERNEL_LM_HEAD, 0, st, true, logits, argmax);
 }
 
 }  // namespace
@@ -344,7 +501,7 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   }
   m->grid = m->num_sms;
   plan(m);
-  if (max_smem(m) > kMaxSmem) {
+  if (max_smem(m) > kMaxSmem || !geoms_supported(m)) {
     delete m;
     return PNB_E_UNSUPPORTED;
   }
@@ -366,6 +523,7 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   if (ok) ok = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
   if (ok) ok = prepare_gemv_kernels(c.dtype, kMaxSmem) == cudaSuccess &&
                prepare_attn_kernel(c.dtype, m->hd, m->ag) == cudaSuccess;
+  if (ok) plan_step(m);
   if (!ok) {
     pnb_model_free(m);
     return PNB_E_CUDA;
@@ -419,7 +577,11 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   const size_t o_idx = take((size_t)k * 4);
   const size_t o_lmv = take((size_t)m->grid * 4);
   const size_t o_lmi = take((size_t)m->grid * 4);
-  const size_t o_cnt = take((size_t)(c.n_kv_head * m->zgroups + 1) * 4);
+  const size_t n_cnt = (size_t)(c.n_kv_head * m->zgroups + 1 + 3);
+  const size_t o_cnt = take(n_cnt * 4);
+  const size_t o_spart = take((size_t)c.n_head * m->grid * (m->hd + 2) * 4);
+  const size_t o_layers = take((size_t)c.n_layer * sizeof(StepLayer));
+  const size_t o_ss = take((size_t)2 * m->grid * 4);
   if (cudaMalloc(&s->ws, off) != cudaSuccess) {
     delete s;
     return PNB_E_NOMEM;
@@ -436,9 +598,37 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   s->lm_idx = reinterpret_cast<int32_t *>(s->ws + o_lmi);
   s->attn_cnt = reinterpret_cast<unsigned *>(s->ws + o_cnt);
   s->lm_cnt = s->attn_cnt + c.n_kv_head * m->zgroups;
+  s->bar_count = s->lm_cnt + 1;
+  s->bar_gen = s->lm_cnt + 2;
+  s->abort_flag = reinterpret_cast<int32_t *>(s->lm_cnt + 3);
   s->counters_off = o_cnt;
-  s->counters_bytes = (size_t)(c.n_kv_head * m->zgroups + 1) * 4;
-  if (cudaMemset(s->ws, 0, off) != cudaSuccess) {
+  s->counters_bytes = n_cnt * 4;
+  s->step_part = reinterpret_cast<float *>(s->ws + o_spart);
+  s->layers = reinterpret_cast<StepLayer *>(s->ws + o_layers);
+  s->ss_part = reinterpret_cast<float *>(s->ws + o_ss);
+  // per-layer table of the persistent kernel
+  std::vector<StepLayer> lt(c.n_layer);
+  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
+  for (int l = 0; l < c.n_layer; ++l) {
+    StepLayer &L = lt[l];
+    L.wqkv = m->wqkv[l];
+    L.wo = m->wo[l];
+    L.attn_norm = m->attn_norm[l];
+    L.ffn_norm = m->ffn_norm[l];
+    if (c.expert_count > 0) {
+      L.w_router = m->w_router[l];
+      L.tab_gate_up = m->tab_gate_up + (size_t)l * c.expert_count;
+      L.tab_down = m->tab_down + (size_t)l * c.expert_count;
+    } else {
+      L.w_gate_up = m->w_gate_up[l];
+      L.w_down = m->w_down[l];
+    }
+    L.kc = s->kv + (size_t)(2 * l) * layer_kv;
+    L.vc = s->kv + (size_t)(2 * l + 1) * layer_kv;
+  }
+  if (cudaMemset(s->ws, 0, off) != cudaSuccess ||
+      cudaMemcpy(s->layers, lt.data(), lt.size() * sizeof(StepLayer), cudaMemcpyHostToDevice) !=
+          cudaSuccess) {
     cudaFree(s->ws);
     delete s;
     return PNB_E_CUDA;
@@ -552,6 +742,18 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
   return PNB_E_UNSUPPORTED;
 }
 
+int pnb_model_set_persistent(pnb_model *m, int enable) {
+  if (!m) return PNB_E_NULL;
+  if (!enable) {
+    m->persistent = false;
+    return PNB_OK;
+  }
+  plan_step(m);
+  return m->persistent ? PNB_OK : PNB_E_UNSUPPORTED;
+}
+
+int pnb_model_is_persistent(const pnb_model *m) { return m && m->persistent ? 1 : 0; }
+
 int pnb_model_set_graphs(pnb_model *m, int enable) {
   if (!m) return PNB_E_NULL;
   m->graphs = enable != 0;
@@ -561,8 +763,38 @@ int pnb_model_set_graphs(pnb_model *m, int enable) {
 int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
   if (!m) return PNB_E_NULL;
   (void)B;
+  if (m->persistent) return 1;
   const int per_layer = m->cfg.expert_count > 0 ? 6 : 5;
   return m->cfg.n_layer * per_layer + 1;
+}
+
+int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb_stream stream) {
+  if (!m || !s) return PNB_E_NULL;
+  if (s->m != m) return PNB_E_INVAL;
+  if (kind < PNB_KERNEL_QKV || kind > PNB_KERNEL_LM_HEAD) return PNB_E_INVAL;
+  if (kind == PNB_KERNEL_ROUTER && m->cfg.expert_count == 0) return PNB_E_INVAL;
+  if (layer < 0 || layer >= m->cfg.n_layer) return PNB_E_INVAL;
+  int rc = check_device(m);
+  if (rc != PNB_OK) return rc;
+  if (enqueue_kernel(m, s, kind, layer, reinterpret_cast<cudaStream_t>(stream), false, nullptr,
+                     nullptr) != cudaSuccess)
+    return PNB_E_CUDA;
+  return PNB_OK;
+}
+
+int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes) {
+  if (!s) return PNB_E_NULL;
+  if (trace_dev) {
+    const size_t need = (size_t)s->m->grid * (5 * s->m->cfg.n_layer + 1) * 6 * 8;
+    if (bytes < need) return PNB_E_INVAL;
+    if (reinterpret_cast<uintptr_t>(trace_dev) & 7u) return PNB_E_ALIGN;
+  }
+  s->trace = reinterpret_cast<unsigned long long *>(trace_dev);
+  if (s->exec) {   // the captured graph holds the old argument
+    cudaGraphExecDestroy(s->exec);
+    s->exec = nullptr;
+  }
+  return PNB_OK;
 }
 
 int pnb_state_activations(const pnb_state *s, pnb_activations *out) {

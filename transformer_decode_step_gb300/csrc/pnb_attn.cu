@@ -58,16 +58,16 @@ __host__ __device__ inline AttnSmem attn_smem(int stage_pos, int nstages, int hd
   AttnSmem L;
   L.ring = 0;
   L.mo = align_up(nstages * 2 * stage_pos * hd * es, 16);
-  L.mm = L.mo + kConsumerWarps * gb * hd * 4;
-  L.ml = L.mm + kConsumerWarps * gb * 4;
-  L.flag = L.ml + kConsumerWarps * gb * 4;
+  L.mm = L.mo + kAttnWarps * gb * hd * 4;
+  L.ml = L.mm + kAttnWarps * gb * 4;
+  L.flag = L.ml + kAttnWarps * gb * 4;
   L.bars = align_up(L.flag + 16, 16);
   L.total = L.bars + 2 * nstages * 8;
   return L;
 }
 
 template <typename T, int HD, int GB>
-__global__ void __launch_bounds__(kThreads, 1) k_attn(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
   constexpr int ES = (int)sizeof(T);
   constexpr int DPL = HD / 8;                             // dims per lane when scoring
   constexpr int UNIT = (DPL * ES < 16) ? DPL * ES : 16;   // bytes per shared-memory load
@@ -100,14 +100,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const AttnArgs a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], kAttnWarps);
     }
     fence_barrier_init();
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kAttnWarps) {
     if (lane == 0) {
       const T *kb = static_cast<const T *>(a.k_cache) + (int64_t)g * a.cap * HD;
       const T *vb = static_cast<const T *>(a.v_cache) + (int64_t)g * a.cap * HD;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const AttnArgs a) {
 #pragma unroll
     for (int d = 0; d < VPL; ++d) o[gh][d] = 0.f;
   }
-  const int PPW = SP / kConsumerWarps;
+  const int PPW = SP / kAttnWarps;
   bool ok = true;
   for (int st = 0; st < nst; ++st) {
     const int slot = st % NS, round = st / NS;
@@ -260,14 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const AttnArgs a) {
 #pragma unroll
     for (int d = 0; d < VPL; ++d) mo[(warp * GB + gh) * HD + lane * VPL + d] = o[gh][d];
   }
-  consumer_sync();
-  for (int idx = tid; idx < GB * HD; idx += kConsumerThreads) {
+  consumer_sync<kAttnConsumers>();
+  for (int idx = tid; idx < GB * HD; idx += kAttnConsumers) {
     const int gh = idx / HD, d = idx - gh * HD;
     float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * GB + gh]);
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mm[w * GB + gh]);
     float Ls = 0.f, Os = 0.f;
     if (M != -INFINITY) {
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < kAttnWarps; ++w) {
         const float f = exp2f(mm[w * GB + gh] - M);
         Ls = fmaf(ml[w * GB + gh], f, Ls);
         Os = fmaf(mo[(w * GB + gh) * HD + d], f, Os);
@@ -281,26 +281,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn(const AttnArgs a) {
     P[2 + d] = Os;
   }
   __threadfence();
-  consumer_sync();
+  consumer_sync<kAttnConsumers>();
   if (tid == 0) {
     const unsigned prev = atomicAdd(&a.counter[g * gridDim.z + z], 1u);
     *flag = (prev == (unsigned)a.n_split - 1u);
   }
-  consumer_sync();
+  consumer_sync<kAttnConsumers>();
   if (*flag) {
     __threadfence();
-    for (int idx = tid; idx < GB * HD; idx += kConsumerThreads) {
+    // one pass over the splits, eight splits' loads in flight at a time
+    const int ns = a.n_split;
+    for (int idx = tid; idx < GB * HD; idx += kAttnConsumers) {
       const int gh = idx / HD, d = idx - gh * HD;
-      const float *P0 = a.part + (int64_t)(h0 + gh) * a.n_split * (HD + 2);
-      float M = -INFINITY;
-      for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, __ldcg(P0 + s * (HD + 2)));
-      float Ls = 0.f, Os = 0.f;
-      for (int s = 0; s < a.n_split; ++s) {
-        const float ms = __ldcg(P0 + s * (HD + 2));
-        if (ms == -INFINITY) continue;
-        const float f = exp2f(ms - M);
-        Ls = fmaf(__ldcg(P0 + s * (HD + 2) + 1), f, Ls);
-        Os = fmaf(__ldcg(P0 + s * (HD + 2) + 2 + d), f, Os);
+      const float *P0 = a.part + (int64_t)(h0 + gh) * ns * (HD + 2);
+      float M = -INFINITY, Ls = 0.f, Os = 0.f;
+      for (int s0 = 0; s0 < ns; s0 += 8) {
+        float pm[8], pl[8], po[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float *P = P0 + (int64_t)(s0 + j < ns ? s0 + j : 0) * (HD + 2);
+          pm[j] = __ldcg(P);
+          pl[j] = __ldcg(P + 1);
+          po[j] = __ldcg(P + 2 + d);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j >= ns) pm[j] = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (pm[j] == -INFINITY) continue;
+          const float Mn = fmaxf(M, pm[j]);
+          const float f0 = exp2f(M - Mn), f1 = exp2f(pm[j] - Mn);
+          Ls = Ls * f0 + pl[j] * f1;
+          Os = Os * f0 + po[j] * f1;
+          M = Mn;
+        }
       }
       a.out[(int64_t)(h0 + gh) * HD + d] = Os / Ls;
     }
@@ -319,7 +334,7 @@ cudaError_t launch_one(const AttnArgs &a, const AttnGeom &ag, cudaStream_t st, b
   const int G = a.n_head / a.n_kv;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_split, a.n_kv, G / GB);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = ag.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

@@ -10,9 +10,14 @@
 namespace pnb {
 
 // ------------------------------------------------------------------ limits
-constexpr int kConsumerWarps = 8;                        // compute warps per CTA
-constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one producer warp
-constexpr int kConsumerThreads = kConsumerWarps * 32;
+// weight-streaming (GEMV) kernels: 16 compute warps + one producer warp
+constexpr int kGemvWarps = 16;
+constexpr int kGemvConsumers = kGemvWarps * 32;
+constexpr int kGemvThreads = kGemvConsumers + 32;
+// attention kernel: 8 compute warps + one producer warp
+constexpr int kAttnWarps = 8;
+constexpr int kAttnConsumers = kAttnWarps * 32;
+constexpr int kAttnThreads = kAttnConsumers + 32;
 constexpr int kMaxSegments = 8;                          // matrices in one GEMV launch
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 
@@ -64,6 +69,20 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// Same, backing off between polls: for the single producer thread, whose
+// polling would otherwise take issue slots from the compute warps.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u) {
+      if (global_ns() - t0 > kWaitLimitNs || it > (1u << 24)) return false;
+    }
+  }
+}
+
 // Wait for the phase with the given parity to complete; gives up after about
 // kWaitLimitNs (or 2^26 polls) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
@@ -88,6 +107,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// hint: bring [src, src + bytes) into L2 (no completion tracking)
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // -------------------------------------------- programmatic dependent launch
 // wait until the preceding kernel in the stream has completed and its writes
 // are visible (no-op when launched without the PDL attribute)
@@ -97,9 +121,26 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// named barrier among the consumer warps only (id 1; id 0 is __syncthreads)
+// named barrier among the N consumer threads only (id 1; id 0 is __syncthreads)
+template <int N>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
+// d = a * b + c on packed pairs of fp32 (one instruction for two FMAs)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<unsigned long long *>(&a)),
+        "l"(*reinterpret_cast<unsigned long long *>(&b)),
+        "l"(*reinterpret_cast<unsigned long long *>(&c)));
+  return *reinterpret_cast<float2 *>(&d);
+}
+
+// the two bf16 of a 32-bit word as an fp32 pair (low half first), exact
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 // ------------------------------------------------------------ arithmetic
@@ -118,12 +159,6 @@ __device__ __forceinline__ float warp_max(float v) {
 // two bf16 packed in a 32-bit word -> two floats (exact)
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Shared-memory layout of an fp32 activation vector read by 16-byte weight
-// vectors: four padding floats after every 32 floats keep the 32-byte x
-// chunks of eight consecutive lanes on distinct banks.
-__device__ __forceinline__ int xpad(int i) { return i + ((i >> 5) << 2); }
-__host__ __device__ constexpr int xpad_size(int n) { return n + ((n + 31) / 32) * 4; }
 
 // storage of one element
 template <typename T>

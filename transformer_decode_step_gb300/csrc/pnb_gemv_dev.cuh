@@ -1,0 +1,353 @@
+// pnb_gemv_dev.cuh - device building blocks shared by the weight-streaming
+// kernels and the persistent decode-step kernel: ring item enumeration,
+// the producer loop, register slices of the activation vector, RMSNorm
+// factor, row dot products, RoPE angles.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "pnb_kernels.cuh"
+
+namespace pnb {
+
+extern __shared__ __align__(128) uint8_t g_smem[];
+
+__device__ __forceinline__ void gemv_sync() { consumer_sync<kGemvConsumers>(); }
+
+struct Item {
+  int seg;       // segment (matrix) index
+  int64_t row;   // first row inside the segment
+  int n;         // rows in this ring slot
+  int local;     // first row relative to the CTA's range
+};
+
+// Ring items of the CTA's rows [r0, r1): whole-row runs inside one segment, at
+// most rows_per_stage rows each.  Summed mode walks the range once per segment.
+// Incremental: one division when constructed, none per item.
+struct ItemIter {
+  int64_t r0, r1, rows, r, seg_base;
+  int nseg, rps, seg;
+  bool summed;
+  __device__ __forceinline__ ItemIter(int64_t r0_, int64_t r1_, int64_t rows_, int nseg_,
+                                      bool summed_, int rps_)
+      : r0(r0_), r1(r1_), rows(rows_), r(r0_), nseg(nseg_), rps(rps_), seg(0), summed(summed_) {
+    if (!summed && r0 < r1) seg = (int)(r0 / rows);
+    seg_base = summed ? 0 : (int64_t)seg * rows;
+  }
+  __device__ __forceinline__ bool next(Item &it) {
+    if (r0 >= r1) return false;
+    if (summed) {
+      if (r >= r1) {
+        ++seg;
+        r = r0;
+      }
+      if (seg >= nseg) return false;
+      const int n = (int)((int64_t)rps < r1 - r ? (int64_t)rps : r1 - r);
+      it.seg = seg;
+      it.row = r;
+      it.n = n;
+      it.local = (int)(r - r0);
+      r += n;
+      return true;
+    }
+    if (r >= r1) return false;
+    if (r >= seg_base + rows) {
+      ++seg;
+      seg_base += rows;
+    }
+    int64_t n64 = (int64_t)rps < r1 - r ? (int64_t)rps : r1 - r;
+    if (seg_base + rows - r < n64) n64 = seg_base + rows - r;
+    it.seg = seg;
+    it.row = r - seg_base;
+    it.n = (int)n64;
+    it.local = (int)(r - r0);
+    r += n64;
+    return true;
+  }
+};
+
+// Position in a ring of n slots: slot index and the parity of its current use.
+struct RingPos {
+  uint32_t slot, phase, n;
+  __device__ __forceinline__ void advance() {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+struct Ctx {
+  uint8_t *ring;
+  float *part, *red;
+  uint64_t *full, *empty;
+  int64_t r0, r1;
+};
+
+// Carve shared memory, compute the CTA's row range, initialise the ring barriers.
+__device__ __forceinline__ Ctx gemv_setup(const Geom &g, int64_t total_rows) {
+  const SmemLayout L = smem_layout(g);
+  Ctx c;
+  c.ring = g_smem + L.ring;
+  c.part = reinterpret_cast<float *>(g_smem + L.part);
+  c.red = reinterpret_cast<float *>(g_smem + L.red);
+  c.full = reinterpret_cast<uint64_t *>(g_smem + L.bars);
+  c.empty = c.full + g.nstages;
+  const int64_t units = total_rows / g.row_align;
+  c.r0 = units * blockIdx.x / gridDim.x * g.row_align;
+  c.r1 = units * (blockIdx.x + 1) / gridDim.x * g.row_align;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < g.nstages; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], kGemvWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  return c;
+}
+
+// Producer: stream the CTA's rows.  With `prefetch`, the first ring's worth is
+// issued before griddepcontrol.wait (weights do not depend on earlier kernels).
+// Always ends by waiting (bounded) for its last copies to land.
+__device__ __forceinline__ void produce(const Geom &g, const Segs &s, bool summed, bool prefetch, const Ctx &c,
+                        int32_t *err) {
+  bool waited = false;
+  if (!prefetch) {
+    pdl_wait();
+    pdl_trigger();
+    waited = true;
+  }
+  const void *w[kMaxSegments];
+  for (int i = 0; i < s.n; ++i) w[i] = s.table ? s.table[s.expert_idx[i]] : s.w[i];
+  ItemIter it(c.r0, c.r1, s.rows, s.n, summed, g.rows_per_stage);
+  Item item;
+  uint32_t i = 0;
+  RingPos rp{0u, 0u, (uint32_t)g.nstages};
+  bool ok = true;
+  while (it.next(item)) {
+    if (!waited && i == (uint32_t)g.nstages) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    if (i >= (uint32_t)g.nstages && !mbar_wait(&c.empty[rp.slot], rp.phase ^ 1u)) {
+      ok = false;
+      break;
+    }
+    const uint32_t bytes = (uint32_t)item.n * (uint32_t)g.row_bytes;
+    mbar_arrive_expect_tx(&c.full[rp.slot], bytes);
+    bulk_g2s(c.ring + rp.slot * (uint32_t)g.stage_bytes,
+             static_cast<const uint8_t *>(w[item.seg]) + item.row * g.row_bytes, bytes,
+             &c.full[rp.slot]);
+    ++i;
+    rp.advance();
+  }
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  if (!ok) set_error(err, kErrTimeout);
+  // wait for the copies still in flight: the last min(i, nstages) items
+  const uint32_t last = i < (uint32_t)g.nstages ? i : (uint32_t)g.nstages;
+  RingPos dp = rp;
+  for (uint32_t j = 0; j < last; ++j) {
+    if (dp.slot == 0) {
+      dp.slot = dp.n;
+      dp.phase ^= 1u;
+    }
+    --dp.slot;
+    if (!mbar_wait(&c.full[dp.slot], dp.phase)) set_error(err, kErrTimeout);
+  }
+}
+
+// ------------------------------------------------------- activation slices
+
+// elements per 16-byte weight vector
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+};
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+};
+
+// A lane's slice of the activation vector: for t < NV, the Vec<T>::N columns
+// of 16-byte vector v(t) = c*32 + lane + t*32*cw (c = the warp's column slot),
+// as fp32 pairs.
+template <typename T, int NV>
+struct XSlice {
+  float2 p[NV][Vec<T>::N / 2];
+};
+
+__device__ __forceinline__ float2 load2(const float *src, int col) {
+  return __ldcg(reinterpret_cast<const float2 *>(src + col));
+}
+__device__ __forceinline__ float2 load2(const __nv_bfloat16 *src, int col) {
+  return bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(src + col));
+}
+
+// xs = src * scale * w (w optional), columns of this lane only.  Every load
+// is issued (from an always-valid address) before any is used, so the lane
+// pays one memory round trip, not one per vector.
+template <typename T, int NV, typename S>
+__device__ __forceinline__ void load_slice(XSlice<T, NV> &xs, const S *src, float scale,
+                                           const float *w, const Geom &g, int warp, int lane) {
+  constexpr int P = Vec<T>::N / 2;
+  const int vpr = g.row_bytes / 16, c = warp % g.cw;
+  float2 xv[NV][P], wv[NV][P];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const int v = c * 32 + lane + t * 32 * g.cw;
+    const int vc = v < vpr ? v : 0;
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      xv[t][e] = load2(src, vc * Vec<T>::N + 2 * e);
+      wv[t][e] = w ? load2(w, vc * Vec<T>::N + 2 * e) : make_float2(1.f, 1.f);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const bool valid = c * 32 + lane + t * 32 * g.cw < vpr;
+#pragma unroll
+    for (int e = 0; e < P; ++e)
+      xs.p[t][e] = valid ? make_float2(xv[t][e].x * scale * wv[t][e].x, xv[t][e].y * scale * wv[t][e].y)
+                         : make_float2(0.f, 0.f);
+  }
+}
+
+// 1 / sqrt(mean(src^2) + eps) over E elements; all consumer threads, ends
+// synced.  Loads go out eight at a time before they are used.
+template <typename S>
+__device__ __forceinline__ float rms_inv(const S *src, int E, float eps, float *red, int tid) {
+  float ss = 0.f;
+  for (int base = tid * 2; base < E; base += kGemvConsumers * 2 * 8) {
+    float2 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + j * kGemvConsumers * 2;
+      v[j] = load2(src, i < E ? i : 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (base + j * kGemvConsumers * 2 < E) {
+        ss = fmaf(v[j].x, v[j].x, ss);
+        ss = fmaf(v[j].y, v[j].y, ss);
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  gemv_sync();
+  float tot = 0.f;
+  for (int k = 0; k < kGemvWarps; ++k) tot += red[k];
+  return 1.0f / sqrtf(tot / (float)E + eps);
+}
+
+// ---------------------------------------------------------------- dot products
+
+template <typename T, int NV>
+__device__ __forceinline__ float dot_row(const uint8_t *row, const XSlice<T, NV> &xs, int vpr,
+                                         int c, int cw, int lane) {
+  constexpr int P = Vec<T>::N / 2;
+  uint4 wv[NV];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const int v = c * 32 + lane + t * 32 * cw;
+    wv[t] = *reinterpret_cast<const uint4 *>(row + 16 * (v < vpr ? v : 0));
+  }
+  float2 acc[P];
+#pragma unroll
+  for (int e = 0; e < P; ++e) acc[e] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    if (c * 32 + lane + t * 32 * cw < vpr) {
+      const uint4 w = wv[t];
+      if constexpr (P == 4) {
+        acc[0] = ffma2(bf16x2_to_float2(w.x), xs.p[t][0], acc[0]);
+        acc[1] = ffma2(bf16x2_to_float2(w.y), xs.p[t][1], acc[1]);
+        acc[2] = ffma2(bf16x2_to_float2(w.z), xs.p[t][2], acc[2]);
+        acc[3] = ffma2(bf16x2_to_float2(w.w), xs.p[t][3], acc[3]);
+      } else {
+        acc[0] = ffma2(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), xs.p[t][0], acc[0]);
+        acc[1] = ffma2(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), xs.p[t][1], acc[1]);
+      }
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < P; ++e) s += acc[e].x + acc[e].y;
+  return s;
+}
+
+// Consumer loop over the CTA's ring items.  `reload(seg)` refreshes the
+// lane's activation slice when a summed launch moves to the next segment.  A
+// wait that expires sets the error bit and the warp stops consuming.
+template <typename T, int NV, typename Reload>
+__device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summed, const Ctx &c,
+                        XSlice<T, NV> &xs, int warp, int lane, int32_t *err, Reload &&reload) {
+  const int cw = g.cw, groups = kGemvWarps / cw;
+  const int grp = warp / cw, cc = warp - grp * cw;
+  const int vpr = g.row_bytes / 16;
+  ItemIter it(c.r0, c.r1, s.rows, s.n, summed, g.rows_per_stage);
+  Item item;
+  RingPos rp{0u, 0u, (uint32_t)g.nstages};
+  int cur = 0;
+  bool ok = true;
+  while (it.next(item)) {
+    if (summed && item.seg != cur) {
+      reload(item.seg);
+      cur = item.seg;
+    }
+    const uint32_t slot = rp.slot;
+    if (ok && !mbar_wait(&c.full[slot], rp.phase)) {
+      ok = false;
+      if (lane == 0) set_error(err, kErrTimeout);
+    }
+    if (ok) {
+      const uint8_t *stage = c.ring + slot * (uint32_t)g.stage_bytes;
+      float *part = c.part + ((summed ? item.seg : 0) * g.rows_cta_max + item.local) * cw;
+      for (int r = grp; r < item.n; r += groups) {
+        const float v = warp_sum(dot_row<T, NV>(stage + (size_t)r * g.row_bytes, xs, vpr, cc, cw, lane));
+        if (lane == 0) part[r * cw + cc] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.empty[slot]);
+    }
+    rp.advance();
+  }
+}
+
+__device__ __forceinline__ float row_total(const float *part, int local, int cw) {
+  float v = 0.f;
+  for (int w = 0; w < cw; ++w) v += part[local * cw + w];
+  return v;
+}
+
+// sin / cos of pos * inv_freq: the angle is formed and reduced to [-pi, pi]
+// in fp64 (two-term Cody-Waite reduction by 2*pi), then evaluated in fp32.
+__device__ __forceinline__ void rope_sincos(int pos, double inv_freq, float *s, float *c) {
+  const double phi = (double)pos * inv_freq;
+  const double k = rint(phi * 0.15915494309189535);  // 1 / (2 pi)
+  double r = fma(-k, 6.283185307179586, phi);          // 2 pi, high part
+  r = fma(-k, 2.4492935982947064e-16, r);              // 2 pi, low part
+  sincosf((float)r, s, c);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void argmax_merge(float &v, int &i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+
+}  // namespace pnb

@@ -5,9 +5,10 @@
 // and streams those rows whole through a ring of shared-memory stages filled
 // by 1-D bulk copies (one elected producer thread, mbarrier completion).  The
 // first ring's worth is issued before griddepcontrol.wait, so a kernel's
-// weight traffic overlaps the tail of the kernel before it.  Eight consumer
-// warps multiply the staged rows by an fp32 activation vector held in shared
-// memory and fold the result into a fused epilogue.
+// weight traffic overlaps the tail of the kernel before it.  Sixteen consumer
+// warps multiply the staged rows by the fp32 activation vector, each lane
+// holding its fixed column slice of that vector in registers, and fold the
+// result into a fused epilogue.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,11 +26,10 @@ struct Geom {
   int rows_per_stage; // power of two <= 64: whole rows per ring slot
   int stage_bytes;    // ring slot size = rows_per_stage * row_bytes
   int nstages;        // ring slots
-  int wpr;            // partial sums per row = max(1, consumer warps / rows_per_stage)
-  int chunk;          // vectors per warp when several warps share a row (multiple of 8)
+  int cw;             // warps sharing one row (its columns); 16 / cw rows in flight
+  int nv;             // 16-byte vectors per lane per row (1, 2 or 4)
   int row_align;      // CTA row ranges are multiples of this
   int rows_cta_max;   // most rows any CTA owns
-  int xs_floats;      // padded activation vector length in shared memory
   int nsum;           // matrices summed into the same rows (1 = concatenated rows)
 };
 
@@ -46,7 +46,7 @@ struct Segs {
 };
 
 struct SmemLayout {
-  int ring, xs, part, red, bars, total;
+  int ring, part, red, bars, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -54,9 +54,8 @@ __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a *
 __host__ __device__ inline SmemLayout smem_layout(const Geom &g) {
   SmemLayout L;
   L.ring = 0;
-  L.xs = align_up(g.nstages * g.stage_bytes, 128);
-  L.part = align_up(L.xs + g.xs_floats * 4, 16);
-  L.red = align_up(L.part + g.rows_cta_max * g.wpr * g.nsum * 4, 16);
+  L.part = align_up(g.nstages * g.stage_bytes, 128);
+  L.red = align_up(L.part + g.rows_cta_max * g.cw * g.nsum * 4, 16);
   L.bars = align_up(L.red + 64 * 4, 16);
   L.total = L.bars + 2 * g.nstages * 8;
   return L;
@@ -178,6 +177,14 @@ cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGe
                         cudaStream_t st, bool pdl);
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st);
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st);
+
+// persistent step kernel (one cooperative launch per decode step); with
+// prepare = true only sets its shared-memory limit and reports occupancy
+struct StepArgs;
+cudaError_t step_bf16(int hd, int G, const StepArgs &a, int grid, int smem, cudaStream_t st,
+                      bool prepare, int *blocks_per_sm);
+cudaError_t step_f32(int hd, int G, const StepArgs &a, int grid, int smem, cudaStream_t st,
+                     bool prepare, int *blocks_per_sm);
 
 // raise the dynamic shared-memory limit of the kernels a model will launch
 // (outside any stream capture)
