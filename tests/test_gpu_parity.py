@@ -215,6 +215,11 @@ SMALL_MOE = wl.Shape(n_vocab=777, n_embd=256, n_head=4, n_kv_head=2, n_layer=2, 
                      dtype=BF16)
 SMALL_G8 = wl.Shape(n_vocab=512, n_embd=2048, n_head=16, n_kv_head=2, n_layer=1, n_ff=1024,
                     n_ctx=64, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
+# KV-head counts that do not divide the SM count: attention ranges cross heads
+SMALL_MHA32 = wl.Shape(n_vocab=1500, n_embd=2048, n_head=32, n_kv_head=32, n_layer=2, n_ff=1024,
+                       n_ctx=400, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
+SMALL_KV5 = wl.Shape(n_vocab=700, n_embd=640, n_head=10, n_kv_head=5, n_layer=2, n_ff=768,
+                     n_ctx=600, rope_theta=1e6, rms_norm_eps=1e-5, sliding_window=200, dtype=BF16)
 SMALL_HD128 = wl.Shape(n_vocab=1000, n_embd=1024, n_head=8, n_kv_head=2, n_layer=1, n_ff=2816,
                        n_ctx=300, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
 
@@ -227,6 +232,8 @@ SMALL_HD128 = wl.Shape(n_vocab=1000, n_embd=1024, n_head=8, n_kv_head=2, n_layer
     ("moe", SMALL_MOE, 9, 12),
     ("hd128", SMALL_HD128, 250, 8),
     ("hd128_gqa8", SMALL_G8, 40, 6),           # 8 query heads per KV head at head_dim 128
+    ("mha32_cross", SMALL_MHA32, 300, 6),      # 32 KV heads: CTA ranges cross head boundaries
+    ("kv5_window_cross", SMALL_KV5, 450, 6),   # 5 KV heads, window ring, crossing ranges
 ])
 def test_small_bf16_models_match_oracle(name, shape, start, steps, mode):
     seed = 77

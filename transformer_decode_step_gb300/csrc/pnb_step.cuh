@@ -350,9 +350,9 @@ __device__ __forceinline__ void prod_attn(RingP &R, const StepArgs &a, const Ste
     const int64_t seg_end = min(ar.f1, (int64_t)(g + 1) * ar.n);
     const T *kb = static_cast<const T *>(ly.kc) + (int64_t)g * a.cap * HD;
     const T *vb = static_cast<const T *>(ly.vc) + (int64_t)g * a.cap * HD;
-    for (; f < seg_end; f += a.sp) {
+    for (int np = 0; f < seg_end; f += np) {
       const int p0 = ar.lo + (int)(f - (int64_t)g * ar.n);
-      const int np = (int)min((int64_t)a.sp, seg_end - f);
+      np = (int)min((int64_t)a.sp, seg_end - f);
       if (!waited && p0 + np > pos && !R.prefetch) {
         // this slot holds the current position, written by this layer's QKV phase
         if (!wait_barriers(a, gen0, qkv_barrier)) R.ok = false;
@@ -437,8 +437,8 @@ __device__ __forceinline__ void cons_attn(RingC &R, const StepArgs &a, int pos, 
 #pragma unroll
       for (int d = 0; d < VPL; ++d) o[gh][d] = 0.f;
     }
-    for (; f < seg_end; f += a.sp) {
-      const int np = (int)min((int64_t)a.sp, seg_end - f);
+    for (int np = 0; f < seg_end; f += np) {
+      np = (int)min((int64_t)a.sp, seg_end - f);
       const uint8_t *stage = R.wait(lane);
       if (stage) {
         const T *ks = reinterpret_cast<const T *>(stage), *vs = ks + a.sp * HD;
