@@ -57,7 +57,8 @@ enum {
   PNB_E_TOKEN = -7,       /* token id outside [0, n_vocab) */
   PNB_E_DEVICE = -8,      /* a device-side check failed (see pnb_state_check) */
   PNB_E_NOMEM = -9,       /* host or device allocation failed */
-  PNB_E_WRONG_DEVICE = -10 /* current device differs from the model's */
+  PNB_E_WRONG_DEVICE = -10, /* current device differs from the model's */
+  PNB_E_TOO_LARGE = -11    /* needs more than PNB_STATIC_SCRATCH_BYTES of static scratch */
 };
 
 /* device-side error bits (pnb_state_check) */
@@ -222,6 +223,39 @@ typedef struct {
   float *x, *q, *attn, *h;
 } pnb_activations;
 int pnb_state_activations(const pnb_state *s, pnb_activations *out);
+
+/* Bytes of the device scratch array behind pnb_attention_decode_static. */
+#define PNB_STATIC_SCRATCH_BYTES (2u << 20)
+
+/* Split-KV decode attention of one layer for callers that may not allocate.
+   No counterpart in the Pantheon pages: it exists for callers that cannot
+   call cudaMalloc - code running where device allocation is forbidden after
+   start-up, frameworks whose own pool owns all device memory, or plugins that
+   only receive input and output buffers.  It allocates nothing (no
+   cudaMalloc, cudaFree or allocating library call): its scratch (per-split
+   partials, arrival counters, an I/O word) is one file-scope device array of
+   PNB_STATIC_SCRATCH_BYTES that every GPU which loads this library holds
+   until the process exits.
+     q_dev   [n_head][head_dim] fp32 queries (already rotated), 16-byte aligned
+     k_dev   one layer's K cache [n_kv_head][cap][head_dim], dtype (PNB_F32 / PNB_BF16)
+     v_dev   the same layer's V cache, same layout
+     out_dev [n_head][head_dim] fp32 output: softmax over positions
+             [max(0, pos - window + 1), pos] (all of [0, pos] when window == 0)
+             of q.k / sqrt(head_dim), applied to V; position j lives in slot j % cap
+   head_dim in {32, 64, 128}; n_head % n_kv_head == 0; pos < cap unless
+   window > 0 and cap >= window.  Returns PNB_E_TOO_LARGE when the partials
+   of even one split, or the counters, do not fit the static scratch.
+   The first call on each device looks up the array's device address with
+   that device current (cudaGetSymbolAddress); make that first call before
+   any stream capture.  Every call uses the same array and leaves its
+   contents behind: each call clears the counters and I/O word it needs, and
+   calls whose work overlaps on the GPU (concurrent streams) race on the
+   array and must be serialised by the caller.  A bounded wait that expires
+   inside the kernel is not reported by this entry point. */
+int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const void *v_dev,
+                                int32_t dtype, int32_t n_head, int32_t n_kv_head, int32_t head_dim,
+                                int32_t cap, int32_t window, int32_t pos, float *out_dev,
+                                pnb_stream stream);
 
 /* Diagnostics: have the persistent kernel record globaltimer stamps (ns) into
    trace_dev, laid out [CTA][phase][6] with CTA < number of SMs, phase < 5 *

@@ -26,7 +26,7 @@ PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT = 1, 2
  PNB_KERNEL_DOWN, PNB_KERNEL_LM_HEAD) = range(7)
 ERRORS = {0: "PNB_OK", -1: "PNB_E_INVAL", -2: "PNB_E_NULL", -3: "PNB_E_ALIGN",
           -4: "PNB_E_CTX_FULL", -5: "PNB_E_UNSUPPORTED", -6: "PNB_E_CUDA", -7: "PNB_E_TOKEN",
-          -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE"}
+          -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE", -11: "PNB_E_TOO_LARGE"}
 
 
 class pnb_config(ctypes.Structure):
@@ -68,6 +68,8 @@ _SIGS = {
     "pnb_state_activations": (_i32, [_p, _p]),
     "pnb_step_kernel": (_i32, [_p, _p, _i32, _i32, _p]),
     "pnb_state_set_trace": (_i32, [_p, _p, _sz]),
+    "pnb_attention_decode_static": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                           _p, _p]),
     "pnb_strerror": (ctypes.c_char_p, [_i32]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -77,6 +79,15 @@ for _name, (_res, _args) in _SIGS.items():
     globals()[_name] = _fn
 
 EXPORTED = tuple(_SIGS)
+
+
+def attention_decode_static(q, k, v, dtype: int, n_head: int, n_kv_head: int, head_dim: int,
+                            cap: int, window: int, pos: int, out, stream=None):
+    """One layer's decode attention with no device allocation
+    (pnb_attention_decode_static): the library's static scratch array is used."""
+    check(pnb_attention_decode_static(_ptr(q), _ptr(k), _ptr(v), dtype, n_head, n_kv_head,
+                                      head_dim, cap, window, pos, _ptr(out), _stream(stream)),
+          "pnb_attention_decode_static")
 
 
 class PnbError(RuntimeError):

@@ -442,6 +442,7 @@ const char *pnb_strerror(int code) {
     case PNB_E_DEVICE: return "device-side check failed";
     case PNB_E_NOMEM: return "allocation failed";
     case PNB_E_WRONG_DEVICE: return "current device differs from the model's device";
+    case PNB_E_TOO_LARGE: return "exceeds the static scratch of the allocation-free entry point";
     default: return "unknown error";
   }
 }
