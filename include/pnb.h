@@ -185,11 +185,12 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
    the kernels one by one (0).  Results are identical either way. */
 int pnb_model_set_graphs(pnb_model *m, int enable);
 
-/* Run each single-sequence step as one persistent cooperative kernel (the
-   default whenever the shape allows it: head_dim in {32, 64, 128}, n_head /
+/* Run each single-sequence step as one persistent cooperative kernel
+   (enable = 1; possible when head_dim is in {32, 64, 128} and n_head /
    n_kv_head in {1, 2, 4, 8} with (n_head / n_kv_head) * head_dim <= 512), or
-   as one kernel per phase (enable = 0).  Results agree to fp32 rounding.
-   Returns PNB_E_UNSUPPORTED when enabling is not possible for this model. */
+   as one kernel per phase (enable = 0, the default).  Results agree to fp32
+   rounding.  Returns PNB_E_UNSUPPORTED when enabling is not possible for this
+   model. */
 int pnb_model_set_persistent(pnb_model *m, int enable);
 int pnb_model_is_persistent(const pnb_model *m);
 

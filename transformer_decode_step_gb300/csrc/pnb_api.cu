@@ -524,7 +524,12 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   if (ok) ok = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
   if (ok) ok = prepare_gemv_kernels(c.dtype, kMaxSmem) == cudaSuccess &&
                prepare_attn_kernel(c.dtype, m->hd, m->ag) == cudaSuccess;
-  if (ok) plan_step(m);
+  // one kernel per phase is the default: on the 7B-class shapes it is the
+  // faster of the two; the persistent kernel is opt-in
+  if (ok) {
+    plan_step(m);
+    m->persistent = false;
+  }
   if (!ok) {
     pnb_model_free(m);
     return PNB_E_CUDA;
