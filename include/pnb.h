@@ -265,7 +265,13 @@ int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const voi
    phase's grid barrier (for the LM-head phase: kernel start), 2 = ns the first compute warp spent on staged GEMV slots after their data
    arrived, 3 = ns it spent waiting for ring data (accumulated: zero the buffer
    first), 4 / 5 = when its last GEMV slot loop of the phase started / ended.
-   NULL turns it off.  bytes must cover the layout. */
+   In per-phase mode the same buffer is laid out [launch][256][8]: launch =
+   6 * layer + kernel kind (PNB_KERNEL_*), 6 * n_layer for the LM head; the
+   CTA's linear index (< 256) picks the row; slots 0 = CTA start, 1 = compute
+   warps past griddepcontrol.wait, 2 = activation prologue done, 3 = first
+   ring slot arrived, 4 = all slots consumed, 5 = epilogue done, 6 / 7 = the
+   producer reached / passed griddepcontrol.wait.  NULL turns it off.  bytes
+   must cover both layouts. */
 int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes);
 
 const char *pnb_strerror(int code);

@@ -230,7 +230,7 @@ class State:
               "pnb_step_kernel")
 
     def set_trace(self, buf):
-        """Phase timestamps of the persistent kernel into `buf` (device int64 tensor) or off."""
+        """Per-CTA timestamps of the step's kernels into `buf` (device int64 tensor) or off."""
         nbytes = buf.numel() * buf.element_size() if buf is not None else 0
         check(pnb_state_set_trace(self._h, _ptr(buf), nbytes), "pnb_state_set_trace")
 

@@ -21,16 +21,27 @@ constexpr int kStageTarget = 32 * 1024;   // bytes of whole rows per GEMV ring s
 constexpr int kRingBudget = 192 * 1024;   // bytes of GEMV ring per CTA
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxBatch = 64;
+#ifndef PNB_INFLIGHT_KB
+#define PNB_INFLIGHT_KB 192
+#endif
+constexpr int kInflightBytes = PNB_INFLIGHT_KB * 1024;  // weight copies in flight per CTA
+#ifndef PNB_STATIC_PCT
+#define PNB_STATIC_PCT 100
+#endif
+constexpr int kStaticPct = PNB_STATIC_PCT;  // share of a launch's items split statically
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int grid) {
+// rows_total: rows over all segments; nseg: segments concatenated in it (0 when
+// the launch sums its segments into the same rows: static row ranges).
+Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int grid, int nseg) {
   Geom g{};
   g.K = K;
   g.es = es;
   g.row_bytes = K * es;
   int rps = 1;
   while (rps * 2 <= 64 && rps * 2 * g.row_bytes <= kStageTarget) rps *= 2;
+  rps = std::max(rps, row_align);   // row pairs never straddle two ring items
   g.rows_per_stage = rps;
   g.stage_bytes = rps * g.row_bytes;
   // warps per row: enough that a lane holds at most 4 column vectors, and no
@@ -45,10 +56,19 @@ Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int g
   const int64_t units = rows_total / row_align;
   g.rows_cta_max = ceil_div(units, grid) * row_align;
   g.nsum = nsum;
+  if (nseg > 0) {
+    const int64_t per_seg = rows_total / nseg;
+    g.n_items = nseg * ceil_div(per_seg, rps);
+    g.n_static_total = kStaticPct >= 100 ? g.n_items
+                        : (int)((int64_t)g.n_items * kStaticPct / (100 * (int64_t)grid)) * grid;
+    const int64_t pool = g.n_items - g.n_static_total;
+    g.cap_items = ceil_div(g.n_static_total, grid) + (pool > 0 ? ceil_div(2 * pool, grid) + 4 : 0);
+  }
   g.nstages = 2;
   const int fixed = smem_layout(g).total - 2 * g.stage_bytes - 2 * 16;  // everything but the ring
   const int ring = std::min(kRingBudget, kMaxSmem - fixed - 1024);
   g.nstages = std::min(8, std::max(2, ring / g.stage_bytes));
+  g.inflight = std::max(1, std::min(g.nstages, ceil_div(kInflightBytes, g.stage_bytes)));
   return g;
 }
 
@@ -94,10 +114,12 @@ struct pnb_state {
   size_t counters_off = 0, counters_bytes = 0;
   unsigned *bar_count = nullptr, *bar_gen = nullptr;
   int32_t *abort_flag = nullptr;
+  unsigned *work = nullptr;              // [launch][claim, done] item counters
   float *step_part = nullptr;            // attention partials of the persistent kernel
   float *ss_part = nullptr;              // per-CTA sums of squares [2][grid]
   StepLayer *layers = nullptr;           // device [n_layer]
   unsigned long long *trace = nullptr;   // optional phase timestamps (persistent kernel)
+  unsigned long long *ktrace = nullptr;  // optional per-CTA timestamps (per-phase kernels)
   cudaGraphExec_t exec = nullptr;
   float *g_logits = nullptr;
   int32_t *g_argmax = nullptr;
@@ -133,11 +155,11 @@ void plan(pnb_model *m) {
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, F = c.n_ff, es = m->es, grid = m->grid;
   const int k = c.expert_count > 0 ? c.expert_used : 1;
-  m->g_qkv = plan_gemv(E, es, m->qkv_rows, 2, 1, grid);
-  m->g_o = plan_gemv(c.n_head * m->hd, es, E, 1, 1, grid);
-  m->g_gateup = plan_gemv(E, es, (int64_t)k * 2 * F, 2, 1, grid);
-  m->g_down = plan_gemv(F, es, E, 1, k, grid);
-  m->g_lm = plan_gemv(E, es, c.n_vocab, 1, 1, grid);
+  m->g_qkv = plan_gemv(E, es, m->qkv_rows, 2, 1, grid, 1);
+  m->g_o = plan_gemv(c.n_head * m->hd, es, E, 1, 1, grid, 1);
+  m->g_gateup = plan_gemv(E, es, (int64_t)k * 2 * F, 2, 1, grid, k);
+  m->g_down = plan_gemv(F, es, E, 1, k, grid, c.expert_count > 0 ? 0 : 1);
+  m->g_lm = plan_gemv(E, es, c.n_vocab, 1, 1, grid, 1);
   const int G = c.n_head / c.n_kv_head;
   m->ag = attn_geom(c.dtype, m->hd, G);
   m->zgroups = G / m->ag.heads_per_cta;
@@ -207,6 +229,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
   const float eps = (float)c.rms_norm_eps;
   const bool moe = c.expert_count > 0;
   const int k = moe ? c.expert_used : 1;
+  const KTrace tr{s->ktrace, kind == PNB_KERNEL_LM_HEAD ? 6 * c.n_layer : 6 * l + kind};
+  unsigned *work = s->work + 2 * tr.phase;
   switch (kind) {
     case PNB_KERNEL_QKV: {
       QkvArgs qa{};
@@ -230,6 +254,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       qa.cap = m->cap;
       qa.window = c.sliding_window;
       qa.io = s->io;
+      qa.tr = tr;
+      qa.work = work;
       return launch_qkv(c.dtype, qa, m->grid, st, pdl);
     }
     case PNB_KERNEL_ATTN: {
@@ -249,6 +275,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       aa.stage_pos = m->ag.stage_pos;
       aa.nstages = m->ag.nstages;
       aa.io = s->io;
+      aa.tr = tr;
       return launch_attn(c.dtype, hd, aa, m->ag, st, pdl);
     }
     case PNB_KERNEL_OPROJ: {
@@ -260,6 +287,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       oa.vec = s->attn;
       oa.x = s->x;
       oa.io = s->io;
+      oa.tr = tr;
+      oa.work = work;
       return launch_resid(c.dtype, oa, m->grid, st, pdl);
     }
     case PNB_KERNEL_ROUTER: {
@@ -275,6 +304,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ra.idx = s->idx;
       ra.gate = s->gate;
       ra.io = s->io;
+      ra.tr = tr;
       return launch_router(c.dtype, ra, st, pdl);
     }
     case PNB_KERNEL_GATE_UP: {
@@ -287,6 +317,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ga.h = s->h;
       ga.n_ff = F;
       ga.io = s->io;
+      ga.tr = tr;
+      ga.work = work;
       ga.s.n = k;
       if (moe) {
         ga.s.table = m->tab_gate_up + (size_t)l * c.expert_count;
@@ -306,6 +338,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
         da.vec = s->h;
         da.x = s->x;
         da.io = s->io;
+        da.tr = tr;
+        da.work = work;
         return launch_resid(c.dtype, da, m->grid, st, pdl);
       }
       DownMoeArgs da{};
@@ -319,6 +353,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       da.gate = s->gate;
       da.x = s->x;
       da.io = s->io;
+      da.tr = tr;
       return launch_down_moe(c.dtype, da, m->grid, st, pdl);
     }
     case PNB_KERNEL_LM_HEAD: {
@@ -336,6 +371,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       la.part_idx = s->lm_idx;
       la.counter = s->lm_cnt;
       la.io = s->io;
+      la.tr = tr;
+      la.work = work;
       return launch_lmhead(c.dtype, la, m->grid, st, pdl);
     }
     default:
@@ -583,7 +620,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   const size_t o_idx = take((size_t)k * 4);
   const size_t o_lmv = take((size_t)m->grid * 4);
   const size_t o_lmi = take((size_t)m->grid * 4);
-  const size_t n_cnt = (size_t)(c.n_kv_head * m->zgroups + 1 + 3);
+  const size_t n_cnt = (size_t)(c.n_kv_head * m->zgroups + 1 + 3) + 2 * (6 * c.n_layer + 1);
   const size_t o_cnt = take(n_cnt * 4);
   const size_t o_spart = take((size_t)c.n_head * m->grid * (m->hd + 2) * 4);
   const size_t o_layers = take((size_t)c.n_layer * sizeof(StepLayer));
@@ -607,6 +644,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   s->bar_count = s->lm_cnt + 1;
   s->bar_gen = s->lm_cnt + 2;
   s->abort_flag = reinterpret_cast<int32_t *>(s->lm_cnt + 3);
+  s->work = s->lm_cnt + 4;
   s->counters_off = o_cnt;
   s->counters_bytes = n_cnt * 4;
   s->step_part = reinterpret_cast<float *>(s->ws + o_spart);
@@ -791,11 +829,14 @@ int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb
 int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes) {
   if (!s) return PNB_E_NULL;
   if (trace_dev) {
-    const size_t need = (size_t)s->m->grid * (5 * s->m->cfg.n_layer + 1) * 6 * 8;
+    const int L = s->m->cfg.n_layer;
+    const size_t need = std::max((size_t)s->m->grid * (5 * L + 1) * 6 * 8,
+                                 (size_t)(6 * L + 1) * kTraceCtas * 8 * 8);
     if (bytes < need) return PNB_E_INVAL;
     if (reinterpret_cast<uintptr_t>(trace_dev) & 7u) return PNB_E_ALIGN;
   }
   s->trace = reinterpret_cast<unsigned long long *>(trace_dev);
+  s->ktrace = s->trace;
   if (s->exec) {   // the captured graph holds the old argument
     cudaGraphExecDestroy(s->exec);
     s->exec = nullptr;

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  if (tid == 0) ktrace(a.tr, 0);
 
   if (warp == kAttnWarps) {
     if (lane == 0) {
@@ -117,8 +118,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
         const int a0 = c0 + st * SP, np = min(SP, npos - st * SP);
         const int slot = st % NS, round = st / NS;
         if (!waited && (a0 + np > pos || st == NS)) {
+          ktrace(a.tr, 6);
           pdl_wait();
           pdl_trigger();
+          ktrace(a.tr, 7);
           waited = true;
         }
         if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1)) {
@@ -148,6 +151,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
 
   // ------------------------------------------------------------ consumers
   pdl_wait();
+  if (tid == 0) ktrace(a.tr, 1);
   const int sub = lane & 7, t = lane >> 3;
   const int rot = sub / ROTDIV;
   float qr[GB][C][EPU];
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
       for (int e = 0; e < EPU; ++e)
         qr[gh][c][e] = a.q[(int64_t)(h0 + gh) * HD + sub * DPL + u * EPU + e] * a.qscale;
     }
+  if (tid == 0) ktrace(a.tr, 2);
   float m[GB], l[GB], o[GB][VPL];
 #pragma unroll
   for (int gh = 0; gh < GB; ++gh) {
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
       ok = false;
       if (lane == 0) set_error(&a.io->error, kErrTimeout);
     }
+    if (st == 0 && tid == 0) ktrace(a.tr, 3);
     if (!ok) continue;
     const T *ks = ring + (size_t)slot * 2 * SP * HD, *vs = ks + SP * HD;
     const int np = min(SP, npos - st * SP);
@@ -250,6 +256,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
     if (lane == 0) mbar_arrive(&empty[slot]);
   }
 
+  if (tid == 0) ktrace(a.tr, 4);
   // merge the eight warps of this CTA
 #pragma unroll
   for (int gh = 0; gh < GB; ++gh) {
@@ -321,6 +328,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
     }
     if (tid == 0) a.counter[g * gridDim.z + z] = 0u;
   }
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 template <typename T, int HD, int GB>

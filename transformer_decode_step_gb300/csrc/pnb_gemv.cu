@@ -23,16 +23,32 @@ namespace {
 #define GEMV_ROLES(ARGS, SUMMED, PREFETCH, ROWS)                                   \
   const Ctx c = gemv_setup(ARGS.g, ROWS);                                          \
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x; \
+  if (tid == 0) ktrace(ARGS.tr, 0);                                                \
   if (warp == kGemvWarps) {                                                        \
-    if (lane == 0) produce(ARGS.g, ARGS.s, SUMMED, PREFETCH, c, &ARGS.io->error);  \
+    if (lane == 0) produce(ARGS.g, ARGS.s, SUMMED, PREFETCH, c, &ARGS.io->error, ARGS.tr); \
+    return;                                                                        \
+  }
+
+// dynamically claimed row chunks (every launch but the summed MoE down projection)
+#define GEMV_ROLES_DYN(ARGS, PREFETCH)                                             \
+  const Ctx c = gemv_setup(ARGS.g, 0);                                             \
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x; \
+  if (tid == 0) ktrace(ARGS.tr, 0);                                                \
+  if (warp == kGemvWarps) {                                                        \
+    if (lane == 0) produce_dyn(ARGS.g, ARGS.s, PREFETCH, c, ARGS.work, &ARGS.io->error, ARGS.tr); \
     return;                                                                        \
   }
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
-  GEMV_ROLES(a, false, true, a.s.rows * a.s.n)
-  pdl_wait();
+  GEMV_ROLES_DYN(a, true)
   XSlice<T, NV> xs;
+  load_weight_slice(xs, a.norm_w, a.g, warp, lane);
+  const int hd = a.head_dim;
+  const double inv_freq = tid < hd / 2 ? a.inv_freq[tid] : 0.0;
+  pdl_wait();
+  if (tid == 0) ktrace(a.tr, 1);
+  const int pos = a.io->pos;
   if (a.emb) {
     int tok = a.io->token;
     if (tok < 0 || tok >= a.n_vocab) {
@@ -40,29 +56,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
       tok = 0;
     }
     const T *row = static_cast<const T *>(a.emb) + (int64_t)tok * a.g.K;
-    const float inv = rms_inv(row, a.g.K, a.eps, c.red, tid);
     if (blockIdx.x == 0)
       for (int i = tid * 2; i < a.g.K; i += kGemvConsumers * 2)
         *reinterpret_cast<float2 *>(a.x_out + i) = load2(row, i);
-    load_slice(xs, row, inv, a.norm_w, a.g, warp, lane);
+    norm_slice(xs, row, a.g.K, a.eps, a.g, c.red, warp, lane);
   } else {
-    const float inv = rms_inv(a.x, a.g.K, a.eps, c.red, tid);
-    load_slice(xs, a.x, inv, a.norm_w, a.g, warp, lane);
+    norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
   }
-  consume<T, NV>(a.g, a.s, false, c, xs, warp, lane, &a.io->error, [](int) {});
+  if (tid == 0) ktrace(a.tr, 2);
+  // RoPE angles of this position, one per dimension pair
+  if (tid < hd / 2) {
+    float sn, cs;
+    rope_sincos(pos, inv_freq, &sn, &cs);
+    c.rope[tid] = make_float2(cs, sn);
+  }
+  consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
+  if (tid == 0) ktrace(a.tr, 4);
 
-  const int pos = a.io->pos;
   const int slot = pos % a.cap;
-  const int hd = a.head_dim;
   const int qrows = a.n_head * hd, krows = a.n_kv * hd;
-  for (int64_t r = c.r0 + 2 * tid; r < c.r1; r += 2 * kGemvConsumers) {
-    const int loc = (int)(r - c.r0), rr = (int)r;
-    float v0 = row_total(c.part, loc, a.g.cw), v1 = row_total(c.part, loc + 1, a.g.cw);
+  for_claimed_rows(a.g, c, a.s.rows, true, tid, [&](int k, int r, int, int64_t row) {
+    const int rr = (int)row;
+    float v0 = item_row_total(a.g, c, k, r), v1 = item_row_total(a.g, c, k, r + 1);
     if (rr < qrows + krows) {
-      float sn, cs;
-      rope_sincos(pos, a.inv_freq[(rr % hd) >> 1], &sn, &cs);
-      const float t0 = v0 * cs - v1 * sn, t1 = v0 * sn + v1 * cs;
+      const float2 cs = c.rope[(rr % hd) >> 1];
+      const float t0 = v0 * cs.x - v1 * cs.y, t1 = v0 * cs.y + v1 * cs.x;
       v0 = t0;
       v1 = t1;
     }
@@ -71,55 +90,65 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
       a.q[rr + 1] = v1;
     } else {
       const bool is_k = rr < qrows + krows;
-      const int k = rr - qrows - (is_k ? 0 : krows);
-      const int gk = k / hd, d = k - gk * hd;
+      const int kx = rr - qrows - (is_k ? 0 : krows);
+      const int gk = kx / hd, d = kx - gk * hd;
       T *dst = static_cast<T *>(is_k ? a.k_cache : a.v_cache) + ((int64_t)gk * a.cap + slot) * hd + d;
       Elem<T>::store(dst, 0, v0);
       Elem<T>::store(dst, 1, v1);
     }
-  }
+  });
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_resid(const ResidArgs a) {
-  GEMV_ROLES(a, false, true, a.s.rows * a.s.n)
+  GEMV_ROLES_DYN(a, true)
   pdl_wait();
+  if (tid == 0) ktrace(a.tr, 1);
   XSlice<T, NV> xs;
   load_slice(xs, a.vec, 1.0f, nullptr, a.g, warp, lane);
-  consume<T, NV>(a.g, a.s, false, c, xs, warp, lane, &a.io->error, [](int) {});
+  if (tid == 0) ktrace(a.tr, 2);
+  consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
-  for (int64_t r = c.r0 + tid; r < c.r1; r += kGemvConsumers)
-    a.x[r] += row_total(c.part, (int)(r - c.r0), a.g.cw);
+  if (tid == 0) ktrace(a.tr, 4);
+  for_claimed_rows(a.g, c, a.s.rows, false, tid, [&](int k, int r, int, int64_t row) {
+    a.x[row] += item_row_total(a.g, c, k, r);
+  });
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup(const GateUpArgs a) {
-  GEMV_ROLES(a, false, a.s.table == nullptr, a.s.rows * a.s.n)
-  pdl_wait();
+  GEMV_ROLES_DYN(a, a.s.table == nullptr)
   XSlice<T, NV> xs;
-  const float inv = rms_inv(a.x, a.g.K, a.eps, c.red, tid);
-  load_slice(xs, a.x, inv, a.norm_w, a.g, warp, lane);
-  consume<T, NV>(a.g, a.s, false, c, xs, warp, lane, &a.io->error, [](int) {});
+  load_weight_slice(xs, a.norm_w, a.g, warp, lane);
+  pdl_wait();
+  if (tid == 0) ktrace(a.tr, 1);
+  norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
+  if (tid == 0) ktrace(a.tr, 2);
+  consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
-  for (int64_t r = c.r0 + 2 * tid; r < c.r1; r += 2 * kGemvConsumers) {
-    const int loc = (int)(r - c.r0);
-    const int seg = (int)(r / a.s.rows);
-    const int i = (int)((r - seg * a.s.rows) >> 1);
-    const float gte = row_total(c.part, loc, a.g.cw), up = row_total(c.part, loc + 1, a.g.cw);
-    a.h[(int64_t)seg * a.n_ff + i] = silu(gte) * up;
-  }
+  if (tid == 0) ktrace(a.tr, 4);
+  for_claimed_rows(a.g, c, a.s.rows, true, tid, [&](int k, int r, int seg, int64_t row) {
+    const float gte = item_row_total(a.g, c, k, r), up = item_row_total(a.g, c, k, r + 1);
+    a.h[(int64_t)seg * a.n_ff + (row >> 1)] = silu(gte) * up;
+  });
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_down_moe(const DownMoeArgs a) {
   GEMV_ROLES(a, true, false, a.s.rows)
   pdl_wait();
+  if (tid == 0) ktrace(a.tr, 1);
   XSlice<T, NV> xs;
   load_slice(xs, a.h, 1.0f, nullptr, a.g, warp, lane);
-  consume<T, NV>(a.g, a.s, true, c, xs, warp, lane, &a.io->error, [&](int seg) {
+  if (tid == 0) ktrace(a.tr, 2);
+  consume<T, NV>(a.g, a.s, true, c, xs, warp, lane, &a.io->error, a.tr, [&](int seg) {
     load_slice(xs, a.h + (int64_t)seg * a.n_ff, 1.0f, nullptr, a.g, warp, lane);
   });
   gemv_sync();
+  if (tid == 0) ktrace(a.tr, 4);
   for (int64_t r = c.r0 + tid; r < c.r1; r += kGemvConsumers) {
     float acc = 0.f;
     for (int s = 0; s < a.s.n; ++s)
@@ -127,24 +156,28 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_moe(const DownMoeArgs 
                  acc);
     a.x[r] += acc;
   }
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 template <typename T, int NV>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_lmhead(const LmArgs a) {
-  GEMV_ROLES(a, false, true, a.s.rows)
-  pdl_wait();
+  GEMV_ROLES_DYN(a, true)
   XSlice<T, NV> xs;
-  const float inv = rms_inv(a.x, a.g.K, a.eps, c.red, tid);
-  load_slice(xs, a.x, inv, a.norm_w, a.g, warp, lane);
-  consume<T, NV>(a.g, a.s, false, c, xs, warp, lane, &a.io->error, [](int) {});
+  load_weight_slice(xs, a.norm_w, a.g, warp, lane);
+  pdl_wait();
+  if (tid == 0) ktrace(a.tr, 1);
+  norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
+  if (tid == 0) ktrace(a.tr, 2);
+  consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
+  if (tid == 0) ktrace(a.tr, 4);
   float best = -FLT_MAX;
   int bi = INT_MAX;
-  for (int64_t r = c.r0 + tid; r < c.r1; r += kGemvConsumers) {
-    const float v = row_total(c.part, (int)(r - c.r0), a.g.cw);
-    if (a.logits) a.logits[r] = v;
-    argmax_merge(best, bi, v, (int)r);
-  }
+  for_claimed_rows(a.g, c, a.s.rows, false, tid, [&](int k, int r, int, int64_t row) {
+    const float v = item_row_total(a.g, c, k, r);
+    if (a.logits) a.logits[row] = v;
+    argmax_merge(best, bi, v, (int)row);
+  });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
     argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
@@ -196,6 +229,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_lmhead(const LmArgs a) {
       *a.counter = 0u;
     }
   }
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 // Router: one CTA of 256 threads.  r = Wr RMSNorm(x); the k largest (lower

@@ -83,6 +83,8 @@ struct RingPos {
 struct Ctx {
   uint8_t *ring;
   float *part, *red;
+  float2 *rope;
+  int *info, *items;
   uint64_t *full, *empty;
   int64_t r0, r1;
 };
@@ -94,6 +96,9 @@ __device__ __forceinline__ Ctx gemv_setup(const Geom &g, int64_t total_rows) {
   c.ring = g_smem + L.ring;
   c.part = reinterpret_cast<float *>(g_smem + L.part);
   c.red = reinterpret_cast<float *>(g_smem + L.red);
+  c.info = reinterpret_cast<int *>(g_smem + L.info);
+  c.items = reinterpret_cast<int *>(g_smem + L.items);
+  c.rope = reinterpret_cast<float2 *>(g_smem + L.rope);
   c.full = reinterpret_cast<uint64_t *>(g_smem + L.bars);
   c.empty = c.full + g.nstages;
   const int64_t units = total_rows / g.row_align;
@@ -110,11 +115,21 @@ __device__ __forceinline__ Ctx gemv_setup(const Geom &g, int64_t total_rows) {
   return c;
 }
 
+// Before issuing copy i, wait until copy i - inflight has landed: a producer
+// keeps only what saturates its share of HBM in flight, so that the
+// activation loads of this and the neighbouring kernels do not queue behind a
+// whole ring of weight requests.
+__device__ __forceinline__ bool inflight_wait(const Geom &g, const Ctx &c, uint32_t i) {
+  if (i < (uint32_t)g.inflight) return true;
+  const uint32_t j = i - (uint32_t)g.inflight;
+  return mbar_wait(&c.full[j % (uint32_t)g.nstages], (j / (uint32_t)g.nstages) & 1u);
+}
+
 // Producer: stream the CTA's rows.  With `prefetch`, the first ring's worth is
 // issued before griddepcontrol.wait (weights do not depend on earlier kernels).
 // Always ends by waiting (bounded) for its last copies to land.
 __device__ __forceinline__ void produce(const Geom &g, const Segs &s, bool summed, bool prefetch, const Ctx &c,
-                        int32_t *err) {
+                        int32_t *err, const KTrace &tr) {
   bool waited = false;
   if (!prefetch) {
     pdl_wait();
@@ -130,11 +145,14 @@ __device__ __forceinline__ void produce(const Geom &g, const Segs &s, bool summe
   bool ok = true;
   while (it.next(item)) {
     if (!waited && i == (uint32_t)g.nstages) {
+      ktrace(tr, 6);
       pdl_wait();
       pdl_trigger();
+      ktrace(tr, 7);
       waited = true;
     }
-    if (i >= (uint32_t)g.nstages && !mbar_wait(&c.empty[rp.slot], rp.phase ^ 1u)) {
+    if (!inflight_wait(g, c, i) ||
+        (i >= (uint32_t)g.nstages && !mbar_wait(&c.empty[rp.slot], rp.phase ^ 1u))) {
       ok = false;
       break;
     }
@@ -147,8 +165,10 @@ __device__ __forceinline__ void produce(const Geom &g, const Segs &s, bool summe
     rp.advance();
   }
   if (!waited) {
+    ktrace(tr, 6);
     pdl_wait();
     pdl_trigger();
+    ktrace(tr, 7);
   }
   if (!ok) set_error(err, kErrTimeout);
   // wait for the copies still in flight: the last min(i, nstages) items
@@ -162,6 +182,155 @@ __device__ __forceinline__ void produce(const Geom &g, const Segs &s, bool summe
     --dp.slot;
     if (!mbar_wait(&c.full[dp.slot], dp.phase)) set_error(err, kErrTimeout);
   }
+}
+
+// ------------------------------------------------------- dynamic claiming
+//
+// Ring items (rows_per_stage rows of one segment) are numbered over all
+// segments.  The first n_static_total items are split evenly over the CTAs
+// and streamed first; the rest (when there are any) are claimed one at a time
+// from the launch's work[0] counter (four claims in flight, issued while the
+// static share streams), so CTAs that started late or stream slowly take
+// fewer.  A CTA takes at most cap_items.  The slot info tells consumers the
+// item's row count and CTA-local index; a row count of -1 ends the stream.  Once its claims
+// have returned, each CTA counts itself in work[1]; the last one puts both
+// counters back to zero for the next launch.
+
+__device__ __forceinline__ void item_rows(const Geom &g, int64_t rows, int item, int &seg,
+                                          int64_t &row0, int &n) {
+  const int ips = (int)((rows + g.rows_per_stage - 1) / g.rows_per_stage);
+  seg = item / ips;
+  row0 = (int64_t)(item - seg * ips) * g.rows_per_stage;
+  n = (int)((int64_t)g.rows_per_stage < rows - row0 ? (int64_t)g.rows_per_stage : rows - row0);
+}
+
+__device__ __forceinline__ void finish_claims(unsigned *work) {
+  __threadfence();
+  const unsigned prev = atomicAdd(work + 1, 1u);
+  if (prev == gridDim.x - 1) {
+    __threadfence();
+    atomicExch(work, 0u);
+    atomicExch(work + 1, 0u);
+  }
+}
+
+__device__ __forceinline__ void produce_dyn(const Geom &g, const Segs &s, bool prefetch, const Ctx &c,
+                                            unsigned *work, int32_t *err, const KTrace &tr) {
+  constexpr int D = 4;
+  bool waited = false;
+  if (!prefetch) {
+    pdl_wait();
+    pdl_trigger();
+    waited = true;
+  }
+  const void *w[kMaxSegments];
+  for (int i = 0; i < s.n; ++i) w[i] = s.table ? s.table[s.expert_idx[i]] : s.w[i];
+  const int cap = g.cap_items;
+  // static share: a balanced split of the static items; the rest are claimed
+  const unsigned base = g.n_static_total;                           // first claimed item
+  const unsigned pool = (unsigned)g.n_items - base;                 // claimable items
+  const int s0 = (int)((int64_t)base * blockIdx.x / gridDim.x);
+  const int n_own = (int)((int64_t)base * (blockIdx.x + 1) / gridDim.x) - s0;
+  int k = 0;                 // items taken
+  uint32_t i = 0;            // copies issued
+  RingPos rp{0u, 0u, (uint32_t)g.nstages};
+  bool ok = true;
+  // one item: wait for room, publish the slot info, issue the copy
+  auto issue = [&](int item) {
+    if (!waited && i == (uint32_t)g.nstages) {
+      ktrace(tr, 6);
+      pdl_wait();
+      pdl_trigger();
+      ktrace(tr, 7);
+      waited = true;
+    }
+    if (!inflight_wait(g, c, i) ||
+        (i >= (uint32_t)g.nstages && !mbar_wait(&c.empty[rp.slot], rp.phase ^ 1u))) {
+      ok = false;
+      return;
+    }
+    int seg, n;
+    int64_t row0;
+    item_rows(g, s.rows, item, seg, row0, n);
+    c.info[2 * rp.slot] = n;
+    c.info[2 * rp.slot + 1] = k;
+    c.items[k] = item;
+    ++k;
+    const uint32_t bytes = (uint32_t)n * (uint32_t)g.row_bytes;
+    mbar_arrive_expect_tx(&c.full[rp.slot], bytes);
+    bulk_g2s(c.ring + rp.slot * (uint32_t)g.stage_bytes,
+             static_cast<const uint8_t *>(w[seg]) + row0 * g.row_bytes, bytes, &c.full[rp.slot]);
+    ++i;
+    rp.advance();
+  };
+  // claims for the shared tail go out first; their results are needed only
+  // once the static share has been issued.  pending counts claims whose
+  // items would still fit under the cap.
+  unsigned q[D];
+  int pending = 0;
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    if (pool > 0 && n_own + pending < cap) {
+      q[d] = atomicAdd(work, 1u);
+      ++pending;
+    } else {
+      q[d] = pool;
+    }
+  }
+  for (int j = 0; j < n_own && ok; ++j) issue(s0 + j);
+  bool more = ok && pool > 0;
+  while (more) {
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (!more) continue;
+      if (q[d] >= pool || !ok) {   // claims return in order: every later one fails too
+        more = false;
+        continue;
+      }
+      issue((int)(base + q[d]));
+      --pending;
+      if (ok && k + pending + 1 <= cap) {
+        q[d] = atomicAdd(work, 1u);
+        ++pending;
+      } else {
+        q[d] = pool;
+      }
+    }
+  }
+  if (!waited) {
+    ktrace(tr, 6);
+    pdl_wait();
+    pdl_trigger();
+    ktrace(tr, 7);
+  }
+  // end of stream, as soon as the last item is out: the end slot's previous
+  // copy has landed once the consumers have released it
+  if (ok && i >= (uint32_t)g.nstages && !mbar_wait(&c.empty[rp.slot], rp.phase ^ 1u)) ok = false;
+  if (ok) {
+    c.items[cap] = k;
+    c.info[2 * rp.slot] = -1;
+    mbar_arrive(&c.full[rp.slot]);
+  }
+  // wait for the other copies still in flight (the CTA must not end before
+  // they land, should its consumers give up early)
+  const uint32_t last = i < (uint32_t)g.nstages - 1u ? i : (uint32_t)g.nstages - 1u;
+  RingPos dp = rp;
+  for (uint32_t j = 0; j < last; ++j) {
+    if (dp.slot == 0) {
+      dp.slot = dp.n;
+      dp.phase ^= 1u;
+    }
+    --dp.slot;
+    if (!mbar_wait(&c.full[dp.slot], dp.phase)) ok = false;
+  }
+  if (!ok) set_error(err, kErrTimeout);
+  // every claim has returned (the comparison waits for the values): count this
+  // CTA out of the launch's claiming
+  unsigned all = 0xffffffffu;
+#pragma unroll
+  for (int d = 0; d < D; ++d) all &= q[d];
+  if (all == 0xfffffffeu) set_error(err, kErrTimeout);
+  if (pool > 0) finish_claims(work);
 }
 
 // ------------------------------------------------------- activation slices
@@ -291,7 +460,8 @@ __device__ __forceinline__ float dot_row(const uint8_t *row, const XSlice<T, NV>
 // wait that expires sets the error bit and the warp stops consuming.
 template <typename T, int NV, typename Reload>
 __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summed, const Ctx &c,
-                        XSlice<T, NV> &xs, int warp, int lane, int32_t *err, Reload &&reload) {
+                        XSlice<T, NV> &xs, int warp, int lane, int32_t *err, const KTrace &tr,
+                        Reload &&reload) {
   const int cw = g.cw, groups = kGemvWarps / cw;
   const int grp = warp / cw, cc = warp - grp * cw;
   const int vpr = g.row_bytes / 16;
@@ -310,6 +480,7 @@ __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summe
       ok = false;
       if (lane == 0) set_error(err, kErrTimeout);
     }
+    if (tr.p && warp == 0 && lane == 0 && item.local == 0 && item.seg == 0) ktrace(tr, 3);
     if (ok) {
       const uint8_t *stage = c.ring + slot * (uint32_t)g.stage_bytes;
       float *part = c.part + ((summed ? item.seg : 0) * g.rows_cta_max + item.local) * cw;
@@ -322,6 +493,122 @@ __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summe
     }
     rp.advance();
   }
+}
+
+// Consumer loop of a dynamically claimed stream: the rows of the CTA's k-th
+// item leave their partial sums in part[(k * rows_per_stage + r) * cw + warp
+// column].  Ends at the end-of-stream slot (or a wait that expires).
+template <typename T, int NV>
+__device__ __forceinline__ void consume_dyn(const Geom &g, const Ctx &c, const XSlice<T, NV> &xs,
+                                            int warp, int lane, int32_t *err, const KTrace &tr) {
+  const int cw = g.cw, groups = kGemvWarps / cw;
+  const int grp = warp / cw, cc = warp - grp * cw;
+  const int vpr = g.row_bytes / 16;
+  RingPos rp{0u, 0u, (uint32_t)g.nstages};
+  bool first = true;
+  for (;;) {
+    const uint32_t slot = rp.slot;
+    if (!mbar_wait(&c.full[slot], rp.phase)) {
+      if (lane == 0) set_error(err, kErrTimeout);
+      return;
+    }
+    if (first && warp == 0 && lane == 0) ktrace(tr, 3);
+    first = false;
+    const int2 inf = *reinterpret_cast<const int2 *>(c.info + 2 * slot);
+    const int n = inf.x, kk = inf.y;
+    if (n < 0) return;
+    const uint8_t *stage = c.ring + slot * (uint32_t)g.stage_bytes;
+    float *part = c.part + (size_t)kk * g.rows_per_stage * cw;
+    for (int r = grp; r < n; r += groups) {
+      const float v = warp_sum(dot_row<T, NV>(stage + (size_t)r * g.row_bytes, xs, vpr, cc, cw, lane));
+      if (lane == 0) part[r * cw + cc] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.empty[slot]);
+    rp.advance();
+  }
+}
+
+// Rows the CTA took, for the fused epilogues: f(k, r, seg, row) for row r of
+// its k-th item (row = the row inside segment seg), spread over the consumer
+// threads; with `pairs`, only even r (the pair's first row).
+template <typename F>
+__device__ __forceinline__ void for_claimed_rows(const Geom &g, const Ctx &c, int64_t rows, bool pairs,
+                                                 int tid, F &&f) {
+  const int k = c.items[g.cap_items];
+  const int rps = g.rows_per_stage, step = pairs ? 2 : 1;
+  const int per = rps / step;
+  for (int idx = tid; idx < k * per; idx += kGemvConsumers) {
+    const int j = idx / per, r = (idx - j * per) * step;
+    int seg, n;
+    int64_t row0;
+    item_rows(g, rows, c.items[j], seg, row0, n);
+    if (r < n) f(j, r, seg, row0 + r);
+  }
+}
+
+__device__ __forceinline__ float item_row_total(const Geom &g, const Ctx &c, int k, int r) {
+  const float *p = c.part + ((size_t)k * g.rows_per_stage + r) * g.cw;
+  float v = 0.f;
+  for (int w = 0; w < g.cw; ++w) v += p[w];
+  return v;
+}
+
+// The multiplier slice of an RMSNorm weight (1 without one): weights do not
+// depend on earlier kernels, so this is loaded before griddepcontrol.wait.
+template <typename T, int NV>
+__device__ __forceinline__ void load_weight_slice(XSlice<T, NV> &ws, const float *w, const Geom &g,
+                                                  int warp, int lane) {
+  constexpr int P = Vec<T>::N / 2;
+  const int vpr = g.row_bytes / 16, c = warp % g.cw;
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const int v = c * 32 + lane + t * 32 * g.cw;
+    const int vc = v < vpr ? v : 0;
+#pragma unroll
+    for (int e = 0; e < P; ++e) ws.p[t][e] = w ? load2(w, vc * Vec<T>::N + 2 * e) : make_float2(1.f, 1.f);
+  }
+}
+
+// xs = RMSNorm(src) * (multiplier already in xs), columns of this lane only,
+// with one round trip to memory: the sum of squares comes from the slices of
+// the first cw warps, which together hold every element once (every row group
+// holds the same columns, so all threads get the same fixed-order total).
+template <typename T, int NV, typename S>
+__device__ __forceinline__ void norm_slice(XSlice<T, NV> &xs, const S *src, int E, float eps,
+                                           const Geom &g, float *red, int warp, int lane) {
+  constexpr int P = Vec<T>::N / 2;
+  const int vpr = g.row_bytes / 16, c = warp % g.cw;
+  float2 xv[NV][P];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const int v = c * 32 + lane + t * 32 * g.cw;
+    const int vc = v < vpr ? v : 0;
+#pragma unroll
+    for (int e = 0; e < P; ++e) xv[t][e] = load2(src, vc * Vec<T>::N + 2 * e);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const bool valid = c * 32 + lane + t * 32 * g.cw < vpr;
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      if (!valid) xv[t][e] = make_float2(0.f, 0.f);
+      ss = fmaf(xv[t][e].x, xv[t][e].x, ss);
+      ss = fmaf(xv[t][e].y, xv[t][e].y, ss);
+    }
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  gemv_sync();
+  float tot = 0.f;
+  for (int w = 0; w < g.cw; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)E + eps);
+#pragma unroll
+  for (int t = 0; t < NV; ++t)
+#pragma unroll
+    for (int e = 0; e < P; ++e)
+      xs.p[t][e] = make_float2(xv[t][e].x * inv * xs.p[t][e].x, xv[t][e].y * inv * xs.p[t][e].y);
 }
 
 __device__ __forceinline__ float row_total(const float *part, int local, int cw) {

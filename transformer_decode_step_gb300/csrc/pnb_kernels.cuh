@@ -29,8 +29,12 @@ struct Geom {
   int cw;             // warps sharing one row (its columns); 16 / cw rows in flight
   int nv;             // 16-byte vectors per lane per row (1, 2 or 4)
   int row_align;      // CTA row ranges are multiples of this
-  int rows_cta_max;   // most rows any CTA owns
+  int rows_cta_max;   // most rows any CTA owns (static row ranges)
   int nsum;           // matrices summed into the same rows (1 = concatenated rows)
+  int n_items;        // ring items over all segments (dynamic claiming)
+  int n_static_total; // items split evenly over the CTAs; the rest are claimed
+  int cap_items;      // most items one CTA may take; 0 = static row ranges
+  int inflight;       // bulk copies a producer keeps in flight at most
 };
 
 // The matrices of one launch.  Rows of segment i are virtual rows
@@ -46,7 +50,7 @@ struct Segs {
 };
 
 struct SmemLayout {
-  int ring, part, red, bars, total;
+  int ring, part, red, info, items, rope, bars, total;
 };
 
 __host__ __device__ inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -55,10 +59,31 @@ __host__ __device__ inline SmemLayout smem_layout(const Geom &g) {
   SmemLayout L;
   L.ring = 0;
   L.part = align_up(g.nstages * g.stage_bytes, 128);
-  L.red = align_up(L.part + g.rows_cta_max * g.cw * g.nsum * 4, 16);
-  L.bars = align_up(L.red + 64 * 4, 16);
+  const int part_rows = g.cap_items > 0 ? g.cap_items * g.rows_per_stage : g.rows_cta_max;
+  L.red = align_up(L.part + part_rows * g.cw * g.nsum * 4, 16);
+  // per ring slot: claimed item and its CTA-local index; then the CTA's
+  // claimed items and their count
+  L.info = align_up(L.red + 64 * 4, 16);
+  L.items = L.info + 2 * g.nstages * 4;
+  L.rope = align_up(L.items + (g.cap_items + 1) * 4, 16);   // 64 (cos, sin) pairs
+  L.bars = L.rope + 64 * 8;
   L.total = L.bars + 2 * g.nstages * 8;
   return L;
+}
+
+// Optional per-CTA timestamps of the per-phase kernels (diagnostics): slot
+// k of CTA c in launch `phase` is p[(phase * kTraceCtas + c) * 8 + k].
+constexpr int kTraceCtas = 256;
+struct KTrace {
+  unsigned long long *p;
+  int phase;
+};
+
+__device__ __forceinline__ void ktrace(const KTrace &t, int k) {
+  if (t.p) {
+    const unsigned c = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (c < (unsigned)kTraceCtas) t.p[((size_t)t.phase * kTraceCtas + c) * 8 + k] = global_ns();
+  }
 }
 
 // ---------------------------------------------------------------- kernels
@@ -79,7 +104,9 @@ struct QkvArgs {
   float *q;
   void *k_cache, *v_cache; // this layer's [n_kv][cap][head_dim]
   int cap, window;
+  unsigned *work;      // [claim, done] item counters of this launch, zero between launches
   StepIO *io;
+  KTrace tr;
 };
 
 // x[r] += (W v)[r]  (output projection, dense down projection)
@@ -88,7 +115,9 @@ struct ResidArgs {
   Segs s;
   const float *vec;
   float *x;
+  unsigned *work;      // [claim, done] item counters of this launch, zero between launches
   StepIO *io;
+  KTrace tr;
 };
 
 // h[s][i] = silu((Wg xn)_i) * (Wu xn)_i with xn = RMSNorm(x); rows of W are
@@ -101,7 +130,9 @@ struct GateUpArgs {
   float eps;
   float *h;  // [nseg][n_ff]
   int n_ff;
+  unsigned *work;      // [claim, done] item counters of this launch, zero between launches
   StepIO *io;
+  KTrace tr;
 };
 
 // x[r] += sum_s gate[s] * (W_s h_s)[r]  (MoE down projections, summed)
@@ -113,6 +144,7 @@ struct DownMoeArgs {
   const float *gate;
   float *x;
   StepIO *io;
+  KTrace tr;
 };
 
 // logits = W RMSNorm(x); greedy token; pos += 1
@@ -127,7 +159,9 @@ struct LmArgs {
   float *part_val;     // [gridDim.x]
   int32_t *part_idx;   // [gridDim.x]
   unsigned int *counter;
+  unsigned *work;      // [claim, done] item counters of this launch, zero between launches
   StepIO *io;
+  KTrace tr;
 };
 
 // router logits, top-k, softmax over the chosen logits
@@ -140,6 +174,7 @@ struct RouterArgs {
   int32_t *idx;
   float *gate;
   StepIO *io;
+  KTrace tr;
 };
 
 // split-KV decode attention of the token at io->pos (grid: n_split x n_kv x zgroups)
@@ -156,6 +191,7 @@ struct AttnArgs {
   int stage_pos;         // positions per ring slot
   int nstages;           // ring slots
   StepIO *io;
+  KTrace tr;
 };
 
 struct AttnGeom {
