@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s and achieved HBM GB/s per step vs ~8 TB/s peak, 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["transformer_decode_step_gb300/csrc/pnb_gemv.cu",
+                  "transformer_decode_step_gb300/csrc/pnb_gemv_dev.cuh",
                   "transformer_decode_step_gb300/csrc/pnb_device.cuh",
                   "transformer_decode_step_gb300/csrc/pnb_kernels.cuh"]
 
