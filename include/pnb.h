@@ -172,12 +172,22 @@ int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, fl
                 int32_t *argmax_dev);
 
 /* One decode step of B sequences together (pn_llama_forward_batch, "Engine
-   Architecture", section "Continuous-Batch VLM Decoder"); slot b reads
-   tokens_dev[b] (or, when tokens_dev is NULL, its own previous argmax) and
-   its own state's KV cache and pos.  Results equal B single-sequence steps up
-   to fp32 summation order.  logits_dev: [B][n_vocab] or NULL; argmax_dev: [B]
-   or NULL.  Distinct states only; 1 <= B <= 64.  MoE models return
-   PNB_E_UNSUPPORTED (as the pages' batched decoder returns -1 for MoE). */
+   Architecture", section "Vision-Language and Bulk OCR": one batched decode
+   over all active slots; "Serve Layer Architecture", section "Batched
+   Decode").  states: host array of B distinct states of this model; slot b
+   reads tokens_dev[b] (device int32, or, when tokens_dev is NULL, its own
+   previous argmax) and its own state's KV cache and pos, and advances that
+   pos by one.  logits_dev: [B][n_vocab] fp32 or NULL; argmax_dev: [B] int32
+   or NULL.  1 <= B <= 64.  Every weight is read once per step for all slots:
+   the projections run on tcgen05 tensor cores with each activation split into
+   a bf16 high and low part, so results equal B single-sequence steps to about
+   1e-5 relative (not bitwise).  Supported: bf16 dense models with n_embd,
+   n_head * head_dim and n_ff multiples of 64; MoE and fp32 models return
+   PNB_E_UNSUPPORTED (as the pages' batched decoder returns -1 for MoE and
+   F32).  PNB_E_CTX_FULL when any slot's pos already reached n_ctx; a token
+   outside [0, n_vocab) sets PNB_DEV_ERR_TOKEN in that slot's state.  The
+   first call allocates the model's batched workspace (make it before any
+   stream capture). */
 int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const int32_t *tokens_dev,
                       pnb_stream stream, float *logits_dev, int32_t *argmax_dev);
 

@@ -1,5 +1,6 @@
 // pnb_api.cu - the C ABI (include/pnb.h): validation, geometry planning,
 // workspace, the per-step launch sequence and its CUDA-graph capture.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -98,6 +99,36 @@ struct pnb_model {
   bool persistent = false;
   int st_nslots = 0, st_slot_bytes = 0, st_sp = 0, st_union = 0, st_smem = 0;
   cudaStream_t cap_stream = nullptr;     // stream used for graph capture
+  struct BatchCtx *batch = nullptr;      // batched-slot step (made on first use)
+};
+
+// One tensor-core GEMM of the batched step: its split and grid.
+struct BPlan {
+  int rows = 0, K = 0, tiles = 0, ksplit = 1, units = 0, grid = 0;
+};
+
+// Device workspace, tensor maps, plans and the captured graph of the
+// batched-slot step of one model.
+struct BatchCtx {
+  uint8_t *ws = nullptr;
+  float *xb = nullptr, *qb = nullptr, *apart = nullptr, *gpart = nullptr, *am_val = nullptr;
+  unsigned *acnt = nullptr, *tile_cnt = nullptr, *am_cnt = nullptr;
+  int32_t *am_idx = nullptr, *pos = nullptr, *err = nullptr;
+  __nv_bfloat16 *xop_e = nullptr, *xop_o = nullptr, *xop_f = nullptr;
+  float2 *rope = nullptr;
+  BSlot *slots = nullptr;
+  std::vector<CUtensorMap> w_qkv, w_o, w_gu, w_dn;
+  CUtensorMap w_lm;
+  CUtensorMap x_e[3], x_o[3], x_f[3];   // per padded slot count 16, 32, 64
+  BPlan p_qkv, p_o, p_gu, p_dn, p_lm;
+  int nstages[3] = {0, 0, 0}, smem[3] = {0, 0, 0};
+  // captured step and what it was captured for
+  cudaGraphExec_t exec = nullptr;
+  int g_B = 0;
+  std::vector<pnb_state *> g_states;
+  const int32_t *g_tokens = nullptr;
+  float *g_logits = nullptr;
+  int32_t *g_argmax = nullptr;
 };
 
 struct pnb_state {
@@ -462,6 +493,298 @@ cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *log
   return enqueue_kernel(m, s, PNB_KERNEL_LM_HEAD, 0, st, true, logits, argmax);
 }
 
+
+// ------------------------------------------------------------ batched step
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over [rows][K] (K contiguous), boxes of 64 columns x box_rows
+// rows, 128-byte swizzle (the layout the tcgen05 descriptors expect)
+bool encode_map(CUtensorMap *map, const void *base, int64_t rows, int K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Split of a GEMM over K so that (tiles x ksplit) units fill whole waves of
+// the SMs: the smallest split reaching 88% wave efficiency, else the best.
+BPlan plan_bgemm(int64_t rows, int K, int num_sms) {
+  BPlan p;
+  p.rows = (int)rows;
+  p.K = K;
+  p.tiles = ceil_div(rows, 128);
+  const int nchunks = K / 64;
+  double best = -1.0;
+  for (int ks = 1; ks <= std::min(16, nchunks); ++ks) {
+    const int64_t U = (int64_t)p.tiles * ks;
+    const int64_t waves = (U + num_sms - 1) / num_sms;
+    const double eff = (double)U / (double)(waves * num_sms);
+    if (eff > best + 1e-9) {
+      best = eff;
+      p.ksplit = ks;
+    }
+    if (eff >= 0.88) {
+      p.ksplit = ks;
+      break;
+    }
+  }
+  p.units = p.tiles * p.ksplit;
+  p.grid = std::min(p.units, num_sms);
+  return p;
+}
+
+int bp_index(int bp) { return bp == 16 ? 0 : (bp == 32 ? 1 : 2); }
+
+int attn_split_b(const pnb_model *m, int B) {
+  const int per = m->cfg.n_kv_head * m->zgroups * B;
+  return std::max(1, std::min(m->num_sms / std::max(1, per), std::max(1, m->cap / 16)));
+}
+
+void batch_free(BatchCtx *b) {
+  if (!b) return;
+  if (b->exec) cudaGraphExecDestroy(b->exec);
+  cudaFree(b->ws);
+  delete b;
+}
+
+// Batched-slot workspace, tensor maps and plans (bf16 dense models; outside
+// any stream capture).
+int batch_setup(pnb_model *m) {
+  if (m->batch) return PNB_OK;
+  const pnb_config &c = m->cfg;
+  const int E = c.n_embd, F = c.n_ff, Hd = c.n_head * m->hd, L = c.n_layer;
+  const int MB = kMaxBatch, BPmax = 64;
+  BatchCtx *b = new (std::nothrow) BatchCtx();
+  if (!b) return PNB_E_NOMEM;
+  b->p_qkv = plan_bgemm(m->qkv_rows, E, m->num_sms);
+  b->p_o = plan_bgemm(E, Hd, m->num_sms);
+  b->p_gu = plan_bgemm(2 * (int64_t)F, E, m->num_sms);
+  b->p_dn = plan_bgemm(E, F, m->num_sms);
+  b->p_lm = plan_bgemm(c.n_vocab, E, m->num_sms);
+  int64_t gpart = 0, tiles = 0;
+  for (const BPlan *p : {&b->p_qkv, &b->p_o, &b->p_gu, &b->p_dn, &b->p_lm}) {
+    if (p->ksplit > 1) gpart = std::max(gpart, (int64_t)p->units * MB * 128);
+    tiles = std::max(tiles, (int64_t)p->tiles);
+  }
+  int64_t apart = 0;
+  for (int B = 1; B <= MB; ++B)
+    apart = std::max(apart, (int64_t)B * attn_split_b(m, B) * c.n_head * (m->hd + 2));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t o_xb = take((size_t)MB * E * 4), o_qb = take((size_t)MB * Hd * 4);
+  const size_t o_ap = take((size_t)apart * 4), o_ac = take((size_t)MB * c.n_kv_head * m->zgroups * 4);
+  const size_t o_xe = take((size_t)2 * BPmax * E * 2), o_xo = take((size_t)2 * BPmax * Hd * 2);
+  const size_t o_xf = take((size_t)2 * BPmax * F * 2);
+  const size_t o_rope = take((size_t)MB * (m->hd / 2) * 8), o_pos = take((size_t)MB * 4);
+  const size_t o_slots = take((size_t)MB * sizeof(BSlot));
+  const size_t o_gp = take((size_t)std::max<int64_t>(gpart, 1) * 4), o_tc = take((size_t)tiles * 4);
+  const size_t o_amv = take((size_t)MB * m->num_sms * 4), o_ami = take((size_t)MB * m->num_sms * 4);
+  const size_t o_amc = take(4), o_err = take(4);
+  if (cudaMalloc(&b->ws, off) != cudaSuccess) {
+    delete b;
+    return PNB_E_NOMEM;
+  }
+  if (cudaMemset(b->ws, 0, off) != cudaSuccess) {
+    batch_free(b);
+    return PNB_E_CUDA;
+  }
+  b->xb = reinterpret_cast<float *>(b->ws + o_xb);
+  b->qb = reinterpret_cast<float *>(b->ws + o_qb);
+  b->apart = reinterpret_cast<float *>(b->ws + o_ap);
+  b->acnt = reinterpret_cast<unsigned *>(b->ws + o_ac);
+  b->xop_e = reinterpret_cast<__nv_bfloat16 *>(b->ws + o_xe);
+  b->xop_o = reinterpret_cast<__nv_bfloat16 *>(b->ws + o_xo);
+  b->xop_f = reinterpret_cast<__nv_bfloat16 *>(b->ws + o_xf);
+  b->rope = reinterpret_cast<float2 *>(b->ws + o_rope);
+  b->pos = reinterpret_cast<int32_t *>(b->ws + o_pos);
+  b->slots = reinterpret_cast<BSlot *>(b->ws + o_slots);
+  b->gpart = reinterpret_cast<float *>(b->ws + o_gp);
+  b->tile_cnt = reinterpret_cast<unsigned *>(b->ws + o_tc);
+  b->am_val = reinterpret_cast<float *>(b->ws + o_amv);
+  b->am_idx = reinterpret_cast<int32_t *>(b->ws + o_ami);
+  b->am_cnt = reinterpret_cast<unsigned *>(b->ws + o_amc);
+  b->err = reinterpret_cast<int32_t *>(b->ws + o_err);
+  bool ok = true;
+  b->w_qkv.resize(L);
+  b->w_o.resize(L);
+  b->w_gu.resize(L);
+  b->w_dn.resize(L);
+  for (int l = 0; l < L && ok; ++l) {
+    ok = encode_map(&b->w_qkv[l], m->wqkv[l], m->qkv_rows, E, 128) &&
+         encode_map(&b->w_o[l], m->wo[l], E, Hd, 128) &&
+         encode_map(&b->w_gu[l], m->w_gate_up[l], 2 * (int64_t)F, E, 128) &&
+         encode_map(&b->w_dn[l], m->w_down[l], E, F, 128);
+  }
+  ok = ok && encode_map(&b->w_lm, m->output, c.n_vocab, E, 128);
+  for (int i = 0; i < 3 && ok; ++i) {
+    const int bp = 16 << i;
+    ok = encode_map(&b->x_e[i], b->xop_e, 2 * bp, E, 2 * bp) &&
+         encode_map(&b->x_o[i], b->xop_o, 2 * bp, Hd, 2 * bp) &&
+         encode_map(&b->x_f[i], b->xop_f, 2 * bp, F, 2 * bp);
+    const int fixed = bgemm_smem(bp, 0);
+    b->nstages[i] = std::min(8, (kMaxSmem - fixed) / (128 * 128 + 2 * bp * 128));
+    b->smem[i] = bgemm_smem(bp, b->nstages[i]);
+  }
+  if (!ok) {
+    batch_free(b);
+    return PNB_E_UNSUPPORTED;
+  }
+  if (prepare_bgemm_kernels(kMaxSmem) != cudaSuccess) {
+    batch_free(b);
+    return PNB_E_CUDA;
+  }
+  m->batch = b;
+  return PNB_OK;
+}
+
+BGemmArgs bgemm_args(const pnb_model *m, const BatchCtx *b, const BPlan &p, int kind, int B, int bp) {
+  BGemmArgs g{};
+  g.rows = p.rows;
+  g.K = p.K;
+  g.nchunks = p.K / 64;
+  g.tiles = p.tiles;
+  g.ksplit = p.ksplit;
+  g.units = p.units;
+  g.B = B;
+  g.bp = bp;
+  g.kind = kind;
+  g.nstages = b->nstages[bp_index(bp)];
+  g.part = b->gpart;
+  g.tile_cnt = b->tile_cnt;
+  g.rope = b->rope;
+  g.slots = b->slots;
+  g.pos = b->pos;
+  g.n_head = m->cfg.n_head;
+  g.n_kv = m->cfg.n_kv_head;
+  g.hd = m->hd;
+  g.cap = m->cap;
+  g.err = b->err;
+  return g;
+}
+
+// Enqueue one batched step: per layer the attention norm, QKV GEMM (RoPE, KV
+// store), attention, o-proj GEMM (residual), FFN norm, gate/up GEMM (SwiGLU),
+// down GEMM (residual); then the final norm and the LM-head GEMM (argmax,
+// position advance).  The first kernel waits for all earlier stream work;
+// every later one uses programmatic stream serialization.
+cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const int32_t *tokens,
+                          cudaStream_t st, float *logits, int32_t *argmax) {
+  BatchCtx *b = m->batch;
+  const pnb_config &c = m->cfg;
+  const int E = c.n_embd, Hd = c.n_head * m->hd, F = c.n_ff;
+  const int bp = B <= 16 ? 16 : (B <= 32 ? 32 : 64), bi = bp_index(bp);
+  const int smem = b->smem[bi];
+  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
+  const float eps = (float)c.rms_norm_eps;
+  cudaError_t e;
+  BNormArgs na{};
+  na.x = b->xb;
+  na.x_out = b->xb;
+  na.n_vocab = c.n_vocab;
+  na.E = E;
+  na.B = B;
+  na.bp = bp;
+  na.eps = eps;
+  na.xop = b->xop_e;
+  na.slots_dev = b->slots;
+  na.pos = b->pos;
+  na.rope = b->rope;
+  na.inv_freq = m->inv_freq;
+  na.hd = m->hd;
+  na.n_ctx = c.n_ctx;
+  na.err = b->err;
+  for (int i = 0; i < B; ++i) na.slots[i] = BSlot{states[i]->kv, states[i]->io};
+  for (int l = 0; l < c.n_layer; ++l) {
+    na.emb = l == 0 ? m->tok_embd : nullptr;
+    na.tokens = l == 0 ? tokens : nullptr;
+    na.norm_w = m->attn_norm[l];
+    if ((e = launch_bnorm(na, st, l > 0)) != cudaSuccess) return e;
+    BGemmArgs g = bgemm_args(m, b, b->p_qkv, kEpiQkv, B, bp);
+    g.q = b->qb;
+    g.kv_off = (size_t)(2 * l) * layer_kv;
+    g.layer_kv_bytes = layer_kv;
+    if ((e = launch_bgemm(&b->w_qkv[l], &b->x_e[bi], g, b->p_qkv.grid, smem, st, true)) != cudaSuccess)
+      return e;
+    AttnArgs aa{};
+    aa.q = b->qb;
+    aa.n_head = c.n_head;
+    aa.n_kv = c.n_kv_head;
+    aa.cap = m->cap;
+    aa.window = c.sliding_window;
+    aa.n_split = attn_split_b(m, B);
+    aa.part = b->apart;
+    aa.counter = b->acnt;
+    aa.qscale = (float)(1.4426950408889634 / std::sqrt((double)m->hd));
+    aa.stage_pos = m->ag.stage_pos;
+    aa.nstages = m->ag.nstages;
+    aa.slots = b->slots;
+    aa.pos = b->pos;
+    aa.kv_off = (size_t)(2 * l) * layer_kv;
+    aa.layer_kv_bytes = layer_kv;
+    aa.xop = b->xop_o;
+    aa.xop_ld = Hd;
+    aa.bp = bp;
+    aa.nb = B;
+    if ((e = launch_attn(c.dtype, m->hd, aa, m->ag, st, true)) != cudaSuccess) return e;
+    g = bgemm_args(m, b, b->p_o, kEpiResid, B, bp);
+    g.x = b->xb;
+    if ((e = launch_bgemm(&b->w_o[l], &b->x_o[bi], g, b->p_o.grid, smem, st, true)) != cudaSuccess)
+      return e;
+    na.emb = nullptr;
+    na.tokens = nullptr;
+    na.norm_w = m->ffn_norm[l];
+    if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
+    g = bgemm_args(m, b, b->p_gu, kEpiGateUp, B, bp);
+    g.xop = b->xop_f;
+    g.xop_ld = F;
+    if ((e = launch_bgemm(&b->w_gu[l], &b->x_e[bi], g, b->p_gu.grid, smem, st, true)) != cudaSuccess)
+      return e;
+    g = bgemm_args(m, b, b->p_dn, kEpiResid, B, bp);
+    g.x = b->xb;
+    if ((e = launch_bgemm(&b->w_dn[l], &b->x_f[bi], g, b->p_dn.grid, smem, st, true)) != cudaSuccess)
+      return e;
+  }
+  na.emb = nullptr;
+  na.tokens = nullptr;
+  na.norm_w = m->out_norm;
+  if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
+  BGemmArgs g = bgemm_args(m, b, b->p_lm, kEpiLm, B, bp);
+  g.logits = logits;
+  g.argmax_out = argmax;
+  g.am_val = b->am_val;
+  g.am_idx = b->am_idx;
+  g.am_cnt = b->am_cnt;
+  return launch_bgemm(&b->w_lm, &b->x_e[bi], g, b->p_lm.grid, smem, st, true);
+}
+
 }  // namespace
 
 extern "C" {
@@ -581,6 +904,7 @@ void pnb_model_free(pnb_model *m) {
   cudaFree(m->tab_gate_up);
   cudaFree(m->tab_down);
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  batch_free(m->batch);
   delete m;
 }
 
@@ -776,14 +1100,65 @@ int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, fl
 
 int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const int32_t *tokens_dev,
                       pnb_stream stream, float *logits_dev, int32_t *argmax_dev) {
-  (void)tokens_dev;
-  (void)stream;
-  (void)logits_dev;
-  (void)argmax_dev;
   if (!m || !states) return PNB_E_NULL;
   if (B < 1 || B > kMaxBatch) return PNB_E_INVAL;
-  if (m->cfg.expert_count > 0) return PNB_E_UNSUPPORTED;
-  return PNB_E_UNSUPPORTED;
+  const pnb_config &c = m->cfg;
+  if (c.expert_count > 0 || c.dtype != PNB_BF16) return PNB_E_UNSUPPORTED;
+  if (c.n_embd % 64 || (c.n_head * m->hd) % 64 || c.n_ff % 64) return PNB_E_UNSUPPORTED;
+  for (int i = 0; i < B; ++i) {
+    if (!states[i]) return PNB_E_NULL;
+    if (states[i]->m != m) return PNB_E_INVAL;
+    for (int j = 0; j < i; ++j)
+      if (states[j] == states[i]) return PNB_E_INVAL;
+  }
+  if ((logits_dev && !aligned16(logits_dev)) ||
+      (argmax_dev && (reinterpret_cast<uintptr_t>(argmax_dev) & 3u)) ||
+      (tokens_dev && (reinterpret_cast<uintptr_t>(tokens_dev) & 3u)))
+    return PNB_E_ALIGN;
+  for (int i = 0; i < B; ++i)
+    if (states[i]->pos >= c.n_ctx) return PNB_E_CTX_FULL;
+  int rc = check_device(m);
+  if (rc != PNB_OK) return rc;
+  if ((rc = batch_setup(m)) != PNB_OK) return rc;
+  BatchCtx *b = m->batch;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!m->graphs) {
+    if (enqueue_batch(m, states, B, tokens_dev, st, logits_dev, argmax_dev) != cudaSuccess)
+      return PNB_E_CUDA;
+  } else {
+    const bool same = b->exec && b->g_B == B && b->g_tokens == tokens_dev && b->g_logits == logits_dev &&
+                      b->g_argmax == argmax_dev &&
+                      std::equal(states, states + B, b->g_states.begin(), b->g_states.end());
+    if (!same) {
+      if (b->exec) {
+        cudaGraphExecDestroy(b->exec);
+        b->exec = nullptr;
+      }
+      cudaGraph_t graph = nullptr;
+      if (cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+        return PNB_E_CUDA;
+      cudaError_t le = enqueue_batch(m, states, B, tokens_dev, m->cap_stream, logits_dev, argmax_dev);
+      cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &graph);
+      if (le != cudaSuccess || ce != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return PNB_E_CUDA;
+      }
+      cudaError_t ie = cudaGraphInstantiate(&b->exec, graph, 0);
+      cudaGraphDestroy(graph);
+      if (ie != cudaSuccess) {
+        b->exec = nullptr;
+        return PNB_E_CUDA;
+      }
+      b->g_B = B;
+      b->g_states.assign(states, states + B);
+      b->g_tokens = tokens_dev;
+      b->g_logits = logits_dev;
+      b->g_argmax = argmax_dev;
+    }
+    if (cudaGraphLaunch(b->exec, st) != cudaSuccess) return PNB_E_CUDA;
+  }
+  for (int i = 0; i < B; ++i) states[i]->pos += 1;
+  return PNB_OK;
 }
 
 int pnb_model_set_persistent(pnb_model *m, int enable) {
@@ -806,7 +1181,7 @@ int pnb_model_set_graphs(pnb_model *m, int enable) {
 
 int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
   if (!m) return PNB_E_NULL;
-  (void)B;
+  if (B > 0) return m->cfg.n_layer * 7 + 2;   // batched: norm, QKV, attention, o, norm, gate/up, down
   if (m->persistent) return 1;
   const int per_layer = m->cfg.expert_count > 0 ? 6 : 5;
   return m->cfg.n_layer * per_layer + 1;

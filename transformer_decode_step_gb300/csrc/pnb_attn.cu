@@ -76,12 +76,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
   constexpr int VPL = HD / 32;                            // dims per lane when accumulating V
   constexpr int ROTDIV = 8 / C;                           // lanes sharing a load order
   const int SP = a.stage_pos, NS = a.nstages;
-  const int split = blockIdx.x, g = blockIdx.y, z = blockIdx.z;
   const int G = a.n_head / a.n_kv;
+  const int zgroups = G / GB;
+  const int split = blockIdx.x, g = blockIdx.y;
+  const int b = blockIdx.z / zgroups, z = blockIdx.z - b * zgroups;   // slot (0 for one sequence)
   const int h0 = g * G + z * GB;
+  const bool batched = a.slots != nullptr;
+  const BSlot bs = batched ? a.slots[b] : BSlot{nullptr, a.io};
+  int32_t *err = &bs.io->error;
+  const float *qb = a.q + (size_t)b * a.n_head * HD;
+  float *part = a.part + (size_t)b * a.n_head * a.n_split * (HD + 2);
+  unsigned *counter = a.counter + (size_t)b * a.n_kv * zgroups;
+  const void *k_cache = batched ? static_cast<const void *>(bs.kv + a.kv_off) : a.k_cache;
+  const void *v_cache = batched ? static_cast<const void *>(bs.kv + a.kv_off + a.layer_kv_bytes)
+                                : a.v_cache;
 
   // positions of this CTA (pos was written by an earlier step: readable before the wait)
-  const int pos = a.io->pos;
+  const int pos = batched ? a.pos[b] : a.io->pos;
   const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
   const int n = pos - lo + 1;
   const int chunk = (n + a.n_split - 1) / a.n_split;
@@ -110,8 +121,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
 
   if (warp == kAttnWarps) {
     if (lane == 0) {
-      const T *kb = static_cast<const T *>(a.k_cache) + (int64_t)g * a.cap * HD;
-      const T *vb = static_cast<const T *>(a.v_cache) + (int64_t)g * a.cap * HD;
+      const T *kb = static_cast<const T *>(k_cache) + (int64_t)g * a.cap * HD;
+      const T *vb = static_cast<const T *>(v_cache) + (int64_t)g * a.cap * HD;
       bool waited = false, ok = true;
       int st = 0;
       for (; st < nst; ++st) {
@@ -142,9 +153,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
         pdl_wait();
         pdl_trigger();
       }
-      if (!ok) set_error(&a.io->error, kErrTimeout);
+      if (!ok) set_error(err, kErrTimeout);
       for (int j = st > NS ? st - NS : 0; j < st; ++j)
-        if (!mbar_wait(&full[j % NS], (j / NS) & 1)) set_error(&a.io->error, kErrTimeout);
+        if (!mbar_wait(&full[j % NS], (j / NS) & 1)) set_error(err, kErrTimeout);
     }
     return;
   }
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
       const int u = (c + rot) % C;
 #pragma unroll
       for (int e = 0; e < EPU; ++e)
-        qr[gh][c][e] = a.q[(int64_t)(h0 + gh) * HD + sub * DPL + u * EPU + e] * a.qscale;
+        qr[gh][c][e] = qb[(int64_t)(h0 + gh) * HD + sub * DPL + u * EPU + e] * a.qscale;
     }
   if (tid == 0) ktrace(a.tr, 2);
   float m[GB], l[GB], o[GB][VPL];
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
     const int slot = st % NS, round = st / NS;
     if (ok && !mbar_wait(&full[slot], round & 1)) {
       ok = false;
-      if (lane == 0) set_error(&a.io->error, kErrTimeout);
+      if (lane == 0) set_error(err, kErrTimeout);
     }
     if (st == 0 && tid == 0) ktrace(a.tr, 3);
     if (!ok) continue;
@@ -280,7 +291,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
         Os = fmaf(mo[(w * GB + gh) * HD + d], f, Os);
       }
     }
-    float *P = a.part + ((int64_t)(h0 + gh) * a.n_split + split) * (HD + 2);
+    float *P = part + ((int64_t)(h0 + gh) * a.n_split + split) * (HD + 2);
     if (d == 0) {
       P[0] = M;
       P[1] = Ls;
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
   __threadfence();
   consumer_sync<kAttnConsumers>();
   if (tid == 0) {
-    const unsigned prev = atomicAdd(&a.counter[g * gridDim.z + z], 1u);
+    const unsigned prev = atomicAdd(&counter[g * zgroups + z], 1u);
     *flag = (prev == (unsigned)a.n_split - 1u);
   }
   consumer_sync<kAttnConsumers>();
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
     const int ns = a.n_split;
     for (int idx = tid; idx < GB * HD; idx += kAttnConsumers) {
       const int gh = idx / HD, d = idx - gh * HD;
-      const float *P0 = a.part + (int64_t)(h0 + gh) * ns * (HD + 2);
+      const float *P0 = part + (int64_t)(h0 + gh) * ns * (HD + 2);
       float M = -INFINITY, Ls = 0.f, Os = 0.f;
       for (int s0 = 0; s0 < ns; s0 += 8) {
         float pm[8], pl[8], po[8];
@@ -324,9 +335,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
           M = Mn;
         }
       }
-      a.out[(int64_t)(h0 + gh) * HD + d] = Os / Ls;
+      const float o = Os / Ls;
+      if (a.xop) {
+        // bf16 hi / lo parts of the next GEMM's operand
+        const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(o - __bfloat162float(hi));
+        const size_t col = (size_t)(h0 + gh) * HD + d;
+        a.xop[(size_t)b * a.xop_ld + col] = hi;
+        a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = lo;
+      } else {
+        a.out[(int64_t)(h0 + gh) * HD + d] = o;
+      }
     }
-    if (tid == 0) a.counter[g * gridDim.z + z] = 0u;
+    if (tid == 0) counter[g * zgroups + z] = 0u;
   }
   if (tid == 0) ktrace(a.tr, 5);
 }
@@ -341,7 +362,7 @@ cudaError_t launch_one(const AttnArgs &a, const AttnGeom &ag, cudaStream_t st, b
   }
   const int G = a.n_head / a.n_kv;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_split, a.n_kv, G / GB);
+  cfg.gridDim = dim3(a.n_split, a.n_kv, (G / GB) * (a.slots ? a.nb : 1));
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = ag.smem;
   cfg.stream = st;

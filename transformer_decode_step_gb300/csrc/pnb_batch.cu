@@ -1,0 +1,542 @@
+// pnb_batch.cu - kernels of the batched-slot decode step: B sequences, each
+// with its own KV cache and position, advance one token together.
+//
+// Every projection is one tensor-core GEMM Y[b][r] = sum_k W[r][k] X[b][k]
+// that streams each weight once for all B slots.  A CTA owns units of
+// (128-row weight tile, K range).  Warp 0 streams 64-column chunks of the
+// weight tile and of the slots' operand with tiled TMA loads (128-byte
+// swizzle) into a ring; warp 1 issues tcgen05.mma (M = 128 rows, N = 2 x the
+// padded slot count: each operand row is split into a bf16 high part and a
+// bf16 low part, so the products keep about 16 bits of the fp32 activation)
+// into one of two TMEM accumulators; warps 2-5 read the accumulator back with
+// tcgen05.ld, add the high and low columns and apply the fused epilogue: RoPE
+// and the per-slot KV store, the residual add, SwiGLU into the next operand,
+// or the LM head with each slot's argmax.  K-split units leave partial tiles
+// that the last arriving CTA sums in a fixed order.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include "pnb_kernels.cuh"
+#include "pnb_tc.cuh"
+
+namespace pnb {
+namespace {
+
+extern __shared__ __align__(1024) uint8_t b_smem[];
+
+constexpr int kBThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kWTile = 128 * 128;    // bytes of a 128-row x 64-column bf16 weight tile
+constexpr int kBExtra = 1024 + 512 + 2048;  // alignment, barriers, argmax scratch
+
+__device__ __forceinline__ float silu_b(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void am_merge(float &v, int &i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+// ------------------------------------------------------------------ norm
+// One CTA per slot: RMSNorm(x_b) * w into the operand's rows b (bf16 of the
+// value) and bp + b (bf16 of what the first rounding left).  On the first
+// layer x_b is the embedding row of the slot's token, and the CTA also
+// publishes the slot table, the slot's position and its RoPE angles.
+__global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
+  __shared__ float red[8];
+  __shared__ int tok_s, pos_s;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const __nv_bfloat16 *row = nullptr;
+  if (a.emb) {
+    if (b == 0 && tid == 0) *a.err = 0;   // the batch's error word, per step
+    if (tid == 0) {
+      const BSlot s = a.slots[b];
+      a.slots_dev[b] = s;
+      int tok = a.tokens ? a.tokens[b] : s.io->token;
+      if (tok < 0 || tok >= a.n_vocab) {
+        set_error(&s.io->error, kErrToken);
+        tok = 0;
+      }
+      int pos = s.io->pos;
+      if (pos < 0 || pos >= a.n_ctx) {
+        set_error(&s.io->error, kErrToken);
+        pos = 0;
+      }
+      tok_s = tok;
+      pos_s = pos;
+      a.pos[b] = pos;
+    }
+    __syncthreads();
+    row = static_cast<const __nv_bfloat16 *>(a.emb) + (size_t)tok_s * a.E;
+    const int half = a.hd / 2;
+    for (int i = tid; i < half; i += 256) {
+      const double phi = (double)pos_s * a.inv_freq[i];
+      const double k = rint(phi * 0.15915494309189535);
+      double r = fma(-k, 6.283185307179586, phi);
+      r = fma(-k, 2.4492935982947064e-16, r);
+      float sn, cs;
+      sincosf((float)r, &sn, &cs);
+      a.rope[(size_t)b * half + i] = make_float2(cs, sn);
+    }
+  }
+  const float *xr = a.x + (size_t)b * a.E;
+  float ss = 0.f;
+  for (int i = tid; i < a.E; i += 256) {
+    const float v = row ? __bfloat162float(row[i]) : xr[i];
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = 1.0f / sqrtf(tot / (float)a.E + a.eps);
+  __nv_bfloat16 *hi = a.xop + (size_t)b * a.E, *lo = a.xop + (size_t)(a.bp + b) * a.E;
+  for (int i = tid; i < a.E; i += 256) {
+    const float v = row ? __bfloat162float(row[i]) : xr[i];
+    if (row) a.x_out[(size_t)b * a.E + i] = v;
+    const float n = v * inv * a.norm_w[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(n);
+    hi[i] = h;
+    lo[i] = __float2bfloat16_rn(n - __bfloat162float(h));
+  }
+}
+
+// ------------------------------------------------------------------ GEMM
+
+struct Smem {
+  uint8_t *ring;
+  uint64_t *full, *empty, *accf, *acce;
+  uint32_t *tslot;
+  int *flag;
+  float *amv;   // [4][64]
+  int *ami;     // [4][64]
+};
+
+template <int BP>
+__device__ __forceinline__ Smem carve(int ns) {
+  constexpr int SB = kWTile + 2 * BP * 128;
+  Smem m;
+  const uint32_t base = smem_addr(b_smem);
+  m.ring = b_smem + ((1024u - (base & 1023u)) & 1023u);
+  m.full = reinterpret_cast<uint64_t *>(m.ring + (size_t)ns * SB);
+  m.empty = m.full + ns;
+  m.accf = m.empty + ns;
+  m.acce = m.accf + 2;
+  m.tslot = reinterpret_cast<uint32_t *>(m.acce + 2);
+  m.flag = reinterpret_cast<int *>(m.tslot + 1);
+  m.amv = reinterpret_cast<float *>(m.ring + (size_t)ns * SB + 512);
+  m.ami = reinterpret_cast<int *>(m.amv + 4 * 64);
+  return m;
+}
+
+// units of this CTA: u = blockIdx.x, +gridDim.x, ...; each is a (tile, k range)
+struct UnitChunks {
+  const BGemmArgs *a;
+  int u, c, c1;
+  __device__ __forceinline__ void range(int unit) {
+    const int ks = unit % a->ksplit;
+    c = (int)((int64_t)a->nchunks * ks / a->ksplit);
+    c1 = (int)((int64_t)a->nchunks * (ks + 1) / a->ksplit);
+  }
+  __device__ __forceinline__ void start(const BGemmArgs *args) {
+    a = args;
+    u = blockIdx.x;
+    if (u < a->units) range(u);
+  }
+  // advance to the next chunk; false at the end
+  __device__ __forceinline__ bool valid() const { return u < a->units; }
+  __device__ __forceinline__ void next() {
+    if (++c >= c1) {
+      u += gridDim.x;
+      if (u < a->units) range(u);
+    }
+  }
+};
+
+// the epilogue of one 128-row tile: thread owns row `row` of tile `tile`;
+// y[b] = (W x_b)[row] for b < B
+template <int BP, int KIND>
+__device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, const float (&y)[BP],
+                                         float (&bv)[BP], int (&bi)[BP]) {
+  const int grow = tile * 128 + row;
+  const bool in = grow < a.rows;
+  if constexpr (KIND == kEpiResid) {
+    if (in) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b)
+        if (b < a.B) a.x[(size_t)b * a.rows + grow] += y[b];
+    }
+  } else if constexpr (KIND == kEpiQkv) {
+    const int hd = a.hd, half = hd / 2;
+    const int qrows = a.n_head * hd, krows = a.n_kv * hd;
+    const bool even = (grow & 1) == 0;
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      const float par = __shfl_xor_sync(0xffffffffu, y[b], 1);
+      if (b < a.B && in) {
+        float v = y[b];
+        if (grow < qrows + krows) {
+          const float2 cs = a.rope[(size_t)b * half + ((grow % hd) >> 1)];
+          const float v0 = even ? y[b] : par, v1 = even ? par : y[b];
+          v = even ? v0 * cs.x - v1 * cs.y : v0 * cs.y + v1 * cs.x;
+        }
+        if (grow < qrows) {
+          a.q[(size_t)b * qrows + grow] = v;
+        } else {
+          const bool is_k = grow < qrows + krows;
+          const int kx = grow - qrows - (is_k ? 0 : krows);
+          const int gk = kx / hd, d = kx - gk * hd;
+          const int slot = a.pos[b] % a.cap;
+          uint8_t *base = a.slots[b].kv + a.kv_off + (is_k ? 0 : a.layer_kv_bytes);
+          reinterpret_cast<__nv_bfloat16 *>(base)[((size_t)gk * a.cap + slot) * hd + d] =
+              __float2bfloat16_rn(v);
+        }
+      }
+    }
+  } else if constexpr (KIND == kEpiGateUp) {
+    const bool even = (grow & 1) == 0;
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      const float par = __shfl_xor_sync(0xffffffffu, y[b], 1);
+      if (b < a.B && in && even) {
+        const float h = silu_b(y[b]) * par;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+        const int i = grow >> 1;
+        a.xop[(size_t)b * a.xop_ld + i] = hi;
+        a.xop[(size_t)(a.bp + b) * a.xop_ld + i] = lo;
+      }
+    }
+  } else {  // kEpiLm
+    if (in) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b) {
+        if (b < a.B) {
+          if (a.logits) a.logits[(size_t)b * a.rows + grow] = y[b];
+          am_merge(bv[b], bi[b], y[b], grow);
+        }
+      }
+    }
+  }
+}
+
+template <int BP, int KIND>
+__global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ CUtensorMap tw,
+                                                        const __grid_constant__ CUtensorMap tx,
+                                                        const BGemmArgs a) {
+  constexpr int N = 2 * BP;
+  constexpr int XB = N * 128, SB = kWTile + XB;
+  constexpr uint32_t ACOLS = N < 32 ? 32u : (uint32_t)N;
+  constexpr uint32_t TCOLS = 2 * ACOLS;
+  const int ns = a.nstages;
+  const Smem m = carve<BP>(ns);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ktrace(a.tr, 0);
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(&m.full[s], 1);
+      mbar_init(&m.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&m.accf[i], 1);
+      mbar_init(&m.acce[i], 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(m.tslot, TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = *m.tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // weights do not depend on earlier kernels: the first ring's weight
+      // tiles go out before griddepcontrol.wait, their operand tiles after it
+      bool ok = true;
+      UnitChunks it;
+      it.start(&a);
+      int n = 0;
+      for (; it.valid() && n < ns; ++n, it.next()) {
+        mbar_arrive_expect_tx(&m.full[n], SB);
+        tma_load_2d(m.ring + (size_t)n * SB, &tw, it.c * 64, (it.u / a.ksplit) * 128, &m.full[n]);
+      }
+      pdl_wait();
+      pdl_trigger();
+      ktrace(a.tr, 7);
+      UnitChunks jt;
+      jt.start(&a);
+      for (int i = 0; jt.valid(); ++i, jt.next()) {
+        const int s = i % ns, r = i / ns;
+        if (i >= n) {
+          if (!mbar_wait(&m.empty[s], (r - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&m.full[s], SB);
+          tma_load_2d(m.ring + (size_t)s * SB, &tw, jt.c * 64, (jt.u / a.ksplit) * 128, &m.full[s]);
+        }
+        tma_load_2d(m.ring + (size_t)s * SB + kWTile, &tx, jt.c * 64, 0, &m.full[s]);
+      }
+      if (!ok) set_error(a.err, kErrTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, N);
+      bool ok = true;
+      int i = 0, j = 0;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++j) {
+        const int acc = j & 1;
+        if (j >= 2 && !mbar_wait(&m.acce[acc], ((j >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = taddr + (uint32_t)acc * ACOLS;
+        const int ks = u % a.ksplit;
+        const int c0 = (int)((int64_t)a.nchunks * ks / a.ksplit);
+        const int c1 = (int)((int64_t)a.nchunks * (ks + 1) / a.ksplit);
+        for (int c = c0; c < c1; ++c, ++i) {
+          const int s = i % ns, r = i / ns;
+          if (!mbar_wait(&m.full[s], r & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t *wt = m.ring + (size_t)s * SB, *xt = wt + kWTile;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(d, desc_k_sw128(wt, k * 32), desc_k_sw128(xt, k * 32), idesc, c > c0 || k > 0);
+          mma_commit(&m.empty[s]);
+        }
+        if (ok) mma_commit(&m.accf[acc]);
+      }
+      if (!ok) set_error(a.err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps 2-5: TMEM lane quarter (warp % 4), one tile row per thread;
+    // positions, RoPE angles, the slot table and the residual come from
+    // earlier kernels
+    pdl_wait();
+    const int q = warp & 3, row = 32 * q + lane;
+    float bv[BP];
+    int bi[BP];
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      bv[b] = -FLT_MAX;
+      bi[b] = INT_MAX;
+    }
+    bool ok = true;
+    int j = 0;
+    for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++j) {
+      const int acc = j & 1;
+      if (ok && !mbar_wait(&m.accf[acc], (j >> 1) & 1)) {
+        ok = false;
+        if (lane == 0) set_error(a.err, kErrTimeout);
+      }
+      float y[BP];
+#pragma unroll
+      for (int b = 0; b < BP; ++b) y[b] = 0.f;
+      if (ok) {
+        tc_fence_after();
+        const uint32_t t0 = taddr + ((uint32_t)(32 * q) << 16) + (uint32_t)acc * ACOLS;
+        if constexpr (BP == 16) {
+          float v[32];
+          tmem_ld32(t0, v);
+#pragma unroll
+          for (int b = 0; b < 16; ++b) y[b] = v[b] + v[16 + b];
+        } else {
+#pragma unroll
+          for (int cb = 0; cb < N / 32; ++cb) {
+            float v[32];
+            tmem_ld32(t0 + 32 * cb, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (32 * cb < BP) y[32 * cb + i] = v[i];
+              else y[32 * cb - BP + i] += v[i];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.acce[acc]);
+      const int tile = u / a.ksplit;
+      if (a.ksplit == 1) {
+        epilogue<BP, KIND>(a, tile, row, y, bv, bi);
+      } else {
+        float *P = a.part + (size_t)u * a.B * 128;
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+          if (b < a.B) P[(size_t)b * 128 + row] = y[b];
+        __threadfence();
+        epi_sync();
+        if (row == 0) *m.flag = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)a.ksplit - 1u;
+        epi_sync();
+        if (*m.flag) {
+          __threadfence();
+          const float *P0 = a.part + (size_t)tile * a.ksplit * a.B * 128;
+          // fixed order over the K parts; each part's loads are independent
+#pragma unroll
+          for (int b = 0; b < BP; ++b) y[b] = 0.f;
+          for (int k = 0; k < a.ksplit; ++k) {
+            float t[BP];
+#pragma unroll
+            for (int b = 0; b < BP; ++b)
+              t[b] = b < a.B ? __ldcg(P0 + ((size_t)k * a.B + b) * 128 + row) : 0.f;
+#pragma unroll
+            for (int b = 0; b < BP; ++b) y[b] += t[b];
+          }
+          epilogue<BP, KIND>(a, tile, row, y, bv, bi);
+          if (row == 0) a.tile_cnt[tile] = 0u;
+        }
+        epi_sync();
+      }
+    }
+    if constexpr (KIND == kEpiLm) {
+      // each slot's best row of this CTA, then of the launch (last CTA)
+#pragma unroll
+      for (int b = 0; b < BP; ++b) {
+        float v = bv[b];
+        int i = bi[b];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+          am_merge(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+        if (lane == 0) {
+          m.amv[(warp - 2) * 64 + b] = v;
+          m.ami[(warp - 2) * 64 + b] = i;
+        }
+      }
+      epi_sync();
+      if (row < a.B) {
+        float v = m.amv[row];
+        int i = m.ami[row];
+        for (int w = 1; w < 4; ++w) am_merge(v, i, m.amv[w * 64 + row], m.ami[w * 64 + row]);
+        a.am_val[(size_t)row * gridDim.x + blockIdx.x] = v;
+        a.am_idx[(size_t)row * gridDim.x + blockIdx.x] = i;
+      }
+      __threadfence();
+      epi_sync();
+      if (row == 0) *m.flag = atomicAdd(a.am_cnt, 1u) == gridDim.x - 1u;
+      epi_sync();
+      if (*m.flag) {
+        __threadfence();
+        if (row < a.B) {
+          float v = -FLT_MAX;
+          int i = INT_MAX;
+          for (int c = 0; c < (int)gridDim.x; ++c)
+            am_merge(v, i, __ldcg(a.am_val + (size_t)row * gridDim.x + c),
+                     __ldcg(a.am_idx + (size_t)row * gridDim.x + c));
+          StepIO *io = a.slots[row].io;
+          if (i < 0 || i >= a.rows) {
+            set_error(&io->error, kErrToken);
+            i = 0;
+          }
+          if (a.argmax_out) a.argmax_out[row] = i;
+          io->token = i;
+          io->pos = a.pos[row] + 1;
+          const int e = *reinterpret_cast<volatile int32_t *>(a.err);
+          if (e) set_error(&io->error, e);
+        }
+        if (row == 0) *a.am_cnt = 0u;
+      }
+    }
+  }
+  if (threadIdx.x == 0) ktrace(a.tr, 5);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(taddr, TCOLS);
+}
+
+template <int BP, int KIND>
+cudaError_t launch_k(const void *tw, const void *tx, const BGemmArgs &a, int grid, int smem,
+                     cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kBThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_bgemm<BP, KIND>, *static_cast<const CUtensorMap *>(tw),
+                            *static_cast<const CUtensorMap *>(tx), a);
+}
+
+template <int BP>
+cudaError_t launch_bp(const void *tw, const void *tx, const BGemmArgs &a, int grid, int smem,
+                      cudaStream_t st, bool pdl) {
+  switch (a.kind) {
+    case kEpiQkv: return launch_k<BP, kEpiQkv>(tw, tx, a, grid, smem, st, pdl);
+    case kEpiResid: return launch_k<BP, kEpiResid>(tw, tx, a, grid, smem, st, pdl);
+    case kEpiGateUp: return launch_k<BP, kEpiGateUp>(tw, tx, a, grid, smem, st, pdl);
+    case kEpiLm: return launch_k<BP, kEpiLm>(tw, tx, a, grid, smem, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int BP>
+cudaError_t prepare_bp(int smem) {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiQkv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiResid>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_bgemm<BP, kEpiLm>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace
+
+int bgemm_smem(int bp, int nstages) { return nstages * (kWTile + 2 * bp * 128) + kBExtra; }
+
+cudaError_t launch_bgemm(const void *tmap_w, const void *tmap_x, const BGemmArgs &a, int grid,
+                         int smem, cudaStream_t st, bool pdl) {
+  switch (a.bp) {
+    case 16: return launch_bp<16>(tmap_w, tmap_x, a, grid, smem, st, pdl);
+    case 32: return launch_bp<32>(tmap_w, tmap_x, a, grid, smem, st, pdl);
+    case 64: return launch_bp<64>(tmap_w, tmap_x, a, grid, smem, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t prepare_bgemm_kernels(int smem_bytes) {
+  cudaError_t e;
+  if ((e = prepare_bp<16>(smem_bytes)) != cudaSuccess) return e;
+  if ((e = prepare_bp<32>(smem_bytes)) != cudaSuccess) return e;
+  return prepare_bp<64>(smem_bytes);
+}
+
+cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_bnorm, a);
+}
+
+}  // namespace pnb

@@ -11,6 +11,7 @@
 // result into a fused epilogue.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -177,6 +178,8 @@ struct RouterArgs {
   KTrace tr;
 };
 
+struct BSlot;
+
 // split-KV decode attention of the token at io->pos (grid: n_split x n_kv x zgroups)
 struct AttnArgs {
   const float *q;        // [n_head][hd]
@@ -192,6 +195,75 @@ struct AttnArgs {
   int nstages;           // ring slots
   StepIO *io;
   KTrace tr;
+  // batched slots (null for one sequence): blockIdx.z = zgroup + zgroups * slot;
+  // slot b's K / V are at slots[b].kv + kv_off / + kv_off + layer_kv_bytes, its
+  // position is pos[b], its q / part / counters are offset by b, and the merged
+  // output goes to the bf16 operand (rows b and bp + b hold hi and lo parts)
+  const BSlot *slots;
+  const int32_t *pos;
+  size_t kv_off, layer_kv_bytes;
+  __nv_bfloat16 *xop;
+  int xop_ld, bp, nb;    // operand row pitch, padded slots, slots
+};
+
+// One slot of a batched step (device table, written at the start of the step).
+struct BSlot {
+  uint8_t *kv;   // the slot's KV buffer [layer][K|V][n_kv][cap][hd]
+  StepIO *io;    // the slot's token / position / error word
+};
+
+// Epilogues of the batched tensor-core GEMM
+enum BEpi { kEpiQkv = 0, kEpiResid = 1, kEpiGateUp = 2, kEpiLm = 3 };
+
+// Y[b][r] = sum_k W[r][k] * X[b][k] for the B slots of a batched step, on
+// tcgen05 (tiles of 128 weight rows, slots as the MMA's N dimension with the
+// operand split into bf16 hi and lo rows), split over K into ksplit parts
+// whose partial tiles the last arriving CTA sums in a fixed order.
+struct BGemmArgs {
+  int rows, K, nchunks;  // weight rows, columns, 64-column chunks
+  int tiles, ksplit, units;
+  int B, bp;             // slots, padded slot count (16, 32 or 64)
+  int kind;              // BEpi
+  int nstages;           // ring slots
+  float *part;           // [units][B][128] split-K partials
+  unsigned *tile_cnt;    // [tiles] arrival counters, zero between launches
+  // epilogue operands
+  float *x;              // kEpiResid: residual streams [B][rows]
+  float *q;              // kEpiQkv: queries [B][n_head * hd]
+  const float2 *rope;    // kEpiQkv: (cos, sin) [B][hd / 2]
+  const BSlot *slots;    // kEpiQkv / kEpiLm
+  const int32_t *pos;    // [B]
+  size_t kv_off, layer_kv_bytes;
+  int n_head, n_kv, hd, cap;
+  __nv_bfloat16 *xop;    // kEpiGateUp: next operand [2 * bp][xop_ld]
+  int xop_ld;
+  float *logits;         // kEpiLm: [B][rows] or null
+  int32_t *argmax_out;   // kEpiLm: [B] or null
+  float *am_val;         // kEpiLm: [B][gridDim.x]
+  int32_t *am_idx;
+  unsigned *am_cnt;
+  int32_t *err;          // batch error word
+  KTrace tr;
+};
+
+// RMSNorm of every slot into the bf16 hi / lo operand; on the first layer
+// also the embedding gather, the step's slot table and RoPE table
+struct BNormArgs {
+  const float *x;          // [B][E] residual streams (layers > 0)
+  float *x_out;            // first layer: embedding rows written here
+  const void *emb;         // first layer: token embedding table, else null
+  const int32_t *tokens;   // first layer: tokens [B] or null (each slot's io->token)
+  int n_vocab, E, B, bp;
+  const float *norm_w;
+  float eps;
+  __nv_bfloat16 *xop;      // [2 * bp][E]
+  BSlot *slots_dev;        // first layer: the table is written here
+  int32_t *pos;            // first layer: positions [B] written here
+  float2 *rope;            // first layer: [B][hd / 2]
+  const double *inv_freq;  // [hd / 2]
+  int hd, n_ctx;
+  int32_t *err;
+  BSlot slots[64];         // first layer: the slots of this step
 };
 
 struct AttnGeom {
@@ -213,6 +285,13 @@ cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGe
                         cudaStream_t st, bool pdl);
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st);
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st);
+
+// batched step (tensor maps are CUtensorMap, passed by value)
+cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_bgemm(const void *tmap_w, const void *tmap_x, const BGemmArgs &a, int grid,
+                         int smem, cudaStream_t st, bool pdl);
+int bgemm_smem(int bp, int nstages);
+cudaError_t prepare_bgemm_kernels(int smem_bytes);
 
 // persistent step kernel (one cooperative launch per decode step); with
 // prepare = true only sets its shared-memory limit and reports occupancy
