@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="use only the first N layers (small cases for ncu captures)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="slots of a batched workload (default: the workload's own)")
     return ap.parse_args()
 
 
@@ -184,7 +186,7 @@ def dist_setup(n_gpus: int):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0):
+def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0, start_pos=None):
     """Time the oracle on the workload in per-token units (layer 0 with the
     embedding, layers 1..L-1, final norm + LM head), rotating through them.
     Returns (tokens/s, units run, seconds, threads)."""
@@ -193,7 +195,7 @@ def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0):
 
     m = oracle.Model(w.shape, seed=w.seed)
     st = m.new_state()
-    lo, hi = wl.kv_prefill_range(w.shape, w.prefill)
+    lo, hi = wl.kv_prefill_range(w.shape, w.prefill if start_pos is None else start_pos)
     st.prefill_synth(w.seed, 0, lo, hi)
     tok = wl.prompt_tokens(w)[0]
     L = w.shape.n_layer
@@ -242,7 +244,10 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     budget = 200.0
-    tps, n, dt, threads = oracle_units(w, budget, max_units=args.steps, warmup=min(args.warmup, 2))
+    import synth.workloads as wl
+    start = wl.slot_positions(w)[0] if w.batch > 1 else None
+    tps, n, dt, threads = oracle_units(w, budget, max_units=args.steps, warmup=min(args.warmup, 2),
+                                       start_pos=start)
     L = w.shape.n_layer
     line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -392,6 +397,143 @@ def run_ours(args, w):
     return 0
 
 
+def batch_step_bytes(shape, positions) -> int:
+    """Algorithmic HBM bytes of one batched step: the weights once, each slot's
+    attended KV entries and its new entry."""
+    es = shape.elem_bytes
+    weights = shape.params_read_per_token() * es + (2 * shape.n_layer + 1) * shape.n_embd * 4
+    per_pos = shape.n_layer * 2 * shape.n_kv_head * shape.head_dim * es
+    kv = 0
+    for p in positions:
+        n_att = p + 1 if shape.sliding_window <= 0 else min(p + 1, shape.sliding_window)
+        kv += (n_att + 1) * per_pos
+    return weights + kv
+
+
+def run_batched(args, w):
+    """The batched-slot workload: B sequences at their own positions, one token
+    each per step, through pnb_forward_batch."""
+    import torch
+
+    import synth.workloads as wl
+    import transformer_decode_step_gb300 as pnb
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    s = w.shape
+    B = args.batch or w.batch
+    starts = wl.slot_positions(w)[:B]
+    budget = s.n_ctx - max(starts)
+    sm = pnb.SynthModel(s, w.seed)
+    # replica r serves its own slots (seeded by slot id r * B + b)
+    states = [sm.new_state(p, slot=rank * B + b) for b, p in enumerate(starts)]
+    tok0 = torch.tensor([wl.prompt_tokens(w, rank * B + b)[0] for b in range(B)],
+                        dtype=torch.int32, device="cuda")
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one_pass_step(i):
+        if i % budget == 0:
+            for b, st in enumerate(states):
+                st.set_pos(starts[b])
+            sm.model.forward_batch(states, tokens=tok0, argmax=am)
+        else:
+            sm.model.forward_batch(states, argmax=am)
+
+    for i in range(max(3, args.warmup)):
+        one_pass_step(i)
+    torch.cuda.synchronize()
+    if any(st.device_error() for st in states):
+        raise SystemExit("device error during warm-up")
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    e0.record(stream)
+    for i in range(args.steps):
+        one_pass_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    err = max(st.device_error() for st in states)
+    clk = clocks.summary()
+    passes = (args.steps + budget - 1) // budget
+    ms_step = ms / args.steps
+    tokens_per_s = world * B * args.steps / (ms / 1000.0)
+    mean_bytes = sum(batch_step_bytes(s, [p + (i % budget) for p in starts])
+                     for i in range(args.steps)) / args.steps
+    step_gbs = mean_bytes / (ms_step / 1000.0) / 1e9
+    peaks, peak_kind = measured_peaks()
+
+    # end to end: every step the B tokens go host -> device from pinned memory
+    # and the B greedy tokens come back
+    pinned_in = torch.tensor([wl.prompt_tokens(w, rank * B + b)[0] for b in range(B)],
+                             dtype=torch.int32).pin_memory()
+    pinned_out = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    tk = torch.empty(B, dtype=torch.int32, device="cuda")
+    e2e_steps = min(args.steps, budget)
+    for b, st in enumerate(states):
+        st.set_pos(starts[b])
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        tk.copy_(pinned_in, non_blocking=True)
+        sm.model.forward_batch(states, tokens=tk, argmax=am)
+        pinned_out.copy_(am, non_blocking=True)
+        stream.synchronize()
+        pinned_in.copy_(pinned_out)
+    e2e_s = time.perf_counter() - t0
+    e2e_tps = world * B * e2e_steps / e2e_s
+
+    cpu = None
+    L = s.n_layer
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, n, dt, threads = oracle_units(w, 15.0, max_units=10 * (L + 1), start_pos=starts[0])
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} per-token units ({L} layers + LM head) = {n / (L + 1):.2f} decode "
+                         f"steps of slot 0 at position {starts[0]} (the oracle runs slots one "
+                         f"at a time), {dt:.1f} s"}
+    if rank == 0:
+        line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded generated weights and KV cache)",
+                "config": workload_config(w, {"batch": B, "parallelism": f"replicas x{world}",
+                                              "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"}),
+                "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"], "bytes_per_step": mean_bytes,
+                "roofline": {"bound": "hbm", "kernel": "whole batched step (weights once + every slot's KV)",
+                             "achieved": step_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": step_gbs / peaks["hbm_gbs"], "traffic": None,
+                             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                             "timing": "CUDA events over the timed steps"},
+                "clocks": clk, "gpu_launches": args.steps * sm.step_kernel_count(B) + passes * B,
+                "device_error": err,
+                "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
+                        "d2h_bytes_per_step": 4 * B, "steps": e2e_steps,
+                        "how": "pnb_forward_batch with the B tokens copied from pinned host memory "
+                               "and the B greedy tokens copied back and synchronised every step"},
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     import dataclasses
@@ -405,6 +547,8 @@ def main():
     __graft_entry__.build(import_package=args.impl == "ours")
     if args.impl == "reference":
         return run_reference(args, w)
+    if w.batch > 1:
+        return run_batched(args, w)
     return run_ours(args, w)
 
 

@@ -280,8 +280,13 @@ int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const voi
    CTA's linear index (< 256) picks the row; slots 0 = CTA start, 1 = compute
    warps past griddepcontrol.wait, 2 = activation prologue done, 3 = first
    ring slot arrived, 4 = all slots consumed, 5 = epilogue done, 6 / 7 = the
-   producer reached / passed griddepcontrol.wait.  NULL turns it off.  bytes
-   must cover both layouts. */
+   producer reached / passed griddepcontrol.wait.  A batched step records into
+   its first slot's buffer with launch = 7 * layer + (0 norm, 1 QKV,
+   2 attention, 3 o-proj, 4 norm, 5 gate/up, 6 down), 7 * n_layer (+1) for the
+   final norm (LM head); its GEMM slots are 0 start, 1 / 2 first / last MMA,
+   3 first accumulator read, 4 epilogue done, 5 end, 6 / 7 producer done /
+   past griddepcontrol.wait.  NULL turns it off.  bytes must cover
+   (7 * n_layer + 2) * 256 * 8 words and the persistent layout. */
 int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes);
 
 const char *pnb_strerror(int code);

@@ -722,12 +722,15 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
   na.n_ctx = c.n_ctx;
   na.err = b->err;
   for (int i = 0; i < B; ++i) na.slots[i] = BSlot{states[i]->kv, states[i]->io};
+  unsigned long long *trace = states[0]->ktrace;   // optional, the first slot's buffer
   for (int l = 0; l < c.n_layer; ++l) {
     na.emb = l == 0 ? m->tok_embd : nullptr;
     na.tokens = l == 0 ? tokens : nullptr;
     na.norm_w = m->attn_norm[l];
+    na.tr = KTrace{trace, 7 * l};
     if ((e = launch_bnorm(na, st, l > 0)) != cudaSuccess) return e;
     BGemmArgs g = bgemm_args(m, b, b->p_qkv, kEpiQkv, B, bp);
+    g.tr = KTrace{trace, 7 * l + 1};
     g.q = b->qb;
     g.kv_off = (size_t)(2 * l) * layer_kv;
     g.layer_kv_bytes = layer_kv;
@@ -753,21 +756,26 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
     aa.xop_ld = Hd;
     aa.bp = bp;
     aa.nb = B;
+    aa.tr = KTrace{trace, 7 * l + 2};
     if ((e = launch_attn(c.dtype, m->hd, aa, m->ag, st, true)) != cudaSuccess) return e;
     g = bgemm_args(m, b, b->p_o, kEpiResid, B, bp);
+    g.tr = KTrace{trace, 7 * l + 3};
     g.x = b->xb;
     if ((e = launch_bgemm(&b->w_o[l], &b->x_o[bi], g, b->p_o.grid, smem, st, true)) != cudaSuccess)
       return e;
     na.emb = nullptr;
     na.tokens = nullptr;
     na.norm_w = m->ffn_norm[l];
+    na.tr = KTrace{trace, 7 * l + 4};
     if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
     g = bgemm_args(m, b, b->p_gu, kEpiGateUp, B, bp);
+    g.tr = KTrace{trace, 7 * l + 5};
     g.xop = b->xop_f;
     g.xop_ld = F;
     if ((e = launch_bgemm(&b->w_gu[l], &b->x_e[bi], g, b->p_gu.grid, smem, st, true)) != cudaSuccess)
       return e;
     g = bgemm_args(m, b, b->p_dn, kEpiResid, B, bp);
+    g.tr = KTrace{trace, 7 * l + 6};
     g.x = b->xb;
     if ((e = launch_bgemm(&b->w_dn[l], &b->x_f[bi], g, b->p_dn.grid, smem, st, true)) != cudaSuccess)
       return e;
@@ -775,8 +783,10 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
   na.emb = nullptr;
   na.tokens = nullptr;
   na.norm_w = m->out_norm;
+  na.tr = KTrace{trace, 7 * c.n_layer};
   if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
   BGemmArgs g = bgemm_args(m, b, b->p_lm, kEpiLm, B, bp);
+  g.tr = KTrace{trace, 7 * c.n_layer + 1};
   g.logits = logits;
   g.argmax_out = argmax;
   g.am_val = b->am_val;
@@ -1206,7 +1216,7 @@ int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes) {
   if (trace_dev) {
     const int L = s->m->cfg.n_layer;
     const size_t need = std::max((size_t)s->m->grid * (5 * L + 1) * 6 * 8,
-                                 (size_t)(6 * L + 1) * kTraceCtas * 8 * 8);
+                                 (size_t)(7 * L + 2) * kTraceCtas * 8 * 8);
     if (bytes < need) return PNB_E_INVAL;
     if (reinterpret_cast<uintptr_t>(trace_dev) & 7u) return PNB_E_ALIGN;
   }

@@ -51,8 +51,12 @@ __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
   __shared__ float red[8];
   __shared__ int tok_s, pos_s;
   const int b = blockIdx.x, tid = threadIdx.x;
+  if (tid == 0) ktrace(a.tr, 0);
+  // norm weights do not depend on earlier kernels
+  constexpr int kPer = 16;   // elements per thread per pass (4 float4)
   pdl_wait();
   pdl_trigger();
+  if (tid == 0) ktrace(a.tr, 1);
   const __nv_bfloat16 *row = nullptr;
   if (a.emb) {
     if (b == 0 && tid == 0) *a.err = 0;   // the batch's error word, per step
@@ -86,11 +90,30 @@ __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
       a.rope[(size_t)b * half + i] = make_float2(cs, sn);
     }
   }
+  // one pass when E <= 256 * kPer (all loads issued before use), else a loop
   const float *xr = a.x + (size_t)b * a.E;
+  float v[kPer];
   float ss = 0.f;
-  for (int i = tid; i < a.E; i += 256) {
-    const float v = row ? __bfloat162float(row[i]) : xr[i];
-    ss = fmaf(v, v, ss);
+  for (int base = 0; base < a.E; base += 256 * kPer) {
+#pragma unroll
+    for (int j = 0; j < kPer / 4; ++j) {
+      const int i = base + (j * 256 + tid) * 4;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < a.E) {
+        if (row) {
+          const uint2 u = *reinterpret_cast<const uint2 *>(row + i);
+          f = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+        } else {
+          f = __ldcg(reinterpret_cast<const float4 *>(xr + i));
+        }
+      }
+      v[4 * j] = f.x;
+      v[4 * j + 1] = f.y;
+      v[4 * j + 2] = f.z;
+      v[4 * j + 3] = f.w;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) ss = fmaf(v[j], v[j], ss);
   }
   ss = warp_sum(ss);
   if ((tid & 31) == 0) red[tid >> 5] = ss;
@@ -99,14 +122,46 @@ __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
   for (int w = 0; w < 8; ++w) tot += red[w];
   const float inv = 1.0f / sqrtf(tot / (float)a.E + a.eps);
   __nv_bfloat16 *hi = a.xop + (size_t)b * a.E, *lo = a.xop + (size_t)(a.bp + b) * a.E;
-  for (int i = tid; i < a.E; i += 256) {
-    const float v = row ? __bfloat162float(row[i]) : xr[i];
-    if (row) a.x_out[(size_t)b * a.E + i] = v;
-    const float n = v * inv * a.norm_w[i];
-    const __nv_bfloat16 h = __float2bfloat16_rn(n);
-    hi[i] = h;
-    lo[i] = __float2bfloat16_rn(n - __bfloat162float(h));
+  for (int base = 0; base < a.E; base += 256 * kPer) {
+    if (a.E > 256 * kPer) {   // reload this pass's values (long rows only)
+#pragma unroll
+      for (int j = 0; j < kPer / 4; ++j) {
+        const int i = base + (j * 256 + tid) * 4;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < a.E) {
+          if (row) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(row + i);
+            f = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+          } else {
+            f = __ldcg(reinterpret_cast<const float4 *>(xr + i));
+          }
+        }
+        v[4 * j] = f.x;
+        v[4 * j + 1] = f.y;
+        v[4 * j + 2] = f.z;
+        v[4 * j + 3] = f.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPer / 4; ++j) {
+      const int i = base + (j * 256 + tid) * 4;
+      if (i >= a.E) continue;
+      const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + i);
+      if (row) *reinterpret_cast<float4 *>(a.x_out + (size_t)b * a.E + i) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      const float n[4] = {v[4 * j] * inv * w.x, v[4 * j + 1] * inv * w.y, v[4 * j + 2] * inv * w.z,
+                          v[4 * j + 3] * inv * w.w};
+      __nv_bfloat16 h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = __float2bfloat16_rn(n[e]);
+        l[e] = __float2bfloat16_rn(n[e] - __bfloat162float(h[e]));
+      }
+      *reinterpret_cast<uint2 *>(hi + i) = *reinterpret_cast<const uint2 *>(h);
+      *reinterpret_cast<uint2 *>(lo + i) = *reinterpret_cast<const uint2 *>(l);
+    }
   }
+  if (tid == 0) ktrace(a.tr, 5);
 }
 
 // ------------------------------------------------------------------ GEMM
@@ -289,6 +344,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         }
         tma_load_2d(m.ring + (size_t)s * SB + kWTile, &tx, jt.c * 64, 0, &m.full[s]);
       }
+      ktrace(a.tr, 6);
       if (!ok) set_error(a.err, kErrTimeout);
     }
   } else if (warp == 1) {
@@ -314,6 +370,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
             break;
           }
           tc_fence_after();
+          if (i == 0) ktrace(a.tr, 1);
           const uint8_t *wt = m.ring + (size_t)s * SB, *xt = wt + kWTile;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -322,6 +379,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         }
         if (ok) mma_commit(&m.accf[acc]);
       }
+      ktrace(a.tr, 2);
       if (!ok) set_error(a.err, kErrTimeout);
     }
     __syncwarp();
@@ -346,6 +404,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         ok = false;
         if (lane == 0) set_error(a.err, kErrTimeout);
       }
+      if (j == 0 && row == 0) ktrace(a.tr, 3);
       float y[BP];
 #pragma unroll
       for (int b = 0; b < BP; ++b) y[b] = 0.f;
@@ -405,6 +464,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         epi_sync();
       }
     }
+    if (row == 0) ktrace(a.tr, 4);
     if constexpr (KIND == kEpiLm) {
       // each slot's best row of this CTA, then of the launch (last CTA)
 #pragma unroll

@@ -263,6 +263,7 @@ struct BNormArgs {
   const double *inv_freq;  // [hd / 2]
   int hd, n_ctx;
   int32_t *err;
+  KTrace tr;
   BSlot slots[64];         // first layer: the slots of this step
 };
 
