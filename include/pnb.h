@@ -204,6 +204,17 @@ int pnb_model_set_graphs(pnb_model *m, int enable);
 int pnb_model_set_persistent(pnb_model *m, int enable);
 int pnb_model_is_persistent(const pnb_model *m);
 
+/* Decode attention on tcgen05 tensor cores (enable = 1, the default where
+   the model allows it: bf16 weights and KV, head_dim 64 or 128, n_head /
+   n_kv_head in {1, 2, 4, 8}, and with a sliding window a cache of a multiple
+   of 128 positions) or on CUDA cores (0).  The scores and the weighted sum of
+   V are MMAs whose fp32-side operands (queries, softmax weights) are split
+   into bf16 high and low parts; results agree with the CUDA-core kernel to
+   about 1e-5 relative.  Affects the single-sequence and batched steps.
+   Returns PNB_E_UNSUPPORTED when enabling is not possible for this model. */
+int pnb_model_set_tensor_attention(pnb_model *m, int enable);
+int pnb_model_is_tensor_attention(const pnb_model *m);
+
 /* Number of this library's kernels one step launches (single sequence when
    B == 0, batched otherwise). */
 int pnb_step_kernel_count(const pnb_model *m, int32_t B);

@@ -64,6 +64,8 @@ _SIGS = {
     "pnb_model_set_graphs": (_i32, [_p, _i32]),
     "pnb_model_set_persistent": (_i32, [_p, _i32]),
     "pnb_model_is_persistent": (_i32, [_p]),
+    "pnb_model_set_tensor_attention": (_i32, [_p, _i32]),
+    "pnb_model_is_tensor_attention": (_i32, [_p]),
     "pnb_step_kernel_count": (_i32, [_p, _i32]),
     "pnb_state_activations": (_i32, [_p, _p]),
     "pnb_step_kernel": (_i32, [_p, _p, _i32, _i32, _p]),
@@ -158,6 +160,14 @@ class Model:
 
     def set_graphs(self, enable: bool):
         check(pnb_model_set_graphs(self._h, 1 if enable else 0), "pnb_model_set_graphs")
+
+    def set_tensor_attention(self, enable: bool):
+        check(pnb_model_set_tensor_attention(self._h, 1 if enable else 0),
+              "pnb_model_set_tensor_attention")
+
+    @property
+    def tensor_attention(self) -> bool:
+        return bool(pnb_model_is_tensor_attention(self._h))
 
     def set_persistent(self, enable: bool):
         check(pnb_model_set_persistent(self._h, 1 if enable else 0), "pnb_model_set_persistent")

@@ -95,6 +95,10 @@ struct pnb_model {
   AttnGeom ag{};
   int n_split = 1, zgroups = 1;
   bool graphs = true;
+  // tensor-core attention (bf16 KV, head_dim 64 / 128, <= 8 query heads per KV head)
+  bool attn_tc_ok = false, attn_tc = false;
+  int n_split_tc = 1;
+  int mode_gen = 0;                      // bumped when a launch mode changes (graphs re-captured)
   // persistent step kernel
   bool persistent = false;
   int st_nslots = 0, st_slot_bytes = 0, st_sp = 0, st_union = 0, st_smem = 0;
@@ -124,7 +128,7 @@ struct BatchCtx {
   int nstages[3] = {0, 0, 0}, smem[3] = {0, 0, 0};
   // captured step and what it was captured for
   cudaGraphExec_t exec = nullptr;
-  int g_B = 0;
+  int g_B = 0, g_gen = -1;
   std::vector<pnb_state *> g_states;
   const int32_t *g_tokens = nullptr;
   float *g_logits = nullptr;
@@ -151,6 +155,8 @@ struct pnb_state {
   StepLayer *layers = nullptr;           // device [n_layer]
   unsigned long long *trace = nullptr;   // optional phase timestamps (persistent kernel)
   unsigned long long *ktrace = nullptr;  // optional per-CTA timestamps (per-phase kernels)
+  void *maps = nullptr;                  // device [layer][K|V] tensor maps over kv (tensor-core attention)
+  int g_gen = -1;                        // model mode generation the graph was captured in
   cudaGraphExec_t exec = nullptr;
   float *g_logits = nullptr;
   int32_t *g_argmax = nullptr;
@@ -197,6 +203,11 @@ void plan(pnb_model *m) {
   // one wave: at most one CTA per SM (the attention CTA's registers allow one)
   const int want = std::max(1, m->num_sms / (c.n_kv_head * m->zgroups));
   m->n_split = std::max(1, std::min(want, std::max(1, m->cap / 16)));
+  // tensor-core attention: 128-position tiles; a ring cache must hold whole tiles
+  m->attn_tc_ok = c.dtype == PNB_BF16 && (m->hd == 64 || m->hd == 128) &&
+                  (G == 1 || G == 2 || G == 4 || G == 8) &&
+                  (c.sliding_window == 0 || m->cap % 128 == 0);
+  m->n_split_tc = std::max(1, std::min(m->num_sms / c.n_kv_head, ceil_div(m->cap, 128)));
 }
 
 bool geoms_supported(const pnb_model *m);
@@ -290,6 +301,25 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       return launch_qkv(c.dtype, qa, m->grid, st, pdl);
     }
     case PNB_KERNEL_ATTN: {
+      if (m->attn_tc) {
+        AttnTcArgs ta{};
+        ta.q = s->q;
+        ta.maps = s->maps;
+        ta.layer = l;
+        ta.n_head = H;
+        ta.n_kv = Hkv;
+        ta.cap = m->cap;
+        ta.window = c.sliding_window;
+        ta.n_split = m->n_split_tc;
+        ta.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
+        ta.part = s->part;
+        ta.counter = s->attn_cnt;
+        ta.out = s->attn;
+        ta.io = s->io;
+        ta.nstages = attn_tc_stages(hd);
+        ta.tr = tr;
+        return launch_attn_tc(hd, H / Hkv, ta, st, pdl);
+      }
       AttnArgs aa{};
       aa.q = s->q;
       aa.k_cache = kc;
@@ -560,8 +590,17 @@ BPlan plan_bgemm(int64_t rows, int K, int num_sms) {
 int bp_index(int bp) { return bp == 16 ? 0 : (bp == 32 ? 1 : 2); }
 
 int attn_split_b(const pnb_model *m, int B) {
+  if (m->attn_tc)
+    return std::max(1, std::min(m->num_sms / (m->cfg.n_kv_head * B), ceil_div(m->cap, 128)));
   const int per = m->cfg.n_kv_head * m->zgroups * B;
   return std::max(1, std::min(m->num_sms / std::max(1, per), std::max(1, m->cap / 16)));
+}
+
+int attn_split_b_max(const pnb_model *m, int B) {
+  const int tc = std::max(1, std::min(m->num_sms / (m->cfg.n_kv_head * B), ceil_div(m->cap, 128)));
+  const int per = m->cfg.n_kv_head * m->zgroups * B;
+  const int cc = std::max(1, std::min(m->num_sms / std::max(1, per), std::max(1, m->cap / 16)));
+  return std::max(tc, cc);
 }
 
 void batch_free(BatchCtx *b) {
@@ -592,7 +631,7 @@ int batch_setup(pnb_model *m) {
   }
   int64_t apart = 0;
   for (int B = 1; B <= MB; ++B)
-    apart = std::max(apart, (int64_t)B * attn_split_b(m, B) * c.n_head * (m->hd + 2));
+    apart = std::max(apart, (int64_t)B * attn_split_b_max(m, B) * c.n_head * (m->hd + 2));
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -721,7 +760,7 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
   na.hd = m->hd;
   na.n_ctx = c.n_ctx;
   na.err = b->err;
-  for (int i = 0; i < B; ++i) na.slots[i] = BSlot{states[i]->kv, states[i]->io};
+  for (int i = 0; i < B; ++i) na.slots[i] = BSlot{states[i]->kv, states[i]->io, states[i]->maps};
   unsigned long long *trace = states[0]->ktrace;   // optional, the first slot's buffer
   for (int l = 0; l < c.n_layer; ++l) {
     na.emb = l == 0 ? m->tok_embd : nullptr;
@@ -736,6 +775,28 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
     g.layer_kv_bytes = layer_kv;
     if ((e = launch_bgemm(&b->w_qkv[l], &b->x_e[bi], g, b->p_qkv.grid, smem, st, true)) != cudaSuccess)
       return e;
+    if (m->attn_tc) {
+      AttnTcArgs ta{};
+      ta.q = b->qb;
+      ta.layer = l;
+      ta.n_head = c.n_head;
+      ta.n_kv = c.n_kv_head;
+      ta.cap = m->cap;
+      ta.window = c.sliding_window;
+      ta.n_split = attn_split_b(m, B);
+      ta.qscale = (float)(1.4426950408889634 / std::sqrt((double)m->hd));
+      ta.part = b->apart;
+      ta.counter = b->acnt;
+      ta.xop = b->xop_o;
+      ta.xop_ld = Hd;
+      ta.bp = bp;
+      ta.nb = B;
+      ta.slots = b->slots;
+      ta.pos = b->pos;
+      ta.nstages = attn_tc_stages(m->hd);
+      ta.tr = KTrace{trace, 7 * l + 2};
+      if ((e = launch_attn_tc(m->hd, c.n_head / c.n_kv_head, ta, st, true)) != cudaSuccess) return e;
+    } else {
     AttnArgs aa{};
     aa.q = b->qb;
     aa.n_head = c.n_head;
@@ -758,6 +819,7 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
     aa.nb = B;
     aa.tr = KTrace{trace, 7 * l + 2};
     if ((e = launch_attn(c.dtype, m->hd, aa, m->ag, st, true)) != cudaSuccess) return e;
+    }
     g = bgemm_args(m, b, b->p_o, kEpiResid, B, bp);
     g.tr = KTrace{trace, 7 * l + 3};
     g.x = b->xb;
@@ -899,6 +961,8 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   if (ok) {
     plan_step(m);
     m->persistent = false;
+    if (m->attn_tc_ok) m->attn_tc_ok = encode_fn() != nullptr && prepare_attn_tc_kernels() == cudaSuccess;
+    m->attn_tc = m->attn_tc_ok;
   }
   if (!ok) {
     pnb_model_free(m);
@@ -949,7 +1013,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   const size_t o_q = take((size_t)c.n_head * m->hd * 4);
   const size_t o_attn = take((size_t)c.n_head * m->hd * 4);
   const size_t o_h = take((size_t)k * c.n_ff * 4);
-  const size_t o_part = take((size_t)c.n_head * m->n_split * (m->hd + 2) * 4);
+  const size_t o_part = take((size_t)c.n_head * std::max(m->n_split, m->n_split_tc) * (m->hd + 2) * 4);
   const size_t o_gate = take((size_t)k * 4);
   const size_t o_idx = take((size_t)k * 4);
   const size_t o_lmv = take((size_t)m->grid * 4);
@@ -959,6 +1023,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   const size_t o_spart = take((size_t)c.n_head * m->grid * (m->hd + 2) * 4);
   const size_t o_layers = take((size_t)c.n_layer * sizeof(StepLayer));
   const size_t o_ss = take((size_t)2 * m->grid * 4);
+  const size_t o_maps = m->attn_tc_ok ? take((size_t)2 * c.n_layer * sizeof(CUtensorMap)) : 0;
   if (cudaMalloc(&s->ws, off) != cudaSuccess) {
     delete s;
     return PNB_E_NOMEM;
@@ -984,6 +1049,21 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   s->step_part = reinterpret_cast<float *>(s->ws + o_spart);
   s->layers = reinterpret_cast<StepLayer *>(s->ws + o_layers);
   s->ss_part = reinterpret_cast<float *>(s->ws + o_ss);
+  std::vector<CUtensorMap> maps;
+  if (m->attn_tc_ok) {
+    // [layer][K|V] maps over this state's cache: rows = n_kv_head * cap positions, hd columns
+    s->maps = s->ws + o_maps;
+    maps.resize((size_t)2 * c.n_layer);
+    const size_t layer_kv_b = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
+    for (int l = 0; l < c.n_layer; ++l)
+      for (int kind = 0; kind < 2; ++kind)
+        if (!encode_map(&maps[2 * l + kind], s->kv + (size_t)(2 * l + kind) * layer_kv_b,
+                        (int64_t)c.n_kv_head * m->cap, m->hd, 128)) {
+          cudaFree(s->ws);
+          delete s;
+          return PNB_E_CUDA;
+        }
+  }
   // per-layer table of the persistent kernel
   std::vector<StepLayer> lt(c.n_layer);
   const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
@@ -1006,7 +1086,9 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   }
   if (cudaMemset(s->ws, 0, off) != cudaSuccess ||
       cudaMemcpy(s->layers, lt.data(), lt.size() * sizeof(StepLayer), cudaMemcpyHostToDevice) !=
-          cudaSuccess) {
+          cudaSuccess ||
+      (s->maps && cudaMemcpy(s->maps, maps.data(), maps.size() * sizeof(CUtensorMap),
+                             cudaMemcpyHostToDevice) != cudaSuccess)) {
     cudaFree(s->ws);
     delete s;
     return PNB_E_CUDA;
@@ -1079,7 +1161,7 @@ int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, fl
   if (!m->graphs) {
     if (enqueue_step(m, s, st, logits_dev, argmax_dev) != cudaSuccess) return PNB_E_CUDA;
   } else {
-    if (!s->exec || s->g_logits != logits_dev || s->g_argmax != argmax_dev) {
+    if (!s->exec || s->g_logits != logits_dev || s->g_argmax != argmax_dev || s->g_gen != m->mode_gen) {
       if (s->exec) {
         cudaGraphExecDestroy(s->exec);
         s->exec = nullptr;
@@ -1101,6 +1183,7 @@ int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, fl
       }
       s->g_logits = logits_dev;
       s->g_argmax = argmax_dev;
+      s->g_gen = m->mode_gen;
     }
     if (cudaGraphLaunch(s->exec, st) != cudaSuccess) return PNB_E_CUDA;
   }
@@ -1136,7 +1219,8 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
     if (enqueue_batch(m, states, B, tokens_dev, st, logits_dev, argmax_dev) != cudaSuccess)
       return PNB_E_CUDA;
   } else {
-    const bool same = b->exec && b->g_B == B && b->g_tokens == tokens_dev && b->g_logits == logits_dev &&
+    const bool same = b->exec && b->g_B == B && b->g_gen == m->mode_gen && b->g_tokens == tokens_dev &&
+                      b->g_logits == logits_dev &&
                       b->g_argmax == argmax_dev &&
                       std::equal(states, states + B, b->g_states.begin(), b->g_states.end());
     if (!same) {
@@ -1160,6 +1244,7 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
         return PNB_E_CUDA;
       }
       b->g_B = B;
+      b->g_gen = m->mode_gen;
       b->g_states.assign(states, states + B);
       b->g_tokens = tokens_dev;
       b->g_logits = logits_dev;
@@ -1173,6 +1258,7 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
 
 int pnb_model_set_persistent(pnb_model *m, int enable) {
   if (!m) return PNB_E_NULL;
+  ++m->mode_gen;
   if (!enable) {
     m->persistent = false;
     return PNB_OK;
@@ -1181,10 +1267,21 @@ int pnb_model_set_persistent(pnb_model *m, int enable) {
   return m->persistent ? PNB_OK : PNB_E_UNSUPPORTED;
 }
 
+int pnb_model_set_tensor_attention(pnb_model *m, int enable) {
+  if (!m) return PNB_E_NULL;
+  if (enable && !m->attn_tc_ok) return PNB_E_UNSUPPORTED;
+  ++m->mode_gen;
+  m->attn_tc = enable != 0;
+  return PNB_OK;
+}
+
+int pnb_model_is_tensor_attention(const pnb_model *m) { return m && m->attn_tc ? 1 : 0; }
+
 int pnb_model_is_persistent(const pnb_model *m) { return m && m->persistent ? 1 : 0; }
 
 int pnb_model_set_graphs(pnb_model *m, int enable) {
   if (!m) return PNB_E_NULL;
+  ++m->mode_gen;
   m->graphs = enable != 0;
   return PNB_OK;
 }

@@ -1,0 +1,605 @@
+// pnb_attn_tc.cu - decode attention on tcgen05 tensor cores (bf16 KV cache).
+//
+// One CTA takes one KV head g of one sequence (slot) and a range of
+// 128-position tiles of its attended positions [lo, pos]; the G query heads
+// that share g are computed together.
+//   warp 0   streams the K and V tiles of each 128 positions with tiled TMA
+//            loads (128-byte swizzle) from the state's tensor maps into a ring;
+//   warp 1   issues S = K Q^T (M = 128 positions, N = 16: rows h and 8 + h of
+//            Q hold the bf16 high and low parts of query head h, scaled by
+//            log2(e) / sqrt(hd)) and O = P V (M = 128 rows of P, N = hd, V as
+//            an MN-major operand), accumulators in TMEM;
+//   warps 2-5 own one position each: they read S back (tcgen05.ld), keep the
+//            running max and sum per head (online softmax in the log2
+//            domain), write P = exp2(s - max) as bf16 high / low parts into
+//            rows h and 8 + h of a swizzled shared tile, and warp 4 (TMEM
+//            lanes 0-31, the rows of P that carry heads) folds each tile's O
+//            into its registers with the rescale factor.
+// Splits of the position range leave (max, sum, O) partials that the last
+// CTA of the KV head merges by log-sum-exp.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pnb_kernels.cuh"
+#include "pnb_tc.cuh"
+
+namespace pnb {
+namespace {
+
+extern __shared__ __align__(1024) uint8_t t_smem[];
+
+constexpr int kTThreads = 192;
+constexpr int kTile = 128;          // positions per tile
+constexpr int kBox = 128 * 128;     // bytes of one 128-row x 64-column bf16 box
+
+// byte offset of (row, byte column) in a [rows][128 B] tile with 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int row, int col_bytes) {
+  return (uint32_t)row * 128u + ((((uint32_t)col_bytes >> 4) ^ ((uint32_t)row & 7u)) << 4) +
+         ((uint32_t)col_bytes & 15u);
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_sync_t() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// descriptor of an MN-major operand tile with 128-byte swizzle: 64-element
+// atoms along N lbo bytes apart, groups of 8 K-rows 1024 bytes apart
+__device__ __forceinline__ uint64_t desc_mn_sw128(const void *tile, uint32_t lbo) {
+  const uint32_t addr = smem_addr(tile);
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// head_dim 128 computes O^T = V^T P^T (M = 128 dims, V as an MN-major A
+// operand, P a 16-row K-major B operand, O^T in 16 TMEM columns: one dim per
+// softmax thread); head_dim 64 computes O = P V (M = 128 rows of P, of which
+// rows h and 8 + h carry head h, V an MN-major B operand, O in 64 columns
+// read by the warp on TMEM lanes 0-31).
+template <int HD>
+struct TL {
+  static constexpr bool VT = HD == 128;
+  static constexpr int KT = HD / 64 * kBox;             // K tile bytes (HD / 64 boxes)
+  static constexpr int STAGE = 2 * KT;                  // K and V
+  static constexpr int PCH = VT ? 2048 : kBox;          // P bytes per 64-position chunk
+  static constexpr int PT = 2 * PCH;                    // P tile: 128 positions
+  static constexpr int QT = HD / 64 * 2048;             // Q tile: 16 rows x HD
+  static constexpr uint32_t TCOLS = VT ? 64u : 256u;    // TMEM columns
+  static constexpr uint32_t OCOL = VT ? 32u : 128u;     // O's first column
+};
+
+struct TBars {
+  uint64_t *full, *empty;
+  uint64_t *s_full, *s_empty, *p_full, *p_empty, *o_full, *o_empty, *q_ready;
+};
+
+template <int HD, int G>
+__global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
+  constexpr int KT = TL<HD>::KT, STAGE = TL<HD>::STAGE, PT = TL<HD>::PT, QT = TL<HD>::QT;
+  constexpr bool VT = TL<HD>::VT;
+  constexpr int PCH = TL<HD>::PCH;
+  constexpr uint32_t TCOLS = TL<HD>::TCOLS;
+  const int NS = a.nstages;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const bool batched = a.slots != nullptr;
+  const BSlot bs = batched ? a.slots[b] : BSlot{nullptr, a.io, a.maps};
+  int32_t *err = &bs.io->error;
+  const CUtensorMap *maps = static_cast<const CUtensorMap *>(bs.maps) + 2 * a.layer;
+  const CUtensorMap *kmap = maps, *vmap = maps + 1;
+  const float *qb = a.q + (size_t)b * a.n_head * HD;
+  float *part = a.part + (size_t)b * a.n_head * a.n_split * (HD + 2);
+  unsigned *counter = a.counter + (size_t)b * a.n_kv;
+  const int h0 = g * G;
+
+  // positions: [lo, pos]; tiles of 128 aligned positions, split evenly
+  const int pos = batched ? a.pos[b] : a.io->pos;
+  const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+  const int t_first = lo / kTile, t_last = pos / kTile;
+  const int nt_all = t_last - t_first + 1;
+  const int tps = (nt_all + a.n_split - 1) / a.n_split;
+  const int tb = t_first + split * tps;
+  const int ntiles = max(0, min(t_last + 1, tb + tps) - tb);
+
+  // shared memory
+  const uint32_t base = smem_addr(t_smem);
+  uint8_t *sm = t_smem + ((1024u - (base & 1023u)) & 1023u);
+  uint8_t *ring = sm;
+  uint8_t *P = ring + (size_t)NS * STAGE;
+  uint8_t *Q = P + 2 * PT;
+  TBars bar;
+  bar.full = reinterpret_cast<uint64_t *>(Q + QT);
+  bar.empty = bar.full + NS;
+  bar.s_full = bar.empty + NS;
+  bar.s_empty = bar.s_full + 1;
+  bar.p_full = bar.s_empty + 1;
+  bar.p_empty = bar.p_full + 2;
+  bar.o_full = bar.p_empty + 2;
+  bar.o_empty = bar.o_full + 1;
+  bar.q_ready = bar.o_empty + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar.q_ready + 1);
+  int *flag = reinterpret_cast<int *>(tslot + 1);
+  float *red = reinterpret_cast<float *>(flag + 4);   // [2][4][8]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ktrace(a.tr, 0);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar.full[s], 1);
+      mbar_init(&bar.empty[s], 1);
+    }
+    mbar_init(bar.s_full, 1);
+    mbar_init(bar.s_empty, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.p_full[i], 4);
+      mbar_init(&bar.p_empty[i], 1);
+    }
+    mbar_init(bar.o_full, 1);
+    mbar_init(bar.o_empty, 1);
+    mbar_init(bar.q_ready, 4);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = *tslot;
+  const uint32_t t_s = taddr, t_o = taddr + TL<HD>::OCOL;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // tiles before the current position were written by earlier steps; the
+      // tile holding pos waits for the kernel that wrote this step's K / V
+      bool waited = false, ok = true;
+      for (int i = 0; i < ntiles; ++i) {
+        const int T = tb + i, s = i % NS, r = i / NS;
+        if (!waited && ((T + 1) * kTile > pos || i == NS)) {
+          ktrace(a.tr, 6);
+          pdl_wait();
+          pdl_trigger();
+          ktrace(a.tr, 7);
+          waited = true;
+        }
+        if (i >= NS && !mbar_wait(&bar.empty[s], (r - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int y = g * a.cap + (T * kTile) % a.cap;
+        uint8_t *kt = ring + (size_t)s * STAGE, *vt = kt + KT;
+        mbar_arrive_expect_tx(&bar.full[s], STAGE);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c) {
+          tma_load_2d(kt + c * kBox, kmap, c * 64, y, &bar.full[s]);
+          tma_load_2d(vt + c * kBox, vmap, c * 64, y, &bar.full[s]);
+        }
+      }
+      if (!waited) {
+        ktrace(a.tr, 6);
+        pdl_wait();
+        pdl_trigger();
+        ktrace(a.tr, 7);
+      }
+      if (!ok) set_error(err, kErrTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16);
+      // V MN-major: as A of O^T = V^T P^T (head_dim 128) or as B of O = P V
+      constexpr uint32_t idesc_o = VT ? (idesc_bf16_f32(128, 16) | (1u << 15))
+                                      : (idesc_bf16_f32(128, HD) | (1u << 16));
+      bool ok = mbar_wait(bar.q_ready, 0);
+      auto issue_s = [&](int t) {
+        const uint8_t *kt = ring + (size_t)(t % NS) * STAGE;
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(t_s, desc_k_sw128(kt + c * kBox, k * 32), desc_k_sw128(Q + c * 2048, k * 32), idesc_s,
+                     c > 0 || k > 0);
+        mma_commit(bar.s_full);
+      };
+      if (ok && ntiles > 0) {
+        ok = mbar_wait(&bar.full[0], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+      }
+      for (int t = 0; t < ntiles && ok; ++t) {
+        if (t + 1 < ntiles) {
+          ok = mbar_wait(&bar.full[(t + 1) % NS], ((t + 1) / NS) & 1) && mbar_wait(bar.s_empty, t & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
+        }
+        ok = mbar_wait(&bar.p_full[t & 1], (t >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t *pt = P + (size_t)(t & 1) * PT;
+        const uint8_t *vt = ring + (size_t)(t % NS) * STAGE + KT;
+        // O accumulates in TMEM over the CTA's tiles (rescaled in place when the
+        // softmax warps raise their reference max)
+#pragma unroll
+        for (int pc = 0; pc < kTile / 16; ++pc) {
+          const uint64_t dp = desc_k_sw128(pt + (pc >> 2) * PCH, (pc & 3) * 32);
+          const uint64_t dv = desc_mn_sw128(vt + pc * 2048, kBox);
+          if constexpr (VT) mma_bf16(t_o, dv, dp, idesc_o, t > 0 || pc > 0);
+          else mma_bf16(t_o, dp, dv, idesc_o, t > 0 || pc > 0);
+        }
+        mma_commit(bar.o_full);
+        mma_commit(&bar.p_empty[t & 1]);
+        mma_commit(&bar.empty[t % NS]);
+      }
+      if (!ok) set_error(err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax warps 2-5
+    const int q = warp & 3, tid = threadIdx.x - 64;   // position 32 q + lane of each tile
+    // Q operand: rows h / 8 + h = high / low bf16 of q_h * qscale, zero rows elsewhere
+    for (int i = tid * 16; i < QT; i += 128 * 16) *reinterpret_cast<uint4 *>(Q + i) = make_uint4(0, 0, 0, 0);
+    pdl_wait();   // q comes from the QKV kernel
+    epi_sync_t();
+    for (int i = tid; i < G * HD; i += 128) {
+      const int h = i / HD, d = i - h * HD;
+      const float v = qb[(size_t)(h0 + h) * HD + d] * a.qscale;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      uint8_t *tile = Q + (d >> 6) * 2048;
+      *reinterpret_cast<__nv_bfloat16 *>(tile + sw128(h, (d & 63) * 2)) = hi;
+      *reinterpret_cast<__nv_bfloat16 *>(tile + sw128(8 + h, (d & 63) * 2)) = lo;
+    }
+    fence_async_smem();
+    epi_sync_t();
+    if (lane == 0) mbar_arrive(bar.q_ready);
+    if (tid == 0) ktrace(a.tr, 1);
+    // P tiles: only rows h and 8 + h are ever written; the rest must be zero
+    // (first used by the first P V product, after this CTA's first softmax)
+    for (int i = tid * 16; i < 2 * PT; i += 128 * 16) *reinterpret_cast<uint4 *>(P + i) = make_uint4(0, 0, 0, 0);
+    fence_async_smem();
+    epi_sync_t();
+
+    // Online softmax with a reference max per head that only moves when a
+    // tile's max exceeds it by more than 2^8: P = exp2(s - ref) stays below
+    // 256, sums stay per thread, and O (in TMEM) is rescaled only on a move.
+    constexpr float kTau = 8.f;
+    float m[G], l[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      if (ok && !mbar_wait(bar.s_full, t & 1)) {
+        ok = false;
+        if (lane == 0) set_error(err, kErrTimeout);
+      }
+      float v[32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(t_s + ((uint32_t)(32 * q) << 16), v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.s_empty);
+      const int p = (tb + t) * kTile + 32 * q + lane;
+      const bool valid = p >= lo && p <= pos;
+      float sc[G];
+      float *rm = red + (t & 1) * 32;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        sc[h] = valid ? v[h] + v[8 + h] : -INFINITY;
+        const float mx = warp_max(sc[h]);
+        if (lane == 0) rm[q * 8 + h] = mx;
+      }
+      epi_sync_t();
+      bool move = false;
+      float scale[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mt = fmaxf(fmaxf(rm[h], rm[8 + h]), fmaxf(rm[16 + h], rm[24 + h]));
+        scale[h] = 1.f;
+        if (mt > m[h] + kTau) {
+          scale[h] = m[h] == -INFINITY ? 0.f : exp2f(m[h] - mt);
+          m[h] = mt;
+          l[h] *= scale[h];
+          move = true;
+        }
+      }
+      if (t > 0 && (VT || q == 0)) {
+        // the previous tile's P V product is done: o_full is consumed phase by
+        // phase (before this tile's P is published, so at most one phase is
+        // ever pending and the parity wait cannot alias); then rescale O if
+        // the reference max moved
+        if (ok && !mbar_wait(bar.o_full, (t - 1) & 1)) {
+          ok = false;
+          if (lane == 0) set_error(err, kErrTimeout);
+        }
+        if (VT && ok && move) {
+          // O^T: this thread's lane is a dim; column h / 8 + h is head h
+          tc_fence_after();
+          float w[32];
+          tmem_ld32(t_o + ((uint32_t)(32 * q) << 16), w);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            w[h] *= scale[h];
+            w[8 + h] *= scale[h];
+          }
+          tmem_st32(t_o + ((uint32_t)(32 * q) << 16), w);
+          tc_fence_before();
+        } else if (!VT && ok && move) {
+          tc_fence_after();
+          float al = 1.f;
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            if ((lane & 7) == h) al = scale[h];
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float w[32];
+            tmem_ld32(t_o + 32 * c, w);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] *= al;
+            tmem_st32(t_o + 32 * c, w);
+          }
+          tc_fence_before();
+        }
+      }
+      float pp[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        pp[h] = (valid && m[h] != -INFINITY) ? exp2f(sc[h] - m[h]) : 0.f;
+        l[h] += pp[h];
+      }
+      // P of this tile into buffer t & 1, once the P V product of tile t - 2 is done
+      if (t >= 2 && ok && !mbar_wait(&bar.p_empty[t & 1], ((t >> 1) - 1) & 1)) {
+        ok = false;
+        if (lane == 0) set_error(err, kErrTimeout);
+      }
+      uint8_t *pt = P + (size_t)(t & 1) * PT + ((32 * q + lane) >> 6) * PCH;
+      const int cb = ((32 * q + lane) & 63) * 2;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(pp[h]);
+        const __nv_bfloat16 lo2 = __float2bfloat16_rn(pp[h] - __bfloat162float(hi));
+        *reinterpret_cast<__nv_bfloat16 *>(pt + sw128(h, cb)) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(pt + sw128(8 + h, cb)) = lo2;
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.p_full[t & 1]);
+    }
+    if (threadIdx.x == 128) ktrace(a.tr, 3);
+    // row sums over the CTA's positions (fixed order: lanes, then warps)
+    float *rs = red + 64;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float sw = warp_sum(l[h]);
+      if (lane == 0) rs[q * 8 + h] = sw;
+    }
+    epi_sync_t();
+#pragma unroll
+    for (int h = 0; h < G; ++h) l[h] = rs[h] + rs[8 + h] + rs[16 + h] + rs[24 + h];
+    if constexpr (VT) {
+      // O^T: thread = dim d, columns h / 8 + h = high / low parts of head h
+      float oh[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) oh[h] = 0.f;
+      if (ntiles > 0) {
+        if (ok && !mbar_wait(bar.o_full, (ntiles - 1) & 1)) {
+          ok = false;
+          if (lane == 0) set_error(err, kErrTimeout);
+        }
+        if (ok) {
+          tc_fence_after();
+          float w[32];
+          tmem_ld32(t_o + ((uint32_t)(32 * q) << 16), w);
+#pragma unroll
+          for (int h = 0; h < G; ++h) oh[h] = w[h] + w[8 + h];
+        }
+      }
+      const int d = 32 * q + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const size_t col = (size_t)(h0 + h) * HD + d;
+        if (a.n_split == 1) {
+          const float x = l[h] > 0.f ? oh[h] / l[h] : 0.f;
+          if (a.xop) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+            a.xop[(size_t)b * a.xop_ld + col] = hi;
+            a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+          } else {
+            a.out[col] = x;
+          }
+        } else {
+          float *Pp = part + ((size_t)(h0 + h) * a.n_split + split) * (HD + 2);
+          Pp[2 + d] = oh[h];
+          if (d == 0) {
+            Pp[0] = m[h];
+            Pp[1] = l[h];
+          }
+        }
+      }
+    } else {
+      float o[HD];   // warp 4 (TMEM lanes 0-31): row lane of O
+  #pragma unroll
+      for (int d = 0; d < HD; ++d) o[d] = 0.f;
+      if (q == 0 && ntiles > 0) {
+        if (ok && !mbar_wait(bar.o_full, (ntiles - 1) & 1)) {
+          ok = false;
+          if (lane == 0) set_error(err, kErrTimeout);
+        }
+        if (ok) {
+          tc_fence_after();
+  #pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float w[32];
+            tmem_ld32(t_o + 32 * c, w);
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) o[32 * c + i] = w[i];
+          }
+        }
+      }
+      // (max, sum, O) per head: lane h adds its low-part row 8 + h; with one split
+      // this is the output, else a partial for the merge
+      if (q == 0) {
+  #pragma unroll
+        for (int d = 0; d < HD; ++d) o[d] += __shfl_down_sync(0xffffffffu, o[d], 8);
+        if (lane < G) {
+          float mh = 0.f, lh = 0.f;
+  #pragma unroll
+          for (int h = 0; h < G; ++h)
+            if (lane == h) {
+              mh = m[h];
+              lh = l[h];
+            }
+          if (a.n_split == 1) {
+            const float inv = lh > 0.f ? 1.f / lh : 0.f;
+            const size_t row = (size_t)(h0 + lane) * HD;
+            if (a.xop) {
+  #pragma unroll
+              for (int d = 0; d < HD; ++d) {
+                const float x = o[d] * inv;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+                a.xop[(size_t)b * a.xop_ld + row + d] = hi;
+                a.xop[(size_t)(a.bp + b) * a.xop_ld + row + d] = __float2bfloat16_rn(x - __bfloat162float(hi));
+              }
+            } else {
+  #pragma unroll
+              for (int d = 0; d < HD; d += 4)
+                *reinterpret_cast<float4 *>(a.out + row + d) =
+                    make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+            }
+          } else {
+            float *Pp = part + ((size_t)(h0 + lane) * a.n_split + split) * (HD + 2);
+            Pp[0] = mh;
+            Pp[1] = lh;
+  #pragma unroll
+            for (int d = 0; d < HD; ++d) Pp[2 + d] = o[d];
+          }
+        }
+      }
+    }
+    if (threadIdx.x == 128) ktrace(a.tr, 4);
+    if (a.n_split > 1) {
+      __threadfence();
+      epi_sync_t();
+      if (tid == 0) *flag = atomicAdd(&counter[g], 1u) == (unsigned)a.n_split - 1u;
+      epi_sync_t();
+      if (*flag) {
+        __threadfence();
+        const int ns = a.n_split;
+        for (int idx = tid; idx < G * HD; idx += 128) {
+          const int h = idx / HD, d = idx - h * HD;
+          const float *P0 = part + (size_t)(h0 + h) * ns * (HD + 2);
+          float M = -INFINITY, Ls = 0.f, Os = 0.f;
+          for (int s0 = 0; s0 < ns; s0 += 8) {
+            float pm[8], pl[8], po[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float *Pj = P0 + (size_t)(s0 + j < ns ? s0 + j : 0) * (HD + 2);
+              pm[j] = __ldcg(Pj);
+              pl[j] = __ldcg(Pj + 1);
+              po[j] = __ldcg(Pj + 2 + d);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (s0 + j >= ns || pm[j] == -INFINITY) continue;
+              const float Mn = fmaxf(M, pm[j]);
+              const float f0 = exp2f(M - Mn), f1 = exp2f(pm[j] - Mn);
+              Ls = Ls * f0 + pl[j] * f1;
+              Os = Os * f0 + po[j] * f1;
+              M = Mn;
+            }
+          }
+          const float x = Ls > 0.f ? Os / Ls : 0.f;
+          const size_t col = (size_t)(h0 + h) * HD + d;
+          if (a.xop) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+            a.xop[(size_t)b * a.xop_ld + col] = hi;
+            a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+          } else {
+            a.out[col] = x;
+          }
+        }
+        if (tid == 0) counter[g] = 0u;
+      }
+    }
+  }
+  if (threadIdx.x == 0) ktrace(a.tr, 5);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(taddr, TCOLS);
+}
+
+template <int HD, int G>
+cudaError_t launch_g(const AttnTcArgs &a, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_split, a.n_kv, a.slots ? a.nb : 1);
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = attn_tc_smem(HD, a.nstages);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_attn_tc<HD, G>, a);
+}
+
+template <int HD>
+cudaError_t launch_hd_tc(int G, const AttnTcArgs &a, cudaStream_t st, bool pdl) {
+  switch (G) {
+    case 1: return launch_g<HD, 1>(a, st, pdl);
+    case 2: return launch_g<HD, 2>(a, st, pdl);
+    case 4: return launch_g<HD, 4>(a, st, pdl);
+    case 8: return launch_g<HD, 8>(a, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int HD>
+cudaError_t prepare_hd_tc() {
+  const int smem = attn_tc_smem(HD, attn_tc_stages(HD));
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_attn_tc<HD, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_attn_tc<HD, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_attn_tc<HD, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_attn_tc<HD, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace
+
+int attn_tc_stages(int head_dim) { return 3; }
+
+int attn_tc_smem(int head_dim, int nstages) {
+  const int stage = 2 * (head_dim / 64) * kBox;
+  const int p_tiles = head_dim == 128 ? 2 * 2 * 2048 : 2 * 2 * kBox;
+  return 1024 + nstages * stage + p_tiles + (head_dim / 64) * 2048 + 1024;
+}
+
+cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl) {
+  if (head_dim == 128) return launch_hd_tc<128>(group, a, st, pdl);
+  if (head_dim == 64) return launch_hd_tc<64>(group, a, st, pdl);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_attn_tc_kernels() {
+  cudaError_t e = prepare_hd_tc<128>();
+  if (e != cudaSuccess) return e;
+  return prepare_hd_tc<64>();
+}
+
+}  // namespace pnb

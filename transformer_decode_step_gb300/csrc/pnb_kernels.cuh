@@ -208,9 +208,36 @@ struct AttnArgs {
 
 // One slot of a batched step (device table, written at the start of the step).
 struct BSlot {
-  uint8_t *kv;   // the slot's KV buffer [layer][K|V][n_kv][cap][hd]
-  StepIO *io;    // the slot's token / position / error word
+  uint8_t *kv;        // the slot's KV buffer [layer][K|V][n_kv][cap][hd]
+  StepIO *io;         // the slot's token / position / error word
+  const void *maps;   // the slot's [layer][K|V] tensor maps over that buffer (or null)
 };
+
+// Tensor-core decode attention (bf16 KV, head_dim 64 or 128, up to 8 query
+// heads per KV head).  Grid (n_split, n_kv, slots); a CTA takes one KV head of
+// one slot and 128-position tiles of its range.
+struct AttnTcArgs {
+  const float *q;          // [slots][n_head][hd]
+  const void *maps;        // one sequence: its state's [layer][K|V] tensor maps
+  int layer;
+  int n_head, n_kv, cap, window, n_split;
+  float qscale;            // log2(e) / sqrt(hd)
+  float *part;             // [slots][n_head][n_split][hd + 2]
+  unsigned *counter;       // [slots][n_kv], zero between launches
+  float *out;              // one sequence: [n_head][hd]
+  __nv_bfloat16 *xop;      // batched: o-proj operand rows b (hi) and bp + b (lo)
+  int xop_ld, bp, nb;
+  const BSlot *slots;      // batched (null for one sequence)
+  const int32_t *pos;      // batched positions
+  StepIO *io;              // one sequence
+  int nstages;
+  KTrace tr;
+};
+
+cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl);
+int attn_tc_smem(int head_dim, int nstages);
+int attn_tc_stages(int head_dim);
+cudaError_t prepare_attn_tc_kernels();
 
 // Epilogues of the batched tensor-core GEMM
 enum BEpi { kEpiQkv = 0, kEpiResid = 1, kEpiGateUp = 2, kEpiLm = 3 };
