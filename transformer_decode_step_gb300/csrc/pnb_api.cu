@@ -775,6 +775,7 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
     g.layer_kv_bytes = layer_kv;
     if ((e = launch_bgemm(&b->w_qkv[l], &b->x_e[bi], g, b->p_qkv.grid, smem, st, true)) != cudaSuccess)
       return e;
+    if (g.ksplit > 1 && (e = launch_bmerge(g, st, true)) != cudaSuccess) return e;
     if (m->attn_tc) {
       AttnTcArgs ta{};
       ta.q = b->qb;
@@ -836,6 +837,7 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
     g.xop_ld = F;
     if ((e = launch_bgemm(&b->w_gu[l], &b->x_e[bi], g, b->p_gu.grid, smem, st, true)) != cudaSuccess)
       return e;
+    if (g.ksplit > 1 && (e = launch_bmerge(g, st, true)) != cudaSuccess) return e;
     g = bgemm_args(m, b, b->p_dn, kEpiResid, B, bp);
     g.tr = KTrace{trace, 7 * l + 6};
     g.x = b->xb;
@@ -1288,7 +1290,13 @@ int pnb_model_set_graphs(pnb_model *m, int enable) {
 
 int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
   if (!m) return PNB_E_NULL;
-  if (B > 0) return m->cfg.n_layer * 7 + 2;   // batched: norm, QKV, attention, o, norm, gate/up, down
+  if (B > 0) {
+    // batched: norm, QKV (+ merge of its K parts), attention, o, norm, gate/up
+    // (+ merge), down per layer; final norm and LM head
+    const int merges = (plan_bgemm(m->qkv_rows, m->cfg.n_embd, m->num_sms).ksplit > 1) +
+                       (plan_bgemm(2 * (int64_t)m->cfg.n_ff, m->cfg.n_embd, m->num_sms).ksplit > 1);
+    return m->cfg.n_layer * (7 + merges) + 2;
+  }
   if (m->persistent) return 1;
   const int per_layer = m->cfg.expert_count > 0 ? 6 : 5;
   return m->cfg.n_layer * per_layer + 1;

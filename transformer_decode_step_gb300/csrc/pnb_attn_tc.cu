@@ -538,9 +538,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
       }
     }
   }
-  if (threadIdx.x == 0) ktrace(a.tr, 5);
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) ktrace(a.tr, 5);
   if (warp == 1) tmem_dealloc(taddr, TCOLS);
 }
 

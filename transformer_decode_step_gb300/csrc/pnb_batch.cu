@@ -218,40 +218,66 @@ struct UnitChunks {
 
 // the epilogue of one 128-row tile: thread owns row `row` of tile `tile`;
 // y[b] = (W x_b)[row] for b < B
+// The epilogue of one 128-row tile: thread owns row `row` of tile `tile`;
+// y[b] = (W x_b)[row] for b < B.  Slots go in chunks of 16 whose loads are all
+// issued before any of the chunk's stores (stores and loads may alias, so the
+// compiler would otherwise keep one round trip per slot).
+constexpr int kEpiChunk = 16;
+
 template <int BP, int KIND>
 __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, const float (&y)[BP],
                                          float (&bv)[BP], int (&bi)[BP]) {
   const int grow = tile * 128 + row;
   const bool in = grow < a.rows;
   if constexpr (KIND == kEpiResid) {
-    if (in) {
 #pragma unroll
-      for (int b = 0; b < BP; ++b)
-        if (b < a.B) a.x[(size_t)b * a.rows + grow] += y[b];
+    for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
+      float xv[kEpiChunk];
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j)
+        xv[j] = (in && c0 + j < a.B) ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j)
+        if (in && c0 + j < a.B) a.x[(size_t)(c0 + j) * a.rows + grow] = xv[j] + y[c0 + j];
     }
   } else if constexpr (KIND == kEpiQkv) {
     const int hd = a.hd, half = hd / 2;
     const int qrows = a.n_head * hd, krows = a.n_kv * hd;
     const bool even = (grow & 1) == 0;
+    const bool rope = grow < qrows + krows;
+    const bool is_q = grow < qrows, is_k = !is_q && rope;
+    const int kx = grow - qrows - (is_k ? 0 : krows);
+    const int gk = kx / hd, d = kx - gk * hd;
+    const int pair = (grow % hd) >> 1;
 #pragma unroll
-    for (int b = 0; b < BP; ++b) {
-      const float par = __shfl_xor_sync(0xffffffffu, y[b], 1);
-      if (b < a.B && in) {
+    for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
+      float par[kEpiChunk];
+      float2 cs[kEpiChunk];
+      int slot[kEpiChunk];
+      uint8_t *base[kEpiChunk];
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j) {
+        const int b = c0 + j;
+        par[j] = __shfl_xor_sync(0xffffffffu, y[b], 1);
+        const bool live = in && b < a.B;
+        cs[j] = (live && rope) ? a.rope[(size_t)b * half + pair] : make_float2(1.f, 0.f);
+        slot[j] = (live && !is_q) ? a.pos[b] : 0;
+        base[j] = (live && !is_q) ? a.slots[b].kv : nullptr;
+      }
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j) {
+        const int b = c0 + j;
+        if (!(in && b < a.B)) continue;
         float v = y[b];
-        if (grow < qrows + krows) {
-          const float2 cs = a.rope[(size_t)b * half + ((grow % hd) >> 1)];
-          const float v0 = even ? y[b] : par, v1 = even ? par : y[b];
-          v = even ? v0 * cs.x - v1 * cs.y : v0 * cs.y + v1 * cs.x;
+        if (rope) {
+          const float v0 = even ? y[b] : par[j], v1 = even ? par[j] : y[b];
+          v = even ? v0 * cs[j].x - v1 * cs[j].y : v0 * cs[j].y + v1 * cs[j].x;
         }
-        if (grow < qrows) {
+        if (is_q) {
           a.q[(size_t)b * qrows + grow] = v;
         } else {
-          const bool is_k = grow < qrows + krows;
-          const int kx = grow - qrows - (is_k ? 0 : krows);
-          const int gk = kx / hd, d = kx - gk * hd;
-          const int slot = a.pos[b] % a.cap;
-          uint8_t *base = a.slots[b].kv + a.kv_off + (is_k ? 0 : a.layer_kv_bytes);
-          reinterpret_cast<__nv_bfloat16 *>(base)[((size_t)gk * a.cap + slot) * hd + d] =
+          uint8_t *kvb = base[j] + a.kv_off + (is_k ? 0 : a.layer_kv_bytes);
+          reinterpret_cast<__nv_bfloat16 *>(kvb)[((size_t)gk * a.cap + slot[j] % a.cap) * hd + d] =
               __float2bfloat16_rn(v);
         }
       }
@@ -435,6 +461,21 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
       const int tile = u / a.ksplit;
       if (a.ksplit == 1) {
         epilogue<BP, KIND>(a, tile, row, y, bv, bi);
+      } else if constexpr (KIND == kEpiResid) {
+        // a residual update is a sum: each K part adds its share with a
+        // fire-and-forget fp32 reduction (summation order not fixed)
+        const int grow = tile * 128 + row;
+        if (grow < a.rows) {
+#pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < a.B) atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
+        }
+      } else if constexpr (KIND == kEpiQkv || KIND == kEpiGateUp) {
+        // partial tile only: k_bmerge sums the K parts and applies the epilogue
+        float *P = a.part + (size_t)u * a.B * 128;
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+          if (b < a.B) P[(size_t)b * 128 + row] = y[b];
       } else {
         float *P = a.part + (size_t)u * a.B * 128;
 #pragma unroll
@@ -496,9 +537,19 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         if (row < a.B) {
           float v = -FLT_MAX;
           int i = INT_MAX;
-          for (int c = 0; c < (int)gridDim.x; ++c)
-            am_merge(v, i, __ldcg(a.am_val + (size_t)row * gridDim.x + c),
-                     __ldcg(a.am_idx + (size_t)row * gridDim.x + c));
+          for (int c0 = 0; c0 < (int)gridDim.x; c0 += 16) {
+            float cv[16];
+            int ci[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int c = c0 + j < (int)gridDim.x ? c0 + j : c0;
+              cv[j] = __ldcg(a.am_val + (size_t)row * gridDim.x + c);
+              ci[j] = __ldcg(a.am_idx + (size_t)row * gridDim.x + c);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < (int)gridDim.x) am_merge(v, i, cv[j], ci[j]);
+          }
           StepIO *io = a.slots[row].io;
           if (i < 0 || i >= a.rows) {
             set_error(&io->error, kErrToken);
@@ -514,10 +565,67 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
       }
     }
   }
-  if (threadIdx.x == 0) ktrace(a.tr, 5);
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) ktrace(a.tr, 5);
   if (warp == 1) tmem_dealloc(taddr, TCOLS);
+}
+
+// The K parts of a split QKV or gate/up GEMM, summed in a fixed order, and
+// the fused epilogue: one thread per (row pair, slot).  Partial tiles are
+// [tile * ksplit + k][slot][128 rows].
+template <int KIND>
+__global__ void __launch_bounds__(256) k_bmerge(const BGemmArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int npair = a.rows / 2;
+  const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (idx >= (int64_t)npair * a.B) return;
+  const int b = (int)(idx / npair), pr = (int)(idx - (int64_t)b * npair);
+  const int r = 2 * pr, tile = r >> 7, i = r & 127;
+  float2 s = make_float2(0.f, 0.f);
+  for (int k0 = 0; k0 < a.ksplit; k0 += 4) {
+    float2 t[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int k = k0 + j < a.ksplit ? k0 + j : k0;
+      t[j] = __ldcg(reinterpret_cast<const float2 *>(
+          a.part + (((size_t)tile * a.ksplit + k) * a.B + b) * 128 + i));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (k0 + j < a.ksplit) {
+        s.x += t[j].x;
+        s.y += t[j].y;
+      }
+  }
+  if constexpr (KIND == kEpiQkv) {
+    const int hd = a.hd, qrows = a.n_head * hd, krows = a.n_kv * hd;
+    float v0 = s.x, v1 = s.y;
+    if (r < qrows + krows) {
+      const float2 cs = a.rope[(size_t)b * (hd / 2) + ((r % hd) >> 1)];
+      const float t0 = v0 * cs.x - v1 * cs.y, t1 = v0 * cs.y + v1 * cs.x;
+      v0 = t0;
+      v1 = t1;
+    }
+    if (r < qrows) {
+      *reinterpret_cast<float2 *>(a.q + (size_t)b * qrows + r) = make_float2(v0, v1);
+    } else {
+      const bool is_k = r < qrows + krows;
+      const int kx = r - qrows - (is_k ? 0 : krows);
+      const int gk = kx / hd, d = kx - gk * hd;
+      uint8_t *base = a.slots[b].kv + a.kv_off + (is_k ? 0 : a.layer_kv_bytes);
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(base) +
+                           ((size_t)gk * a.cap + a.pos[b] % a.cap) * hd + d;
+      dst[0] = __float2bfloat16_rn(v0);
+      dst[1] = __float2bfloat16_rn(v1);
+    }
+  } else {
+    const float h = silu_b(s.x) * s.y;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+    a.xop[(size_t)b * a.xop_ld + pr] = hi;
+    a.xop[(size_t)(a.bp + b) * a.xop_ld + pr] = __float2bfloat16_rn(h - __bfloat162float(hi));
+  }
 }
 
 template <int BP, int KIND>
@@ -576,6 +684,22 @@ cudaError_t launch_bgemm(const void *tmap_w, const void *tmap_x, const BGemmArgs
     case 64: return launch_bp<64>(tmap_w, tmap_x, a, grid, smem, st, pdl);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_bmerge(const BGemmArgs &a, cudaStream_t st, bool pdl) {
+  const int64_t n = (int64_t)(a.rows / 2) * a.B;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (a.kind == kEpiQkv) return cudaLaunchKernelEx(&cfg, k_bmerge<kEpiQkv>, a);
+  if (a.kind == kEpiGateUp) return cudaLaunchKernelEx(&cfg, k_bmerge<kEpiGateUp>, a);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t prepare_bgemm_kernels(int smem_bytes) {

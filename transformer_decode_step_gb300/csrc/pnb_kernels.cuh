@@ -319,6 +319,8 @@ cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_bgemm(const void *tmap_w, const void *tmap_x, const BGemmArgs &a, int grid,
                          int smem, cudaStream_t st, bool pdl);
 int bgemm_smem(int bp, int nstages);
+// sums the K parts of a split QKV / gate-up GEMM and applies its epilogue
+cudaError_t launch_bmerge(const BGemmArgs &a, cudaStream_t st, bool pdl);
 cudaError_t prepare_bgemm_kernels(int smem_bytes);
 
 // persistent step kernel (one cooperative launch per decode step); with
