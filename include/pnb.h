@@ -184,7 +184,8 @@ int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, fl
    1e-5 relative (not bitwise).  Supported: bf16 dense models with n_embd,
    n_head * head_dim and n_ff multiples of 64; MoE and fp32 models return
    PNB_E_UNSUPPORTED (as the pages' batched decoder returns -1 for MoE and
-   F32).  PNB_E_CTX_FULL when any slot's pos already reached n_ctx; a token
+   F32).  B = 1 runs the single-sequence step (the faster path for one
+   slot).  PNB_E_CTX_FULL when any slot's pos already reached n_ctx; a token
    outside [0, n_vocab) sets PNB_DEV_ERR_TOKEN in that slot's state.  The
    first call allocates the model's batched workspace (make it before any
    stream capture). */

@@ -1214,6 +1214,13 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
     if (states[i]->pos >= c.n_ctx) return PNB_E_CTX_FULL;
   int rc = check_device(m);
   if (rc != PNB_OK) return rc;
+  if (B == 1) {
+    // one slot: the single-sequence step (weight-streaming GEMVs) is the faster
+    // way through a batch of one; the slot's token is copied on the device
+    cudaStream_t st1 = reinterpret_cast<cudaStream_t>(stream);
+    if (tokens_dev && launch_copy_token(states[0]->io, tokens_dev, st1) != cudaSuccess) return PNB_E_CUDA;
+    return pnb_forward(m, states[0], PNB_TOKEN_PREV, stream, logits_dev, argmax_dev);
+  }
   if ((rc = batch_setup(m)) != PNB_OK) return rc;
   BatchCtx *b = m->batch;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -1290,7 +1297,8 @@ int pnb_model_set_graphs(pnb_model *m, int enable) {
 
 int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
   if (!m) return PNB_E_NULL;
-  if (B > 0) {
+  if (B == 1) return pnb_step_kernel_count(m, 0) + 1;   // token copy + the single-sequence step
+  if (B > 1) {
     // batched: norm, QKV (+ merge of its K parts), attention, o, norm, gate/up
     // (+ merge), down per layer; final norm and LM head
     const int merges = (plan_bgemm(m->qkv_rows, m->cfg.n_embd, m->num_sms).ksplit > 1) +

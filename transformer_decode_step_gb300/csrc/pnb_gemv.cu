@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(256, 1) k_router(const RouterArgs a) {
 }
 
 __global__ void k_set_token(StepIO *io, int32_t token) { io->token = token; }
+__global__ void k_copy_token(StepIO *io, const int32_t *token) { io->token = *token; }
 __global__ void k_set_pos(StepIO *io, int32_t pos) { io->pos = pos; }
 
 template <typename Kern, typename Args>
@@ -367,6 +368,10 @@ cudaError_t prepare_gemv_kernels(int dtype, int smem_bytes) {
 }
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st) {
   k_set_token<<<1, 1, 0, st>>>(io, token);
+  return cudaGetLastError();
+}
+cudaError_t launch_copy_token(StepIO *io, const int32_t *token, cudaStream_t st) {
+  k_copy_token<<<1, 1, 0, st>>>(io, token);
   return cudaGetLastError();
 }
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st) {

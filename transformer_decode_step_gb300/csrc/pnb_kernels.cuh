@@ -313,6 +313,7 @@ cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGe
                         cudaStream_t st, bool pdl);
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st);
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st);
+cudaError_t launch_copy_token(StepIO *io, const int32_t *token, cudaStream_t st);
 
 // batched step (tensor maps are CUtensorMap, passed by value)
 cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl);
