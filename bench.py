@@ -225,14 +225,15 @@ def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0, star
 
 # ------------------------------------------------------------------ main arms
 
-def workload_config(w, extra=None):
+def workload_config(w, extra=None, batch=None):
     s = w.shape
+    batch = batch or w.batch or 1
     cfg = {"workload": f"{w.name}: E{s.n_embd} H{s.n_head} Hkv{s.n_kv_head} L{s.n_layer} "
                        f"F{s.n_ff} V{s.n_vocab} theta{s.rope_theta:g}"
                        + (f" window{s.sliding_window}" if s.sliding_window else "")
                        + (f" experts{s.expert_count}top{s.expert_used}" if s.expert_count else "")
-                       + f", KV pre-filled to {w.prefill}, greedy decode of {w.steps} tokens, batch {w.batch if w.batch else 1}",
-           "batch": 1, "weights_dtype": "bf16" if s.dtype == 1 else "f32",
+                       + f", KV pre-filled to {w.prefill}, greedy decode of {w.steps} tokens, batch {batch}",
+           "batch": batch, "weights_dtype": "bf16" if s.dtype == 1 else "f32",
            "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)"}
     if extra:
         cfg.update(extra)
@@ -253,7 +254,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, batch=args.batch),
             "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": f"{n} per-token units ({L} layers + LM head, rotated) of the "
                                        f"workload's first decode step, {dt:.1f} s"},
@@ -512,8 +513,8 @@ def run_batched(args, w):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded generated weights and KV cache)",
-                "config": workload_config(w, {"batch": B, "parallelism": f"replicas x{world}",
-                                              "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"}),
+                "config": workload_config(w, {"parallelism": f"replicas x{world}",
+                                              "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"}, batch=B),
                 "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"], "bytes_per_step": mean_bytes,
                 "roofline": {"bound": "hbm", "kernel": "whole batched step (weights once + every slot's KV)",

@@ -45,11 +45,13 @@ Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int g
   rps = std::max(rps, row_align);   // row pairs never straddle two ring items
   g.rows_per_stage = rps;
   g.stage_bytes = rps * g.row_bytes;
-  // warps per row: enough that a lane holds at most 4 column vectors, and no
-  // more row groups than rows per ring slot
+  // warps per row: as many as the row has 32-lane column groups (up to all
+  // sixteen), so that each activation element is loaded by one lane of the
+  // CTA only: the load after griddepcontrol.wait shares the SM's ingress with
+  // the weight ring, and its latency grows with its volume
   const int vpr = g.row_bytes / 16;
   int cw = 1;
-  while (cw < kGemvWarps && (cw * 32 * 4 < vpr || kGemvWarps / cw > rps)) cw *= 2;
+  while (cw < kGemvWarps && (cw * 2 * 32 <= vpr || kGemvWarps / cw > rps)) cw *= 2;
   g.cw = cw;
   const int nv = ceil_div(vpr, 32 * cw);
   g.nv = nv <= 1 ? 1 : (nv <= 2 ? 2 : (nv <= 4 ? 4 : 8));  // 8 = unsupported
@@ -98,6 +100,11 @@ struct pnb_model {
   // tensor-core attention (bf16 KV, head_dim 64 / 128, <= 8 query heads per KV head)
   bool attn_tc_ok = false, attn_tc = false;
   int n_split_tc = 1;
+  // fused attention block (one cluster per query head): geometry, per-layer Wo maps
+  bool block_ok = false, block = false;
+  BlockGeom bgeom{};
+  int block_clusters = 0;                // clusters that fit on the GPU at once
+  std::vector<CUtensorMap> wo_maps;
   int mode_gen = 0;                      // bumped when a launch mode changes (graphs re-captured)
   // persistent step kernel
   bool persistent = false;
@@ -144,6 +151,7 @@ struct pnb_state {
   StepIO *io = nullptr;
   float *x = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *part = nullptr;
   float *gate = nullptr, *lm_val = nullptr;
+  long long *acc = nullptr;              // [n_embd] attention-output accumulator (2^-32 units)
   int32_t *idx = nullptr, *lm_idx = nullptr;
   unsigned *attn_cnt = nullptr, *lm_cnt = nullptr;
   size_t counters_off = 0, counters_bytes = 0;
@@ -271,7 +279,9 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
   const float eps = (float)c.rms_norm_eps;
   const bool moe = c.expert_count > 0;
   const int k = moe ? c.expert_used : 1;
-  const KTrace tr{s->ktrace, kind == PNB_KERNEL_LM_HEAD ? 6 * c.n_layer : 6 * l + kind};
+  const KTrace tr{s->ktrace, kind == PNB_KERNEL_LM_HEAD    ? 6 * c.n_layer
+                            : kind == PNB_KERNEL_ATTN_BLOCK ? 6 * l
+                                                            : 6 * l + kind};
   unsigned *work = s->work + 2 * tr.phase;
   switch (kind) {
     case PNB_KERNEL_QKV: {
@@ -299,6 +309,32 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       qa.tr = tr;
       qa.work = work;
       return launch_qkv(c.dtype, qa, m->grid, st, pdl);
+    }
+    case PNB_KERNEL_ATTN_BLOCK: {
+      if (!m->block_ok) return cudaErrorInvalidValue;
+      BlockArgs ba{};
+      ba.b = m->bgeom;
+      ba.H = H;
+      ba.Hkv = Hkv;
+      ba.cap = m->cap;
+      ba.window = c.sliding_window;
+      ba.wqkv = m->wqkv[l];
+      ba.x = s->x;
+      ba.emb = l == 0 ? m->tok_embd : nullptr;
+      ba.x_out = s->x;
+      ba.n_vocab = c.n_vocab;
+      ba.norm_w = m->attn_norm[l];
+      ba.eps = eps;
+      ba.inv_freq = m->inv_freq;
+      ba.k_cache = kc;
+      ba.v_cache = vc;
+      ba.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
+      ba.acc = s->acc;
+      ba.q_out = s->q;
+      ba.o_out = s->attn;
+      ba.io = s->io;
+      ba.tr = tr;
+      return launch_attn_block(c.dtype, hd, &m->wo_maps[l], ba, st, pdl);
     }
     case PNB_KERNEL_ATTN: {
       if (m->attn_tc) {
@@ -360,6 +396,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ra.k = k;
       ra.E = E;
       ra.x = s->x;
+      ra.acc = m->block ? s->acc : nullptr;
       ra.norm_w = m->ffn_norm[l];
       ra.eps = eps;
       ra.idx = s->idx;
@@ -373,6 +410,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ga.g = m->g_gateup;
       ga.s.rows = 2 * (int64_t)F;
       ga.x = s->x;
+      ga.acc = m->block ? s->acc : nullptr;
       ga.norm_w = m->ffn_norm[l];
       ga.eps = eps;
       ga.h = s->h;
@@ -398,6 +436,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
         da.s.w[0] = m->w_down[l];
         da.vec = s->h;
         da.x = s->x;
+        da.acc = m->block ? s->acc : nullptr;
         da.io = s->io;
         da.tr = tr;
         da.work = work;
@@ -413,6 +452,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       da.n_ff = F;
       da.gate = s->gate;
       da.x = s->x;
+      da.acc = m->block ? s->acc : nullptr;
       da.io = s->io;
       da.tr = tr;
       return launch_down_moe(c.dtype, da, m->grid, st, pdl);
@@ -506,12 +546,18 @@ cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *log
   const bool moe = m->cfg.expert_count > 0;
   cudaError_t e;
   for (int l = 0; l < m->cfg.n_layer; ++l) {
-    if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
-      return e;
-    if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN, l, st, true, nullptr, nullptr)) != cudaSuccess)
-      return e;
-    if ((e = enqueue_kernel(m, s, PNB_KERNEL_OPROJ, l, st, true, nullptr, nullptr)) != cudaSuccess)
-      return e;
+    if (m->block) {
+      if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN_BLOCK, l, st, l > 0, nullptr, nullptr)) !=
+          cudaSuccess)
+        return e;
+    } else {
+      if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
+        return e;
+      if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN, l, st, true, nullptr, nullptr)) != cudaSuccess)
+        return e;
+      if ((e = enqueue_kernel(m, s, PNB_KERNEL_OPROJ, l, st, true, nullptr, nullptr)) != cudaSuccess)
+        return e;
+    }
     if (moe && (e = enqueue_kernel(m, s, PNB_KERNEL_ROUTER, l, st, true, nullptr, nullptr)) !=
                    cudaSuccess)
       return e;
@@ -558,6 +604,56 @@ bool encode_map(CUtensorMap *map, const void *base, int64_t rows, int K, int box
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D tensor map over one layer's Wo [n_embd rows][H * hd columns] (bf16 or
+// fp32), boxes of hd columns x o_item rows, no swizzle: a box is one head's
+// column block of o_item rows, stored row after row.
+bool encode_wo_map(CUtensorMap *map, const void *base, int dtype, int E, int HHD, int hd, int o_item) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int es = dtype ? 2 : 4;
+  const cuuint64_t dims[2] = {(cuuint64_t)HHD, (cuuint64_t)E};
+  const cuuint64_t strides[1] = {(cuuint64_t)HHD * es};
+  const cuuint32_t box[2] = {(cuuint32_t)hd, (cuuint32_t)o_item};
+  const cuuint32_t el[2] = {1, 1};
+  return fn(map, dtype ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void *>(base), dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Geometry of the fused attention block: the largest cluster (<= 8 CTAs, a
+// power of two) with one cluster per query head on at most one CTA per SM,
+// 32 KB ring items of whole Wqkv rows / K and V positions / Wo rows.
+bool plan_block(pnb_model *m) {
+  const pnb_config &c = m->cfg;
+  const int hd = m->hd, H = c.n_head, E = c.n_embd, es = m->es;
+  if (!(hd == 32 || hd == 64 || hd == 128)) return false;
+  int C = 8;
+  while (C > 1 && H * C > m->num_sms) C >>= 1;
+  if (H * C > m->num_sms || E % C) return false;
+  BlockGeom b{};
+  b.C = C;
+  b.rows_cta = 3 * hd / C;
+  b.g = plan_gemv(E, es, 3 * hd, 1, 1, H * C, 1);
+  if (b.g.nv > 4) return false;
+  int kv = 64;
+  while (kv > 4 && 2 * kv * hd * es > kStageTarget) kv >>= 1;
+  b.kv_item = kv;
+  int oi = 256;
+  while (oi > 1 && ((E / C) % oi || oi * hd * es > kStageTarget)) oi >>= 1;
+  if (oi < 8) return false;
+  b.o_item = oi;
+  b.stage_bytes = align_up(std::max({b.g.rows_per_stage * b.g.row_bytes, 2 * kv * hd * es, oi * hd * es}), 1024);
+  b.nstages = 0;
+  const int fixed = block_smem(b, hd).total;
+  b.nstages = std::min(8, std::min(kRingBudget, kMaxSmem - fixed) / b.stage_bytes);
+  if (b.nstages < 2) return false;
+  b.smem = block_smem(b, hd).total;
+  if (b.smem > kMaxSmem) return false;
+  m->bgeom = b;
+  return true;
 }
 
 // Split of a GEMM over K so that (tiles x ksplit) units fill whole waves of
@@ -965,6 +1061,26 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
     m->persistent = false;
     if (m->attn_tc_ok) m->attn_tc_ok = encode_fn() != nullptr && prepare_attn_tc_kernels() == cudaSuccess;
     m->attn_tc = m->attn_tc_ok;
+    // the fused attention block (default where the model allows it)
+    if (plan_block(m) && encode_fn() != nullptr &&
+        prepare_attn_block_kernels(c.dtype, m->bgeom.smem) == cudaSuccess) {
+      m->block_clusters = attn_block_max_clusters(c.dtype, m->hd, m->bgeom, c.n_head);
+      bool maps_ok = m->block_clusters > 0;
+      try {
+        m->wo_maps.resize(c.n_layer);
+      } catch (...) {
+        maps_ok = false;
+      }
+      for (int l = 0; maps_ok && l < c.n_layer; ++l)
+        maps_ok = encode_wo_map(&m->wo_maps[l], m->wo[l], c.dtype, c.n_embd, c.n_head * m->hd, m->hd,
+                                m->bgeom.o_item);
+      m->block_ok = maps_ok;
+    }
+    cudaGetLastError();   // a declined option leaves no sticky launch error behind
+    // opt-in: with one cluster per query head the block runs on n_head * C
+    // SMs (128 of 152 for 32 heads), and on the 7B-class shapes the three
+    // per-phase kernels on every SM are the faster of the two
+    m->block = false;
   }
   if (!ok) {
     pnb_model_free(m);
@@ -1016,6 +1132,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   const size_t o_attn = take((size_t)c.n_head * m->hd * 4);
   const size_t o_h = take((size_t)k * c.n_ff * 4);
   const size_t o_part = take((size_t)c.n_head * std::max(m->n_split, m->n_split_tc) * (m->hd + 2) * 4);
+  const size_t o_acc = take((size_t)c.n_embd * 8);
   const size_t o_gate = take((size_t)k * 4);
   const size_t o_idx = take((size_t)k * 4);
   const size_t o_lmv = take((size_t)m->grid * 4);
@@ -1036,6 +1153,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   s->attn = reinterpret_cast<float *>(s->ws + o_attn);
   s->h = reinterpret_cast<float *>(s->ws + o_h);
   s->part = reinterpret_cast<float *>(s->ws + o_part);
+  s->acc = reinterpret_cast<long long *>(s->ws + o_acc);
   s->gate = reinterpret_cast<float *>(s->ws + o_gate);
   s->idx = reinterpret_cast<int32_t *>(s->ws + o_idx);
   s->lm_val = reinterpret_cast<float *>(s->ws + o_lmv);
@@ -1113,6 +1231,7 @@ int pnb_state_reset(pnb_state *s, pnb_stream stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(s->kv, 0, pnb_state_kv_bytes(s->m), st) != cudaSuccess ||
       cudaMemsetAsync(s->io, 0, sizeof(StepIO), st) != cudaSuccess ||
+      cudaMemsetAsync(s->acc, 0, (size_t)s->m->cfg.n_embd * 8, st) != cudaSuccess ||
       cudaMemsetAsync(s->ws + s->counters_off, 0, s->counters_bytes, st) != cudaSuccess)
     return PNB_E_CUDA;
   s->pos = 0;
@@ -1286,6 +1405,16 @@ int pnb_model_set_tensor_attention(pnb_model *m, int enable) {
 
 int pnb_model_is_tensor_attention(const pnb_model *m) { return m && m->attn_tc ? 1 : 0; }
 
+int pnb_model_set_fused_attention(pnb_model *m, int enable) {
+  if (!m) return PNB_E_NULL;
+  if (enable && !m->block_ok) return PNB_E_UNSUPPORTED;
+  if (m->block != (enable != 0)) ++m->mode_gen;
+  m->block = enable != 0;
+  return PNB_OK;
+}
+
+int pnb_model_is_fused_attention(const pnb_model *m) { return m && m->block ? 1 : 0; }
+
 int pnb_model_is_persistent(const pnb_model *m) { return m && m->persistent ? 1 : 0; }
 
 int pnb_model_set_graphs(pnb_model *m, int enable) {
@@ -1306,14 +1435,15 @@ int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
     return m->cfg.n_layer * (7 + merges) + 2;
   }
   if (m->persistent) return 1;
-  const int per_layer = m->cfg.expert_count > 0 ? 6 : 5;
+  const int per_layer = (m->block ? 1 : 3) + (m->cfg.expert_count > 0 ? 3 : 2);
   return m->cfg.n_layer * per_layer + 1;
 }
 
 int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb_stream stream) {
   if (!m || !s) return PNB_E_NULL;
   if (s->m != m) return PNB_E_INVAL;
-  if (kind < PNB_KERNEL_QKV || kind > PNB_KERNEL_LM_HEAD) return PNB_E_INVAL;
+  if (kind < PNB_KERNEL_QKV || kind > PNB_KERNEL_ATTN_BLOCK) return PNB_E_INVAL;
+  if (kind == PNB_KERNEL_ATTN_BLOCK && !m->block_ok) return PNB_E_UNSUPPORTED;
   if (kind == PNB_KERNEL_ROUTER && m->cfg.expert_count == 0) return PNB_E_INVAL;
   if (layer < 0 || layer >= m->cfg.n_layer) return PNB_E_INVAL;
   int rc = check_device(m);

@@ -21,35 +21,6 @@ namespace {
 
 extern __shared__ __align__(128) uint8_t a_smem[];
 
-template <typename T, int N>
-__device__ __forceinline__ void load_vals(const T *p, float (&f)[N]) {
-  if constexpr (sizeof(T) == 2) {
-    if constexpr (N == 8) {
-      const uint4 u = *reinterpret_cast<const uint4 *>(p);
-      f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-      f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
-    } else if constexpr (N == 4) {
-      const uint2 u = *reinterpret_cast<const uint2 *>(p);
-      f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-    } else if constexpr (N == 2) {
-      const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
-      f[0] = bf16lo(u); f[1] = bf16hi(u);
-    } else {
-      f[0] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
-    }
-  } else {
-    if constexpr (N == 4) {
-      const float4 u = *reinterpret_cast<const float4 *>(p);
-      f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
-    } else if constexpr (N == 2) {
-      const float2 u = *reinterpret_cast<const float2 *>(p);
-      f[0] = u.x; f[1] = u.y;
-    } else {
-      f[0] = *p;
-    }
-  }
-}
-
 struct AttnSmem {
   int ring, mo, mm, ml, flag, bars, total;
 };

@@ -24,6 +24,7 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 
 // device-side error bits (mirror of PNB_DEV_ERR_*)
 constexpr int kErrToken = 1;
 constexpr int kErrTimeout = 2;
+constexpr int kErrRange = 4;
 
 // -------------------------------------------------------------- shared mem
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -177,6 +178,43 @@ struct Elem<__nv_bfloat16> {
     p[i] = __float2bfloat16_rn(v);
   }
 };
+
+// N consecutive elements at p (4-, 8- or 16-byte aligned as their size) as fp32
+template <typename T, int N>
+__device__ __forceinline__ void load_vals(const T *p, float (&f)[N]) {
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (N == 8) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(p);
+      f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+      f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+    } else if constexpr (N == 4) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(p);
+      f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+    } else if constexpr (N == 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+      f[0] = bf16lo(u); f[1] = bf16hi(u);
+    } else {
+      f[0] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
+    }
+  } else {
+    if constexpr (N == 4) {
+      const float4 u = *reinterpret_cast<const float4 *>(p);
+      f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+    } else if constexpr (N == 2) {
+      const float2 u = *reinterpret_cast<const float2 *>(p);
+      f[0] = u.x; f[1] = u.y;
+    } else {
+      f[0] = *p;
+    }
+  }
+}
+
+// fp32 -> storage type -> fp32 (round to nearest even for bf16)
+template <typename T>
+__device__ __forceinline__ float round_to(float v) {
+  if constexpr (sizeof(T) == 2) return __bfloat162float(__float2bfloat16_rn(v));
+  else return v;
+}
 
 // The state's device I/O block: next input token, position, error bits.
 struct StepIO {

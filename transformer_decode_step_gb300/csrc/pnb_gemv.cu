@@ -45,9 +45,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
   XSlice<T, NV> xs;
   load_weight_slice(xs, a.norm_w, a.g, warp, lane);
   const int hd = a.head_dim;
-  const double inv_freq = tid < hd / 2 ? a.inv_freq[tid] : 0.0;
   pdl_wait();
   if (tid == 0) ktrace(a.tr, 1);
+  const double inv_freq = tid < hd / 2 ? a.inv_freq[tid] : 0.0;
   const int pos = a.io->pos;
   if (a.emb) {
     int tok = a.io->token;
@@ -112,7 +112,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_resid(const ResidArgs a) {
   gemv_sync();
   if (tid == 0) ktrace(a.tr, 4);
   for_claimed_rows(a.g, c, a.s.rows, false, tid, [&](int k, int r, int, int64_t row) {
-    a.x[row] += item_row_total(a.g, c, k, r);
+    const float d = item_row_total(a.g, c, k, r);
+    if (a.acc) {   // fold the fused block's attention output in, then clear it
+      a.x[row] = (a.x[row] + fix_to_float(a.acc[row])) + d;
+      a.acc[row] = 0;
+    } else {
+      a.x[row] += d;
+    }
   });
   if (tid == 0) ktrace(a.tr, 5);
 }
@@ -124,7 +130,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup(const GateUpArgs a) 
   load_weight_slice(xs, a.norm_w, a.g, warp, lane);
   pdl_wait();
   if (tid == 0) ktrace(a.tr, 1);
-  norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
+  if (a.acc) {
+    const XAcc xa{a.x, a.acc};
+    norm_slice(xs, &xa, a.g.K, a.eps, a.g, c.red, warp, lane);
+  } else {
+    norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
+  }
   if (tid == 0) ktrace(a.tr, 2);
   consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
@@ -154,7 +165,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_moe(const DownMoeArgs 
     for (int s = 0; s < a.s.n; ++s)
       acc = fmaf(a.gate[s], row_total(c.part + s * a.g.rows_cta_max * a.g.cw, (int)(r - c.r0), a.g.cw),
                  acc);
-    a.x[r] += acc;
+    if (a.acc) {   // fold the fused block's attention output in, then clear it
+      a.x[r] = (a.x[r] + fix_to_float(a.acc[r])) + acc;
+      a.acc[r] = 0;
+    } else {
+      a.x[r] += acc;
+    }
   }
   if (tid == 0) ktrace(a.tr, 5);
 }
@@ -242,15 +258,17 @@ __global__ void __launch_bounds__(256, 1) k_router(const RouterArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
   pdl_trigger();
+  // the residual (with the fused block's pending attention output)
+  for (int i = tid; i < a.E; i += 256) xs[i] = a.acc ? a.x[i] + fix_to_float(a.acc[i]) : a.x[i];
   float ss = 0.f;
-  for (int i = tid; i < a.E; i += 256) ss = fmaf(a.x[i], a.x[i], ss);
+  for (int i = tid; i < a.E; i += 256) ss = fmaf(xs[i], xs[i], ss);
   ss = warp_sum(ss);
   if (lane == 0) red[warp] = ss;
   __syncthreads();
   float tot = 0.f;
   for (int k = 0; k < 8; ++k) tot += red[k];
   const float inv = 1.0f / sqrtf(tot / (float)a.E + a.eps);
-  for (int i = tid; i < a.E; i += 256) xs[i] = a.x[i] * inv * a.norm_w[i];
+  for (int i = tid; i < a.E; i += 256) xs[i] = xs[i] * inv * a.norm_w[i];
   __syncthreads();
   for (int e = warp; e < a.n_expert; e += 8) {
     const T *row = static_cast<const T *>(a.w) + (int64_t)e * a.E;

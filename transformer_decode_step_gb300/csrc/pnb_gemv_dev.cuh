@@ -355,6 +355,19 @@ struct XSlice {
   float2 p[NV][Vec<T>::N / 2];
 };
 
+// The residual stream while an attention-output accumulator is pending:
+// element i is x[i] + acc[i] * 2^-32 (fp32, acc word rounded once).
+struct XAcc {
+  const float *x;
+  const long long *acc;
+};
+
+__device__ __forceinline__ float2 load2(const XAcc *src, int col) {
+  const float2 v = __ldcg(reinterpret_cast<const float2 *>(src->x + col));
+  const longlong2 f = __ldcg(reinterpret_cast<const longlong2 *>(src->acc + col));
+  return make_float2(v.x + fix_to_float(f.x), v.y + fix_to_float(f.y));
+}
+
 __device__ __forceinline__ float2 load2(const float *src, int col) {
   return __ldcg(reinterpret_cast<const float2 *>(src + col));
 }
@@ -455,6 +468,54 @@ __device__ __forceinline__ float dot_row(const uint8_t *row, const XSlice<T, NV>
   return s;
 }
 
+// Warp partials of four rows at once: the lane's products p[i] of rows i are
+// summed over the warp with six shuffles (two halving exchanges, then three
+// steps over the remaining eight lanes); lanes 8i .. 8i + 7 end with row i.
+__device__ __forceinline__ float warp_sum4(float p0, float p1, float p2, float p3, int lane) {
+  const bool hi = lane & 16, mid = lane & 8;
+  const float a0 = (hi ? p2 : p0) + __shfl_xor_sync(0xffffffffu, hi ? p0 : p2, 16);
+  const float a1 = (hi ? p3 : p1) + __shfl_xor_sync(0xffffffffu, hi ? p1 : p3, 16);
+  float v = (mid ? a1 : a0) + __shfl_xor_sync(0xffffffffu, mid ? a0 : a1, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v;
+}
+
+// How a warp shares the staged rows: kGemvWarps / cw row groups of cw warps;
+// this warp is column slot cc of row group grp (computed once per kernel).
+struct RowSplit {
+  int cw, groups, grp, cc, vpr;
+  __device__ __forceinline__ RowSplit(int cw_, int row_bytes, int warp)
+      : cw(cw_), groups(kGemvWarps / cw_), grp(warp / cw_), cc(warp % cw_), vpr(row_bytes / 16) {}
+};
+
+// Partial sums of the n staged rows at `stage` into part[(base + r) * cw + cc];
+// with one row group (cw == 16) and rows short enough that a ring slot holds
+// several, the rows go four at a time through warp_sum4.
+template <typename T, int NV>
+__device__ __forceinline__ void dot_item(const uint8_t *stage, int n, int row_bytes, const XSlice<T, NV> &xs,
+                                         float *part, int base, const RowSplit &sp, int lane) {
+  const int groups = sp.groups, cc = sp.cc, cw = sp.cw, vpr = sp.vpr;
+  int r = sp.grp;
+  if constexpr (NV <= 2) {   // rows of at most 16 KB: ring slots hold four or more
+   if (groups == 1) {
+    for (; r + 4 <= n; r += 4) {
+      const uint8_t *rw = stage + (size_t)r * row_bytes;
+      const float v = warp_sum4(dot_row<T, NV>(rw, xs, vpr, cc, cw, lane),
+                                dot_row<T, NV>(rw + row_bytes, xs, vpr, cc, cw, lane),
+                                dot_row<T, NV>(rw + 2 * row_bytes, xs, vpr, cc, cw, lane),
+                                dot_row<T, NV>(rw + 3 * row_bytes, xs, vpr, cc, cw, lane), lane);
+      if ((lane & 7) == 0) part[(base + r + (lane >> 3)) * cw + cc] = v;
+    }
+   }
+  }
+  for (; r < n; r += groups) {
+    const float v = warp_sum(dot_row<T, NV>(stage + (size_t)r * row_bytes, xs, vpr, cc, cw, lane));
+    if (lane == 0) part[(base + r) * cw + cc] = v;
+  }
+}
+
 // Consumer loop over the CTA's ring items.  `reload(seg)` refreshes the
 // lane's activation slice when a summed launch moves to the next segment.  A
 // wait that expires sets the error bit and the warp stops consuming.
@@ -462,9 +523,8 @@ template <typename T, int NV, typename Reload>
 __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summed, const Ctx &c,
                         XSlice<T, NV> &xs, int warp, int lane, int32_t *err, const KTrace &tr,
                         Reload &&reload) {
-  const int cw = g.cw, groups = kGemvWarps / cw;
-  const int grp = warp / cw, cc = warp - grp * cw;
-  const int vpr = g.row_bytes / 16;
+  const int cw = g.cw;
+  const RowSplit sp(cw, g.row_bytes, warp);
   ItemIter it(c.r0, c.r1, s.rows, s.n, summed, g.rows_per_stage);
   Item item;
   RingPos rp{0u, 0u, (uint32_t)g.nstages};
@@ -484,10 +544,7 @@ __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summe
     if (ok) {
       const uint8_t *stage = c.ring + slot * (uint32_t)g.stage_bytes;
       float *part = c.part + ((summed ? item.seg : 0) * g.rows_cta_max + item.local) * cw;
-      for (int r = grp; r < item.n; r += groups) {
-        const float v = warp_sum(dot_row<T, NV>(stage + (size_t)r * g.row_bytes, xs, vpr, cc, cw, lane));
-        if (lane == 0) part[r * cw + cc] = v;
-      }
+      dot_item<T, NV>(stage, item.n, g.row_bytes, xs, part, 0, sp, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.empty[slot]);
     }
@@ -501,9 +558,8 @@ __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summe
 template <typename T, int NV>
 __device__ __forceinline__ void consume_dyn(const Geom &g, const Ctx &c, const XSlice<T, NV> &xs,
                                             int warp, int lane, int32_t *err, const KTrace &tr) {
-  const int cw = g.cw, groups = kGemvWarps / cw;
-  const int grp = warp / cw, cc = warp - grp * cw;
-  const int vpr = g.row_bytes / 16;
+  const int cw = g.cw;
+  const RowSplit sp(cw, g.row_bytes, warp);
   RingPos rp{0u, 0u, (uint32_t)g.nstages};
   bool first = true;
   for (;;) {
@@ -519,10 +575,7 @@ __device__ __forceinline__ void consume_dyn(const Geom &g, const Ctx &c, const X
     if (n < 0) return;
     const uint8_t *stage = c.ring + slot * (uint32_t)g.stage_bytes;
     float *part = c.part + (size_t)kk * g.rows_per_stage * cw;
-    for (int r = grp; r < n; r += groups) {
-      const float v = warp_sum(dot_row<T, NV>(stage + (size_t)r * g.row_bytes, xs, vpr, cc, cw, lane));
-      if (lane == 0) part[r * cw + cc] = v;
-    }
+    dot_item<T, NV>(stage, n, g.row_bytes, xs, part, 0, sp, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.empty[slot]);
     rp.advance();
@@ -555,7 +608,9 @@ __device__ __forceinline__ float item_row_total(const Geom &g, const Ctx &c, int
 }
 
 // The multiplier slice of an RMSNorm weight (1 without one): weights do not
-// depend on earlier kernels, so this is loaded before griddepcontrol.wait.
+// depend on earlier kernels, so this is loaded before griddepcontrol.wait
+// (the wait holds until such loads return; with one lane per column the
+// slice is a few hundred bytes per warp).
 template <typename T, int NV>
 __device__ __forceinline__ void load_weight_slice(XSlice<T, NV> &ws, const float *w, const Geom &g,
                                                   int warp, int lane) {
