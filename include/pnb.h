@@ -219,20 +219,23 @@ int pnb_model_is_persistent(const pnb_model *m);
 int pnb_model_set_tensor_attention(pnb_model *m, int enable);
 int pnb_model_is_tensor_attention(const pnb_model *m);
 
-/* The attention half of each layer of the single-sequence step (RMSNorm,
-   q / k / v projections, RoPE, KV append, attention, output projection) as
-   one kernel per layer (enable = 1; possible when head_dim is in {32, 64,
-   128}, n_head <= the SM count, n_embd is divisible by the cluster size and
-   an output-projection tile has at least 8 rows) or as three (0, the
-   default: the fused kernel runs on n_head * cluster-size SMs only, and on
-   the 7B-class shapes the three kernels on every SM are faster).  The fused kernel runs one thread-block cluster of up to 8 CTAs
-   per query head; the heads' output-projection values meet in a 64-bit
+/* How the attention half of each layer of the single-sequence step runs.
+   PNB_FUSED_OFF (the default): three kernels - QKV (with RMSNorm, RoPE and
+   the KV append), attention, output projection.  PNB_FUSED_ATTN_OPROJ: the
+   QKV kernel, then attention and the output projection as one kernel.
+   PNB_FUSED_BLOCK: all of it as one kernel.  The fused kernel runs one
+   thread-block cluster of up to 8 CTAs per query head (so n_head * cluster
+   size SMs); the heads' output-projection values meet in a 64-bit
    fixed-point accumulator (units of 2^-32, |value| < 2^30 per head) that the
    following kernels fold into the residual, so the step stays bitwise
-   reproducible.  Results agree with the three-kernel path to fp32 rounding.
-   Returns PNB_E_UNSUPPORTED when enabling is not possible for this model. */
-int pnb_model_set_fused_attention(pnb_model *m, int enable);
-int pnb_model_is_fused_attention(const pnb_model *m);
+   reproducible.  Results agree with the default to fp32 rounding.  Possible
+   when head_dim is in {32, 64, 128}, n_head <= the SM count, n_embd is
+   divisible by the cluster size and an output-projection tile has at least
+   8 rows; else setting a fused mode returns PNB_E_UNSUPPORTED.  An unknown
+   mode returns PNB_E_INVAL. */
+enum { PNB_FUSED_OFF = 0, PNB_FUSED_ATTN_OPROJ = 1, PNB_FUSED_BLOCK = 2 };
+int pnb_model_set_fused_attention(pnb_model *m, int mode);
+int pnb_model_fused_attention(const pnb_model *m);
 
 /* Number of this library's kernels one step launches (single sequence when
    B == 0, batched otherwise). */
@@ -247,9 +250,10 @@ enum {
   PNB_KERNEL_GATE_UP = 4, /* RMSNorm, gate/up (chosen experts), SwiGLU */
   PNB_KERNEL_DOWN = 5,    /* down projection(s) + residual */
   PNB_KERNEL_LM_HEAD = 6, /* final RMSNorm, LM head, argmax, pos += 1 */
-  PNB_KERNEL_ATTN_BLOCK = 7 /* fused attention block: QKV + attention + output projection
-                               into the attention-output accumulator (replaces kinds 0-2
-                               in a step when pnb_model_is_fused_attention) */
+  PNB_KERNEL_ATTN_BLOCK = 7 /* fused attention block into the attention-output accumulator:
+                               QKV + attention + output projection, or, in mode
+                               PNB_FUSED_ATTN_OPROJ, attention + output projection after
+                               the QKV kernel (replaces kinds 0-2 / 1-2 in a fused step) */
 };
 
 /* Launch one kernel of the single-sequence step for `layer` in isolation
@@ -259,8 +263,9 @@ enum {
    head kernel still advances the device position, as in a step).  The
    fused attention block adds into the state's attention-output accumulator,
    which the next router / gate-up kernel reads and the down-projection kernel
-   folds into the residual while the model is in fused mode.  PNB_KERNEL_ATTN_BLOCK returns PNB_E_UNSUPPORTED
-   where the model has no fused block. */
+   folds into the residual while the model is in a fused mode.
+   PNB_KERNEL_ATTN_BLOCK returns PNB_E_UNSUPPORTED unless the model is in a
+   fused mode. */
 int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb_stream stream);
 
 /* Device pointers of a state's fp32 activation buffers after its last step
@@ -318,7 +323,8 @@ int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const voi
    warps past griddepcontrol.wait, 2 = activation prologue done, 3 = first
    ring slot arrived, 4 = all slots consumed, 5 = epilogue done, 6 / 7 = the
    producer reached / passed griddepcontrol.wait; the fused attention block
-   records as launch 6 * layer with 4 = the head's q / k / v exchanged,
+   records as launch 6 * layer (6 * layer + 1 after the QKV kernel in mode
+   PNB_FUSED_ATTN_OPROJ) with 4 = the head's q / k / v exchanged,
    5 = the cluster's softmax partials exchanged, 6 = its producer reached
    griddepcontrol.wait and 7 = the CTA's end.  A batched step records into
    its first slot's buffer with launch = 7 * layer + (0 norm, 1 QKV,

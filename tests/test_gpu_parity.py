@@ -33,10 +33,14 @@ def tol(shape):
     return 1e-3 if shape.dtype == F32 else 2e-2
 
 
+FUSED = {"kernels": pnb.PNB_FUSED_OFF, "fused_ao": pnb.PNB_FUSED_ATTN_OPROJ, "fused": pnb.PNB_FUSED_BLOCK}
+
+
 def set_mode(sm, mode):
     """'persistent': one cooperative kernel per step; 'kernels': one kernel per
-    phase; 'fused': one kernel per phase with the attention half of each layer
-    (QKV, attention, output projection) as one cluster kernel."""
+    phase; 'fused_ao': attention and output projection as one cluster kernel;
+    'fused': the whole attention half of each layer (QKV, attention, output
+    projection) as one cluster kernel."""
     if mode == "persistent":
         try:
             sm.model.set_persistent(True)
@@ -48,19 +52,15 @@ def set_mode(sm, mode):
         return
     sm.model.set_persistent(False)
     assert not sm.model.persistent
-    if mode == "fused":
-        try:
-            sm.model.set_fused_attention(True)
-        except pnb.PnbError as e:
-            if e.code == -5:
-                pytest.skip("the fused attention block does not cover this shape")
-            raise
-        assert sm.model.fused_attention
-    else:
-        sm.model.set_fused_attention(False)
-        assert not sm.model.fused_attention
+    try:
+        sm.model.set_fused_attention(FUSED[mode])
+    except pnb.PnbError as e:
+        if e.code == -5:
+            pytest.skip("the fused attention block does not cover this shape")
+        raise
+    assert sm.model.fused_attention == FUSED[mode]
     moe = sm.shape.expert_count > 0
-    per_layer = (1 if mode == "fused" else 3) + (3 if moe else 2)
+    per_layer = {"kernels": 3, "fused_ao": 2, "fused": 1}[mode] + (3 if moe else 2)
     assert sm.model.step_kernel_count() == sm.shape.n_layer * per_layer + 1
 
 
@@ -148,7 +148,7 @@ def _tiny_tokens():
     return prompt, gen
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused"])
+@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
 def test_tiny_teacher_forced_matches_oracle(mode):
     w = wl.TINY
     prompt, gen = _tiny_tokens()
@@ -161,7 +161,7 @@ def test_tiny_teacher_forced_matches_oracle(mode):
     assert gam[len(prompt) - 1:] == gen
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused"])
+@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
 def test_tiny_free_running_greedy_matches_stored_oracle_run(mode):
     w = wl.TINY
     prompt, gen = _tiny_tokens()
@@ -179,7 +179,7 @@ def test_tiny_free_running_greedy_matches_stored_oracle_run(mode):
     assert st.pos == len(prompt) + len(gen) - 1
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused"])
+@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
 def test_graph_replay_equals_eager_launches_bitwise(mode):
     w = wl.TINY
     prompt, gen = _tiny_tokens()
@@ -240,7 +240,7 @@ SMALL_HD128 = wl.Shape(n_vocab=1000, n_embd=1024, n_head=8, n_kv_head=2, n_layer
                        n_ctx=300, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused"])
+@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
 @pytest.mark.parametrize("name,shape,start,steps", [
     ("window_ring", SMALL_WIN, 40, 24),       # ring of 24 slots, pre-fill wraps it
     ("window_short", SMALL_WIN, 0, 30),       # empty cache, window fills then slides
@@ -269,7 +269,7 @@ def test_persistent_and_per_kernel_steps_agree():
     shape, seed = SMALL_WIN, 13
     tokens = [5, 17, 400, 3000, 9, 9, 1]
     outs = []
-    for mode in ("persistent", "kernels", "fused"):
+    for mode in ("persistent", "kernels", "fused_ao", "fused"):
         sm = pnb.SynthModel(shape, seed, device=DEV)
         set_mode(sm, mode)
         outs.append(gpu_run(sm, sm.new_state(start_pos=30), tokens))
@@ -278,30 +278,31 @@ def test_persistent_and_per_kernel_steps_agree():
             assert np.max(np.abs(a - b)) <= 1e-4 * np.max(np.abs(a))
 
 
+@pytest.mark.parametrize("fused", ["fused_ao", "fused"])
 @pytest.mark.parametrize("name,shape,start", [
     ("window_ring", SMALL_WIN, 40), ("mha", SMALL_MHA, 17), ("hd128_gqa8", SMALL_G8, 40),
     ("kv5_window_cross", SMALL_KV5, 450), ("empty_cache", SMALL_HD128, 0)])
-def test_fused_block_activations_match_three_kernel_path(name, shape, start):
+def test_fused_block_activations_match_three_kernel_path(name, shape, start, fused):
     """One layer's attention half run alone both ways from the same state: the
     rotated queries, the KV slot of the position and the attention output agree
     to fp32 rounding, and the residual after the down projection (which folds
-    the fused block's fixed-point accumulator) agrees too."""
+    the fused kernel's fixed-point accumulator) agrees too."""
     seed = 29
     sm = pnb.SynthModel(shape, seed, device=DEV)
     L = shape.n_layer
     acts = {}
-    for mode in ("kernels", "fused"):
-        sm.model.set_fused_attention(False)
+    for mode in ("kernels", fused):
+        sm.model.set_fused_attention(pnb.PNB_FUSED_OFF)
         st = sm.new_state(start_pos=start)
         st.forward(7)                      # one whole step: x is a real residual stream
         st.set_pos(start + 1)
-        sm.model.set_fused_attention(mode == "fused")   # the down kernel folds the accumulator
+        sm.model.set_fused_attention(FUSED[mode])   # the down kernel folds the accumulator
         layer = L - 1
-        if mode == "fused":
-            st.run_kernel(pnb.PNB_KERNEL_ATTN_BLOCK, layer)
-        else:
-            for k in (pnb.PNB_KERNEL_QKV, pnb.PNB_KERNEL_ATTN, pnb.PNB_KERNEL_OPROJ):
-                st.run_kernel(k, layer)
+        kinds = {"kernels": (pnb.PNB_KERNEL_QKV, pnb.PNB_KERNEL_ATTN, pnb.PNB_KERNEL_OPROJ),
+                 "fused_ao": (pnb.PNB_KERNEL_QKV, pnb.PNB_KERNEL_ATTN_BLOCK),
+                 "fused": (pnb.PNB_KERNEL_ATTN_BLOCK,)}[mode]
+        for k in kinds:
+            st.run_kernel(k, layer)
         if shape.expert_count:
             st.run_kernel(pnb.PNB_KERNEL_ROUTER, layer)
         st.run_kernel(pnb.PNB_KERNEL_GATE_UP, layer)
@@ -319,7 +320,7 @@ def test_fused_block_activations_match_three_kernel_path(name, shape, start):
         acts[mode]["kv"] = kv[layer, :, :, (start + 1) % cap].float().cpu().numpy()
         del st
     for k in ("q", "attn", "x", "kv"):
-        ref, got = acts["kernels"][k], acts["fused"][k]
+        ref, got = acts["kernels"][k], acts[fused][k]
         scale = float(np.max(np.abs(ref)))
         assert scale > 0 and np.all(np.isfinite(got)), k
         assert float(np.max(np.abs(got - ref))) <= 1e-5 * scale, f"{name} {k}"

@@ -22,6 +22,7 @@ _lib = ctypes.CDLL(LIB)
 PNB_F32, PNB_BF16 = 0, 1
 PNB_TOKEN_PREV = -1
 PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT, PNB_DEV_ERR_RANGE = 1, 2, 4
+PNB_FUSED_OFF, PNB_FUSED_ATTN_OPROJ, PNB_FUSED_BLOCK = 0, 1, 2
 (PNB_KERNEL_QKV, PNB_KERNEL_ATTN, PNB_KERNEL_OPROJ, PNB_KERNEL_ROUTER, PNB_KERNEL_GATE_UP,
  PNB_KERNEL_DOWN, PNB_KERNEL_LM_HEAD, PNB_KERNEL_ATTN_BLOCK) = range(8)
 ERRORS = {0: "PNB_OK", -1: "PNB_E_INVAL", -2: "PNB_E_NULL", -3: "PNB_E_ALIGN",
@@ -67,7 +68,7 @@ _SIGS = {
     "pnb_model_set_tensor_attention": (_i32, [_p, _i32]),
     "pnb_model_is_tensor_attention": (_i32, [_p]),
     "pnb_model_set_fused_attention": (_i32, [_p, _i32]),
-    "pnb_model_is_fused_attention": (_i32, [_p]),
+    "pnb_model_fused_attention": (_i32, [_p]),
     "pnb_step_kernel_count": (_i32, [_p, _i32]),
     "pnb_state_activations": (_i32, [_p, _p]),
     "pnb_step_kernel": (_i32, [_p, _p, _i32, _i32, _p]),
@@ -171,13 +172,15 @@ class Model:
     def tensor_attention(self) -> bool:
         return bool(pnb_model_is_tensor_attention(self._h))
 
-    def set_fused_attention(self, enable: bool):
-        check(pnb_model_set_fused_attention(self._h, 1 if enable else 0),
-              "pnb_model_set_fused_attention")
+    def set_fused_attention(self, mode: int):
+        """PNB_FUSED_OFF, PNB_FUSED_ATTN_OPROJ or PNB_FUSED_BLOCK."""
+        if isinstance(mode, bool):
+            raise TypeError("pass a PNB_FUSED_* mode, not a bool")
+        check(pnb_model_set_fused_attention(self._h, int(mode)), "pnb_model_set_fused_attention")
 
     @property
-    def fused_attention(self) -> bool:
-        return bool(pnb_model_is_fused_attention(self._h))
+    def fused_attention(self) -> int:
+        return int(pnb_model_fused_attention(self._h))
 
     def set_persistent(self, enable: bool):
         check(pnb_model_set_persistent(self._h, 1 if enable else 0), "pnb_model_set_persistent")

@@ -101,10 +101,11 @@ struct pnb_model {
   bool attn_tc_ok = false, attn_tc = false;
   int n_split_tc = 1;
   // fused attention block (one cluster per query head): geometry, per-layer Wo maps
-  bool block_ok = false, block = false;
+  bool block_ok = false;
+  int block = 0;                         // PNB_FUSED_*: off, attention + o-proj, whole block
   BlockGeom bgeom{};
   int block_clusters = 0;                // clusters that fit on the GPU at once
-  std::vector<CUtensorMap> wo_maps;
+  std::vector<CUtensorMap> wo_maps;      // per layer: Wo boxes of one head's columns
   int mode_gen = 0;                      // bumped when a launch mode changes (graphs re-captured)
   // persistent step kernel
   bool persistent = false;
@@ -279,8 +280,11 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
   const float eps = (float)c.rms_norm_eps;
   const bool moe = c.expert_count > 0;
   const int k = moe ? c.expert_used : 1;
+  // the fused block records in its layer's QKV slot, or in the attention
+  // slot when it follows the QKV kernel
+  const int block_slot = m->block == PNB_FUSED_ATTN_OPROJ ? PNB_KERNEL_ATTN : PNB_KERNEL_QKV;
   const KTrace tr{s->ktrace, kind == PNB_KERNEL_LM_HEAD    ? 6 * c.n_layer
-                            : kind == PNB_KERNEL_ATTN_BLOCK ? 6 * l
+                            : kind == PNB_KERNEL_ATTN_BLOCK ? 6 * l + block_slot
                                                             : 6 * l + kind};
   unsigned *work = s->work + 2 * tr.phase;
   switch (kind) {
@@ -332,6 +336,8 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ba.acc = s->acc;
       ba.q_out = s->q;
       ba.o_out = s->attn;
+      ba.q_in = m->block == PNB_FUSED_ATTN_OPROJ ? s->q : nullptr;
+      if (ba.q_in) ba.q_out = nullptr;   // the QKV kernel wrote them
       ba.io = s->io;
       ba.tr = tr;
       return launch_attn_block(c.dtype, hd, &m->wo_maps[l], ba, st, pdl);
@@ -546,8 +552,14 @@ cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *log
   const bool moe = m->cfg.expert_count > 0;
   cudaError_t e;
   for (int l = 0; l < m->cfg.n_layer; ++l) {
-    if (m->block) {
+    if (m->block == PNB_FUSED_BLOCK) {
       if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN_BLOCK, l, st, l > 0, nullptr, nullptr)) !=
+          cudaSuccess)
+        return e;
+    } else if (m->block == PNB_FUSED_ATTN_OPROJ) {
+      if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
+        return e;
+      if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN_BLOCK, l, st, true, nullptr, nullptr)) !=
           cudaSuccess)
         return e;
     } else {
@@ -1080,7 +1092,7 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
     // opt-in: with one cluster per query head the block runs on n_head * C
     // SMs (128 of 152 for 32 heads), and on the 7B-class shapes the three
     // per-phase kernels on every SM are the faster of the two
-    m->block = false;
+    m->block = PNB_FUSED_OFF;
   }
   if (!ok) {
     pnb_model_free(m);
@@ -1405,15 +1417,16 @@ int pnb_model_set_tensor_attention(pnb_model *m, int enable) {
 
 int pnb_model_is_tensor_attention(const pnb_model *m) { return m && m->attn_tc ? 1 : 0; }
 
-int pnb_model_set_fused_attention(pnb_model *m, int enable) {
+int pnb_model_set_fused_attention(pnb_model *m, int mode) {
   if (!m) return PNB_E_NULL;
-  if (enable && !m->block_ok) return PNB_E_UNSUPPORTED;
-  if (m->block != (enable != 0)) ++m->mode_gen;
-  m->block = enable != 0;
+  if (mode < PNB_FUSED_OFF || mode > PNB_FUSED_BLOCK) return PNB_E_INVAL;
+  if (mode != PNB_FUSED_OFF && !m->block_ok) return PNB_E_UNSUPPORTED;
+  if (m->block != mode) ++m->mode_gen;
+  m->block = mode;
   return PNB_OK;
 }
 
-int pnb_model_is_fused_attention(const pnb_model *m) { return m && m->block ? 1 : 0; }
+int pnb_model_fused_attention(const pnb_model *m) { return m ? m->block : 0; }
 
 int pnb_model_is_persistent(const pnb_model *m) { return m && m->persistent ? 1 : 0; }
 
@@ -1435,7 +1448,8 @@ int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
     return m->cfg.n_layer * (7 + merges) + 2;
   }
   if (m->persistent) return 1;
-  const int per_layer = (m->block ? 1 : 3) + (m->cfg.expert_count > 0 ? 3 : 2);
+  const int attn = m->block == PNB_FUSED_BLOCK ? 1 : (m->block == PNB_FUSED_ATTN_OPROJ ? 2 : 3);
+  const int per_layer = attn + (m->cfg.expert_count > 0 ? 3 : 2);
   return m->cfg.n_layer * per_layer + 1;
 }
 
@@ -1443,7 +1457,8 @@ int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb
   if (!m || !s) return PNB_E_NULL;
   if (s->m != m) return PNB_E_INVAL;
   if (kind < PNB_KERNEL_QKV || kind > PNB_KERNEL_ATTN_BLOCK) return PNB_E_INVAL;
-  if (kind == PNB_KERNEL_ATTN_BLOCK && !m->block_ok) return PNB_E_UNSUPPORTED;
+  if (kind == PNB_KERNEL_ATTN_BLOCK && (!m->block_ok || m->block == PNB_FUSED_OFF))
+    return PNB_E_UNSUPPORTED;
   if (kind == PNB_KERNEL_ROUTER && m->cfg.expert_count == 0) return PNB_E_INVAL;
   if (layer < 0 || layer >= m->cfg.n_layer) return PNB_E_INVAL;
   int rc = check_device(m);

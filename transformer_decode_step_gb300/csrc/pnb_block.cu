@@ -73,6 +73,11 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr, float2 v, uint32_t ba
                "f"(v.x), "f"(v.y), "r"(bar)
                : "memory");
 }
+// fire-and-forget 64-bit integer add in global memory (no value returned)
+__device__ __forceinline__ void red_add_u64(unsigned long long *addr, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
 // bounded wait for a phase whose bytes come from the cluster's CTAs
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
   const unsigned long long t0 = global_ns();
@@ -111,7 +116,7 @@ struct BlockRange {
 
 template <typename T, int HD>
 __device__ __forceinline__ void produce_block(const BlockArgs &a, const CUtensorMap *wo_map,
-                                              const BlockRange &R, int h, int g, uint8_t *ring,
+                                              const BlockRange &R, int h, int g, int pos, uint8_t *ring,
                                               uint64_t *full, uint64_t *empty, int32_t *err) {
   constexpr int ES = (int)sizeof(T);
   const BlockGeom &b = a.b;
@@ -120,9 +125,10 @@ __device__ __forceinline__ void produce_block(const BlockArgs &a, const CUtensor
   RingPos rp{0u, 0u, NS};
   bool waited = false, ok = true;
   // room for copy i (the first ring's worth goes out before griddepcontrol.wait:
-  // weights and the cache's earlier positions do not depend on earlier kernels)
-  auto room = [&]() -> bool {
-    if (!waited && i == NS) {
+  // weights and the cache's earlier positions do not depend on earlier kernels;
+  // a copy with `dep` set reads what the previous kernel wrote)
+  auto room = [&](bool dep) -> bool {
+    if (!waited && (i == NS || dep)) {
       ktrace(a.tr, 6);
       pdl_wait();
       pdl_trigger();
@@ -137,7 +143,7 @@ __device__ __forceinline__ void produce_block(const BlockArgs &a, const CUtensor
     const int blk = r / HD, rin = r - blk * HD;
     const int64_t src = blk == 0 ? (int64_t)h * HD + rin
                                  : (int64_t)(a.H + (blk - 1) * a.Hkv + g) * HD + rin;
-    if (!room()) {
+    if (!room(false)) {
       ok = false;
       break;
     }
@@ -153,7 +159,7 @@ __device__ __forceinline__ void produce_block(const BlockArgs &a, const CUtensor
   const uint8_t *vb = static_cast<const uint8_t *>(a.v_cache) + (size_t)g * head_bytes;
   for (int p = R.p0; p < R.p1 && ok;) {
     const int n = kv_item_pos(p, R.p1, b.kv_item, a.cap);
-    if (!room()) {
+    if (!room(p + n > pos)) {   // the current position: written by the QKV kernel
       ok = false;
       break;
     }
@@ -168,7 +174,7 @@ __device__ __forceinline__ void produce_block(const BlockArgs &a, const CUtensor
     p += n;
   }
   for (int r = R.e0; r < R.e1 && ok; r += b.o_item) {
-    if (!room()) {
+    if (!room(false)) {
       ok = false;
       break;
     }
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     fence_barrier_init();
     // bytes the cluster's CTAs store here: every row of [q; k; v], and one
     // (weighted V, max, sum) per CTA
-    mbar_arrive_expect_tx(xq, 3u * HD * 4u);
+    if (!a.q_in) mbar_arrive_expect_tx(xq, 3u * HD * 4u);
     mbar_arrive_expect_tx(xa, (uint32_t)C * (HD * 4u + 8u));
   }
   __syncthreads();
@@ -240,20 +246,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
   // this CTA's share of the three streams.  pos was written by an earlier step
   // (the first layer's launch waits for all earlier work): readable before the wait.
+  const bool own_qkv = a.q_in == nullptr;
   const int pos = a.io->pos;
   const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
-  const int npos = pos - lo;   // cached positions; the current one comes from the exchange
+  // cached positions: with its own q / k / v the current one comes from the
+  // exchange, else the QKV kernel has stored it
+  const int npos = pos - lo + (own_qkv ? 0 : 1);
   const int E = b.g.K;
   BlockRange R;
-  R.r0 = b.rows_cta * (int)rank;
-  R.r1 = R.r0 + b.rows_cta;
+  R.r0 = own_qkv ? b.rows_cta * (int)rank : 0;
+  R.r1 = own_qkv ? R.r0 + b.rows_cta : 0;
   R.p0 = lo + (int)((int64_t)npos * rank / C);
   R.p1 = lo + (int)((int64_t)npos * (rank + 1) / C);
   R.e0 = E / C * (int)rank;
   R.e1 = R.e0 + E / C;
 
   if (warp == kGemvWarps) {
-    if (lane == 0) produce_block<T, HD>(a, &wo_map, R, h, g, ring, full, empty, err);
+    if (lane == 0) produce_block<T, HD>(a, &wo_map, R, h, g, pos, ring, full, empty, err);
     __syncwarp();
     cluster_wait();
     cluster_arrive();   // no CTA ends while a peer may still store into it
@@ -262,32 +271,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   }
 
   // ------------------------------------------------- (a) q / k / v rows
-  XSlice<T, NV> xs;
-  load_weight_slice(xs, a.norm_w, b.g, warp, lane);
-  pdl_wait();
-  if (tid == 0) ktrace(a.tr, 1);
-  const double inv_freq = tid < HD / 2 ? a.inv_freq[tid] : 0.0;
-  if (a.emb) {
-    int tok = a.io->token;
-    if (tok < 0 || tok >= a.n_vocab) {
-      if (tid == 0 && blockIdx.x == 0) set_error(err, kErrToken);
-      tok = 0;
-    }
-    const T *row = static_cast<const T *>(a.emb) + (int64_t)tok * E;
-    if (blockIdx.x == 0)
-      for (int i = tid * 2; i < E; i += kGemvConsumers * 2)
-        *reinterpret_cast<float2 *>(a.x_out + i) = load2(row, i);
-    norm_slice(xs, row, E, a.eps, b.g, red, warp, lane);
-  } else {
-    norm_slice(xs, a.x, E, a.eps, b.g, red, warp, lane);
-  }
-  if (tid == 0) ktrace(a.tr, 2);
-  if (tid < HD / 2) {
-    float sn, cs;
-    rope_sincos(pos, inv_freq, &sn, &cs);
-    rope[tid] = make_float2(cs, sn);
-  }
-
   const int cw = b.g.cw;
   const RowSplit sp(cw, b.g.row_bytes, warp);
   const uint32_t SB = (uint32_t)b.stage_bytes;
@@ -304,56 +287,92 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
   };
-  for (int r = R.r0; r < R.r1;) {
-    const int n = qkv_item_rows<HD>(r, R.r1, b.g.rows_per_stage);
-    const uint32_t slot = rp.slot;
-    const bool first = r == R.r0;
-    if (take(slot)) {
-      if (first && tid == 0) ktrace(a.tr, 3);
-      dot_item<T, NV>(ring + slot * SB, n, b.g.row_bytes, xs, part, r - R.r0, sp, lane);
-      release(slot);
+  if (own_qkv) {
+    XSlice<T, NV> xs;
+    load_weight_slice(xs, a.norm_w, b.g, warp, lane);
+    pdl_wait();
+    if (tid == 0) ktrace(a.tr, 1);
+    const double inv_freq = tid < HD / 2 ? a.inv_freq[tid] : 0.0;
+    if (a.emb) {
+      int tok = a.io->token;
+      if (tok < 0 || tok >= a.n_vocab) {
+        if (tid == 0 && blockIdx.x == 0) set_error(err, kErrToken);
+        tok = 0;
+      }
+      const T *row = static_cast<const T *>(a.emb) + (int64_t)tok * E;
+      if (blockIdx.x == 0)
+        for (int i = tid * 2; i < E; i += kGemvConsumers * 2)
+          *reinterpret_cast<float2 *>(a.x_out + i) = load2(row, i);
+      norm_slice(xs, row, E, a.eps, b.g, red, warp, lane);
+    } else {
+      norm_slice(xs, a.x, E, a.eps, b.g, red, warp, lane);
     }
-    rp.advance();
-    r += n;
-  }
-  gemv_sync();
-
-  // exchange 1: every CTA of the cluster gets this CTA's rows
-  cluster_wait();
-  if (tid < b.rows_cta / 4) {
-    float4 v;
-    v.x = row_total(part, 4 * tid + 0, cw);
-    v.y = row_total(part, 4 * tid + 1, cw);
-    v.z = row_total(part, 4 * tid + 2, cw);
-    v.w = row_total(part, 4 * tid + 3, cw);
-    float *dst = qkv + R.r0 + 4 * tid;
-    for (int p = 0; p < C; ++p) st_async_v4(peer_addr(dst, p), v, peer_addr(xq, p));
-  }
-  if (!mbar_wait_cluster(xq, 0) && lane == 0) set_error(err, kErrTimeout);
-  if (tid == 0) ktrace(a.tr, 4);
-
-  // RoPE on q and k (adjacent pairs), then k and v in the cache's precision
-  if (tid < HD) {
-    const int j = tid % (HD / 2);
-    float *v = qkv + (tid < HD / 2 ? 0 : HD) + 2 * j;
-    const float2 cs = rope[j];
-    const float v0 = v[0], v1 = v[1];
-    v[0] = v0 * cs.x - v1 * cs.y;
-    v[1] = v0 * cs.y + v1 * cs.x;
-  }
-  gemv_sync();
-  if (tid < HD) {
-    const float kr = round_to<T>(qkv[HD + tid]), vr = round_to<T>(qkv[2 * HD + tid]);
-    if (rank == 0 && h % (a.H / a.Hkv) == 0) {   // the KV head's first query head appends
-      const size_t at = ((size_t)g * a.cap + pos % a.cap) * HD + tid;
-      Elem<T>::store(static_cast<T *>(a.k_cache), at, kr);
-      Elem<T>::store(static_cast<T *>(a.v_cache), at, vr);
+    if (tid == 0) ktrace(a.tr, 2);
+    if (tid < HD / 2) {
+      float sn, cs;
+      rope_sincos(pos, inv_freq, &sn, &cs);
+      rope[tid] = make_float2(cs, sn);
     }
-    qkv[HD + tid] = kr;
-    qkv[2 * HD + tid] = vr;
-    if (rank == 0 && a.q_out) a.q_out[(size_t)h * HD + tid] = qkv[tid];
+
+    for (int r = R.r0; r < R.r1;) {
+      const int n = qkv_item_rows<HD>(r, R.r1, b.g.rows_per_stage);
+      const uint32_t slot = rp.slot;
+      const bool first = r == R.r0;
+      if (take(slot)) {
+        if (first && tid == 0) ktrace(a.tr, 3);
+        dot_item<T, NV>(ring + slot * SB, n, b.g.row_bytes, xs, part, r - R.r0, sp, lane);
+        release(slot);
+      }
+      rp.advance();
+      r += n;
+    }
+    gemv_sync();
+
+    // exchange 1: every CTA of the cluster gets this CTA's rows
+    cluster_wait();
+    if (tid < b.rows_cta / 4) {
+      float4 v;
+      v.x = row_total(part, 4 * tid + 0, cw);
+      v.y = row_total(part, 4 * tid + 1, cw);
+      v.z = row_total(part, 4 * tid + 2, cw);
+      v.w = row_total(part, 4 * tid + 3, cw);
+      float *dst = qkv + R.r0 + 4 * tid;
+      for (int p = 0; p < C; ++p) st_async_v4(peer_addr(dst, p), v, peer_addr(xq, p));
+    }
+    if (!mbar_wait_cluster(xq, 0) && lane == 0) set_error(err, kErrTimeout);
+    if (tid == 0) ktrace(a.tr, 4);
+
+    // RoPE on q and k (adjacent pairs), then k and v in the cache's precision
+    if (tid < HD) {
+      const int j = tid % (HD / 2);
+      float *v = qkv + (tid < HD / 2 ? 0 : HD) + 2 * j;
+      const float2 cs = rope[j];
+      const float v0 = v[0], v1 = v[1];
+      v[0] = v0 * cs.x - v1 * cs.y;
+      v[1] = v0 * cs.y + v1 * cs.x;
+    }
+    gemv_sync();
+    if (tid < HD) {
+      const float kr = round_to<T>(qkv[HD + tid]), vr = round_to<T>(qkv[2 * HD + tid]);
+      if (rank == 0 && h % (a.H / a.Hkv) == 0) {   // the KV head's first query head appends
+        const size_t at = ((size_t)g * a.cap + pos % a.cap) * HD + tid;
+        Elem<T>::store(static_cast<T *>(a.k_cache), at, kr);
+        Elem<T>::store(static_cast<T *>(a.v_cache), at, vr);
+      }
+      qkv[HD + tid] = kr;
+      qkv[2 * HD + tid] = vr;
+      if (rank == 0 && a.q_out) a.q_out[(size_t)h * HD + tid] = qkv[tid];
+    }
+    gemv_sync();
+
+  } else {
+    // the QKV kernel has rotated the queries and stored the current K / V
+    pdl_wait();
+    if (tid == 0) ktrace(a.tr, 1);
+    if (tid < HD) qkv[tid] = a.q_in[(size_t)h * HD + tid];
+    gemv_sync();
+    cluster_wait();
   }
-  gemv_sync();
 
   // ------------------------------------------------- (b) attention
   constexpr int DPL = HD / 8;                             // dims per lane when scoring
@@ -441,7 +460,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     p += n;
   }
   // the current position (rounded k, v from the exchange) on the last CTA
-  if (rank == (uint32_t)C - 1 && warp == 0) {
+  if (own_qkv && rank == (uint32_t)C - 1 && warp == 0) {
     float s = 0.f;
 #pragma unroll
     for (int d = 0; d < VPL; ++d) s = fmaf(qkv[lane * VPL + d] * a.qscale, qkv[HD + lane * VPL + d], s);
@@ -531,7 +550,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             set_error(err, kErrRange);
             y = y > 0.f ? kFixLimit : (y < 0.f ? -kFixLimit : 0.f);
           }
-          atomicAdd(acc + r + row, (unsigned long long)__float2ll_rn(y * kFixScale));
+          red_add_u64(acc + r + row, (unsigned long long)__float2ll_rn(y * kFixScale));
         }
       }
       release(slot);

@@ -361,6 +361,9 @@ struct BlockArgs {
   float qscale;            // log2(e) / sqrt(hd)
   long long *acc;          // [n_embd] attention-output accumulator
   float *q_out, *o_out;    // [H][hd] rotated queries and attention output (diagnostics)
+  const float *q_in;       // attention + output projection only: [H][hd] rotated queries
+                           // of the QKV kernel, which also stored the current K / V;
+                           // null: the kernel computes q / k / v itself
   StepIO *io;
   KTrace tr;
 };
