@@ -216,7 +216,8 @@ void plan(pnb_model *m) {
   m->attn_tc_ok = c.dtype == PNB_BF16 && (m->hd == 64 || m->hd == 128) &&
                   (G == 1 || G == 2 || G == 4 || G == 8) &&
                   (c.sliding_window == 0 || m->cap % 128 == 0);
-  m->n_split_tc = std::max(1, std::min(m->num_sms / c.n_kv_head, ceil_div(m->cap, 128)));
+  // the splits of a KV head form one thread-block cluster (merged in shared memory)
+  m->n_split_tc = std::max(1, std::min({attn_tc_max_split(), m->num_sms / c.n_kv_head, ceil_div(m->cap, 128)}));
 }
 
 bool geoms_supported(const pnb_model *m);
@@ -354,8 +355,6 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
         ta.window = c.sliding_window;
         ta.n_split = m->n_split_tc;
         ta.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
-        ta.part = s->part;
-        ta.counter = s->attn_cnt;
         ta.out = s->attn;
         ta.io = s->io;
         ta.nstages = attn_tc_stages(hd);
@@ -699,13 +698,15 @@ int bp_index(int bp) { return bp == 16 ? 0 : (bp == 32 ? 1 : 2); }
 
 int attn_split_b(const pnb_model *m, int B) {
   if (m->attn_tc)
-    return std::max(1, std::min(m->num_sms / (m->cfg.n_kv_head * B), ceil_div(m->cap, 128)));
+    return std::max(1, std::min({attn_tc_max_split(), m->num_sms / (m->cfg.n_kv_head * B),
+                                 ceil_div(m->cap, 128)}));
   const int per = m->cfg.n_kv_head * m->zgroups * B;
   return std::max(1, std::min(m->num_sms / std::max(1, per), std::max(1, m->cap / 16)));
 }
 
 int attn_split_b_max(const pnb_model *m, int B) {
-  const int tc = std::max(1, std::min(m->num_sms / (m->cfg.n_kv_head * B), ceil_div(m->cap, 128)));
+  const int tc = std::max(1, std::min({attn_tc_max_split(), m->num_sms / (m->cfg.n_kv_head * B),
+                                       ceil_div(m->cap, 128)}));
   const int per = m->cfg.n_kv_head * m->zgroups * B;
   const int cc = std::max(1, std::min(m->num_sms / std::max(1, per), std::max(1, m->cap / 16)));
   return std::max(tc, cc);
@@ -894,8 +895,6 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
       ta.window = c.sliding_window;
       ta.n_split = attn_split_b(m, B);
       ta.qscale = (float)(1.4426950408889634 / std::sqrt((double)m->hd));
-      ta.part = b->apart;
-      ta.counter = b->acnt;
       ta.xop = b->xop_o;
       ta.xop_ld = Hd;
       ta.bp = bp;

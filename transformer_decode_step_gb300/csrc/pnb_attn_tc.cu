@@ -15,8 +15,11 @@
 //            rows h and 8 + h of a swizzled shared tile, and warp 4 (TMEM
 //            lanes 0-31, the rows of P that carry heads) folds each tile's O
 //            into its registers with the rescale factor.
-// Splits of the position range leave (max, sum, O) partials that the last
-// CTA of the KV head merges by log-sum-exp.
+// The splits of a KV head's position range form one thread-block cluster:
+// each CTA sends its (max, sum, O) partial of query head h to cluster CTA
+// h mod n_split through distributed shared memory (st.async completing on the
+// receiver's mbarrier), and the receiving CTAs merge by log-sum-exp in split
+// order and write the output.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -44,6 +47,55 @@ __device__ __forceinline__ void fence_async_smem() {
 }
 
 __device__ __forceinline__ void epi_sync_t() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// address of the same shared-memory object in the cluster's CTA `rank`
+__device__ __forceinline__ uint32_t cl_peer(const void *local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
+  return r;
+}
+// stores into a cluster CTA's shared memory; the bytes complete on its mbarrier
+__device__ __forceinline__ void cl_st_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr),
+               "f"(v), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cl_st_v2(uint32_t addr, float2 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                   addr),
+               "f"(v.x), "f"(v.y), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cl_st_v4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+// bounded wait for bytes stored by the cluster's CTAs
+__device__ __forceinline__ bool cl_mbar_wait(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 255u) == 255u && (global_ns() - t0 > kWaitLimitNs || it > (1u << 26))) return false;
+  }
+}
+
+// The split partials a CTA merges: query heads h with h % n_split == rank,
+// [local head][split][hd + 4] floats (O, then max and sum).
+constexpr int kMaxSplit = 8;   // portable cluster size (16-CTA clusters measured slower)
+__host__ __device__ constexpr int merge_floats(int hd) { return 16 * (hd + 4); }
 
 // descriptor of an MN-major operand tile with 128-byte swizzle: 64-element
 // atoms along N lbo bytes apart, groups of 8 K-rows 1024 bytes apart
@@ -77,7 +129,7 @@ struct TL {
 
 struct TBars {
   uint64_t *full, *empty;
-  uint64_t *s_full, *s_empty, *p_full, *p_empty, *o_full, *o_empty, *q_ready;
+  uint64_t *s_full, *s_empty, *p_full, *p_empty, *o_full, *o_empty, *q_ready, *merge_full;
 };
 
 template <int HD, int G>
@@ -94,18 +146,19 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
   const CUtensorMap *maps = static_cast<const CUtensorMap *>(bs.maps) + 2 * a.layer;
   const CUtensorMap *kmap = maps, *vmap = maps + 1;
   const float *qb = a.q + (size_t)b * a.n_head * HD;
-  float *part = a.part + (size_t)b * a.n_head * a.n_split * (HD + 2);
-  unsigned *counter = a.counter + (size_t)b * a.n_kv;
   const int h0 = g * G;
+  const int ns = a.n_split;         // splits = CTAs of this KV head's cluster
+  const bool clustered = ns > 1;
+  // query heads this CTA merges: h = split + j * ns < G
+  const int nloc = split < G ? (G - 1 - split) / ns + 1 : 0;
 
   // positions: [lo, pos]; tiles of 128 aligned positions, split evenly
   const int pos = batched ? a.pos[b] : a.io->pos;
   const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
   const int t_first = lo / kTile, t_last = pos / kTile;
   const int nt_all = t_last - t_first + 1;
-  const int tps = (nt_all + a.n_split - 1) / a.n_split;
-  const int tb = t_first + split * tps;
-  const int ntiles = max(0, min(t_last + 1, tb + tps) - tb);
+  const int tb = t_first + (int)((int64_t)nt_all * split / ns);
+  const int ntiles = t_first + (int)((int64_t)nt_all * (split + 1) / ns) - tb;
 
   // shared memory
   const uint32_t base = smem_addr(t_smem);
@@ -123,9 +176,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
   bar.o_full = bar.p_empty + 2;
   bar.o_empty = bar.o_full + 1;
   bar.q_ready = bar.o_empty + 1;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar.q_ready + 1);
-  int *flag = reinterpret_cast<int *>(tslot + 1);
-  float *red = reinterpret_cast<float *>(flag + 4);   // [2][4][8]
+  bar.merge_full = bar.q_ready + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(bar.merge_full + 1);
+  float *red = reinterpret_cast<float *>(tslot + 4);   // [2][4][8] maxima, then [4][8] sums
+  float *recv = reinterpret_cast<float *>(Q + QT + 1024);   // merge_floats(HD)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -143,7 +197,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
     mbar_init(bar.o_full, 1);
     mbar_init(bar.o_empty, 1);
     mbar_init(bar.q_ready, 4);
+    mbar_init(bar.merge_full, 1);
     fence_barrier_init();
+    // bytes the cluster's CTAs will store here: (O, max, sum) per split and head
+    if (clustered && nloc > 0) mbar_arrive_expect_tx(bar.merge_full, (uint32_t)(nloc * ns * (HD * 4 + 8)));
   }
   if (warp == 1) {
     tmem_alloc(tslot, TCOLS);
@@ -152,6 +209,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (clustered) cl_arrive();   // the merge barrier is armed before any peer stores into it
+  bool cl_waited = false;
   const uint32_t taddr = *tslot;
   const uint32_t t_s = taddr, t_o = taddr + TL<HD>::OCOL;
 
@@ -411,10 +470,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
         }
       }
       const int d = 32 * q + lane;
+      if (!clustered) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const size_t col = (size_t)(h0 + h) * HD + d;
-        if (a.n_split == 1) {
+        for (int h = 0; h < G; ++h) {
+          const size_t col = (size_t)(h0 + h) * HD + d;
           const float x = l[h] > 0.f ? oh[h] / l[h] : 0.f;
           if (a.xop) {
             const __nv_bfloat16 hi = __float2bfloat16_rn(x);
@@ -423,13 +482,17 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
           } else {
             a.out[col] = x;
           }
-        } else {
-          float *Pp = part + ((size_t)(h0 + h) * a.n_split + split) * (HD + 2);
-          Pp[2 + d] = oh[h];
-          if (d == 0) {
-            Pp[0] = m[h];
-            Pp[1] = l[h];
-          }
+        }
+      } else {
+        cl_wait();
+        cl_waited = true;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const uint32_t rr = (uint32_t)(h % ns);
+          float *dst = recv + ((h / ns) * ns + split) * (HD + 4);
+          const uint32_t mb = cl_peer(bar.merge_full, rr);
+          cl_st_f32(cl_peer(dst + d, rr), oh[h], mb);
+          if (d == 0) cl_st_v2(cl_peer(dst + HD, rr), make_float2(m[h], l[h]), mb);
         }
       }
     } else {
@@ -454,6 +517,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
       }
       // (max, sum, O) per head: lane h adds its low-part row 8 + h; with one split
       // this is the output, else a partial for the merge
+      if (clustered) {
+        cl_wait();
+        cl_waited = true;
+      }
       if (q == 0) {
   #pragma unroll
         for (int d = 0; d < HD; ++d) o[d] += __shfl_down_sync(0xffffffffu, o[d], 8);
@@ -483,62 +550,52 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
                     make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
             }
           } else {
-            float *Pp = part + ((size_t)(h0 + lane) * a.n_split + split) * (HD + 2);
-            Pp[0] = mh;
-            Pp[1] = lh;
+            const uint32_t rr = (uint32_t)(lane % ns);
+            float *dst = recv + ((lane / ns) * ns + split) * (HD + 4);
+            const uint32_t mb = cl_peer(bar.merge_full, rr);
   #pragma unroll
-            for (int d = 0; d < HD; ++d) Pp[2 + d] = o[d];
+            for (int d = 0; d < HD; d += 4)
+              cl_st_v4(cl_peer(dst + d, rr), make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]), mb);
+            cl_st_v2(cl_peer(dst + HD, rr), make_float2(mh, lh), mb);
           }
         }
       }
     }
     if (threadIdx.x == 128) ktrace(a.tr, 4);
-    if (a.n_split > 1) {
-      __threadfence();
-      epi_sync_t();
-      if (tid == 0) *flag = atomicAdd(&counter[g], 1u) == (unsigned)a.n_split - 1u;
-      epi_sync_t();
-      if (*flag) {
-        __threadfence();
-        const int ns = a.n_split;
-        for (int idx = tid; idx < G * HD; idx += 128) {
-          const int h = idx / HD, d = idx - h * HD;
-          const float *P0 = part + (size_t)(h0 + h) * ns * (HD + 2);
-          float M = -INFINITY, Ls = 0.f, Os = 0.f;
-          for (int s0 = 0; s0 < ns; s0 += 8) {
-            float pm[8], pl[8], po[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float *Pj = P0 + (size_t)(s0 + j < ns ? s0 + j : 0) * (HD + 2);
-              pm[j] = __ldcg(Pj);
-              pl[j] = __ldcg(Pj + 1);
-              po[j] = __ldcg(Pj + 2 + d);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (s0 + j >= ns || pm[j] == -INFINITY) continue;
-              const float Mn = fmaxf(M, pm[j]);
-              const float f0 = exp2f(M - Mn), f1 = exp2f(pm[j] - Mn);
-              Ls = Ls * f0 + pl[j] * f1;
-              Os = Os * f0 + po[j] * f1;
-              M = Mn;
-            }
-          }
-          const float x = Ls > 0.f ? Os / Ls : 0.f;
-          const size_t col = (size_t)(h0 + h) * HD + d;
-          if (a.xop) {
-            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-            a.xop[(size_t)b * a.xop_ld + col] = hi;
-            a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
-          } else {
-            a.out[col] = x;
-          }
+    if (clustered && nloc > 0) {
+      // merge this CTA's query heads over the splits, in split order
+      if (!cl_mbar_wait(bar.merge_full, 0) && lane == 0) set_error(err, kErrTimeout);
+      for (int idx = tid; idx < nloc * HD; idx += 128) {
+        const int j = idx / HD, d = idx - j * HD;
+        const float *R = recv + (size_t)j * ns * (HD + 4);
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, R[s2 * (HD + 4) + HD]);
+        float Ls = 0.f, Os = 0.f;
+        for (int s2 = 0; s2 < ns; ++s2) {
+          const float *Rs = R + s2 * (HD + 4);
+          if (Rs[HD] == -INFINITY) continue;
+          const float f = exp2f(Rs[HD] - M);
+          Ls = fmaf(Rs[HD + 1], f, Ls);
+          Os = fmaf(Rs[d], f, Os);
         }
-        if (tid == 0) counter[g] = 0u;
+        const float x = Ls > 0.f ? Os / Ls : 0.f;
+        const size_t col = (size_t)(h0 + split + j * ns) * HD + d;
+        if (a.xop) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+          a.xop[(size_t)b * a.xop_ld + col] = hi;
+          a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        } else {
+          a.out[col] = x;
+        }
       }
     }
   }
   tc_fence_before();
+  if (clustered) {   // no CTA ends while a peer may still store into it
+    if (!cl_waited) cl_wait();
+    cl_arrive();
+    cl_wait();
+  }
   __syncthreads();
   if (threadIdx.x == 0) ktrace(a.tr, 5);
   if (warp == 1) tmem_dealloc(taddr, TCOLS);
@@ -551,11 +608,21 @@ cudaError_t launch_g(const AttnTcArgs &a, cudaStream_t st, bool pdl) {
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = attn_tc_smem(HD, a.nstages);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (a.n_split < 1 || a.n_split > kMaxSplit) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;   // the splits of one KV head
+  attr[na].val.clusterDim.x = a.n_split;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, k_attn_tc<HD, G>, a);
 }
 
@@ -584,10 +651,12 @@ cudaError_t prepare_hd_tc() {
 
 int attn_tc_stages(int head_dim) { return 3; }
 
+int attn_tc_max_split() { return kMaxSplit; }
+
 int attn_tc_smem(int head_dim, int nstages) {
   const int stage = 2 * (head_dim / 64) * kBox;
   const int p_tiles = head_dim == 128 ? 2 * 2 * 2048 : 2 * 2 * kBox;
-  return 1024 + nstages * stage + p_tiles + (head_dim / 64) * 2048 + 1024;
+  return 1024 + nstages * stage + p_tiles + (head_dim / 64) * 2048 + 1024 + merge_floats(head_dim) * 4;
 }
 
 cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl) {

@@ -224,10 +224,9 @@ struct AttnTcArgs {
   const float *q;          // [slots][n_head][hd]
   const void *maps;        // one sequence: its state's [layer][K|V] tensor maps
   int layer;
-  int n_head, n_kv, cap, window, n_split;
+  int n_head, n_kv, cap, window;
+  int n_split;             // CTAs per KV head (one cluster), 1 .. attn_tc_max_split()
   float qscale;            // log2(e) / sqrt(hd)
-  float *part;             // [slots][n_head][n_split][hd + 2]
-  unsigned *counter;       // [slots][n_kv], zero between launches
   float *out;              // one sequence: [n_head][hd]
   __nv_bfloat16 *xop;      // batched: o-proj operand rows b (hi) and bp + b (lo)
   int xop_ld, bp, nb;
@@ -241,6 +240,7 @@ struct AttnTcArgs {
 cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl);
 int attn_tc_smem(int head_dim, int nstages);
 int attn_tc_stages(int head_dim);
+int attn_tc_max_split();
 cudaError_t prepare_attn_tc_kernels();
 
 // Epilogues of the batched tensor-core GEMM
