@@ -49,6 +49,9 @@ def parse():
                     help="use only the first N layers (small cases for ncu captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="slots of a batched workload (default: the workload's own)")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="instead of decode steps, time pnb_prefill of this many prompt tokens "
+                         "from position 0 (one step = one prefill)")
     return ap.parse_args()
 
 
@@ -535,6 +538,74 @@ def run_batched(args, w):
     return 0
 
 
+def run_prefill(args, w):
+    """Prompt tokens per second of pnb_prefill: a seeded prompt of --prefill
+    tokens fed to a state from position 0, --steps times (the position is set
+    back to 0 before each; the prefill rewrites every cache position it reads)."""
+    import torch
+
+    import synth.workloads as wl
+    import transformer_decode_step_gb300 as pnb
+
+    rank, world, local = dist_setup(args.gpus)
+    if world > 1 and rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    s = w.shape
+    T = min(args.prefill, s.n_ctx)
+    sm = pnb.SynthModel(s, w.seed)
+    st = sm.new_state()
+    rng = __import__("numpy").random.default_rng(w.seed)
+    prompt = torch.tensor(rng.integers(0, s.n_vocab, size=T), dtype=torch.int32, device="cuda")
+    am = torch.empty(T, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        st.set_pos(0)
+        st.prefill(prompt, argmax=am)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = 0.0
+    for _ in range(args.steps):
+        st.set_pos(0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st.prefill(prompt, argmax=am)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms += e0.elapsed_time(e1)
+    clocks.stop()
+    err = st.device_error()
+    # end to end: the prompt from pinned host memory, the last greedy token back
+    pinned = prompt.cpu().pin_memory()
+    out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    tk = torch.empty_like(prompt)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.set_pos(0)
+        tk.copy_(pinned, non_blocking=True)
+        st.prefill(tk, argmax=am)
+        out.copy_(am[-1:], non_blocking=True)
+        stream.synchronize()
+    e2e = T * args.steps / (time.perf_counter() - t0)
+    tps = T * args.steps / (ms / 1000.0)
+    chunks = -(-T // 64)
+    line = {"metric": "prefill_tokens_per_s", "value": tps, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded generated weights, seeded prompt)",
+            "config": workload_config(w, {"prefill_tokens": T, "chunks_of_64": chunks,
+                                          "parallelism": "replicas x1"}),
+            "weight_bytes_per_chunk": s.params_read_per_token() * s.elem_bytes,
+            "clocks": clocks.summary(), "device_error": err,
+            "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * T,
+                    "d2h_bytes_per_step": 4, "how": "prompt copied from pinned host memory, "
+                    "the last greedy token read back, per prefill"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     import dataclasses
@@ -548,6 +619,8 @@ def main():
     __graft_entry__.build(import_package=args.impl == "ours")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.prefill:
+        return run_prefill(args, w)
     if w.batch > 1:
         return run_batched(args, w)
     return run_ours(args, w)

@@ -237,6 +237,26 @@ enum { PNB_FUSED_OFF = 0, PNB_FUSED_ATTN_OPROJ = 1, PNB_FUSED_BLOCK = 2 };
 int pnb_model_set_fused_attention(pnb_model *m, int mode);
 int pnb_model_fused_attention(const pnb_model *m);
 
+/* Prefill: feed T >= 1 prompt tokens (tokens_dev [T], device int32) to a
+   state, advancing its position by T, with every token's logits and greedy
+   token written like a step's ("Core Engine API": the engine's prefill entry
+   point; "Engine Architecture", "Chunked prefill").
+   Chunks of up to 64 tokens run as one batched step of "virtual slots" that
+   share the state's KV cache at positions pos .. pos + n - 1. Their K / V are
+   stored by the chunk's QKV kernel before its attention kernel reads them,
+   and each token attends to the positions up to its own. A sliding-window
+   ring must not wrap inside a chunk, so once the ring is full the remaining
+   tokens go one per step, as do models the batched step does not cover (MoE,
+   fp32); a chunk of one token is a single-sequence step.
+   logits_dev: optional [T][n_vocab] fp32 (16-byte aligned); argmax_dev:
+   optional [T]. After the call the state's device token is the last token's
+   argmax (PNB_TOKEN_PREV continues from it). Stream-ordered; it uses the
+   model's batched workspace, so prefills and batched steps of one model must
+   not overlap on the GPU. Returns PNB_E_CTX_FULL when pos + T > n_ctx and
+   PNB_E_INVAL when T < 1. */
+int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T, pnb_stream stream,
+                float *logits_dev, int32_t *argmax_dev);
+
 /* Number of this library's kernels one step launches (single sequence when
    B == 0, batched otherwise). */
 int pnb_step_kernel_count(const pnb_model *m, int32_t B);

@@ -62,6 +62,7 @@ _SIGS = {
     "pnb_state_check": (_i32, [_p, _p]),
     "pnb_forward": (_i32, [_p, _p, _i32, _p, _p, _p]),
     "pnb_forward_batch": (_i32, [_p, _p, _i32, _p, _p, _p, _p]),
+    "pnb_prefill": (_i32, [_p, _p, _p, _i32, _p, _p, _p]),
     "pnb_model_set_graphs": (_i32, [_p, _i32]),
     "pnb_model_set_persistent": (_i32, [_p, _i32]),
     "pnb_model_is_persistent": (_i32, [_p]),
@@ -227,6 +228,12 @@ class State:
     def forward(self, token: int, logits=None, argmax=None, stream=None):
         check(pnb_forward(self.model.handle, self._h, token, _stream(stream), _ptr(logits),
                           _ptr(argmax)), "pnb_forward")
+
+    def prefill(self, tokens, logits=None, argmax=None, stream=None):
+        """Feed the prompt `tokens` (device int32 tensor [T]); logits [T][n_vocab]
+        and argmax [T] optional device tensors."""
+        check(pnb_prefill(self.model.handle, self._h, _ptr(tokens), int(tokens.numel()),
+                          _stream(stream), _ptr(logits), _ptr(argmax)), "pnb_prefill")
 
     def reset(self, stream=None):
         check(pnb_state_reset(self._h, _stream(stream)), "pnb_state_reset")

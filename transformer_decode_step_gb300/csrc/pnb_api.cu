@@ -126,6 +126,7 @@ struct BatchCtx {
   float *xb = nullptr, *qb = nullptr, *apart = nullptr, *gpart = nullptr, *am_val = nullptr;
   unsigned *acnt = nullptr, *tile_cnt = nullptr, *am_cnt = nullptr;
   int32_t *am_idx = nullptr, *pos = nullptr, *err = nullptr;
+  StepIO *pio = nullptr;                 // prefill: the I/O words of a chunk's virtual slots
   __nv_bfloat16 *xop_e = nullptr, *xop_o = nullptr, *xop_f = nullptr;
   float2 *rope = nullptr;
   BSlot *slots = nullptr;
@@ -755,7 +756,7 @@ int batch_setup(pnb_model *m) {
   const size_t o_slots = take((size_t)MB * sizeof(BSlot));
   const size_t o_gp = take((size_t)std::max<int64_t>(gpart, 1) * 4), o_tc = take((size_t)tiles * 4);
   const size_t o_amv = take((size_t)MB * m->num_sms * 4), o_ami = take((size_t)MB * m->num_sms * 4);
-  const size_t o_amc = take(4), o_err = take(4);
+  const size_t o_amc = take(4), o_err = take(4), o_pio = take((size_t)MB * sizeof(StepIO));
   if (cudaMalloc(&b->ws, off) != cudaSuccess) {
     delete b;
     return PNB_E_NOMEM;
@@ -780,6 +781,7 @@ int batch_setup(pnb_model *m) {
   b->am_idx = reinterpret_cast<int32_t *>(b->ws + o_ami);
   b->am_cnt = reinterpret_cast<unsigned *>(b->ws + o_amc);
   b->err = reinterpret_cast<int32_t *>(b->ws + o_err);
+  b->pio = reinterpret_cast<StepIO *>(b->ws + o_pio);
   bool ok = true;
   b->w_qkv.resize(L);
   b->w_o.resize(L);
@@ -843,8 +845,8 @@ BGemmArgs bgemm_args(const pnb_model *m, const BatchCtx *b, const BPlan &p, int 
 // down GEMM (residual); then the final norm and the LM-head GEMM (argmax,
 // position advance).  The first kernel waits for all earlier stream work;
 // every later one uses programmatic stream serialization.
-cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const int32_t *tokens,
-                          cudaStream_t st, float *logits, int32_t *argmax) {
+cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t *tokens,
+                          unsigned long long *trace, cudaStream_t st, float *logits, int32_t *argmax) {
   BatchCtx *b = m->batch;
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, Hd = c.n_head * m->hd, F = c.n_ff;
@@ -869,8 +871,7 @@ cudaError_t enqueue_batch(pnb_model *m, pnb_state *const *states, int B, const i
   na.hd = m->hd;
   na.n_ctx = c.n_ctx;
   na.err = b->err;
-  for (int i = 0; i < B; ++i) na.slots[i] = BSlot{states[i]->kv, states[i]->io, states[i]->maps};
-  unsigned long long *trace = states[0]->ktrace;   // optional, the first slot's buffer
+  for (int i = 0; i < B; ++i) na.slots[i] = slots[i];
   for (int l = 0; l < c.n_layer; ++l) {
     na.emb = l == 0 ? m->tok_embd : nullptr;
     na.tokens = l == 0 ? tokens : nullptr;
@@ -1354,8 +1355,11 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
   if ((rc = batch_setup(m)) != PNB_OK) return rc;
   BatchCtx *b = m->batch;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  BSlot slots[kMaxBatch];
+  for (int i = 0; i < B; ++i) slots[i] = BSlot{states[i]->kv, states[i]->io, states[i]->maps};
+  unsigned long long *trace = states[0]->ktrace;   // optional, the first slot's buffer
   if (!m->graphs) {
-    if (enqueue_batch(m, states, B, tokens_dev, st, logits_dev, argmax_dev) != cudaSuccess)
+    if (enqueue_batch(m, slots, B, tokens_dev, trace, st, logits_dev, argmax_dev) != cudaSuccess)
       return PNB_E_CUDA;
   } else {
     const bool same = b->exec && b->g_B == B && b->g_gen == m->mode_gen && b->g_tokens == tokens_dev &&
@@ -1370,7 +1374,7 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
       cudaGraph_t graph = nullptr;
       if (cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
         return PNB_E_CUDA;
-      cudaError_t le = enqueue_batch(m, states, B, tokens_dev, m->cap_stream, logits_dev, argmax_dev);
+      cudaError_t le = enqueue_batch(m, slots, B, tokens_dev, trace, m->cap_stream, logits_dev, argmax_dev);
       cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &graph);
       if (le != cudaSuccess || ce != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);
@@ -1392,6 +1396,52 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
     if (cudaGraphLaunch(b->exec, st) != cudaSuccess) return PNB_E_CUDA;
   }
   for (int i = 0; i < B; ++i) states[i]->pos += 1;
+  return PNB_OK;
+}
+
+int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T, pnb_stream stream,
+                float *logits_dev, int32_t *argmax_dev) {
+  if (!m || !s || !tokens_dev) return PNB_E_NULL;
+  if (s->m != m || T < 1) return PNB_E_INVAL;
+  if ((logits_dev && !aligned16(logits_dev)) ||
+      (argmax_dev && (reinterpret_cast<uintptr_t>(argmax_dev) & 3u)) ||
+      (reinterpret_cast<uintptr_t>(tokens_dev) & 3u))
+    return PNB_E_ALIGN;
+  const pnb_config &c = m->cfg;
+  if ((int64_t)s->pos + T > c.n_ctx) return PNB_E_CTX_FULL;
+  int rc = check_device(m);
+  if (rc != PNB_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool batched = c.expert_count == 0 && c.dtype == PNB_BF16 && c.n_embd % 64 == 0 &&
+                       (c.n_head * m->hd) % 64 == 0 && c.n_ff % 64 == 0;
+  if (batched && (rc = batch_setup(m)) != PNB_OK) return rc;
+  const bool ring = c.sliding_window > 0 && m->cap < c.n_ctx;
+  const size_t V = (size_t)c.n_vocab;
+  for (int i = 0; i < T;) {
+    int n = std::min(kMaxBatch, T - i);
+    // a ring cache must not wrap inside a chunk: a later chunk position would
+    // overwrite a slot inside an earlier chunk token's window
+    if (ring) n = s->pos >= m->cap ? 1 : std::min(n, m->cap - s->pos);
+    float *lg = logits_dev ? logits_dev + (size_t)i * V : nullptr;
+    int32_t *am = argmax_dev ? argmax_dev + i : nullptr;
+    if (n == 1 || !batched) {
+      // one token: the single-sequence step (launched directly, not as a graph)
+      n = 1;
+      if (launch_copy_token(s->io, tokens_dev + i, st) != cudaSuccess ||
+          enqueue_step(m, s, st, lg, am) != cudaSuccess)
+        return PNB_E_CUDA;
+    } else {
+      BatchCtx *b = m->batch;
+      BSlot slots[kMaxBatch];
+      for (int j = 0; j < n; ++j) slots[j] = BSlot{s->kv, &b->pio[j], s->maps};
+      if (launch_prefill_begin(b->pio, s->io, n, st) != cudaSuccess ||
+          enqueue_batch(m, slots, n, tokens_dev + i, nullptr, st, lg, am) != cudaSuccess ||
+          launch_prefill_end(s->io, b->pio, n, st) != cudaSuccess)
+        return PNB_E_CUDA;
+    }
+    s->pos += n;
+    i += n;
+  }
   return PNB_OK;
 }
 

@@ -300,6 +300,21 @@ __global__ void __launch_bounds__(256, 1) k_router(const RouterArgs a) {
   }
 }
 
+// Prefill chunks: n virtual slots at the state's next n positions; then the
+// state takes the last slot's token and position and every slot's error bits.
+__global__ void k_prefill_begin(StepIO *pio, const StepIO *state, int n) {
+  const int b = threadIdx.x;
+  if (b < n) pio[b] = StepIO{0, state->pos + b, 0, 0};
+}
+__global__ void k_prefill_end(StepIO *state, const StepIO *pio, int n) {
+  if (threadIdx.x != 0) return;
+  int32_t e = 0;
+  for (int b = 0; b < n; ++b) e |= pio[b].error;
+  state->token = pio[n - 1].token;
+  state->pos = pio[n - 1].pos;
+  if (e) set_error(&state->error, e);
+}
+
 __global__ void k_set_token(StepIO *io, int32_t token) { io->token = token; }
 __global__ void k_copy_token(StepIO *io, const int32_t *token) { io->token = *token; }
 __global__ void k_set_pos(StepIO *io, int32_t pos) { io->pos = pos; }
@@ -390,6 +405,14 @@ cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st) {
 }
 cudaError_t launch_copy_token(StepIO *io, const int32_t *token, cudaStream_t st) {
   k_copy_token<<<1, 1, 0, st>>>(io, token);
+  return cudaGetLastError();
+}
+cudaError_t launch_prefill_begin(StepIO *pio, const StepIO *state, int n, cudaStream_t st) {
+  k_prefill_begin<<<1, 64, 0, st>>>(pio, state, n);
+  return cudaGetLastError();
+}
+cudaError_t launch_prefill_end(StepIO *state, const StepIO *pio, int n, cudaStream_t st) {
+  k_prefill_end<<<1, 32, 0, st>>>(state, pio, n);
   return cudaGetLastError();
 }
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st) {

@@ -395,6 +395,10 @@ cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGe
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st);
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st);
 cudaError_t launch_copy_token(StepIO *io, const int32_t *token, cudaStream_t st);
+// prefill chunk of n <= 64 virtual slots: pio[b] = {pos: state->pos + b}; then
+// the state takes pio[n - 1]'s token and position and every slot's error bits
+cudaError_t launch_prefill_begin(StepIO *pio, const StepIO *state, int n, cudaStream_t st);
+cudaError_t launch_prefill_end(StepIO *state, const StepIO *pio, int n, cudaStream_t st);
 
 // batched step (tensor maps are CUtensorMap, passed by value)
 cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl);
