@@ -62,7 +62,8 @@ def step_bytes(shape, pos: int) -> int:
     (one embedding row, all projections of the chosen experts, router, norms,
     LM head), KV entries attended (window-limited) and the new KV entry."""
     es = shape.elem_bytes
-    weights = shape.params_read_per_token() * es + (2 * shape.n_layer + 1) * shape.n_embd * 4
+    weights = int(shape.params_read_per_token() * shape.weight_bytes_per_param) + \
+        (2 * shape.n_layer + 1) * shape.n_embd * 4
     n_att = pos + 1 if shape.sliding_window <= 0 else min(pos + 1, shape.sliding_window)
     per_pos = shape.n_layer * 2 * shape.n_kv_head * shape.head_dim * es
     return weights + n_att * per_pos + per_pos
@@ -72,7 +73,7 @@ def gateup_bytes(shape) -> int:
     """Algorithmic bytes of one gate/up launch: the chosen experts' [2F][E]
     weights, the residual and norm vectors read, the SwiGLU output written."""
     k = shape.expert_used if shape.expert_count > 0 else 1
-    return k * 2 * shape.n_ff * shape.n_embd * shape.elem_bytes + 2 * shape.n_embd * 4 + \
+    return k * shape.matrix_bytes(2 * shape.n_ff, shape.n_embd) + 2 * shape.n_embd * 4 + \
         k * shape.n_ff * 4
 
 
@@ -236,7 +237,7 @@ def workload_config(w, extra=None, batch=None):
                        + (f" window{s.sliding_window}" if s.sliding_window else "")
                        + (f" experts{s.expert_count}top{s.expert_used}" if s.expert_count else "")
                        + f", KV pre-filled to {w.prefill}, greedy decode of {w.steps} tokens, batch {batch}",
-           "batch": batch, "weights_dtype": "bf16" if s.dtype == 1 else "f32",
+           "batch": batch, "weights_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype],
            "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)"}
     if extra:
         cfg.update(extra)
@@ -376,7 +377,7 @@ def run_ours(args, w):
         line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic (seeded generated weights and KV cache)",
+                "dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype], "data": "synthetic (seeded generated weights and KV cache)",
                 "config": workload_config(w, {"parallelism": f"replicas x{world}",
                                               "positions": f"{P}..{P + budget - 1}"}),
                 "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
@@ -405,7 +406,8 @@ def batch_step_bytes(shape, positions) -> int:
     """Algorithmic HBM bytes of one batched step: the weights once, each slot's
     attended KV entries and its new entry."""
     es = shape.elem_bytes
-    weights = shape.params_read_per_token() * es + (2 * shape.n_layer + 1) * shape.n_embd * 4
+    weights = int(shape.params_read_per_token() * shape.weight_bytes_per_param) + \
+        (2 * shape.n_layer + 1) * shape.n_embd * 4
     per_pos = shape.n_layer * 2 * shape.n_kv_head * shape.head_dim * es
     kv = 0
     for p in positions:
@@ -597,7 +599,7 @@ def run_prefill(args, w):
             "data": "synthetic (seeded generated weights, seeded prompt)",
             "config": workload_config(w, {"prefill_tokens": T, "chunks_of_64": chunks,
                                           "parallelism": "replicas x1"}),
-            "weight_bytes_per_chunk": s.params_read_per_token() * s.elem_bytes,
+            "weight_bytes_per_chunk": int(s.params_read_per_token() * s.weight_bytes_per_param),
             "clocks": clocks.summary(), "device_error": err,
             "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * T,
                     "d2h_bytes_per_step": 4, "how": "prompt copied from pinned host memory, "

@@ -32,8 +32,11 @@
  * does the same: every intermediate vector is stored as fp32, while every
  * reduction (dot product, sum of squares, softmax sum) is accumulated in fp64
  * and rounded once to fp32.  Weights and the KV cache hold their storage type
- * (fp32, or bf16 values widened exactly to fp32).  New K/V entries are
- * rounded fp32 -> bf16 (nearest even) before they are stored when the cache
+ * (fp32, or bf16 values widened exactly to fp32; Q8 weights are their
+ * block's fp16 scale times the int8 value, the dequantization of a GGUF
+ * Q8_0 block: "Engine Architecture", "Weight Loading Modes", quantized mode,
+ * per-block dequantization inside the matvec - exact in fp32).  New K/V
+ * entries are rounded fp32 -> bf16 (nearest even) before they are stored when the cache
  * is bf16; the argmax is taken over the fp32 logits, lowest id on ties.
  */
 #include <math.h>
@@ -52,7 +55,8 @@ typedef struct {
   int32_t sliding_window; /* 0 = no window */
   int32_t expert_count;   /* 0 = dense FFN */
   int32_t expert_used;    /* top-k */
-  int32_t dtype;          /* storage of weights and KV: 0 fp32, 1 bf16 */
+  int32_t dtype;          /* storage of weights: 0 fp32, 1 bf16, 2 Q8 (blocks of 32: int8
+                             values times an fp16 scale); KV: fp32 for 0, bf16 otherwise */
 } orc_config;
 
 enum { ORC_EXPLICIT = 0, ORC_SYNTH = 1, ORC_CONST = 2 };
@@ -123,6 +127,17 @@ static const orc_tensor *ltensor(const orc_model *m, int l, int slot) {
 static void get_row(const orc_tensor *t, int64_t r, int64_t cols, int dtype, float *out) {
   if (t->mode == ORC_EXPLICIT) {
     memcpy(out, t->data + r * cols, (size_t)cols * sizeof(float));
+  } else if (t->mode == ORC_SYNTH && dtype == SYNTH_Q8) {
+    /* Q8 weights: per block of 32, the weight is the block's fp16 scale
+       times the element's int8 value (GGUF Q8_0 dequantization) */
+    const uint64_t base = (uint64_t)(r * cols);
+    for (int64_t b = 0; b + SYNTH_Q8_BLOCK <= cols; b += SYNTH_Q8_BLOCK) {
+      int8_t q[SYNTH_Q8_BLOCK];
+      uint16_t d;
+      synth_q8_block(t->key, base + (uint64_t)b, t->sigma, q, &d);
+      const float df = synth_f16_to_f32(d);
+      for (int j = 0; j < SYNTH_Q8_BLOCK; ++j) out[b + j] = df * (float)q[j];
+    }
   } else if (t->mode == ORC_SYNTH) {
     const uint64_t base = (uint64_t)(r * cols);
     for (int64_t c = 0; c < cols; ++c) out[c] = synth_value(t->key, base + (uint64_t)c, t->sigma, dtype);
@@ -361,7 +376,8 @@ int orc_state_prefill_synth(orc_state *s, uint64_t seed, uint32_t sub, int64_t j
 #pragma omp parallel for schedule(static)
       for (int64_t j = j_lo; j < P; ++j)
         for (int64_t e = 0; e < per_pos; ++e)
-          dst[j * per_pos + e] = synth_value(key, (uint64_t)(j * per_pos + e), sigma, c->dtype);
+          dst[j * per_pos + e] = synth_value(key, (uint64_t)(j * per_pos + e), sigma,
+                                             c->dtype == SYNTH_F32 ? SYNTH_F32 : SYNTH_BF16);
     }
   }
   s->pos = P;

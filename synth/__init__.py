@@ -19,7 +19,7 @@ _DIR = os.path.dirname(os.path.abspath(__file__))
 HOST_LIB = os.path.join(_DIR, "libsynth_host.so")
 CUDA_LIB = os.path.join(_DIR, "libsynth_cuda.so")
 
-F32, BF16 = 0, 1
+F32, BF16, Q8 = 0, 1, 2
 
 TOK_EMBD, ATTN_NORM, WQ, WK, WV, WO, FFN_NORM = 1, 2, 3, 4, 5, 6, 7
 WGATE, WUP, WDOWN, WROUTER, OUT_NORM, OUTPUT = 8, 9, 10, 11, 12, 13
@@ -29,7 +29,7 @@ KCACHE, VCACHE, TOKENS, POSITIONS = 14, 15, 16, 17
 def build_commands(cuda_arch: str = "103a"):
     """Compiler command lines that build this package's shared libraries."""
     host = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-o", HOST_LIB,
-            os.path.join(_DIR, "synth_host.c")]
+            os.path.join(_DIR, "synth_host.c"), "-lm"]
     dev = ["nvcc", "-O3", "-shared", "-Xcompiler", "-fPIC", "-std=c++17", "-fmad=false",
            f"-gencode=arch=compute_{cuda_arch},code=sm_{cuda_arch}",
            "-o", CUDA_LIB, os.path.join(_DIR, "synth_cuda.cu")]
@@ -57,6 +57,11 @@ def _host():
         lib.synth_host_words.argtypes = [p, u64, u64, i64]
         lib.synth_host_f32_to_bf16.restype = ctypes.c_uint16
         lib.synth_host_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.synth_host_fill_q8_rows.argtypes = [p, p, u64, i64, i64, i64, ctypes.c_float]
+        lib.synth_host_f32_to_f16.restype = ctypes.c_uint16
+        lib.synth_host_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.synth_host_f16_to_f32.restype = ctypes.c_float
+        lib.synth_host_f16_to_f32.argtypes = [ctypes.c_uint16]
         _host_lib = lib
     return _host_lib
 
@@ -121,6 +126,23 @@ def words(k: int, n0: int, n: int) -> np.ndarray:
 
 def f32_to_bf16_bits(x: float) -> int:
     return int(_host().synth_host_f32_to_bf16(x))
+
+
+def f32_to_f16_bits(x: float) -> int:
+    return int(_host().synth_host_f32_to_f16(x))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(_host().synth_host_f16_to_f32(h))
+
+
+def q8_rows(k: int, row0: int, nrows: int, cols: int, sigma: float):
+    """Q8 rows [row0, row0 + nrows) of a [.][cols] matrix: (the row bytes in the
+    library's layout, uint8 [nrows][cols + cols / 16]; the weights d * q, fp32)."""
+    raw = np.empty((nrows, cols + cols // 16), dtype=np.uint8)
+    w = np.empty((nrows, cols), dtype=np.float32)
+    _host().synth_host_fill_q8_rows(raw.ctypes.data, w.ctypes.data, k, row0, nrows, cols, sigma)
+    return raw, w
 
 
 # ---------------------------------------------------------------- device side

@@ -28,6 +28,7 @@
 #ifndef SYNTH_H
 #define SYNTH_H
 
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -39,8 +40,9 @@
 
 #define SYNTH_GAMMA 0x9E3779B97F4A7C15ULL
 
-/* storage types of generated values */
-enum { SYNTH_F32 = 0, SYNTH_BF16 = 1 };
+/* storage types of generated values (SYNTH_Q8: weight matrices only, in
+   blocks of 32 along a row; see synth_q8_block) */
+enum { SYNTH_F32 = 0, SYNTH_BF16 = 1, SYNTH_Q8 = 2 };
 
 /* logical tensor kinds (part of a stream key) */
 enum {
@@ -120,6 +122,73 @@ SYNTH_FN float synth_value(uint64_t key, uint64_t idx, float sigma, int dtype) {
   float v = synth_normal_f32(key, idx, sigma);
   return dtype == SYNTH_BF16 ? synth_bf16_to_f32(synth_f32_to_bf16(v)) : v;
 }
+
+/* fp32 -> IEEE binary16 bit pattern, round to nearest even, for finite
+   non-negative inputs below 65520 (normal and subnormal results) */
+SYNTH_FN uint16_t synth_f32_to_f16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  const int e = (int)(u >> 23) - 127 + 15;    /* biased binary16 exponent */
+  const uint32_t m = (u & 0x7FFFFFu) | (e > -64 ? 0x800000u : 0u);
+  if ((u & 0x7FFFFFFFu) == 0u) return 0;
+  if (e >= 1) {                                /* normal: drop 13 mantissa bits */
+    uint32_t h = ((uint32_t)e << 10) | ((u & 0x7FFFFFu) >> 13);
+    const uint32_t rem = u & 0x1FFFu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) ++h;
+    return (uint16_t)h;
+  }
+  const int sh = 14 - e;                       /* subnormal: value = m * 2^(e - 15 - 23 + 1) */
+  if (sh > 24) return 0;
+  uint32_t h = m >> sh;
+  const uint32_t rem = m & ((1u << sh) - 1u), half = 1u << (sh - 1);
+  if (rem > half || (rem == half && (h & 1u))) ++h;
+  return (uint16_t)h;
+}
+
+/* IEEE binary16 bit pattern (finite, non-negative) -> fp32, exact */
+SYNTH_FN float synth_f16_to_f32(uint16_t h) {
+  const uint32_t e = (h >> 10) & 0x1Fu, m = h & 0x3FFu;
+  uint32_t u;
+  if (e == 0) {
+    if (m == 0) return 0.0f;
+    return (float)m * (1.0f / 16777216.0f);   /* m * 2^-24, exact */
+  }
+  u = ((e - 15u + 127u) << 23) | (m << 13);
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Q8 weights, in blocks of 32 consecutive elements of a row (element indices
+   idx0 .. idx0 + 31, idx0 a multiple of 32): w_i are the generated fp32
+   values; the block's scale is d = fp16(max_i |w_i| / 127) (one fp32
+   division, one rounding to fp16, nearest even); q_i = w_i / float(d)
+   rounded to the nearest integer (ties to even, rintf) and clamped to
+   [-127, 127], or 0 when d is 0.  The element's weight is float(d) * q_i,
+   exact in fp32. */
+#define SYNTH_Q8_BLOCK 32
+SYNTH_FN void synth_q8_block(uint64_t key, uint64_t idx0, float sigma, int8_t *q, uint16_t *d_out) {
+  float w[SYNTH_Q8_BLOCK];
+  float amax = 0.0f;
+  for (int i = 0; i < SYNTH_Q8_BLOCK; ++i) {
+    w[i] = synth_normal_f32(key, idx0 + (uint64_t)i, sigma);
+    const float a = w[i] < 0.0f ? -w[i] : w[i];
+    if (a > amax) amax = a;
+  }
+  const uint16_t d = synth_f32_to_f16(amax / 127.0f);
+  const float df = synth_f16_to_f32(d);
+  for (int i = 0; i < SYNTH_Q8_BLOCK; ++i) {
+    float r = df > 0.0f ? rintf(w[i] / df) : 0.0f;
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    q[i] = (int8_t)r;
+  }
+  *d_out = d;
+}
+
+/* bytes of one Q8 row of `cols` weights: the int8 values, then one fp16
+   scale per 32 (the layout of the decode-step library's Q8 matrices) */
+SYNTH_FN int64_t synth_q8_row_bytes(int64_t cols) { return cols + cols / 16; }
 
 /* uniform integer in [lo, lo + n) for element idx (multiply-shift on 32 high bits) */
 SYNTH_FN int64_t synth_uniform_int(uint64_t key, uint64_t idx, int64_t lo, uint32_t n) {

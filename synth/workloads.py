@@ -6,7 +6,8 @@ decoder with a 4096-position sliding window, a Mixtral-shaped 8-expert top-2
 MoE decoder and a Llama-8B-shaped batched-slot decoder.  The recipe:
 
 * weights (embeddings, projections, router, LM head) ~ N(0, 0.02^2), stored in
-  the model's dtype; every norm weight is 1.0 (fp32);
+  the model's dtype (Q8: blocks of 32 quantized as the generator defines);
+  every norm weight is 1.0 (fp32);
 * the KV cache of positions below the start position ~ N(0, 1) in the cache
   dtype (raw cache contents, i.e. keys already rotated);
 * prompt / start tokens uniform in [0, n_vocab); batched slot s starts at a
@@ -18,7 +19,7 @@ from __future__ import annotations
 from dataclasses import dataclass, field, replace
 from typing import List, Optional
 
-from . import (ATTN_NORM, BF16, F32, FFN_NORM, OUT_NORM, OUTPUT, POSITIONS, TOK_EMBD,
+from . import (ATTN_NORM, BF16, F32, FFN_NORM, OUT_NORM, OUTPUT, POSITIONS, Q8, TOK_EMBD,
                TOKENS, WDOWN, WGATE, WK, WO, WQ, WROUTER, WUP, WV, key, uniform_int)
 
 WEIGHT_SIGMA = 0.02
@@ -55,7 +56,23 @@ class Shape:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == BF16 else 4
+        """Bytes of one KV-cache element (bf16 for bf16 and Q8 weights)."""
+        return 4 if self.dtype == F32 else 2
+
+    @property
+    def kv_dtype(self) -> int:
+        return F32 if self.dtype == F32 else BF16
+
+    def matrix_bytes(self, rows: int, cols: int) -> int:
+        """Bytes of a [rows][cols] weight matrix in the library's layout (Q8 rows:
+        cols int8 values, then one fp16 scale per 32)."""
+        if self.dtype == Q8:
+            return rows * (cols + cols // 16)
+        return rows * cols * (4 if self.dtype == F32 else 2)
+
+    @property
+    def weight_bytes_per_param(self) -> float:
+        return {F32: 4.0, BF16: 2.0, Q8: 1.0625}[self.dtype]
 
     def params_read_per_token(self) -> int:
         """Weight elements one decode step reads (top-k experts only for MoE)."""

@@ -520,3 +520,59 @@ def test_step_in_parts_equals_forward():
         lb, amb = b.head(x)
         b.pos = b.pos + 1
         assert np.array_equal(la, lb) and ama == amb
+
+
+# ------------------------------------------------------------------ Q8 weights
+
+def test_f16_conversion_matches_numpy():
+    """The generator's fp32 -> fp16 rounding (nearest even) is numpy's, normal and subnormal."""
+    vals = np.concatenate([RNG.uniform(1e-8, 6.1e-5, 2000), RNG.uniform(6.1e-5, 6.0e4, 4000),
+                           np.float32(1.0) + np.float32(2.0 ** -11) * np.arange(8, dtype=np.float32),
+                           [0.0, 5.960464477539063e-08, 6.103515625e-05, 65504.0]]).astype(np.float32)
+    for v in vals:
+        want = int(np.float32(v).astype(np.float16).view(np.uint16))
+        got = synth.f32_to_f16_bits(float(v))
+        assert got == want, (float(v), hex(got), hex(want))
+        assert synth.f16_to_f32(got) == float(np.uint16(want).view(np.float16).astype(np.float32))
+
+
+@pytest.mark.parametrize("cols,sigma", [(64, 0.02), (256, 1.0), (96, 3e-4)])
+def test_q8_blocks_follow_their_definition(cols, sigma):
+    """Each block of 32: d = fp16(max|w| / 127), q = clip(rint(w / d), -127, 127), from the
+    generator's fp32 values, recomputed here with numpy; an unclamped weight d * q is
+    within d / 2 of w (sigma 3e-4 gives subnormal fp16 scales)."""
+    k = synth.key(5, synth.WQ, 3, 0)
+    rows = 6
+    raw, deq = synth.q8_rows(k, 2, rows, cols, sigma)
+    for r in range(rows):
+        w = synth.values(k, (2 + r) * cols, cols, sigma, F32)
+        q = raw[r, :cols].view(np.int8)
+        d = raw[r, cols:].view(np.uint16)
+        for b in range(cols // 32):
+            wb = w[32 * b:32 * b + 32]
+            dw = (np.float32(np.max(np.abs(wb))) / np.float32(127)).astype(np.float16)
+            assert d[b] == dw.view(np.uint16)
+            df = np.float32(dw)
+            qw = np.clip(np.rint(wb / df), -127, 127).astype(np.int8)
+            assert np.array_equal(q[32 * b:32 * b + 32], qw)
+            assert np.array_equal(deq[r, 32 * b:32 * b + 32], df * qw.astype(np.float32))
+            inner = np.abs(qw) < 127   # clamped values (a coarse subnormal d) excepted
+            assert np.all(np.abs(wb - df * qw)[inner] <= 0.5 * df * (1 + 2.0 ** -9))
+            if df >= 2.0 ** -14:   # normal fp16 scale: the largest value uses the range
+                assert np.max(np.abs(qw)) >= 126
+
+
+def test_q8_model_is_the_model_of_its_dequantized_weights():
+    """A seeded Q8 oracle model equals the bf16-cache model given d * q explicitly."""
+    shape = dataclasses.replace(TS, dtype=synth.Q8, n_embd=64, n_head=4, n_kv_head=2, n_ff=96)
+    arrays = {}
+    for spec in wl.weight_specs(shape):
+        k = spec.name if spec.name in ("tok_embd", "out_norm", "output") else (spec.name, spec.layer, spec.sub)
+        if spec.const is None:
+            arrays[k] = synth.q8_rows(spec.key(11), 0, spec.rows, spec.cols, wl.WEIGHT_SIGMA)[1]
+    a, _ = _oracle_run(dataclasses.replace(shape, dtype=BF16), arrays, [1, 2, 3])
+    m = oracle.Model(shape, seed=11)
+    s = m.new_state()
+    b = [s.forward(t)[0] for t in [1, 2, 3]]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

@@ -4,7 +4,8 @@ The seeded generator (``synth``) writes every weight and pre-filled cache
 entry straight into device memory; the values equal the host generator's, so
 the CPU oracle sees the same model.  Layout per include/pnb.h: Wq, Wk, Wv
 rows stacked into one [(n_head + 2 n_kv_head) hd][n_embd] matrix; gate and
-up rows interleaved (row 2i = gate row i, row 2i+1 = up row i).
+up rows interleaved (row 2i = gate row i, row 2i+1 = up row i); Q8 rows hold
+their int8 values, then one fp16 scale per 32.
 """
 from __future__ import annotations
 
@@ -36,20 +37,20 @@ class SynthModel:
         self.shape, self.seed = shape, seed
         dev = torch.device(device or "cuda")
         s = shape
-        es = s.elem_bytes
+        mb = s.matrix_bytes
         E, H, Hkv, hd, F, V, L = (s.n_embd, s.n_head, s.n_kv_head, s.head_dim, s.n_ff, s.n_vocab,
                                   s.n_layer)
         nsets = max(1, s.expert_count)
         ar = _Arena()
-        o_emb, o_onorm, o_out = ar.add(V * E * es), ar.add(E * 4), ar.add(V * E * es)
+        o_emb, o_onorm, o_out = ar.add(mb(V, E)), ar.add(E * 4), ar.add(mb(V, E))
         lay = []
         for l in range(L):
-            d = {"attn_norm": ar.add(E * 4), "wqkv": ar.add((H + 2 * Hkv) * hd * E * es),
-                 "wo": ar.add(E * H * hd * es), "ffn_norm": ar.add(E * 4)}
+            d = {"attn_norm": ar.add(E * 4), "wqkv": ar.add(mb((H + 2 * Hkv) * hd, E)),
+                 "wo": ar.add(mb(E, H * hd)), "ffn_norm": ar.add(E * 4)}
             if s.expert_count > 0:
-                d["w_router"] = ar.add(s.expert_count * E * es)
-            d["w_gate_up"] = [ar.add(2 * F * E * es) for _ in range(nsets)]
-            d["w_down"] = [ar.add(E * F * es) for _ in range(nsets)]
+                d["w_router"] = ar.add(mb(s.expert_count, E))
+            d["w_gate_up"] = [ar.add(mb(2 * F, E)) for _ in range(nsets)]
+            d["w_down"] = [ar.add(mb(E, F)) for _ in range(nsets)]
             lay.append(d)
         self.buf = torch.empty(ar.size, dtype=torch.uint8, device=dev)
         base = self.buf.data_ptr()
@@ -112,7 +113,7 @@ class SynthModel:
         base = state.kv.data_ptr()
         for l in range(s.n_layer):
             for kind, kk in ((0, synth.KCACHE), (1, synth.VCACHE)):
-                synth.dev_fill_kv(base + (2 * l + kind) * block, s.dtype, Hkv, cap, hd, lo, hi,
+                synth.dev_fill_kv(base + (2 * l + kind) * block, s.kv_dtype, Hkv, cap, hd, lo, hi,
                                   synth.key(self.seed, kk, l, slot), KV_SIGMA, st)
         state.set_pos(start_pos, stream)
 
