@@ -43,8 +43,13 @@ extern "C" {
 /* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
 typedef struct CUstream_st *pnb_stream;
 
-/* storage type of weights and of the KV cache */
-enum { PNB_F32 = 0, PNB_BF16 = 1 };
+/* storage type of the weights; the KV cache is fp32 for PNB_F32 and bf16
+   otherwise.  PNB_Q8_0: the pages' quantized weight mode ("Engine
+   Architecture", "Weight Loading Modes": weights stay in their GGUF blocks
+   and are dequantized per block inside the matvec), with GGUF Q8_0 blocks of
+   32 int8 values and one fp16 scale (weight = scale * value), stored per row
+   as all K values followed by the row's K / 32 scales (K + K / 16 bytes). */
+enum { PNB_F32 = 0, PNB_BF16 = 1, PNB_Q8_0 = 2 };
 
 enum {
   PNB_OK = 0,
@@ -85,7 +90,7 @@ typedef struct {
   int32_t sliding_window; /* 0 = attend to every position */
   int32_t expert_count;   /* 0 = dense SwiGLU FFN */
   int32_t expert_used;    /* top-k experts per token when expert_count > 0 */
-  int32_t dtype;          /* PNB_F32 or PNB_BF16: weights and KV cache */
+  int32_t dtype;          /* PNB_F32, PNB_BF16 or PNB_Q8_0: weights (KV: fp32 / bf16 / bf16) */
 } pnb_config;
 
 /* Device weights, caller-owned, in the library's layout (row-major; "dtype" =
@@ -125,12 +130,16 @@ typedef struct pnb_state pnb_state;
    forward, "Architecture registry").  Checks: n_embd = n_head * head_dim,
    head_dim even and in {32, 64, 128}, n_head % n_kv_head == 0, n_embd and
    n_ff multiples of 8, 0 < expert_used <= expert_count <= 64 when MoE,
-   pointer non-NULL and 16-byte aligned.  *out is set on success. */
+   pointer non-NULL and 16-byte aligned.  PNB_Q8_0 needs n_embd and n_ff
+   multiples of 256 (whole 16-byte vectors per row) and a dense FFN
+   (PNB_E_UNSUPPORTED otherwise); its models run the per-phase kernels only
+   (no persistent, fused-attention or batched form; pnb_prefill goes one
+   token per step).  *out is set on success. */
 int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **out);
 void pnb_model_free(pnb_model *m);
 
 /* Bytes of the KV buffer a state needs: n_layer * 2 * n_kv_head * cap *
-   head_dim * sizeof(dtype), with cap = min(n_ctx, sliding_window) when the
+   head_dim * (4 for PNB_F32, else 2), with cap = min(n_ctx, sliding_window) when the
    window is set, else n_ctx.  Layout, row-major:
      [n_layer][2 (K, V)][n_kv_head][cap][head_dim]
    Position j lives in slot j % cap (a ring when the window is set: the last

@@ -130,7 +130,12 @@ LLAMA8B_BATCHED = Workload(
           n_ctx=4096 + 64, rope_theta=500000.0, rms_norm_eps=1e-5, dtype=BF16),
     seed=5, batch=64, slot_pos_range=(512, 4096), steps=64)
 
-ALL = [TINY, LLAMA7B, MISTRAL7B, MIXTRAL, LLAMA8B_BATCHED]
+# the Llama-7B decode step with GGUF Q8_0-style weights (blocks of 32 int8
+# values and an fp16 scale); bf16 KV cache
+LLAMA7B_Q8 = Workload("llama7b_q8_0", replace(LLAMA7B.shape, dtype=Q8), seed=2, prefill=2048,
+                      steps=128)
+
+ALL = [TINY, LLAMA7B, MISTRAL7B, MIXTRAL, LLAMA8B_BATCHED, LLAMA7B_Q8]
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -19,7 +19,7 @@ if not os.path.exists(LIB):
 
 _lib = ctypes.CDLL(LIB)
 
-PNB_F32, PNB_BF16 = 0, 1
+PNB_F32, PNB_BF16, PNB_Q8_0 = 0, 1, 2
 PNB_TOKEN_PREV = -1
 PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT, PNB_DEV_ERR_RANGE = 1, 2, 4
 PNB_FUSED_OFF, PNB_FUSED_ATTN_OPROJ, PNB_FUSED_BLOCK = 0, 1, 2

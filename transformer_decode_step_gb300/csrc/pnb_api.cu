@@ -18,7 +18,7 @@ using namespace pnb;
 
 namespace {
 
-constexpr int kStageTarget = 32 * 1024;   // bytes of whole rows per GEMV ring slot
+constexpr int kStageTarget = 36 * 1024;   // bytes of whole rows per GEMV ring slot
 constexpr int kRingBudget = 192 * 1024;   // bytes of GEMV ring per CTA
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxBatch = 64;
@@ -35,11 +35,13 @@ int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // rows_total: rows over all segments; nseg: segments concatenated in it (0 when
 // the launch sums its segments into the same rows: static row ranges).
-Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int grid, int nseg) {
+// wt: weight storage type (PNB_F32, PNB_BF16 or PNB_Q8_0)
+Geom plan_gemv(int K, int wt, int64_t rows_total, int row_align, int nsum, int grid, int nseg) {
   Geom g{};
   g.K = K;
-  g.es = es;
-  g.row_bytes = K * es;
+  g.es = wt == PNB_Q8_0 ? 1 : (wt == PNB_BF16 ? 2 : 4);
+  g.row_bytes = wt == PNB_Q8_0 ? K + K / 16 : K * g.es;   // Q8: the values, then fp16 scales
+  g.vpr = wt == PNB_Q8_0 ? K / 8 : g.row_bytes / 16;   // Q8: 8-byte vectors of values
   int rps = 1;
   while (rps * 2 <= 64 && rps * 2 * g.row_bytes <= kStageTarget) rps *= 2;
   rps = std::max(rps, row_align);   // row pairs never straddle two ring items
@@ -49,7 +51,7 @@ Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int g
   // sixteen), so that each activation element is loaded by one lane of the
   // CTA only: the load after griddepcontrol.wait shares the SM's ingress with
   // the weight ring, and its latency grows with its volume
-  const int vpr = g.row_bytes / 16;
+  const int vpr = g.vpr;
   int cw = 1;
   while (cw < kGemvWarps && (cw * 2 * 32 <= vpr || kGemvWarps / cw > rps)) cw *= 2;
   g.cw = cw;
@@ -70,7 +72,7 @@ Geom plan_gemv(int K, int es, int64_t rows_total, int row_align, int nsum, int g
   g.nstages = 2;
   const int fixed = smem_layout(g).total - 2 * g.stage_bytes - 2 * 16;  // everything but the ring
   const int ring = std::min(kRingBudget, kMaxSmem - fixed - 1024);
-  g.nstages = std::min(8, std::max(2, ring / g.stage_bytes));
+  g.nstages = std::min(12, std::max(2, ring / g.stage_bytes));
   g.inflight = std::max(1, std::min(g.nstages, ceil_div(kInflightBytes, g.stage_bytes)));
   return g;
 }
@@ -84,7 +86,9 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 struct pnb_model {
   pnb_config cfg;
   int device = 0, num_sms = 0, grid = 0;
-  int hd = 0, n_sets = 0, qkv_rows = 0, es = 0, cap = 0;
+  int hd = 0, n_sets = 0, qkv_rows = 0, cap = 0;
+  int kv_es = 0;                         // KV-cache element bytes (bf16 for bf16 and Q8 weights)
+  int kv_dt = 0;                         // KV-cache element type (PNB_F32 or PNB_BF16)
   const void *tok_embd = nullptr;
   const float *out_norm = nullptr;
   const void *output = nullptr;
@@ -190,7 +194,11 @@ int validate_config(const pnb_config *c) {
   if (hd != 32 && hd != 64 && hd != 128) return PNB_E_UNSUPPORTED;
   if (c->n_embd % 8 || c->n_ff % 8) return PNB_E_INVAL;
   if (c->sliding_window < 0 || !(c->rope_theta > 0.0) || !(c->rms_norm_eps >= 0.0)) return PNB_E_INVAL;
-  if (c->dtype != PNB_F32 && c->dtype != PNB_BF16) return PNB_E_INVAL;
+  if (c->dtype != PNB_F32 && c->dtype != PNB_BF16 && c->dtype != PNB_Q8_0) return PNB_E_INVAL;
+  // Q8 rows (K values, then K / 32 fp16 scales) are whole 16-byte vectors;
+  // MoE models keep fp32 / bf16 weights
+  if (c->dtype == PNB_Q8_0 && (c->n_embd % 256 || c->n_ff % 256 || c->expert_count > 0))
+    return PNB_E_UNSUPPORTED;
   if (c->expert_count < 0 || c->expert_count > 64) return PNB_E_INVAL;
   if (c->expert_count > 0 &&
       (c->expert_used <= 0 || c->expert_used > c->expert_count || c->expert_used > kMaxSegments))
@@ -200,21 +208,21 @@ int validate_config(const pnb_config *c) {
 
 void plan(pnb_model *m) {
   const pnb_config &c = m->cfg;
-  const int E = c.n_embd, F = c.n_ff, es = m->es, grid = m->grid;
+  const int E = c.n_embd, F = c.n_ff, wt = c.dtype, grid = m->grid;
   const int k = c.expert_count > 0 ? c.expert_used : 1;
-  m->g_qkv = plan_gemv(E, es, m->qkv_rows, 2, 1, grid, 1);
-  m->g_o = plan_gemv(c.n_head * m->hd, es, E, 1, 1, grid, 1);
-  m->g_gateup = plan_gemv(E, es, (int64_t)k * 2 * F, 2, 1, grid, k);
-  m->g_down = plan_gemv(F, es, E, 1, k, grid, c.expert_count > 0 ? 0 : 1);
-  m->g_lm = plan_gemv(E, es, c.n_vocab, 1, 1, grid, 1);
+  m->g_qkv = plan_gemv(E, wt, m->qkv_rows, 2, 1, grid, 1);
+  m->g_o = plan_gemv(c.n_head * m->hd, wt, E, 1, 1, grid, 1);
+  m->g_gateup = plan_gemv(E, wt, (int64_t)k * 2 * F, 2, 1, grid, k);
+  m->g_down = plan_gemv(F, wt, E, 1, k, grid, c.expert_count > 0 ? 0 : 1);
+  m->g_lm = plan_gemv(E, wt, c.n_vocab, 1, 1, grid, 1);
   const int G = c.n_head / c.n_kv_head;
-  m->ag = attn_geom(c.dtype, m->hd, G);
+  m->ag = attn_geom(m->kv_dt, m->hd, G);
   m->zgroups = G / m->ag.heads_per_cta;
   // one wave: at most one CTA per SM (the attention CTA's registers allow one)
   const int want = std::max(1, m->num_sms / (c.n_kv_head * m->zgroups));
   m->n_split = std::max(1, std::min(want, std::max(1, m->cap / 16)));
   // tensor-core attention: 128-position tiles; a ring cache must hold whole tiles
-  m->attn_tc_ok = c.dtype == PNB_BF16 && (m->hd == 64 || m->hd == 128) &&
+  m->attn_tc_ok = m->kv_dt == PNB_BF16 && (m->hd == 64 || m->hd == 128) &&
                   (G == 1 || G == 2 || G == 4 || G == 8) &&
                   (c.sliding_window == 0 || m->cap % 128 == 0);
   // the splits of a KV head form one thread-block cluster (merged in shared memory)
@@ -228,8 +236,9 @@ bool geoms_supported(const pnb_model *m);
 // partial array or the attention merge area.
 void plan_step(pnb_model *m) {
   const pnb_config &c = m->cfg;
-  const int G = c.n_head / c.n_kv_head, hd = m->hd, es = m->es;
+  const int G = c.n_head / c.n_kv_head, hd = m->hd, es = m->kv_es;
   m->persistent = false;
+  if (c.dtype == PNB_Q8_0) return;   // the persistent kernel streams fp32 / bf16 weights
   if (!(hd == 32 || hd == 64 || hd == 128) || !(G == 1 || G == 2 || G == 4 || G == 8) ||
       G * hd > 512)
     return;
@@ -277,7 +286,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
                            float *logits, int32_t *argmax) {
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, H = c.n_head, Hkv = c.n_kv_head, hd = m->hd, F = c.n_ff;
-  const size_t layer_kv = (size_t)Hkv * m->cap * hd * m->es;
+  const size_t layer_kv = (size_t)Hkv * m->cap * hd * m->kv_es;
   uint8_t *kc = s->kv + (size_t)(2 * l) * layer_kv, *vc = kc + layer_kv;
   const float eps = (float)c.rms_norm_eps;
   const bool moe = c.expert_count > 0;
@@ -379,7 +388,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       aa.nstages = m->ag.nstages;
       aa.io = s->io;
       aa.tr = tr;
-      return launch_attn(c.dtype, hd, aa, m->ag, st, pdl);
+      return launch_attn(m->kv_dt, hd, aa, m->ag, st, pdl);
     }
     case PNB_KERNEL_OPROJ: {
       ResidArgs oa{};
@@ -640,15 +649,15 @@ bool encode_wo_map(CUtensorMap *map, const void *base, int dtype, int E, int HHD
 // 32 KB ring items of whole Wqkv rows / K and V positions / Wo rows.
 bool plan_block(pnb_model *m) {
   const pnb_config &c = m->cfg;
-  const int hd = m->hd, H = c.n_head, E = c.n_embd, es = m->es;
-  if (!(hd == 32 || hd == 64 || hd == 128)) return false;
+  const int hd = m->hd, H = c.n_head, E = c.n_embd, es = m->kv_es;
+  if (!(hd == 32 || hd == 64 || hd == 128) || c.dtype == PNB_Q8_0) return false;
   int C = 8;
   while (C > 1 && H * C > m->num_sms) C >>= 1;
   if (H * C > m->num_sms || E % C) return false;
   BlockGeom b{};
   b.C = C;
   b.rows_cta = 3 * hd / C;
-  b.g = plan_gemv(E, es, 3 * hd, 1, 1, H * C, 1);
+  b.g = plan_gemv(E, c.dtype, 3 * hd, 1, 1, H * C, 1);
   if (b.g.nv > 4) return false;
   int kv = 64;
   while (kv > 4 && 2 * kv * hd * es > kStageTarget) kv >>= 1;
@@ -852,7 +861,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
   const int E = c.n_embd, Hd = c.n_head * m->hd, F = c.n_ff;
   const int bp = B <= 16 ? 16 : (B <= 32 ? 32 : 64), bi = bp_index(bp);
   const int smem = b->smem[bi];
-  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
+  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->kv_es;
   const float eps = (float)c.rms_norm_eps;
   cudaError_t e;
   BNormArgs na{};
@@ -927,7 +936,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
     aa.bp = bp;
     aa.nb = B;
     aa.tr = KTrace{trace, 7 * l + 2};
-    if ((e = launch_attn(c.dtype, m->hd, aa, m->ag, st, true)) != cudaSuccess) return e;
+    if ((e = launch_attn(m->kv_dt, m->hd, aa, m->ag, st, true)) != cudaSuccess) return e;
     }
     g = bgemm_args(m, b, b->p_o, kEpiResid, B, bp);
     g.tr = KTrace{trace, 7 * l + 3};
@@ -1021,7 +1030,8 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
     m->hd = c.n_embd / c.n_head;
     m->n_sets = n_sets;
     m->qkv_rows = (c.n_head + 2 * c.n_kv_head) * m->hd;
-    m->es = c.dtype == PNB_BF16 ? 2 : 4;
+    m->kv_dt = c.dtype == PNB_F32 ? PNB_F32 : PNB_BF16;
+    m->kv_es = m->kv_dt == PNB_BF16 ? 2 : 4;
     m->cap = c.sliding_window > 0 ? std::min(c.sliding_window, c.n_ctx) : c.n_ctx;
     m->tok_embd = w->tok_embd;
     m->out_norm = w->out_norm;
@@ -1065,7 +1075,7 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   }
   if (ok) ok = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
   if (ok) ok = prepare_gemv_kernels(c.dtype, kMaxSmem) == cudaSuccess &&
-               prepare_attn_kernel(c.dtype, m->hd, m->ag) == cudaSuccess;
+               prepare_attn_kernel(m->kv_dt, m->hd, m->ag) == cudaSuccess;
   // one kernel per phase is the default: on the 7B-class shapes it is the
   // faster of the two; the persistent kernel is opt-in
   if (ok) {
@@ -1114,7 +1124,7 @@ void pnb_model_free(pnb_model *m) {
 
 size_t pnb_state_kv_bytes(const pnb_model *m) {
   if (!m) return 0;
-  return (size_t)m->cfg.n_layer * 2 * m->cfg.n_kv_head * m->cap * m->hd * m->es;
+  return (size_t)m->cfg.n_layer * 2 * m->cfg.n_kv_head * m->cap * m->hd * m->kv_es;
 }
 
 int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) {
@@ -1186,7 +1196,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
     // [layer][K|V] maps over this state's cache: rows = n_kv_head * cap positions, hd columns
     s->maps = s->ws + o_maps;
     maps.resize((size_t)2 * c.n_layer);
-    const size_t layer_kv_b = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
+    const size_t layer_kv_b = (size_t)c.n_kv_head * m->cap * m->hd * m->kv_es;
     for (int l = 0; l < c.n_layer; ++l)
       for (int kind = 0; kind < 2; ++kind)
         if (!encode_map(&maps[2 * l + kind], s->kv + (size_t)(2 * l + kind) * layer_kv_b,
@@ -1198,7 +1208,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   }
   // per-layer table of the persistent kernel
   std::vector<StepLayer> lt(c.n_layer);
-  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->es;
+  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->kv_es;
   for (int l = 0; l < c.n_layer; ++l) {
     StepLayer &L = lt[l];
     L.wqkv = m->wqkv[l];

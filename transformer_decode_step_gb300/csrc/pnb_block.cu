@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 
   // ------------------------------------------------- (a) q / k / v rows
   const int cw = b.g.cw;
-  const RowSplit sp(cw, b.g.row_bytes, warp);
+  const RowSplit sp(cw, b.g.vpr, warp);
   const uint32_t SB = (uint32_t)b.stage_bytes;
   RingPos rp{0u, 0u, (uint32_t)NS};
   bool ok = true;

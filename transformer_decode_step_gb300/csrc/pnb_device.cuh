@@ -216,6 +216,20 @@ __device__ __forceinline__ float round_to(float v) {
   else return v;
 }
 
+// Tag type of Q8 weight rows: K int8 values, then K / 32 fp16 scales (one per
+// block of 32 consecutive values); weight k = scale[k / 32] * value[k].
+struct Q8 {};
+
+// KV-cache element type of a model with weights of type T (bf16 for Q8)
+template <typename T>
+struct KvOf {
+  using type = T;
+};
+template <>
+struct KvOf<Q8> {
+  using type = __nv_bfloat16;
+};
+
 // The state's device I/O block: next input token, position, error bits.
 struct StepIO {
   int32_t token;

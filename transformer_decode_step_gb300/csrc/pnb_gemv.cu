@@ -55,11 +55,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
       if (tid == 0 && blockIdx.x == 0) set_error(&a.io->error, kErrToken);
       tok = 0;
     }
-    const T *row = static_cast<const T *>(a.emb) + (int64_t)tok * a.g.K;
-    if (blockIdx.x == 0)
-      for (int i = tid * 2; i < a.g.K; i += kGemvConsumers * 2)
-        *reinterpret_cast<float2 *>(a.x_out + i) = load2(row, i);
-    norm_slice(xs, row, a.g.K, a.eps, a.g, c.red, warp, lane);
+    auto embed = [&](const auto *row) {
+      if (blockIdx.x == 0)
+        for (int i = tid * 2; i < a.g.K; i += kGemvConsumers * 2)
+          *reinterpret_cast<float2 *>(a.x_out + i) = load2(row, i);
+      norm_slice(xs, row, a.g.K, a.eps, a.g, c.red, warp, lane);
+    };
+    if constexpr (std::is_same<T, Q8>::value) {
+      const Q8Row row{static_cast<const uint8_t *>(a.emb) + (int64_t)tok * a.g.row_bytes, a.g.K};
+      embed(&row);
+    } else {
+      embed(static_cast<const T *>(a.emb) + (int64_t)tok * a.g.K);
+    }
   } else {
     norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
   }
@@ -92,9 +99,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
       const bool is_k = rr < qrows + krows;
       const int kx = rr - qrows - (is_k ? 0 : krows);
       const int gk = kx / hd, d = kx - gk * hd;
-      T *dst = static_cast<T *>(is_k ? a.k_cache : a.v_cache) + ((int64_t)gk * a.cap + slot) * hd + d;
-      Elem<T>::store(dst, 0, v0);
-      Elem<T>::store(dst, 1, v1);
+      using C = typename KvOf<T>::type;
+      C *dst = static_cast<C *>(is_k ? a.k_cache : a.v_cache) + ((int64_t)gk * a.cap + slot) * hd + d;
+      Elem<C>::store(dst, 0, v0);
+      Elem<C>::store(dst, 1, v1);
     }
   });
   if (tid == 0) ktrace(a.tr, 5);
@@ -356,7 +364,8 @@ cudaError_t prepare_nv(int bytes) {
   if ((e = ensure_smem(k_qkv<T, NV>, bytes)) != cudaSuccess) return e;
   if ((e = ensure_smem(k_resid<T, NV>, bytes)) != cudaSuccess) return e;
   if ((e = ensure_smem(k_gateup<T, NV>, bytes)) != cudaSuccess) return e;
-  if ((e = ensure_smem(k_down_moe<T, NV>, bytes)) != cudaSuccess) return e;
+  if constexpr (!std::is_same<T, Q8>::value)   // MoE: fp32 / bf16 weights
+    if ((e = ensure_smem(k_down_moe<T, NV>, bytes)) != cudaSuccess) return e;
   return ensure_smem(k_lmhead<T, NV>, bytes);
 }
 
@@ -366,37 +375,43 @@ cudaError_t prepare_t(int bytes) {
   if ((e = prepare_nv<T, 1>(bytes)) != cudaSuccess) return e;
   if ((e = prepare_nv<T, 2>(bytes)) != cudaSuccess) return e;
   if ((e = prepare_nv<T, 4>(bytes)) != cudaSuccess) return e;
-  return ensure_smem(k_router<T>, bytes);
+  if constexpr (std::is_same<T, Q8>::value) return cudaSuccess;
+  else return ensure_smem(k_router<T>, bytes);
 }
 
 }  // namespace
 
+// weight storage type: 0 fp32, 1 bf16, 2 Q8
+#define GEMV_DTYPES(KERNEL, ARGS, GRID, ST, PDL)                       \
+  if (dtype == 2) { GEMV_LAUNCH(KERNEL, Q8, ARGS, GRID, ST, PDL) }      \
+  if (dtype == 1) { GEMV_LAUNCH(KERNEL, __nv_bfloat16, ARGS, GRID, ST, PDL) } \
+  GEMV_LAUNCH(KERNEL, float, ARGS, GRID, ST, PDL)
+
 cudaError_t launch_qkv(int dtype, const QkvArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype) { GEMV_LAUNCH(k_qkv, __nv_bfloat16, a, grid, st, pdl) }
-  GEMV_LAUNCH(k_qkv, float, a, grid, st, pdl)
+  GEMV_DTYPES(k_qkv, a, grid, st, pdl)
 }
 cudaError_t launch_resid(int dtype, const ResidArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype) { GEMV_LAUNCH(k_resid, __nv_bfloat16, a, grid, st, pdl) }
-  GEMV_LAUNCH(k_resid, float, a, grid, st, pdl)
+  GEMV_DTYPES(k_resid, a, grid, st, pdl)
 }
 cudaError_t launch_gateup(int dtype, const GateUpArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype) { GEMV_LAUNCH(k_gateup, __nv_bfloat16, a, grid, st, pdl) }
-  GEMV_LAUNCH(k_gateup, float, a, grid, st, pdl)
+  GEMV_DTYPES(k_gateup, a, grid, st, pdl)
 }
 cudaError_t launch_down_moe(int dtype, const DownMoeArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype) { GEMV_LAUNCH(k_down_moe, __nv_bfloat16, a, grid, st, pdl) }
+  if (dtype == 2) return cudaErrorInvalidValue;   // MoE: fp32 / bf16 weights
+  if (dtype == 1) { GEMV_LAUNCH(k_down_moe, __nv_bfloat16, a, grid, st, pdl) }
   GEMV_LAUNCH(k_down_moe, float, a, grid, st, pdl)
 }
 cudaError_t launch_lmhead(int dtype, const LmArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype) { GEMV_LAUNCH(k_lmhead, __nv_bfloat16, a, grid, st, pdl) }
-  GEMV_LAUNCH(k_lmhead, float, a, grid, st, pdl)
+  GEMV_DTYPES(k_lmhead, a, grid, st, pdl)
 }
 cudaError_t launch_router(int dtype, const RouterArgs &a, cudaStream_t st, bool pdl) {
   const int smem = (a.E + 32 + a.n_expert) * 4;
-  if (dtype) return launch(k_router<__nv_bfloat16>, a, dim3(1), dim3(256), smem, st, pdl);
+  if (dtype == 2) return cudaErrorInvalidValue;
+  if (dtype == 1) return launch(k_router<__nv_bfloat16>, a, dim3(1), dim3(256), smem, st, pdl);
   return launch(k_router<float>, a, dim3(1), dim3(256), smem, st, pdl);
 }
 cudaError_t prepare_gemv_kernels(int dtype, int smem_bytes) {
+  if (dtype == 2) return prepare_t<Q8>(smem_bytes);
   return dtype ? prepare_t<__nv_bfloat16>(smem_bytes) : prepare_t<float>(smem_bytes);
 }
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st) {

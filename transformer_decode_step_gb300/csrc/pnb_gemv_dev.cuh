@@ -5,9 +5,12 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <float.h>
 #include <limits.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "pnb_kernels.cuh"
 
@@ -346,6 +349,10 @@ template <>
 struct Vec<float> {
   static constexpr int N = 4;
 };
+template <>
+struct Vec<Q8> {
+  static constexpr int N = 8;   // 8-byte vectors of int8 values (the row's fp16 scales follow)
+};
 
 // A lane's slice of the activation vector: for t < NV, the Vec<T>::N columns
 // of 16-byte vector v(t) = c*32 + lane + t*32*cw (c = the warp's column slot),
@@ -375,6 +382,18 @@ __device__ __forceinline__ float2 load2(const __nv_bfloat16 *src, int col) {
   return bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(src + col));
 }
 
+// One Q8 row (the embedding row of a token): values at p, scales at p + K.
+struct Q8Row {
+  const uint8_t *p;
+  int K;
+};
+
+__device__ __forceinline__ float2 load2(const Q8Row *src, int col) {
+  const int8_t *v = reinterpret_cast<const int8_t *>(src->p);
+  const float d = __half2float(reinterpret_cast<const __half *>(src->p + src->K)[col / 32]);
+  return make_float2(d * (float)v[col], d * (float)v[col + 1]);
+}
+
 // xs = src * scale * w (w optional), columns of this lane only.  Every load
 // is issued (from an always-valid address) before any is used, so the lane
 // pays one memory round trip, not one per vector.
@@ -382,7 +401,7 @@ template <typename T, int NV, typename S>
 __device__ __forceinline__ void load_slice(XSlice<T, NV> &xs, const S *src, float scale,
                                            const float *w, const Geom &g, int warp, int lane) {
   constexpr int P = Vec<T>::N / 2;
-  const int vpr = g.row_bytes / 16, c = warp % g.cw;
+  const int vpr = g.vpr, c = warp % g.cw;
   float2 xv[NV][P], wv[NV][P];
 #pragma unroll
   for (int t = 0; t < NV; ++t) {
@@ -434,9 +453,16 @@ __device__ __forceinline__ float rms_inv(const S *src, int E, float eps, float *
 
 // ---------------------------------------------------------------- dot products
 
+template <int NV>
+__device__ __forceinline__ float dot_row_q8(const uint8_t *row, const XSlice<Q8, NV> &xs, int vpr,
+                                            int c, int cw, int lane);
+
 template <typename T, int NV>
 __device__ __forceinline__ float dot_row(const uint8_t *row, const XSlice<T, NV> &xs, int vpr,
                                          int c, int cw, int lane) {
+  if constexpr (std::is_same<T, Q8>::value) {
+    return dot_row_q8<NV>(row, xs, vpr, c, cw, lane);
+  } else {
   constexpr int P = Vec<T>::N / 2;
   uint4 wv[NV];
 #pragma unroll
@@ -466,6 +492,48 @@ __device__ __forceinline__ float dot_row(const uint8_t *row, const XSlice<T, NV>
 #pragma unroll
   for (int e = 0; e < P; ++e) s += acc[e].x + acc[e].y;
   return s;
+  }
+}
+
+// Q8 rows: each 8-byte vector is 8 int8 values of one quarter of a block of
+// 32, scaled once by the block's fp16 scale (stored after the row's K
+// values).  A byte permute makes the float 2^23 + (q + 128) of each value
+// (the value biased to unsigned, in the low mantissa bits) and one packed FMA
+// removes 2^23 + 128 exactly, so each q is exact before it is multiplied.
+template <int NV>
+__device__ __forceinline__ float dot_row_q8(const uint8_t *row, const XSlice<Q8, NV> &xs, int vpr,
+                                            int c, int cw, int lane) {
+  uint2 wv[NV];
+  float dv[NV];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const int v = c * 32 + lane + t * 32 * cw;
+    const int vc = v < vpr ? v : 0;
+    wv[t] = *reinterpret_cast<const uint2 *>(row + 8 * vc);
+    dv[t] = __half2float(reinterpret_cast<const __half *>(row + 8 * vpr)[vc >> 2]);
+  }
+  const float2 off = make_float2(-8388736.0f, -8388736.0f), one = make_float2(1.f, 1.f);
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    if (c * 32 + lane + t * 32 * cw < vpr) {
+      const uint32_t w2[2] = {wv[t].x ^ 0x80808080u, wv[t].y ^ 0x80808080u};
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float2 q0 = ffma2(make_float2(__uint_as_float(__byte_perm(w2[k], 0x4B000000u, 0x7440)),
+                                            __uint_as_float(__byte_perm(w2[k], 0x4B000000u, 0x7441))),
+                                one, off);
+        const float2 q1 = ffma2(make_float2(__uint_as_float(__byte_perm(w2[k], 0x4B000000u, 0x7442)),
+                                            __uint_as_float(__byte_perm(w2[k], 0x4B000000u, 0x7443))),
+                                one, off);
+        acc = ffma2(q0, xs.p[t][2 * k], acc);
+        acc = ffma2(q1, xs.p[t][2 * k + 1], acc);
+      }
+      s = fmaf(acc.x + acc.y, dv[t], s);
+    }
+  }
+  return s;
 }
 
 // Warp partials of four rows at once: the lane's products p[i] of rows i are
@@ -486,8 +554,8 @@ __device__ __forceinline__ float warp_sum4(float p0, float p1, float p2, float p
 // this warp is column slot cc of row group grp (computed once per kernel).
 struct RowSplit {
   int cw, groups, grp, cc, vpr;
-  __device__ __forceinline__ RowSplit(int cw_, int row_bytes, int warp)
-      : cw(cw_), groups(kGemvWarps / cw_), grp(warp / cw_), cc(warp % cw_), vpr(row_bytes / 16) {}
+  __device__ __forceinline__ RowSplit(int cw_, int vpr_, int warp)
+      : cw(cw_), groups(kGemvWarps / cw_), grp(warp / cw_), cc(warp % cw_), vpr(vpr_) {}
 };
 
 // Partial sums of the n staged rows at `stage` into part[(base + r) * cw + cc];
@@ -524,7 +592,7 @@ __device__ __forceinline__ void consume(const Geom &g, const Segs &s, bool summe
                         XSlice<T, NV> &xs, int warp, int lane, int32_t *err, const KTrace &tr,
                         Reload &&reload) {
   const int cw = g.cw;
-  const RowSplit sp(cw, g.row_bytes, warp);
+  const RowSplit sp(cw, g.vpr, warp);
   ItemIter it(c.r0, c.r1, s.rows, s.n, summed, g.rows_per_stage);
   Item item;
   RingPos rp{0u, 0u, (uint32_t)g.nstages};
@@ -559,7 +627,7 @@ template <typename T, int NV>
 __device__ __forceinline__ void consume_dyn(const Geom &g, const Ctx &c, const XSlice<T, NV> &xs,
                                             int warp, int lane, int32_t *err, const KTrace &tr) {
   const int cw = g.cw;
-  const RowSplit sp(cw, g.row_bytes, warp);
+  const RowSplit sp(cw, g.vpr, warp);
   RingPos rp{0u, 0u, (uint32_t)g.nstages};
   bool first = true;
   for (;;) {
@@ -615,7 +683,7 @@ template <typename T, int NV>
 __device__ __forceinline__ void load_weight_slice(XSlice<T, NV> &ws, const float *w, const Geom &g,
                                                   int warp, int lane) {
   constexpr int P = Vec<T>::N / 2;
-  const int vpr = g.row_bytes / 16, c = warp % g.cw;
+  const int vpr = g.vpr, c = warp % g.cw;
 #pragma unroll
   for (int t = 0; t < NV; ++t) {
     const int v = c * 32 + lane + t * 32 * g.cw;
@@ -633,7 +701,7 @@ template <typename T, int NV, typename S>
 __device__ __forceinline__ void norm_slice(XSlice<T, NV> &xs, const S *src, int E, float eps,
                                            const Geom &g, float *red, int warp, int lane) {
   constexpr int P = Vec<T>::N / 2;
-  const int vpr = g.row_bytes / 16, c = warp % g.cw;
+  const int vpr = g.vpr, c = warp % g.cw;
   float2 xv[NV][P];
 #pragma unroll
   for (int t = 0; t < NV; ++t) {

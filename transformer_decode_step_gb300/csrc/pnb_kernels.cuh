@@ -22,8 +22,9 @@ namespace pnb {
 // Geometry of one streaming GEMV launch (host-computed).
 struct Geom {
   int K;              // columns (elements)
-  int es;             // element bytes (2 bf16, 4 fp32)
-  int row_bytes;      // K * es
+  int es;             // weight storage type: 4 fp32, 2 bf16, 1 Q8
+  int row_bytes;      // K * es (Q8: K + K / 16: the values, then one fp16 scale per 32)
+  int vpr;            // weight vectors per row: 16-byte (K / 4, K / 8), Q8: 8-byte (K / 8)
   int rows_per_stage; // power of two <= 64: whole rows per ring slot
   int stage_bytes;    // ring slot size = rows_per_stage * row_bytes
   int nstages;        // ring slots

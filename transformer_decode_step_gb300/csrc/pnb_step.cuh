@@ -286,7 +286,7 @@ __device__ __forceinline__ void cons_gemv(RingC &R, const Geom &g, int nseg, int
   if (R.timing) R.t_start = global_ns();
   const int cw = g.cw, groups = kGemvWarps / cw;
   const int grp = warp / cw, cc = warp - grp * cw;
-  const int vpr = g.row_bytes / 16;
+  const int vpr = g.vpr;
   ItemIter it(r0, r1, rows, nseg, summed, g.rows_per_stage);
   Item item;
   int cur = 0;
