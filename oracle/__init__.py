@@ -94,6 +94,10 @@ def lib():
         L.orc_layer.restype = i32
         L.orc_layer.argtypes = [p, p, i32, p]
         L.orc_head.argtypes = [p, p, p, p]
+        L.orc_sample.restype = ctypes.c_int32
+        L.orc_sample.argtypes = [p, i64, f, f, p, i64, i64, f, d, p, p, p]
+        L.orc_sample_uniform.restype = d
+        L.orc_sample_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         L.orc_set_threads.argtypes = [i32]
         L.orc_max_threads.restype = i32
         _lib = L
@@ -178,6 +182,25 @@ def topk_softmax(r: np.ndarray, k: int):
 def argmax(x: np.ndarray) -> int:
     x = _f32(x)
     return int(lib().orc_argmax(x.ctypes.data, x.size))
+
+
+def sample(logits, temperature: float, repeat_penalty: float = 1.0, recent=(), top_k: int = 0,
+           top_p: float = 1.0, u: float = 0.0):
+    """(token, kept token ids in draw order, their cumulative probabilities)."""
+    x = _f32(logits)
+    rec = np.asarray(recent, dtype=np.int32)
+    V = x.size
+    idx = np.empty(V, dtype=np.int32)
+    cum = np.empty(V, dtype=np.float64)
+    n = ctypes.c_int64(0)
+    tok = lib().orc_sample(x.ctypes.data, V, temperature, repeat_penalty,
+                           rec.ctypes.data if rec.size else None, rec.size, top_k, top_p, u,
+                           idx.ctypes.data, cum.ctypes.data, ctypes.byref(n))
+    return int(tok), idx[:n.value].copy(), cum[:n.value].copy()
+
+
+def sample_uniform(seed: int, draw: int) -> float:
+    return float(lib().orc_sample_uniform(seed, draw))
 
 
 # ----------------------------------------------------------------- whole model

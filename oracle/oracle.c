@@ -290,6 +290,106 @@ int32_t orc_argmax(const float *x, int64_t n) {
   return (int32_t)best;
 }
 
+/* Sampling ("Engine Architecture", "Sampling"): applied in the pages' order -
+   (1) temperature: z = logit / T, T = 0 meaning the greedy argmax;
+   (2) repetition penalty on the tokens of the recent window [READING: the
+       pages name it only; each distinct recent token's z is divided by the
+       penalty when positive and multiplied by it otherwise];
+   (3) top-k: the k largest z, lower token id first on ties (k <= 0: all);
+   (4) top-p: in that order, the tokens up to and including the first at
+       which the cumulative probability exceeds p (p >= 1: all);
+   (5) softmax over the kept tokens;
+   (6) multinomial: the first kept token whose cumulative probability exceeds
+       u times the kept total, u uniform in [0, 1).
+   z, and so the order and the top-k set, are fp32, as the engine keeps its
+   logits; a temperature <= 0 is greedy; probabilities and cumulative sums
+   are fp64.  Returns the token;
+   cand_idx / cand_cum (optional, n_vocab long) receive the kept tokens in
+   draw order and their cumulative probabilities (normalised to the kept
+   total), *n_cand their count. */
+static int z_before(float za, int32_t a, float zb, int32_t b) { return za > zb || (za == zb && a < b); }
+
+static int cmp_zi(const void *pa, const void *pb) {
+  const float za = ((const float *)pa)[0], zb = ((const float *)pb)[0];
+  int32_t a, b;
+  memcpy(&a, (const float *)pa + 1, 4);
+  memcpy(&b, (const float *)pb + 1, 4);
+  return z_before(za, a, zb, b) ? -1 : (z_before(zb, b, za, a) ? 1 : 0);
+}
+
+int32_t orc_sample(const float *logits, int64_t V, float temperature, float repeat_penalty,
+                   const int32_t *recent, int64_t n_recent, int64_t top_k, float top_p, double u,
+                   int32_t *cand_idx, double *cand_cum, int64_t *n_cand) {
+  if (temperature <= 0.0f) {
+    if (n_cand) *n_cand = 0;
+    return orc_argmax(logits, V);
+  }
+  float *z = (float *)malloc((size_t)V * sizeof(float));
+  for (int64_t i = 0; i < V; ++i) z[i] = logits[i] / temperature;
+  for (int64_t j = 0; j < n_recent; ++j) {
+    const int32_t t = recent[j];
+    int seen = 0;
+    for (int64_t k = 0; k < j; ++k) seen |= recent[k] == t;
+    if (seen || t < 0 || t >= V) continue;
+    z[t] = z[t] > 0.0f ? z[t] / repeat_penalty : z[t] * repeat_penalty;
+  }
+  /* top-k: every token as a (z, id) pair in the draw order, then the first k */
+  const int64_t k = (top_k <= 0 || top_k > V) ? V : top_k;
+  float *pairs = (float *)malloc((size_t)V * 2 * sizeof(float));
+  for (int64_t i = 0; i < V; ++i) {
+    const int32_t id = (int32_t)i;
+    pairs[2 * i] = z[i];
+    memcpy(&pairs[2 * i + 1], &id, 4);
+  }
+  qsort(pairs, (size_t)V, 2 * sizeof(float), cmp_zi);
+  float *kz = (float *)malloc((size_t)k * sizeof(float));
+  int32_t *kid = (int32_t *)malloc((size_t)k * sizeof(int32_t));
+  for (int64_t r = 0; r < k; ++r) {
+    kz[r] = pairs[2 * r];
+    memcpy(&kid[r], &pairs[2 * r + 1], 4);
+  }
+  free(pairs);
+  /* softmax and cumulative probabilities in draw order (fp64) */
+  double *cum = (double *)malloc((size_t)k * sizeof(double));
+  double acc = 0.0;
+  for (int64_t r = 0; r < k; ++r) {
+    acc += exp((double)kz[r] - (double)kz[0]);
+    cum[r] = acc;
+  }
+  /* top-p: up to and including the first token whose cumulative
+     probability exceeds p */
+  int64_t m = k;
+  if (top_p < 1.0f) {
+    m = 0;
+    while (m < k && cum[m] <= (double)top_p * acc) ++m;
+    m = m < k ? m + 1 : k;
+  }
+  const double total = cum[m - 1], target = u * total;
+  int64_t pick = 0;
+  while (pick < m - 1 && cum[pick] <= target) ++pick;
+  if (cand_idx)
+    for (int64_t r = 0; r < m; ++r) cand_idx[r] = kid[r];
+  if (cand_cum)
+    for (int64_t r = 0; r < m; ++r) cand_cum[r] = cum[r] / total;
+  if (n_cand) *n_cand = m;
+  const int32_t tok = kid[pick];
+  free(cum);
+  free(kz);
+  free(kid);
+  free(z);
+  return tok;
+}
+
+/* the sampler's uniform draw: word `draw` of the SplitMix64 sequence of
+   `seed` (Steele, Lea & Flood, OOPSLA 2014), top 24 bits scaled to [0, 1) */
+double orc_sample_uniform(uint64_t seed, uint64_t draw) {
+  uint64_t z = seed + (draw + 1ULL) * 0x9E3779B97F4A7C15ULL;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  z ^= z >> 31;
+  return (double)(z >> 40) * (1.0 / 16777216.0);
+}
+
 /* ------------------------------------------------------ model / state */
 
 orc_model *orc_model_new(const orc_config *cfg, const orc_tensor *glob, const orc_tensor *layers) {

@@ -576,3 +576,133 @@ def test_q8_model_is_the_model_of_its_dequantized_weights():
     b = [s.forward(t)[0] for t in [1, 2, 3]]
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+# ------------------------------------------------------------------ sampling
+
+def test_sample_uniform_is_splitmix64_published_sequence():
+    # SplitMix64 seeded with 1234567: the first three outputs of the published
+    # generator (Steele, Lea & Flood 2014; the sequence Vigna's reference C
+    # code prints), top 24 bits scaled to [0, 1)
+    for n, word in enumerate((6457827717110365317, 3203168211198807973, 9817491932198370423)):
+        assert oracle.sample_uniform(1234567, n) == (word >> 40) / 2.0**24
+    u = np.array([oracle.sample_uniform(99, n) for n in range(20000)])
+    assert u.min() >= 0.0 and u.max() < 1.0
+    assert abs(u.mean() - 0.5) < 0.01 and abs(u.var() - 1 / 12) < 0.005
+
+
+def test_sample_temperature_zero_is_argmax_lowest_id():
+    lg = f32([0.5, 3.0, -1.0, 3.0, 2.9])
+    for T in (0.0, -1.0):
+        for u in (0.0, 0.5, 0.999):
+            assert oracle.sample(lg, T, u=u)[0] == 1
+
+
+def test_sample_top_k_one_is_argmax_at_any_temperature():
+    rng = np.random.default_rng(4)
+    lg = f32(rng.normal(size=300))
+    for T in (0.1, 1.0, 7.0):
+        for u in (0.0, 0.37, 0.9999):
+            tok, idx, cum = oracle.sample(lg, T, top_k=1, u=u)
+            assert tok == int(np.argmax(lg)) and list(idx) == [tok] and cum[-1] == 1.0
+
+
+def test_sample_three_token_closed_form():
+    # logits ln 1, ln 2, ln 4 at T = 1: probabilities 1/7, 2/7, 4/7, drawn in
+    # the order token 2, 1, 0 (cumulative 4/7, 6/7, 1)
+    lg = f32(np.log([1.0, 2.0, 4.0]))
+    tok, idx, cum = oracle.sample(lg, 1.0)
+    assert list(idx) == [2, 1, 0]
+    assert np.allclose(cum, [4 / 7, 6 / 7, 1.0], rtol=1e-6)
+    for u, want in ((0.0, 2), (0.5, 2), (0.58, 1), (0.85, 1), (0.86, 0), (0.9999, 0)):
+        assert oracle.sample(lg, 1.0, u=u)[0] == want
+    # top-p 0.5: token 2 alone exceeds it; top-p 0.6: tokens 2 and 1 (2/3, 1/3)
+    for u in (0.0, 0.5, 0.99):
+        assert oracle.sample(lg, 1.0, top_p=0.5, u=u)[0] == 2
+    _, idx, cum = oracle.sample(lg, 1.0, top_p=0.6)
+    assert list(idx) == [2, 1] and np.allclose(cum, [2 / 3, 1.0])
+    assert oracle.sample(lg, 1.0, top_p=0.6, u=0.66)[0] == 2
+    assert oracle.sample(lg, 1.0, top_p=0.6, u=0.67)[0] == 1
+    # top-k 2 keeps 2 and 1 whatever p
+    _, idx, cum = oracle.sample(lg, 1.0, top_k=2)
+    assert list(idx) == [2, 1] and np.allclose(cum, [2 / 3, 1.0])
+
+
+def test_sample_top_p_boundary_is_exceeds_not_reaches():
+    # four equal logits: probabilities 1/4 each (exact in binary), cumulative
+    # 1/4, 1/2, 3/4, 1 - it reaches p = 1/2 at the second token and exceeds
+    # it only at the third
+    lg = f32([0.7, 0.7, 0.7, 0.7])
+    _, idx, cum = oracle.sample(lg, 1.0, top_p=0.5)
+    assert list(idx) == [0, 1, 2] and np.array_equal(cum, [1 / 3, 2 / 3, 1.0])
+    _, idx, _ = oracle.sample(lg, 1.0, top_p=0.49)
+    assert list(idx) == [0, 1]
+    _, idx, _ = oracle.sample(lg, 1.0, top_p=0.0)
+    assert list(idx) == [0]
+    _, idx, _ = oracle.sample(lg, 1.0, top_p=1.0)
+    assert list(idx) == [0, 1, 2, 3]
+
+
+def test_sample_temperature_scales_the_logits():
+    # logits 0, ln 2 at T = 1/2: z = 0, 2 ln 2, probabilities 1/5, 4/5
+    lg = f32([0.0, np.log(2.0)])
+    _, idx, cum = oracle.sample(lg, 0.5)
+    assert list(idx) == [1, 0] and np.allclose(cum, [0.8, 1.0], rtol=1e-6)
+    # very high temperature: uniform
+    lg = f32(np.arange(10.0))
+    _, idx, cum = oracle.sample(lg, 1e6)
+    assert list(idx) == list(range(9, -1, -1)) and np.allclose(cum, np.arange(1, 11) / 10, atol=1e-4)
+
+
+@pytest.mark.parametrize("a", [1.5, -1.5])
+def test_sample_repetition_penalty_two_token_logistic(a):
+    # token 0 has logit a, token 1 logit 0; token 0 repeated (twice: once
+    # counts). Penalised z0 = a / 1.3 when a > 0, a * 1.3 when a < 0, so
+    # p0 = 1 / (1 + exp(-z0))
+    lg = f32([a, 0.0])
+    z0 = a / 1.3 if a > 0 else a * 1.3
+    p0 = 1.0 / (1.0 + math.exp(-z0))
+    _, idx, cum = oracle.sample(lg, 1.0, repeat_penalty=1.3, recent=[0, 0, 7, -2])
+    first = 0 if a > 0 else 1
+    assert idx[0] == first
+    assert math.isclose(cum[0], p0 if first == 0 else 1 - p0, rel_tol=1e-6)
+    # penalty 1 and an empty window change nothing
+    for kw in ({"repeat_penalty": 1.0, "recent": [0, 1]}, {"repeat_penalty": 2.0, "recent": []}):
+        _, _, c = oracle.sample(lg, 1.0, **kw)
+        assert math.isclose(c[0], max(1 / (1 + math.exp(-a)), 1 / (1 + math.exp(a))), rel_tol=1e-6)
+
+
+def test_sample_penalty_follows_temperature():
+    # temperature first, then the penalty: logit 2 at T = 2 is z = 1, divided
+    # by 4 gives 0.25 - below token 1's z = 0.3 (logit 0.6)
+    lg = f32([2.0, 0.6])
+    _, idx, _ = oracle.sample(lg, 2.0, repeat_penalty=4.0, recent=[0])
+    assert list(idx[:2]) == [1, 0]
+
+
+def test_sample_ties_keep_lower_ids_in_top_k():
+    lg = f32([1.0, 5.0, 5.0, 5.0, 0.0, 5.0])
+    _, idx, cum = oracle.sample(lg, 1.0, top_k=3)
+    assert list(idx) == [1, 2, 3] and np.allclose(cum, [1 / 3, 2 / 3, 1.0])
+
+
+def test_sample_empirical_frequencies_match_kept_probabilities():
+    # brute force: draws with uniform u land on each kept token with its
+    # probability (the renormalised softmax of the kept z), nothing else is drawn
+    rng = np.random.default_rng(8)
+    lg = f32(rng.normal(size=40) * 2)
+    T, k, p = 0.8, 12, 0.9
+    _, idx, cum = oracle.sample(lg, T, top_k=k, top_p=p)
+    z = lg.astype(np.float64) / T
+    order = np.argsort(-z, kind="stable")[:k]
+    assert list(idx) == list(order[:len(idx)])
+    pk = sp.softmax(z[order])
+    assert np.sum(pk[:len(idx) - 1]) <= p < np.sum(pk[:len(idx)])
+    probs = sp.softmax(z[idx])
+    n = 20000
+    counts = np.zeros(40)
+    for i in range(n):
+        counts[oracle.sample(lg, T, top_k=k, top_p=p, u=oracle.sample_uniform(5, i))[0]] += 1
+    assert counts.sum() == n and np.all(counts[np.setdiff1d(np.arange(40), idx)] == 0)
+    sd = np.sqrt(n * probs * (1 - probs))
+    assert np.all(np.abs(counts[idx] - n * probs) < 5 * sd + 1)
