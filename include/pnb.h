@@ -19,9 +19,9 @@
  *    16-byte aligned (PNB_E_ALIGN otherwise).
  *  - Calls that take a stream are stream-ordered: they validate arguments on
  *    the host, enqueue work and return without waiting.  The caller
- *    synchronises (or records an event) to read results.  This replaces the
- *    pages' begin / poll pair ("Core Engine API", section "Async forward-step
- *    seam"), where begin returns at once and poll reports running / done / error.
+ *    synchronises (or records an event) to read results; pnb_forward_begin /
+ *    pnb_forward_poll wrap this as the pages' begin / poll pair ("Core Engine
+ *    API", section "Async forward-step seam").
  *  - At most one step may be in flight per state, and one batched step per
  *    model (the pages' per-model gen_lock gives the same guarantee).
  *  - Return value: PNB_OK (0) or a negative PNB_E_* code; nothing is enqueued
@@ -63,7 +63,8 @@ enum {
   PNB_E_DEVICE = -8,      /* a device-side check failed (see pnb_state_check) */
   PNB_E_NOMEM = -9,       /* host or device allocation failed */
   PNB_E_WRONG_DEVICE = -10, /* current device differs from the model's */
-  PNB_E_TOO_LARGE = -11    /* needs more than PNB_STATIC_SCRATCH_BYTES of static scratch */
+  PNB_E_TOO_LARGE = -11,   /* needs more than PNB_STATIC_SCRATCH_BYTES of static scratch */
+  PNB_E_BUSY = -12         /* the state has begun work that has not been polled to completion */
 };
 
 /* device-side error bits (pnb_state_check) */
@@ -156,7 +157,8 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out);
 void pnb_state_free(pnb_state *s);
 
 /* Zero every K and V entry and set pos = 0 (pn_state_reset, "Core Engine
-   API", section "State lifecycle"); also clears the device error word. */
+   API", section "State lifecycle"); also clears the device error word and
+   the sampler's draw counter. */
 int pnb_state_reset(pnb_state *s, pnb_stream stream);
 
 /* Set pos, e.g. after the caller has filled cache positions [0, pos) itself.
@@ -170,7 +172,8 @@ int pnb_state_get_pos(const pnb_state *s, int32_t *pos);
    (PNB_DEV_ERR_* bits, 0 = none).  Returns PNB_E_DEVICE when it is nonzero. */
 int pnb_state_check(pnb_state *s, int32_t *device_error);
 
-/* Token value meaning "the greedy token of this state's previous step". */
+/* Token value meaning "this state's current next token": the greedy token
+   of its previous step, or the token pnb_sample drew after it. */
 #define PNB_TOKEN_PREV (-1)
 
 /* One decode step of one sequence (model->forward(model, token, state)).
@@ -265,6 +268,76 @@ int pnb_model_fused_attention(const pnb_model *m);
    PNB_E_INVAL when T < 1. */
 int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T, pnb_stream stream,
                 float *logits_dev, int32_t *argmax_dev);
+
+/* Sampling parameters ("Engine Architecture", section "Sampling": applied
+   in the order temperature, repetition penalty, top-k, top-p, softmax,
+   multinomial draw; the fields of the pages' pn_sampling_params). */
+typedef struct {
+  float temperature;    /* z = logit / temperature; <= 0: greedy argmax (lowest id on ties) */
+  float repeat_penalty; /* > 0; each distinct recent token's z is divided by it when
+                           positive, multiplied by it otherwise; 1 = off */
+  int32_t top_k;        /* keep the k largest z; <= 0 or >= n_vocab: all */
+  float top_p;          /* keep tokens in order until the cumulative probability
+                           exceeds top_p (that token included); >= 1: all */
+  uint64_t seed;        /* draw d of a state uses word d of SplitMix64(seed) */
+} pnb_sampling_params;
+
+/* Draw the next token from a step's logits (pn_sample_next_token, "Core
+   Engine API", section "Sampler seam"), on the device, stream-ordered.
+   logits_dev: [n_vocab] fp32, 16-byte aligned; as in the pages' sampler it is
+   changed in place (it holds logit / temperature after the penalty when
+   temperature > 0).  recent_dev: n_recent device int32 tokens the penalty
+   applies to (ids outside [0, n_vocab) are ignored; NULL when n_recent is 0).
+   The order of the candidates is z descending, lower id first on ties; the
+   draw takes u = (word >> 40) * 2^-24 of SplitMix64 word d, where d is the
+   state's draw counter (zeroed by pnb_state_reset, set by
+   pnb_state_set_draw, advanced by one per call), and returns the first kept
+   token whose cumulative probability exceeds u times the kept total.
+   Probabilities are exp(z - max z) summed in 64-bit fixed point (units of
+   2^-40), so the result is deterministic; it matches an exact computation
+   except when u or top_p falls within about 1e-6 of a cumulative boundary.
+   The token becomes the state's next token (pnb_forward with PNB_TOKEN_PREV,
+   pnb_forward_batch with tokens_dev NULL) and is written to token_dev
+   ([1] device int32) when given.  Logits must not be NaN and logit /
+   temperature must be finite.  PNB_E_UNSUPPORTED when n_vocab >= 2^24 or
+   its recent-token bitmap (n_vocab / 8 bytes) does not fit in shared memory
+   beside the kernel's 37 KB; PNB_E_INVAL for a NaN or infinite temperature,
+   a penalty that is not a positive finite number or a NaN top_p. */
+int pnb_sample(pnb_model *m, pnb_state *s, float *logits_dev, const pnb_sampling_params *params,
+               const int32_t *recent_dev, int32_t n_recent, pnb_stream stream, int32_t *token_dev);
+
+/* pnb_sample for B <= 64 distinct states at once (the pages' batch
+   scheduler samples every slot after each batched step: "Serve Layer
+   Architecture", section "L3 - in-driver sampling"), one launch: logits_dev
+   [B][n_vocab]; params, recent_dev and n_recent are host arrays of B
+   (recent_dev and n_recent may be NULL: no penalty window); tokens_dev [B]
+   optional. */
+int pnb_sample_batch(pnb_model *m, pnb_state *const *states, int32_t B, float *logits_dev,
+                     const pnb_sampling_params *params, const int32_t *const *recent_dev,
+                     const int32_t *n_recent, pnb_stream stream, int32_t *tokens_dev);
+
+/* Set the state's draw counter (stream-ordered). */
+int pnb_state_set_draw(pnb_state *s, uint32_t draw, pnb_stream stream);
+
+/* Begin / poll ("Core Engine API", section "Async forward-step seam").
+   pnb_forward_begin enqueues pnb_forward on the state's own non-blocking
+   stream (pnb_state_stream; work for this state on other streams must be
+   ordered before it by the caller), records an event and returns at once.
+   pnb_sample_begin enqueues pnb_sample on the same stream and moves the
+   event after it.  pnb_forward_poll returns 1 while the begun work runs;
+   when it has finished, PNB_OK with *logits_out (if not NULL) set to the
+   logits buffer of the begun step, PNB_E_DEVICE when the state's device
+   error word is set, PNB_E_CUDA on a CUDA error - each of these ends the
+   begun work.  Begin while work is outstanding returns PNB_E_BUSY; poll
+   without begun work PNB_E_INVAL.  Every model supports it (the pages'
+   begin answers 1, "unsupported", for all but one model family). */
+int pnb_forward_begin(pnb_model *m, pnb_state *s, int32_t token, float *logits_dev,
+                      int32_t *argmax_dev);
+int pnb_sample_begin(pnb_model *m, pnb_state *s, float *logits_dev,
+                     const pnb_sampling_params *params, const int32_t *recent_dev,
+                     int32_t n_recent, int32_t *token_dev);
+int pnb_forward_poll(pnb_model *m, pnb_state *s, float **logits_out);
+int pnb_state_stream(pnb_state *s, pnb_stream *out);
 
 /* Number of this library's kernels one step launches (single sequence when
    B == 0, batched otherwise). */

@@ -27,7 +27,8 @@ PNB_FUSED_OFF, PNB_FUSED_ATTN_OPROJ, PNB_FUSED_BLOCK = 0, 1, 2
  PNB_KERNEL_DOWN, PNB_KERNEL_LM_HEAD, PNB_KERNEL_ATTN_BLOCK) = range(8)
 ERRORS = {0: "PNB_OK", -1: "PNB_E_INVAL", -2: "PNB_E_NULL", -3: "PNB_E_ALIGN",
           -4: "PNB_E_CTX_FULL", -5: "PNB_E_UNSUPPORTED", -6: "PNB_E_CUDA", -7: "PNB_E_TOKEN",
-          -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE", -11: "PNB_E_TOO_LARGE"}
+          -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE", -11: "PNB_E_TOO_LARGE",
+          -12: "PNB_E_BUSY"}
 
 
 class pnb_config(ctypes.Structure):
@@ -43,6 +44,16 @@ class pnb_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("tok_embd", "out_norm", "output", "attn_norm", "wqkv", "wo", "ffn_norm",
                  "w_router", "w_gate_up", "w_down")]
+
+
+class pnb_sampling_params(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("repeat_penalty", ctypes.c_float),
+                ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float), ("seed", ctypes.c_uint64)]
+
+
+def sampling_params(temperature: float = 0.0, repeat_penalty: float = 1.0, top_k: int = 0,
+                    top_p: float = 1.0, seed: int = 0) -> pnb_sampling_params:
+    return pnb_sampling_params(temperature, repeat_penalty, top_k, top_p, seed)
 
 
 class pnb_activations(ctypes.Structure):
@@ -63,6 +74,13 @@ _SIGS = {
     "pnb_forward": (_i32, [_p, _p, _i32, _p, _p, _p]),
     "pnb_forward_batch": (_i32, [_p, _p, _i32, _p, _p, _p, _p]),
     "pnb_prefill": (_i32, [_p, _p, _p, _i32, _p, _p, _p]),
+    "pnb_sample": (_i32, [_p, _p, _p, _p, _p, _i32, _p, _p]),
+    "pnb_sample_batch": (_i32, [_p, _p, _i32, _p, _p, _p, _p, _p, _p]),
+    "pnb_state_set_draw": (_i32, [_p, ctypes.c_uint32, _p]),
+    "pnb_forward_begin": (_i32, [_p, _p, _i32, _p, _p]),
+    "pnb_sample_begin": (_i32, [_p, _p, _p, _p, _p, _i32, _p]),
+    "pnb_forward_poll": (_i32, [_p, _p, _p]),
+    "pnb_state_stream": (_i32, [_p, _p]),
     "pnb_model_set_graphs": (_i32, [_p, _i32]),
     "pnb_model_set_persistent": (_i32, [_p, _i32]),
     "pnb_model_is_persistent": (_i32, [_p]),
@@ -207,6 +225,22 @@ class Model:
                                 _ptr(logits), _ptr(argmax)), "pnb_forward_batch")
 
 
+    def sample_batch(self, states: Sequence["State"], logits, params, recent=None, tokens=None,
+                     stream=None):
+        """pnb_sample_batch: params a list of pnb_sampling_params (one per state),
+        recent a list of device int32 tensors (or None) - the penalty windows."""
+        n = len(states)
+        arr = (ctypes.c_void_p * n)(*[s.handle for s in states])
+        ps = (pnb_sampling_params * n)(*params)
+        rec = nrec = None
+        if recent is not None:
+            rec = (ctypes.c_void_p * n)(*[_ptr(r) if r is not None and r.numel() else None
+                                          for r in recent])
+            nrec = (ctypes.c_int32 * n)(*[int(r.numel()) if r is not None else 0 for r in recent])
+        check(pnb_sample_batch(self._h, arr, n, _ptr(logits), ps, rec, nrec, _stream(stream),
+                               _ptr(tokens)), "pnb_sample_batch")
+
+
 class State:
     def __init__(self, model: Model, kv):
         self.model = model
@@ -234,6 +268,43 @@ class State:
         and argmax [T] optional device tensors."""
         check(pnb_prefill(self.model.handle, self._h, _ptr(tokens), int(tokens.numel()),
                           _stream(stream), _ptr(logits), _ptr(argmax)), "pnb_prefill")
+
+    def sample(self, logits, params: pnb_sampling_params, recent=None, token=None, stream=None):
+        """Draw the next token from `logits` (changed in place); `recent` a device
+        int32 tensor of the penalty window; `token` an optional device int32 [1]."""
+        n = int(recent.numel()) if recent is not None else 0
+        check(pnb_sample(self.model.handle, self._h, _ptr(logits), ctypes.byref(params),
+                         _ptr(recent) if n else None, n, _stream(stream), _ptr(token)),
+              "pnb_sample")
+
+    def set_draw(self, draw: int, stream=None):
+        check(pnb_state_set_draw(self._h, draw, _stream(stream)), "pnb_state_set_draw")
+
+    # begin / poll: the step (and a sampling) on the state's own stream
+    def forward_begin(self, token: int, logits=None, argmax=None):
+        self._begun_logits = logits
+        check(pnb_forward_begin(self.model.handle, self._h, token, _ptr(logits), _ptr(argmax)),
+              "pnb_forward_begin")
+
+    def sample_begin(self, logits, params: pnb_sampling_params, recent=None, token=None):
+        n = int(recent.numel()) if recent is not None else 0
+        check(pnb_sample_begin(self.model.handle, self._h, _ptr(logits), ctypes.byref(params),
+                               _ptr(recent) if n else None, n, _ptr(token)), "pnb_sample_begin")
+
+    def poll(self) -> bool:
+        """True when the begun work is done (raises PnbError on its errors)."""
+        out = ctypes.c_void_p()
+        rc = pnb_forward_poll(self.model.handle, self._h, ctypes.byref(out))
+        if rc == 1:
+            return False
+        check(rc, "pnb_forward_poll")
+        return True
+
+    def stream(self) -> int:
+        """The state's own CUDA stream (as an int handle)."""
+        out = ctypes.c_void_p()
+        check(pnb_state_stream(self._h, ctypes.byref(out)), "pnb_state_stream")
+        return out.value or 0
 
     def reset(self, stream=None):
         check(pnb_state_reset(self._h, _stream(stream)), "pnb_state_reset")

@@ -106,6 +106,7 @@ struct pnb_model {
   int n_split_tc = 1;
   // fused attention block (one cluster per query head): geometry, per-layer Wo maps
   bool block_ok = false;
+  bool sample_ok = false;                // the sampler kernel fits this vocabulary
   int block = 0;                         // PNB_FUSED_*: off, attention + o-proj, whole block
   BlockGeom bgeom{};
   int block_clusters = 0;                // clusters that fit on the GPU at once
@@ -174,6 +175,12 @@ struct pnb_state {
   cudaGraphExec_t exec = nullptr;
   float *g_logits = nullptr;
   int32_t *g_argmax = nullptr;
+  // begin / poll seam: the state's own stream, the event of its last begun
+  // work, whether it is outstanding and the logits buffer it writes
+  cudaStream_t astream = nullptr;
+  cudaEvent_t aevent = nullptr;
+  bool pending = false;
+  float *a_logits = nullptr;
 };
 
 namespace {
@@ -994,6 +1001,7 @@ const char *pnb_strerror(int code) {
     case PNB_E_NOMEM: return "allocation failed";
     case PNB_E_WRONG_DEVICE: return "current device differs from the model's device";
     case PNB_E_TOO_LARGE: return "exceeds the static scratch of the allocation-free entry point";
+    case PNB_E_BUSY: return "a begun step of this state has not been polled to completion";
     default: return "unknown error";
   }
 }
@@ -1076,6 +1084,10 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   if (ok) ok = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
   if (ok) ok = prepare_gemv_kernels(c.dtype, kMaxSmem) == cudaSuccess &&
                prepare_attn_kernel(m->kv_dt, m->hd, m->ag) == cudaSuccess;
+  // the sampler: fixed-point masses need n_vocab < 2^24, its recent-token
+  // bitmap one bit per token in shared memory
+  if (ok && c.n_vocab < (1 << 24) && sample_smem_bytes(c.n_vocab) <= (size_t)kMaxSmem)
+    m->sample_ok = prepare_sample_kernel(c.n_vocab) == cudaSuccess;
   // one kernel per phase is the default: on the 7B-class shapes it is the
   // faster of the two; the persistent kernel is opt-in
   if (ok) {
@@ -1242,6 +1254,9 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
 void pnb_state_free(pnb_state *s) {
   if (!s) return;
   if (s->exec) cudaGraphExecDestroy(s->exec);
+  if (s->astream) cudaStreamSynchronize(s->astream);
+  if (s->aevent) cudaEventDestroy(s->aevent);
+  if (s->astream) cudaStreamDestroy(s->astream);
   cudaFree(s->ws);
   delete s;
 }
@@ -1406,6 +1421,128 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
     if (cudaGraphLaunch(b->exec, st) != cudaSuccess) return PNB_E_CUDA;
   }
   for (int i = 0; i < B; ++i) states[i]->pos += 1;
+  return PNB_OK;
+}
+
+int pnb_sample_batch(pnb_model *m, pnb_state *const *states, int32_t B, float *logits_dev,
+                     const pnb_sampling_params *params, const int32_t *const *recent_dev,
+                     const int32_t *n_recent, pnb_stream stream, int32_t *tokens_dev) {
+  if (!m || !states || !logits_dev || !params) return PNB_E_NULL;
+  if (B < 1 || B > kSampleMaxSlots) return PNB_E_INVAL;
+  if (!aligned16(logits_dev) || (tokens_dev && (reinterpret_cast<uintptr_t>(tokens_dev) & 3u)))
+    return PNB_E_ALIGN;
+  const int V = m->cfg.n_vocab;
+  SampleArgs a;
+  a.n_vocab = V;
+  for (int b = 0; b < B; ++b) {
+    pnb_state *s = states[b];
+    const pnb_sampling_params &p = params[b];
+    if (!s) return PNB_E_NULL;
+    if (s->m != m) return PNB_E_INVAL;
+    for (int j = 0; j < b; ++j)
+      if (states[j] == s) return PNB_E_INVAL;
+    const int32_t nr = n_recent ? n_recent[b] : 0;
+    const int32_t *rec = recent_dev ? recent_dev[b] : nullptr;
+    if (nr < 0) return PNB_E_INVAL;
+    if (nr > 0 && !rec) return PNB_E_NULL;
+    if (rec && (reinterpret_cast<uintptr_t>(rec) & 3u)) return PNB_E_ALIGN;
+    if (std::isnan(p.temperature) || std::isinf(p.temperature) || !(p.repeat_penalty > 0.0f) ||
+        std::isinf(p.repeat_penalty) || std::isnan(p.top_p))
+      return PNB_E_INVAL;
+    a.slot[b] = SampleSlot{logits_dev + (size_t)b * V, rec, nr, p.top_k, p.temperature,
+                           p.repeat_penalty, p.top_p, (unsigned long long)p.seed, s->io,
+                           tokens_dev ? tokens_dev + b : nullptr};
+  }
+  if (!m->sample_ok) return PNB_E_UNSUPPORTED;
+  int rc = check_device(m);
+  if (rc != PNB_OK) return rc;
+  return launch_sample(a, B, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? PNB_OK
+                                                                                    : PNB_E_CUDA;
+}
+
+int pnb_sample(pnb_model *m, pnb_state *s, float *logits_dev, const pnb_sampling_params *params,
+               const int32_t *recent_dev, int32_t n_recent, pnb_stream stream, int32_t *token_dev) {
+  return pnb_sample_batch(m, &s, 1, logits_dev, params, &recent_dev, &n_recent, stream, token_dev);
+}
+
+int pnb_state_set_draw(pnb_state *s, uint32_t draw, pnb_stream stream) {
+  if (!s) return PNB_E_NULL;
+  int rc = check_device(s->m);
+  if (rc != PNB_OK) return rc;
+  return launch_set_draws(s->io, draw, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PNB_OK
+             : PNB_E_CUDA;
+}
+
+namespace {
+int async_setup(pnb_state *s) {
+  if (!s->astream && cudaStreamCreateWithFlags(&s->astream, cudaStreamNonBlocking) != cudaSuccess) {
+    s->astream = nullptr;
+    return PNB_E_CUDA;
+  }
+  if (!s->aevent && cudaEventCreateWithFlags(&s->aevent, cudaEventDisableTiming) != cudaSuccess) {
+    s->aevent = nullptr;
+    return PNB_E_CUDA;
+  }
+  return PNB_OK;
+}
+}  // namespace
+
+int pnb_state_stream(pnb_state *s, pnb_stream *out) {
+  if (!s || !out) return PNB_E_NULL;
+  int rc = check_device(s->m);
+  if (rc == PNB_OK) rc = async_setup(s);
+  if (rc != PNB_OK) return rc;
+  *out = reinterpret_cast<pnb_stream>(s->astream);
+  return PNB_OK;
+}
+
+int pnb_forward_begin(pnb_model *m, pnb_state *s, int32_t token, float *logits_dev,
+                      int32_t *argmax_dev) {
+  if (!m || !s) return PNB_E_NULL;
+  if (s->m != m) return PNB_E_INVAL;
+  if (s->pending) return PNB_E_BUSY;
+  int rc = check_device(m);
+  if (rc == PNB_OK) rc = async_setup(s);
+  if (rc != PNB_OK) return rc;
+  rc = pnb_forward(m, s, token, reinterpret_cast<pnb_stream>(s->astream), logits_dev, argmax_dev);
+  if (rc != PNB_OK) return rc;
+  if (cudaEventRecord(s->aevent, s->astream) != cudaSuccess) return PNB_E_CUDA;
+  s->pending = true;
+  s->a_logits = logits_dev;
+  return PNB_OK;
+}
+
+int pnb_sample_begin(pnb_model *m, pnb_state *s, float *logits_dev,
+                     const pnb_sampling_params *params, const int32_t *recent_dev,
+                     int32_t n_recent, int32_t *token_dev) {
+  if (!m || !s) return PNB_E_NULL;
+  if (s->m != m) return PNB_E_INVAL;
+  int rc = check_device(m);
+  if (rc == PNB_OK) rc = async_setup(s);
+  if (rc != PNB_OK) return rc;
+  rc = pnb_sample(m, s, logits_dev, params, recent_dev, n_recent,
+                  reinterpret_cast<pnb_stream>(s->astream), token_dev);
+  if (rc != PNB_OK) return rc;
+  if (cudaEventRecord(s->aevent, s->astream) != cudaSuccess) return PNB_E_CUDA;
+  if (!s->pending) s->a_logits = logits_dev;
+  s->pending = true;
+  return PNB_OK;
+}
+
+int pnb_forward_poll(pnb_model *m, pnb_state *s, float **logits_out) {
+  if (!m || !s) return PNB_E_NULL;
+  if (s->m != m || !s->pending) return PNB_E_INVAL;
+  const cudaError_t q = cudaEventQuery(s->aevent);
+  if (q == cudaErrorNotReady) return 1;
+  s->pending = false;
+  if (q != cudaSuccess) return PNB_E_CUDA;
+  StepIO io;
+  if (cudaMemcpyAsync(&io, s->io, sizeof(io), cudaMemcpyDeviceToHost, s->astream) != cudaSuccess ||
+      cudaStreamSynchronize(s->astream) != cudaSuccess)
+    return PNB_E_CUDA;
+  if (io.error) return PNB_E_DEVICE;
+  if (logits_out) *logits_out = s->a_logits;
   return PNB_OK;
 }
 

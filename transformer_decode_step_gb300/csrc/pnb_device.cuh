@@ -235,7 +235,7 @@ struct StepIO {
   int32_t token;
   int32_t pos;
   int32_t error;
-  int32_t pad;
+  uint32_t draws;  // sampler draws taken by this sequence (picks its uniform)
 };
 
 __device__ __forceinline__ void set_error(int32_t *err, int bits) { atomicOr(err, bits); }

@@ -426,4 +426,30 @@ cudaError_t prepare_attn_kernel(int dtype, int head_dim, const AttnGeom &ag);
 // attention geometry for a head_dim / group size (host)
 AttnGeom attn_geom(int dtype, int head_dim, int group);
 
+// ------------------------------------------------------------------ sampler
+// one sequence's sampling: logits [n_vocab] (overwritten with logit / T after
+// the penalty), the recent tokens the penalty applies to, the parameters, the
+// state's StepIO (its token becomes the sampled one, its draw counter picks u
+// and is advanced) and an optional output word
+struct SampleSlot {
+  float *logits;
+  const int32_t *recent;
+  int32_t n_recent;
+  int32_t top_k;
+  float temperature, repeat_penalty, top_p;
+  unsigned long long seed;
+  StepIO *io;
+  int32_t *out;
+};
+constexpr int kSampleMaxSlots = 64;
+struct SampleArgs {
+  int n_vocab;
+  SampleSlot slot[kSampleMaxSlots];
+};
+size_t sample_smem_bytes(int n_vocab);
+cudaError_t prepare_sample_kernel(int n_vocab);
+// one CTA per slot (slots 0 .. n_slots - 1 of a)
+cudaError_t launch_sample(const SampleArgs &a, int n_slots, cudaStream_t st);
+cudaError_t launch_set_draws(StepIO *io, uint32_t draws, cudaStream_t st);
+
 }  // namespace pnb
