@@ -299,9 +299,9 @@ typedef struct {
    The token becomes the state's next token (pnb_forward with PNB_TOKEN_PREV,
    pnb_forward_batch with tokens_dev NULL) and is written to token_dev
    ([1] device int32) when given.  Logits must not be NaN and logit /
-   temperature must be finite.  PNB_E_UNSUPPORTED when n_vocab >= 2^24 or
+   temperature must be finite.  PNB_E_UNSUPPORTED when n_vocab >= 2^22 or
    its recent-token bitmap (n_vocab / 8 bytes) does not fit in shared memory
-   beside the kernel's 37 KB; PNB_E_INVAL for a NaN or infinite temperature,
+   beside the kernel's other 137 KB; PNB_E_INVAL for a NaN or infinite temperature,
    a penalty that is not a positive finite number or a NaN top_p. */
 int pnb_sample(pnb_model *m, pnb_state *s, float *logits_dev, const pnb_sampling_params *params,
                const int32_t *recent_dev, int32_t n_recent, pnb_stream stream, int32_t *token_dev);

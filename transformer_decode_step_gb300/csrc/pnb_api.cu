@@ -1084,9 +1084,9 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   if (ok) ok = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) == cudaSuccess;
   if (ok) ok = prepare_gemv_kernels(c.dtype, kMaxSmem) == cudaSuccess &&
                prepare_attn_kernel(m->kv_dt, m->hd, m->ag) == cudaSuccess;
-  // the sampler: fixed-point masses need n_vocab < 2^24, its recent-token
-  // bitmap one bit per token in shared memory
-  if (ok && c.n_vocab < (1 << 24) && sample_smem_bytes(c.n_vocab) <= (size_t)kMaxSmem)
+  // the sampler: its fixed-point mass counters need n_vocab < 2^22, its
+  // recent-token bitmap one bit per token in shared memory
+  if (ok && c.n_vocab < (1 << 22) && sample_smem_bytes(c.n_vocab) <= (size_t)kMaxSmem)
     m->sample_ok = prepare_sample_kernel(c.n_vocab) == cudaSuccess;
   // one kernel per phase is the default: on the 7B-class shapes it is the
   // faster of the two; the persistent kernel is opt-in
