@@ -49,6 +49,10 @@ def parse():
                     help="use only the first N layers (small cases for ncu captures)")
     ap.add_argument("--batch", type=int, default=0,
                     help="slots of a batched workload (default: the workload's own)")
+    ap.add_argument("--sample", action="store_true",
+                    help="each step also draws the next token on the GPU (pnb_sample: "
+                         "temperature 0.8, top-k 40, top-p 0.95, repetition penalty 1.1 "
+                         "over 64 recent tokens) instead of taking the greedy one")
     ap.add_argument("--prefill", type=int, default=0,
                     help="instead of decode steps, time pnb_prefill of this many prompt tokens "
                          "from position 0 (one step = one prefill)")
@@ -285,17 +289,26 @@ def run_ours(args, w):
     budget = s.n_ctx - P                       # decode steps one pass can take
     sm = pnb.SynthModel(s, w.seed)
     st = sm.new_state(start_pos=P, slot=rank)
+    import synth
     import synth.workloads as wl
     tok0 = wl.prompt_tokens(w, rank)[0]
     am = torch.empty(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
+    sampling = pnb.sampling_params(0.8, 1.1, 40, 0.95, 1234 + rank) if args.sample else None
+    lg = torch.empty(s.n_vocab, dtype=torch.float32, device="cuda") if args.sample else None
+    # the penalty window: 64 seeded token ids
+    recent = torch.tensor(synth.uniform_int(synth.key(w.seed, synth.TOKENS, 1, rank), 0, 64, 0,
+                                            s.n_vocab), dtype=torch.int32,
+                          device="cuda") if args.sample else None
 
     def one_pass_step(i):
         if i % budget == 0:
             st.set_pos(P)
-            st.forward(tok0, argmax=am)
+            st.forward(tok0, argmax=am, logits=lg)
         else:
-            st.forward(pnb.PNB_TOKEN_PREV, argmax=am)
+            st.forward(pnb.PNB_TOKEN_PREV, argmax=am, logits=lg)
+        if sampling is not None:
+            st.sample(lg, sampling, recent=recent, token=am)
 
     # warm-up (captures the graph)
     for i in range(max(3, args.warmup)):
@@ -327,7 +340,7 @@ def run_ours(args, w):
     err = st.device_error()
     clk = clocks.summary()
     passes = (args.steps + budget - 1) // budget
-    launches = args.steps * sm.step_kernel_count() + 2 * passes
+    launches = args.steps * (sm.step_kernel_count() + (1 if args.sample else 0)) + 2 * passes
     ms_step = ms / args.steps
     tokens_per_s = world * args.steps / (ms / 1000.0)
     mean_bytes = sum(step_bytes(s, P + (i % budget)) for i in range(args.steps)) / args.steps
@@ -359,7 +372,9 @@ def run_ours(args, w):
     tok = tok0
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        st.forward(tok, argmax=am)
+        st.forward(tok, argmax=am, logits=lg)
+        if sampling is not None:
+            st.sample(lg, sampling, recent=recent, token=am)
         pinned.copy_(am, non_blocking=True)
         stream.synchronize()
         tok = int(pinned[0])
@@ -379,7 +394,11 @@ def run_ours(args, w):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype], "data": "synthetic (seeded generated weights and KV cache)",
                 "config": workload_config(w, {"parallelism": f"replicas x{world}",
-                                              "positions": f"{P}..{P + budget - 1}"}),
+                                              "positions": f"{P}..{P + budget - 1}",
+                                              "next_token": "sampled on the GPU: temperature 0.8, "
+                                                            "top-k 40, top-p 0.95, penalty 1.1 "
+                                                            "over 64 tokens" if args.sample
+                                                            else "greedy (argmax)"}),
                 "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"],
                 "bytes_per_step": mean_bytes,

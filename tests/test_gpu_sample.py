@@ -301,3 +301,81 @@ def test_begin_poll_seam():
         while not c.poll():
             pass
     assert e.value.code == -8
+
+
+# a model the batched step covers (bf16, dense, n_embd / n_head * hd / n_ff multiples of 64)
+BATCH_SHAPE = wl.Shape(n_vocab=3001, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_ff=1024,
+                       n_ctx=160, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
+
+
+def test_continuous_batching_join_leave_with_in_loop_sampling():
+    """The batch decoder loop of the pages' serve layer: sequences join (prefill,
+    then a first sampled token) and leave (budget reached) between batched
+    steps; after each step every active slot is sampled in one launch.  Each
+    sequence, replayed alone with its recorded tokens, must see the same logits
+    (1e-3: batched and single-sequence steps differ only in summation order and
+    the tensor-core split of activations), and each recorded token must be a
+    draw the oracle sampler accepts from the logits the slot had."""
+    sm = pnb.SynthModel(BATCH_SHAPE, 19, device=DEV)
+    V = BATCH_SHAPE.n_vocab
+    rng = np.random.default_rng(12)
+    reqs = []
+    for r in range(6):
+        reqs.append({"prompt": [int(t) for t in rng.integers(0, V, size=int(rng.integers(3, 20)))],
+                     "budget": int(rng.integers(3, 9)),
+                     "params": pnb.sampling_params(0.7 + 0.1 * r, 1.0 + 0.05 * r, [0, 20, 40][r % 3],
+                                                   [0.9, 1.0, 0.8][r % 3], 900 + r),
+                     "tokens": [], "logits": []})
+    queue, active = list(range(6)), []
+    states = {}
+    max_active = 3
+    sizes = []
+    while queue or active:
+        while queue and len(active) < max_active:             # join
+            r = queue.pop(0)
+            q = reqs[r]
+            st = sm.new_state(0)
+            T = len(q["prompt"])
+            pl = torch.empty(T, V, dtype=torch.float32, device=DEV)
+            st.prefill(torch.tensor(q["prompt"], dtype=torch.int32, device=DEV), logits=pl)
+            last = pl[T - 1].clone()
+            q["logits"].append(last.cpu().numpy())
+            tok = torch.empty(1, dtype=torch.int32, device=DEV)
+            st.sample(last, q["params"], token=tok)
+            q["tokens"].append(int(tok.item()))
+            states[r] = st
+            active.append(r)
+        B = len(active)
+        sizes.append(B)
+        lg = torch.empty(B, V, dtype=torch.float32, device=DEV)
+        sm.model.forward_batch([states[r] for r in active], logits=lg)
+        raw = lg.cpu().numpy()
+        toks = torch.empty(B, dtype=torch.int32, device=DEV)
+        sm.model.sample_batch([states[r] for r in active], lg, [reqs[r]["params"] for r in active],
+                              tokens=toks)
+        for j, r in enumerate(active):
+            reqs[r]["logits"].append(raw[j].copy())
+            reqs[r]["tokens"].append(int(toks[j].item()))
+        for r in list(active):                                # leave
+            if len(reqs[r]["tokens"]) >= reqs[r]["budget"]:
+                active.remove(r)
+                assert states.pop(r).device_error() == 0
+    assert max(sizes) == max_active and min(sizes) < max_active   # membership changed
+    for r, q in enumerate(reqs):
+        p = q["params"]
+        # every recorded token is a draw the oracle accepts from the slot's logits
+        for d, (lgt, t) in enumerate(zip(q["logits"], q["tokens"])):
+            assert t in oracle_accepts(lgt, p.temperature, p.repeat_penalty, [], p.top_k, p.top_p,
+                                       oracle.sample_uniform(p.seed, d))[1], f"request {r} draw {d}"
+        # alone, fed the recorded tokens, the sequence sees the same logits
+        st = sm.new_state(0)
+        one = torch.empty(V, dtype=torch.float32, device=DEV)
+        for t in q["prompt"]:
+            st.forward(t, logits=one)
+        ref = [one.cpu().numpy()]
+        for t in q["tokens"][:-1]:
+            st.forward(t, logits=one)
+            ref.append(one.cpu().numpy())
+        for d, (a, b) in enumerate(zip(ref, q["logits"])):
+            scale = float(np.max(np.abs(a)))
+            assert float(np.max(np.abs(a - b))) <= 1e-3 * scale, f"request {r} step {d}"
