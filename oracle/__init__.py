@@ -37,7 +37,8 @@ class OrcConfig(ctypes.Structure):
                 ("n_layer", ctypes.c_int32), ("n_ff", ctypes.c_int32), ("n_ctx", ctypes.c_int32),
                 ("rope_theta", ctypes.c_double), ("rms_norm_eps", ctypes.c_double),
                 ("sliding_window", ctypes.c_int32), ("expert_count", ctypes.c_int32),
-                ("expert_used", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("expert_used", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("qkv_bias", ctypes.c_int32), ("rope_neox", ctypes.c_int32)]
 
 
 class OrcTensor(ctypes.Structure):
@@ -66,6 +67,7 @@ def lib():
         L.orc_matvec.argtypes = [p, i64, i64, i32, p, p]
         L.orc_rmsnorm.argtypes = [p, p, i64, d, p]
         L.orc_rope.argtypes = [p, i32, i64, d]
+        L.orc_rope_neox.argtypes = [p, i32, i64, d]
         L.orc_attention.argtypes = [p, p, p, i32, i32, i32, i64, i32, p]
         L.orc_silu.restype = d
         L.orc_silu.argtypes = [d]
@@ -147,6 +149,12 @@ def rope(v: np.ndarray, pos: int, theta: float) -> np.ndarray:
     return v
 
 
+def rope_neox(v: np.ndarray, pos: int, theta: float) -> np.ndarray:
+    v = _f32(v).copy()
+    lib().orc_rope_neox(v.ctypes.data, v.size, pos, theta)
+    return v
+
+
 def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_head: int, n_kv: int, p: int,
               window: int = 0) -> np.ndarray:
     """q [n_head*hd]; K, V [n_pos][n_kv][hd] with positions 0..p valid."""
@@ -208,7 +216,8 @@ def sample_uniform(seed: int, draw: int) -> float:
 def _config(shape: Shape) -> OrcConfig:
     return OrcConfig(shape.n_vocab, shape.n_embd, shape.n_head, shape.n_kv_head, shape.n_layer,
                      shape.n_ff, shape.n_ctx, shape.rope_theta, shape.rms_norm_eps,
-                     shape.sliding_window, shape.expert_count, shape.expert_used, shape.dtype)
+                     shape.sliding_window, shape.expert_count, shape.expert_used, shape.dtype,
+                     int(shape.qkv_bias), int(shape.rope_neox))
 
 
 class Model:
@@ -222,7 +231,7 @@ class Model:
         self.shape = shape
         self._keep = []  # explicit arrays must outlive the C model
         nsets = max(1, shape.expert_count)
-        slots = 7 + 3 * nsets
+        slots = 7 + 3 * nsets + 3   # ..., experts, then the q / k / v biases
         glob = (OrcTensor * 3)()
         layers = (OrcTensor * (shape.n_layer * slots))()
         for spec in weight_specs(shape):
@@ -235,7 +244,9 @@ class Model:
                 slot = {"attn_norm": L_ATTN_NORM, "wq": L_WQ, "wk": L_WK, "wv": L_WV,
                         "wo": L_WO, "ffn_norm": L_FFN_NORM, "wrouter": L_WROUTER,
                         "wgate": L_EXPERT0 + 3 * spec.sub, "wup": L_EXPERT0 + 3 * spec.sub + 1,
-                        "wdown": L_EXPERT0 + 3 * spec.sub + 2}[spec.name]
+                        "wdown": L_EXPERT0 + 3 * spec.sub + 2,
+                        "bq": L_EXPERT0 + 3 * nsets, "bk": L_EXPERT0 + 3 * nsets + 1,
+                        "bv": L_EXPERT0 + 3 * nsets + 2}[spec.name]
                 tgt = layers[base + slot]
             if arrays is not None and akey in arrays:
                 a = _f32(arrays[akey]).reshape(spec.rows, spec.cols)
@@ -246,7 +257,7 @@ class Model:
             else:
                 if seed is None:
                     raise ValueError(f"no values for {akey} and no seed")
-                tgt.mode, tgt.key, tgt.sigma = SYNTH, spec.key(seed), WEIGHT_SIGMA
+                tgt.mode, tgt.key, tgt.sigma = SYNTH, spec.key(seed), spec.sigma
         cfg = _config(shape)
         self._h = lib().orc_model_new(ctypes.byref(cfg), glob, layers)
         if not self._h:

@@ -57,6 +57,8 @@ typedef struct {
   int32_t expert_used;    /* top-k */
   int32_t dtype;          /* storage of weights: 0 fp32, 1 bf16, 2 Q8 (blocks of 32: int8
                              values times an fp16 scale); KV: fp32 for 0, bf16 otherwise */
+  int32_t qkv_bias;       /* 1: bias vectors added to q, k, v (Qwen2) */
+  int32_t rope_neox;      /* 1: RoPE pairs dimension i with i + hd/2 (Phi-3) */
 } orc_config;
 
 enum { ORC_EXPLICIT = 0, ORC_SYNTH = 1, ORC_CONST = 2 };
@@ -71,7 +73,8 @@ typedef struct {
   float value;       /* ORC_CONST: every element */
 } orc_tensor;
 
-/* per-layer tensor slots; experts follow as (gate, up, down) triples */
+/* per-layer tensor slots; experts follow as (gate, up, down) triples, then
+   the q, k and v bias vectors (fp32; used when qkv_bias is set) */
 enum {
   ORC_L_ATTN_NORM = 0,
   ORC_L_WQ = 1,
@@ -117,7 +120,8 @@ float orc_round_bf16(float f) {
   return r;
 }
 
-static int64_t layer_slots(const orc_model *m) { return 7 + 3 * (int64_t)m->n_ffn_sets; }
+static int64_t layer_slots(const orc_model *m) { return 7 + 3 * (int64_t)m->n_ffn_sets + 3; }
+static int bias_slot(const orc_model *m, int which) { return 7 + 3 * m->n_ffn_sets + which; }
 
 static const orc_tensor *ltensor(const orc_model *m, int l, int slot) {
   return &m->layer[(int64_t)l * layer_slots(m) + slot];
@@ -193,6 +197,21 @@ void orc_rope(float *v, int hd, int64_t pos, double theta) {
     const double a = v[2 * i], b = v[2 * i + 1];
     v[2 * i] = (float)(a * c - b * s);
     v[2 * i + 1] = (float)(a * s + b * c);
+  }
+}
+
+/* NeoX-style RoPE (the Phi-3 forward, "Engine Architecture", "Architecture
+   Detection"): pair i is dimensions (i, i + hd/2), turned by the same angle
+   pos * theta^(-2i/hd) as adjacent pair i of the Llama form. */
+void orc_rope_neox(float *v, int hd, int64_t pos, double theta) {
+  const int h2 = hd / 2;
+  for (int i = 0; i < h2; ++i) {
+    const double freq = pow(theta, -2.0 * (double)i / (double)hd);
+    const double phi = (double)pos * freq;
+    const double c = cos(phi), s = sin(phi);
+    const double a = v[i], b = v[i + h2];
+    v[i] = (float)(a * c - b * s);
+    v[i + h2] = (float)(a * s + b * c);
   }
 }
 
@@ -522,8 +541,22 @@ int orc_layer(const orc_model *m, orc_state *s, int l, float *x) {
   orc_matvec(ltensor(m, l, ORC_L_WQ), H * hd, E, dt, xn, q);
   orc_matvec(ltensor(m, l, ORC_L_WK), Hkv * hd, E, dt, xn, kn);
   orc_matvec(ltensor(m, l, ORC_L_WV), Hkv * hd, E, dt, xn, vn);
-  for (int64_t h = 0; h < H; ++h) orc_rope(q + h * hd, (int)hd, p, c->rope_theta);
-  for (int64_t g = 0; g < Hkv; ++g) orc_rope(kn + g * hd, (int)hd, p, c->rope_theta);
+  if (c->qkv_bias) {
+    /* Qwen2: q, k, v each get their bias before RoPE ("Engine Architecture",
+       "Architecture Detection": attention biases set by config flags) */
+    float *dst[3] = {q, kn, vn};
+    const int64_t n[3] = {H * hd, Hkv * hd, Hkv * hd};
+    for (int j = 0; j < 3; ++j) {
+      float *b = (float *)malloc((size_t)n[j] * sizeof(float));
+      get_row(ltensor(m, l, bias_slot(m, j)), 0, n[j], 0, b);
+      for (int64_t e = 0; e < n[j]; ++e) dst[j][e] = dst[j][e] + b[e];
+      free(b);
+    }
+  }
+  for (int64_t h = 0; h < H; ++h)
+    (c->rope_neox ? orc_rope_neox : orc_rope)(q + h * hd, (int)hd, p, c->rope_theta);
+  for (int64_t g = 0; g < Hkv; ++g)
+    (c->rope_neox ? orc_rope_neox : orc_rope)(kn + g * hd, (int)hd, p, c->rope_theta);
   float *Kl = orc_state_kv(s, l, 0), *Vl = orc_state_kv(s, l, 1);
   for (int64_t e = 0; e < Hkv * hd; ++e) {
     Kl[p * Hkv * hd + e] = dt ? orc_round_bf16(kn[e]) : kn[e];

@@ -24,6 +24,7 @@ F32, BF16, Q8 = 0, 1, 2
 TOK_EMBD, ATTN_NORM, WQ, WK, WV, WO, FFN_NORM = 1, 2, 3, 4, 5, 6, 7
 WGATE, WUP, WDOWN, WROUTER, OUT_NORM, OUTPUT = 8, 9, 10, 11, 12, 13
 KCACHE, VCACHE, TOKENS, POSITIONS = 14, 15, 16, 17
+BQ, BK, BV = 18, 19, 20   # q / k / v bias vectors
 
 
 def build_commands(cuda_arch: str = "103a"):

@@ -7,6 +7,7 @@ MoE decoder and a Llama-8B-shaped batched-slot decoder.  The recipe:
 
 * weights (embeddings, projections, router, LM head) ~ N(0, 0.02^2), stored in
   the model's dtype (Q8: blocks of 32 quantized as the generator defines);
+  q / k / v biases (models with qkv_bias) ~ N(0, 0.5^2), fp32;
   every norm weight is 1.0 (fp32);
 * the KV cache of positions below the start position ~ N(0, 1) in the cache
   dtype (raw cache contents, i.e. keys already rotated);
@@ -19,10 +20,11 @@ from __future__ import annotations
 from dataclasses import dataclass, field, replace
 from typing import List, Optional
 
-from . import (ATTN_NORM, BF16, F32, FFN_NORM, OUT_NORM, OUTPUT, POSITIONS, Q8, TOK_EMBD,
-               TOKENS, WDOWN, WGATE, WK, WO, WQ, WROUTER, WUP, WV, key, uniform_int)
+from . import (ATTN_NORM, BF16, BK, BQ, BV, F32, FFN_NORM, OUT_NORM, OUTPUT, POSITIONS, Q8,
+               TOK_EMBD, TOKENS, WDOWN, WGATE, WK, WO, WQ, WROUTER, WUP, WV, key, uniform_int)
 
 WEIGHT_SIGMA = 0.02
+BIAS_SIGMA = 0.5        # q / k / v biases (fp32), on the scale of the projections' outputs
 KV_SIGMA = 1.0
 NORM_VALUE = 1.0
 
@@ -42,6 +44,8 @@ class Shape:
     expert_count: int = 0
     expert_used: int = 0
     dtype: int = BF16
+    qkv_bias: bool = False    # Qwen2: bias vectors on q, k, v
+    rope_neox: bool = False   # Phi-3: RoPE pairs dimension i with i + head_dim / 2
 
     @property
     def head_dim(self) -> int:
@@ -151,6 +155,7 @@ class TensorSpec:
     rows: int
     cols: int
     const: Optional[float] = None   # constant tensors (norm weights)
+    sigma: float = WEIGHT_SIGMA
 
     def key(self, seed: int) -> int:
         return key(seed, self.kind, self.layer, self.sub)
@@ -170,6 +175,10 @@ def weight_specs(shape: Shape) -> List[TensorSpec]:
                 TensorSpec("wv", WV, l, 0, Hkv * hd, E),
                 TensorSpec("wo", WO, l, 0, E, H * hd),
                 TensorSpec("ffn_norm", FFN_NORM, l, 0, 1, E, const=NORM_VALUE)]
+        if shape.qkv_bias:
+            out += [TensorSpec("bq", BQ, l, 0, 1, H * hd, sigma=BIAS_SIGMA),
+                    TensorSpec("bk", BK, l, 0, 1, Hkv * hd, sigma=BIAS_SIGMA),
+                    TensorSpec("bv", BV, l, 0, 1, Hkv * hd, sigma=BIAS_SIGMA)]
         if shape.expert_count > 0:
             out.append(TensorSpec("wrouter", WROUTER, l, 0, shape.expert_count, E))
         for e in range(max(1, shape.expert_count)):

@@ -117,6 +117,42 @@ def test_rope_dot_products_depend_on_relative_position_only():
         assert abs(d0 - d1) < 1e-4 * (np.linalg.norm(q) * np.linalg.norm(k))
 
 
+def _complex_rotation_halves(v, p, theta):
+    """Textbook NeoX RoPE: pair (i, i + d/2) as a complex number times exp(i p theta^(-2i/d))."""
+    d = v.size
+    z = v[: d // 2].astype(np.float64) + 1j * v[d // 2:].astype(np.float64)
+    z = z * np.exp(1j * p * np.power(theta, -2.0 * np.arange(d // 2) / d))
+    return np.concatenate([z.real, z.imag])
+
+
+@pytest.mark.parametrize("hd", [32, 128])
+@pytest.mark.parametrize("p", [1, 7, 2049])
+@pytest.mark.parametrize("theta", [1e4, 1e6])
+def test_rope_neox_is_complex_rotation_of_half_pairs(hd, p, theta):
+    v = f32(RNG.standard_normal(hd))
+    got = oracle.rope_neox(v, p, theta)
+    assert np.allclose(got, _complex_rotation_halves(v, p, theta), rtol=0,
+                       atol=1e-6 * np.abs(v).max())
+    assert np.array_equal(oracle.rope_neox(v, 0, theta), v)
+
+
+def test_rope_neox_is_adjacent_rope_on_interleaved_halves():
+    # the layout the GPU library uses for NeoX models: a head's dimensions in
+    # the order 0, d/2, 1, d/2 + 1, ... make the NeoX pairs adjacent, and the
+    # adjacent-pair rotation of the reordered vector is the reordered NeoX
+    # rotation (same angle per pair)
+    hd = 64
+    perm = np.empty(hd, dtype=np.int64)
+    perm[0::2], perm[1::2] = np.arange(hd // 2), np.arange(hd // 2) + hd // 2
+    for p in (1, 5, 300):
+        v = f32(RNG.standard_normal(hd))
+        assert np.allclose(oracle.rope(v[perm], p, 1e4), oracle.rope_neox(v, p, 1e4)[perm],
+                           rtol=0, atol=1e-6)
+    # and the two forms differ on the same vector
+    v = f32(RNG.standard_normal(hd))
+    assert not np.allclose(oracle.rope(v, 3, 1e4), oracle.rope_neox(v, 3, 1e4), atol=1e-3)
+
+
 # ------------------------------------------------------------------- attention
 
 def _rand_kv(npos, nkv, hd):
@@ -303,6 +339,8 @@ def _library_forward(shape: Shape, arrays, tokens):
         return d(w).ravel() * x / math.sqrt(np.linalg.norm(x) ** 2 / x.size + eps)
 
     def rot(v, p):
+        if shape.rope_neox:
+            return _complex_rotation_halves(v, p, shape.rope_theta)
         return _complex_rotation(v, p, shape.rope_theta)
 
     def store(v):
@@ -321,6 +359,10 @@ def _library_forward(shape: Shape, arrays, tokens):
             q = d(arrays[("wq", l, 0)]) @ xn
             k = d(arrays[("wk", l, 0)]) @ xn
             v = d(arrays[("wv", l, 0)]) @ xn
+            if shape.qkv_bias:
+                q = q + d(arrays[("bq", l, 0)]).ravel()
+                k = k + d(arrays[("bk", l, 0)]).ravel()
+                v = v + d(arrays[("bv", l, 0)]).ravel()
             q = np.concatenate([rot(q[h * hd:(h + 1) * hd], p) for h in range(H)])
             k = np.concatenate([rot(k[g * hd:(g + 1) * hd], p) for g in range(Hkv)])
             Kc[l].append(store(k))
@@ -353,7 +395,7 @@ def _oracle_run(shape, arrays, tokens):
 
 
 @pytest.mark.parametrize("variant", ["mha_f32", "gqa_f32", "gqa_bf16", "window_bf16", "moe_f32",
-                                     "moe_bf16"])
+                                     "moe_bf16", "qkv_bias_bf16", "neox_f32", "bias_neox_f32"])
 def test_whole_step_matches_library_composition(variant):
     shape = {
         "mha_f32": dataclasses.replace(TS, n_kv_head=4),
@@ -362,6 +404,9 @@ def test_whole_step_matches_library_composition(variant):
         "window_bf16": dataclasses.replace(TS, dtype=BF16, sliding_window=3),
         "moe_f32": dataclasses.replace(TS, expert_count=4, expert_used=2),
         "moe_bf16": dataclasses.replace(TS, expert_count=3, expert_used=2, dtype=BF16),
+        "qkv_bias_bf16": dataclasses.replace(TS, dtype=BF16, qkv_bias=True),
+        "neox_f32": dataclasses.replace(TS, rope_neox=True),
+        "bias_neox_f32": dataclasses.replace(TS, qkv_bias=True, rope_neox=True),
     }[variant]
     arrays = _rand_arrays(shape)
     tokens = [int(t) for t in RNG.integers(0, shape.n_vocab, size=shape.n_ctx)]
@@ -706,3 +751,40 @@ def test_sample_empirical_frequencies_match_kept_probabilities():
     assert counts.sum() == n and np.all(counts[np.setdiff1d(np.arange(40), idx)] == 0)
     sd = np.sqrt(n * probs * (1 - probs))
     assert np.all(np.abs(counts[idx] - n * probs) < 5 * sd + 1)
+
+
+def test_qkv_bias_on_zero_projections_is_the_bias():
+    # with Wq = Wk = Wv = 0 every value vector is the v bias, so whatever the
+    # attention weights, each head's output is its KV head's v bias; with the
+    # FFN zeroed the logits then have a closed form
+    shape = dataclasses.replace(TS, qkv_bias=True, n_layer=1)
+    arrays = _rand_arrays(shape)
+    H, Hkv, hd = shape.n_head, shape.n_kv_head, shape.head_dim
+    for name in ("wq", "wk", "wv"):
+        arrays[(name, 0, 0)] = np.zeros_like(arrays[(name, 0, 0)])
+    for name in ("wgate", "wup", "wdown"):
+        arrays[(name, 0, 0)] = np.zeros_like(arrays[(name, 0, 0)])
+    m = oracle.Model(shape, arrays=arrays)
+    s = m.new_state()
+    bv = arrays[("bv", 0, 0)].ravel().astype(np.float64)
+    o = np.concatenate([bv[(h // (H // Hkv)) * hd:(h // (H // Hkv) + 1) * hd] for h in range(H)])
+    for p, tok in enumerate((3, 9, 4)):
+        lg, _ = s.forward(tok)
+        x = arrays["tok_embd"][tok].astype(np.float64) + arrays[("wo", 0, 0)].astype(np.float64) @ o
+        xn = arrays["out_norm"].ravel() * x / math.sqrt(np.mean(x * x) + shape.rms_norm_eps)
+        want = arrays["output"].astype(np.float64) @ xn
+        assert np.allclose(lg, want, rtol=0, atol=1e-5 * np.abs(want).max()), p
+
+
+def test_bias_and_neox_models_differ_from_the_plain_model():
+    # each variant flag changes the result (a dropped bias or rotation form fails here)
+    base = dataclasses.replace(TS, qkv_bias=True)
+    arrays = _rand_arrays(base)
+    tokens = [int(t) for t in RNG.integers(0, TS.n_vocab, size=6)]
+    plain = {k: v for k, v in arrays.items() if not (isinstance(k, tuple) and k[0][0] == "b")}
+    runs = {}
+    for name, shape, arr in (("plain", TS, plain), ("bias", base, arrays),
+                             ("neox", dataclasses.replace(TS, rope_neox=True), plain)):
+        runs[name] = _oracle_run(shape, arr, tokens)[0]
+    for other in ("bias", "neox"):
+        assert not np.allclose(runs["plain"][-1], runs[other][-1], atol=1e-3)
