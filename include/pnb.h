@@ -84,7 +84,15 @@ enum {
    Detection"; the arena reserves n_experts + 2*n_experts_used floats for the
    router, "Core Engine API", section "Scratch (arena) estimation").
    The library applies no defaults: every field is used as given.
-   head_dim = n_embd / n_head. */
+   head_dim = n_embd / n_head.
+   rope_neox = 1 selects the NeoX-style rotation of the Phi-3 forward, which
+   pairs dimension i of a head with dimension i + head_dim / 2 ("Engine
+   Architecture", "Architecture Detection"); 0 the Llama form, adjacent pairs
+   (2i, 2i + 1).  Both turn pair i by pos * rope_theta^(-2i/head_dim).  The
+   kernels rotate adjacent pairs only: a NeoX model gives each head's Wq and
+   Wk rows (and its q / k bias entries) in the order 0, hd/2, 1, hd/2 + 1,
+   ..., hd/2 - 1, hd - 1, which makes each NeoX pair adjacent (the reordering
+   a loader applies once), and its cached keys are in that order. */
 typedef struct {
   int32_t n_vocab, n_embd, n_head, n_kv_head, n_layer, n_ff, n_ctx;
   double rope_theta, rms_norm_eps;
@@ -92,6 +100,7 @@ typedef struct {
   int32_t expert_count;   /* 0 = dense SwiGLU FFN */
   int32_t expert_used;    /* top-k experts per token when expert_count > 0 */
   int32_t dtype;          /* PNB_F32, PNB_BF16 or PNB_Q8_0: weights (KV: fp32 / bf16 / bf16) */
+  int32_t rope_neox;      /* 0 Llama-style RoPE, 1 NeoX-style (see above) */
 } pnb_config;
 
 /* Device weights, caller-owned, in the library's layout (row-major; "dtype" =
@@ -108,7 +117,11 @@ typedef struct {
      ffn_norm[l]         [E]                                   fp32
      w_router[l]         [expert_count][E]                     dtype  (NULL array when dense)
      w_gate_up[l*S + e]  [2 n_ff][E]                           dtype  row 2i = gate row i, 2i+1 = up row i
-     w_down[l*S + e]     [E][n_ff]                             dtype                                     */
+     w_down[l*S + e]     [E][n_ff]                             dtype
+     bqkv[l]             [(n_head + 2 n_kv_head) hd]           fp32   q, k, v biases in wqkv's row order
+                                                                      (Qwen2; NULL array: no biases)
+   A model with biases runs the per-phase and batched kernels (not the
+   persistent kernel or the fused attention block: PNB_E_UNSUPPORTED). */
 typedef struct {
   const void *tok_embd;
   const float *out_norm;
@@ -120,6 +133,7 @@ typedef struct {
   const void *const *w_router;
   const void *const *w_gate_up;
   const void *const *w_down;
+  const float *const *bqkv;
 } pnb_weights;
 
 typedef struct pnb_model pnb_model;

@@ -37,13 +37,14 @@ class pnb_config(ctypes.Structure):
                 ("n_layer", ctypes.c_int32), ("n_ff", ctypes.c_int32), ("n_ctx", ctypes.c_int32),
                 ("rope_theta", ctypes.c_double), ("rms_norm_eps", ctypes.c_double),
                 ("sliding_window", ctypes.c_int32), ("expert_count", ctypes.c_int32),
-                ("expert_used", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("expert_used", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("rope_neox", ctypes.c_int32)]
 
 
 class pnb_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("tok_embd", "out_norm", "output", "attn_norm", "wqkv", "wo", "ffn_norm",
-                 "w_router", "w_gate_up", "w_down")]
+                 "w_router", "w_gate_up", "w_down", "bqkv")]
 
 
 class pnb_sampling_params(ctypes.Structure):
@@ -151,18 +152,18 @@ class Model:
     with n_layer * max(1, expert_count) entries (layout: include/pnb.h)."""
 
     def __init__(self, cfg: pnb_config, *, tok_embd, out_norm, output, attn_norm, wqkv, wo,
-                 ffn_norm, w_gate_up, w_down, w_router=None, keepalive=None):
+                 ffn_norm, w_gate_up, w_down, w_router=None, bqkv=None, keepalive=None):
         self.cfg = cfg
         self._keep = [keepalive]
         arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs) if xs else None
         self._arrays = [arr(attn_norm), arr(wqkv), arr(wo), arr(ffn_norm), arr(w_router),
-                        arr(w_gate_up), arr(w_down)]
+                        arr(w_gate_up), arr(w_down), arr(bqkv)]
         w = pnb_weights()
         w.tok_embd, w.out_norm, w.output = tok_embd, out_norm, output
-        (an, qkv, o, fn, rt, gu, dn) = self._arrays
+        (an, qkv, o, fn, rt, gu, dn, bq) = self._arrays
         cast = lambda a: ctypes.cast(a, ctypes.c_void_p) if a is not None else None
         w.attn_norm, w.wqkv, w.wo, w.ffn_norm = cast(an), cast(qkv), cast(o), cast(fn)
-        w.w_router, w.w_gate_up, w.w_down = cast(rt), cast(gu), cast(dn)
+        w.w_router, w.w_gate_up, w.w_down, w.bqkv = cast(rt), cast(gu), cast(dn), cast(bq)
         h = ctypes.c_void_p()
         check(pnb_model_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)),
               "pnb_model_create")

@@ -94,6 +94,7 @@ struct pnb_model {
   const void *output = nullptr;
   std::vector<const float *> attn_norm, ffn_norm;
   std::vector<const void *> wqkv, wo, w_router, w_gate_up, w_down;
+  std::vector<const float *> bqkv;       // per layer q / k / v bias, empty when the model has none
   double *inv_freq = nullptr;            // device [hd/2]
   const void **tab_gate_up = nullptr;    // device [n_layer][expert_count]
   const void **tab_down = nullptr;
@@ -196,6 +197,7 @@ int validate_config(const pnb_config *c) {
       c->n_layer <= 0 || c->n_ff <= 0 || c->n_ctx <= 0)
     return PNB_E_INVAL;
   if (c->n_embd % c->n_head || c->n_head % c->n_kv_head) return PNB_E_INVAL;
+  if (c->rope_neox != 0 && c->rope_neox != 1) return PNB_E_INVAL;
   const int hd = c->n_embd / c->n_head;
   if (hd % 2) return PNB_E_INVAL;
   if (hd != 32 && hd != 64 && hd != 128) return PNB_E_UNSUPPORTED;
@@ -246,6 +248,7 @@ void plan_step(pnb_model *m) {
   const int G = c.n_head / c.n_kv_head, hd = m->hd, es = m->kv_es;
   m->persistent = false;
   if (c.dtype == PNB_Q8_0) return;   // the persistent kernel streams fp32 / bf16 weights
+  if (!m->bqkv.empty()) return;      // nor does it add q / k / v biases
   if (!(hd == 32 || hd == 64 || hd == 128) || !(G == 1 || G == 2 || G == 4 || G == 8) ||
       G * hd > 512)
     return;
@@ -322,6 +325,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       qa.n_kv = Hkv;
       qa.head_dim = hd;
       qa.inv_freq = m->inv_freq;
+      qa.bias = m->bqkv.empty() ? nullptr : m->bqkv[l];
       qa.q = s->q;
       qa.k_cache = kc;
       qa.v_cache = vc;
@@ -657,7 +661,7 @@ bool encode_wo_map(CUtensorMap *map, const void *base, int dtype, int E, int HHD
 bool plan_block(pnb_model *m) {
   const pnb_config &c = m->cfg;
   const int hd = m->hd, H = c.n_head, E = c.n_embd, es = m->kv_es;
-  if (!(hd == 32 || hd == 64 || hd == 128) || c.dtype == PNB_Q8_0) return false;
+  if (!(hd == 32 || hd == 64 || hd == 128) || c.dtype == PNB_Q8_0 || !m->bqkv.empty()) return false;
   int C = 8;
   while (C > 1 && H * C > m->num_sms) C >>= 1;
   if (H * C > m->num_sms || E % C) return false;
@@ -896,6 +900,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
     if ((e = launch_bnorm(na, st, l > 0)) != cudaSuccess) return e;
     BGemmArgs g = bgemm_args(m, b, b->p_qkv, kEpiQkv, B, bp);
     g.tr = KTrace{trace, 7 * l + 1};
+    g.bias = m->bqkv.empty() ? nullptr : m->bqkv[l];
     g.q = b->qb;
     g.kv_off = (size_t)(2 * l) * layer_kv;
     g.layer_kv_bytes = layer_kv;
@@ -1030,6 +1035,10 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
       if (!gu || !dn) return PNB_E_NULL;
       if (!aligned16(gu) || !aligned16(dn)) return PNB_E_ALIGN;
     }
+    if (w->bqkv) {
+      if (!w->bqkv[l]) return PNB_E_NULL;
+      if (!aligned16(w->bqkv[l])) return PNB_E_ALIGN;
+    }
   }
   pnb_model *m = new (std::nothrow) pnb_model();
   if (!m) return PNB_E_NOMEM;
@@ -1047,6 +1056,7 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
     m->attn_norm.assign(w->attn_norm, w->attn_norm + c.n_layer);
     m->ffn_norm.assign(w->ffn_norm, w->ffn_norm + c.n_layer);
     m->wqkv.assign(w->wqkv, w->wqkv + c.n_layer);
+    if (w->bqkv) m->bqkv.assign(w->bqkv, w->bqkv + c.n_layer);
     m->wo.assign(w->wo, w->wo + c.n_layer);
     if (moe) m->w_router.assign(w->w_router, w->w_router + c.n_layer);
     m->w_gate_up.assign(w->w_gate_up, w->w_gate_up + (size_t)c.n_layer * n_sets);

@@ -249,16 +249,18 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
     const int kx = grow - qrows - (is_k ? 0 : krows);
     const int gk = kx / hd, d = kx - gk * hd;
     const int pair = (grow % hd) >> 1;
+    const float bias = (a.bias && in) ? a.bias[grow] : 0.f;
 #pragma unroll
     for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
-      float par[kEpiChunk];
+      float yv[kEpiChunk], par[kEpiChunk];
       float2 cs[kEpiChunk];
       int slot[kEpiChunk];
       uint8_t *base[kEpiChunk];
 #pragma unroll
       for (int j = 0; j < kEpiChunk; ++j) {
         const int b = c0 + j;
-        par[j] = __shfl_xor_sync(0xffffffffu, y[b], 1);
+        yv[j] = y[b] + bias;
+        par[j] = __shfl_xor_sync(0xffffffffu, yv[j], 1);
         const bool live = in && b < a.B;
         cs[j] = (live && rope) ? a.rope[(size_t)b * half + pair] : make_float2(1.f, 0.f);
         slot[j] = (live && !is_q) ? a.pos[b] : 0;
@@ -268,9 +270,9 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
       for (int j = 0; j < kEpiChunk; ++j) {
         const int b = c0 + j;
         if (!(in && b < a.B)) continue;
-        float v = y[b];
+        float v = yv[j];
         if (rope) {
-          const float v0 = even ? y[b] : par[j], v1 = even ? par[j] : y[b];
+          const float v0 = even ? yv[j] : par[j], v1 = even ? par[j] : yv[j];
           v = even ? v0 * cs[j].x - v1 * cs[j].y : v0 * cs[j].y + v1 * cs[j].x;
         }
         if (is_q) {
@@ -602,6 +604,10 @@ __global__ void __launch_bounds__(256) k_bmerge(const BGemmArgs a) {
   if constexpr (KIND == kEpiQkv) {
     const int hd = a.hd, qrows = a.n_head * hd, krows = a.n_kv * hd;
     float v0 = s.x, v1 = s.y;
+    if (a.bias) {
+      v0 += a.bias[r];
+      v1 += a.bias[r + 1];
+    }
     if (r < qrows + krows) {
       const float2 cs = a.rope[(size_t)b * (hd / 2) + ((r % hd) >> 1)];
       const float t0 = v0 * cs.x - v1 * cs.y, t1 = v0 * cs.y + v1 * cs.x;

@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
   for_claimed_rows(a.g, c, a.s.rows, true, tid, [&](int k, int r, int, int64_t row) {
     const int rr = (int)row;
     float v0 = item_row_total(a.g, c, k, r), v1 = item_row_total(a.g, c, k, r + 1);
+    if (a.bias) {
+      v0 += a.bias[rr];
+      v1 += a.bias[rr + 1];
+    }
     if (rr < qrows + krows) {
       const float2 cs = c.rope[(rr % hd) >> 1];
       const float t0 = v0 * cs.x - v1 * cs.y, t1 = v0 * cs.y + v1 * cs.x;

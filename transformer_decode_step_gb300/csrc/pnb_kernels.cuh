@@ -103,6 +103,7 @@ struct QkvArgs {
   float eps;
   int n_head, n_kv, head_dim;
   const double *inv_freq;  // [head_dim / 2] = rope_theta^(-2i/head_dim)
+  const float *bias;       // [rows] q / k / v bias added before RoPE, or nullptr
   float *q;
   void *k_cache, *v_cache; // this layer's [n_kv][cap][head_dim]
   int cap, window;
@@ -263,6 +264,7 @@ struct BGemmArgs {
   float *x;              // kEpiResid: residual streams [B][rows]
   float *q;              // kEpiQkv: queries [B][n_head * hd]
   const float2 *rope;    // kEpiQkv: (cos, sin) [B][hd / 2]
+  const float *bias;     // kEpiQkv: q / k / v bias [rows] added before RoPE, or null
   const BSlot *slots;    // kEpiQkv / kEpiLm
   const int32_t *pos;    // [B]
   size_t kv_off, layer_kv_bytes;

@@ -12,7 +12,7 @@ from __future__ import annotations
 import ctypes
 
 import synth
-from synth.workloads import KV_SIGMA, WEIGHT_SIGMA, Shape, kv_prefill_range
+from synth.workloads import BIAS_SIGMA, KV_SIGMA, WEIGHT_SIGMA, Shape, kv_prefill_range
 
 
 class _Arena:
@@ -47,6 +47,8 @@ class SynthModel:
         for l in range(L):
             d = {"attn_norm": ar.add(E * 4), "wqkv": ar.add(mb((H + 2 * Hkv) * hd, E)),
                  "wo": ar.add(mb(E, H * hd)), "ffn_norm": ar.add(E * 4)}
+            if s.qkv_bias:
+                d["bqkv"] = ar.add((H + 2 * Hkv) * hd * 4)
             if s.expert_count > 0:
                 d["w_router"] = ar.add(mb(s.expert_count, E))
             d["w_gate_up"] = [ar.add(mb(2 * F, E)) for _ in range(nsets)]
@@ -69,6 +71,15 @@ class SynthModel:
             synth.dev_fill_matrix(q, dt, H * hd, 1, Hkv * hd, E, key(synth.WK, l), WEIGHT_SIGMA, st)
             synth.dev_fill_matrix(q, dt, (H + Hkv) * hd, 1, Hkv * hd, E, key(synth.WV, l),
                                   WEIGHT_SIGMA, st)
+            if s.qkv_bias:
+                b = base + d["bqkv"]
+                for j, (kind, n) in enumerate(((synth.BQ, H * hd), (synth.BK, Hkv * hd),
+                                               (synth.BV, Hkv * hd))):
+                    off = (0, H * hd, (H + Hkv) * hd)[j] * 4
+                    synth.dev_fill_matrix(b + off, synth.F32, 0, 1, 1, n, key(kind, l), BIAS_SIGMA,
+                                          st)
+            if s.rope_neox:
+                self._interleave_halves(d, H, Hkv, hd, mb(1, E), s.qkv_bias)
             synth.dev_fill_matrix(base + d["wo"], dt, 0, 1, E, H * hd, key(synth.WO, l),
                                   WEIGHT_SIGMA, st)
             if s.expert_count > 0:
@@ -82,15 +93,33 @@ class SynthModel:
                                       WEIGHT_SIGMA, st)
 
         cfg = pnb_config(V, E, H, Hkv, L, F, s.n_ctx, s.rope_theta, s.rms_norm_eps,
-                         s.sliding_window, s.expert_count, s.expert_used, dt)
+                         s.sliding_window, s.expert_count, s.expert_used, dt, int(s.rope_neox))
         self.model = Model(
             cfg, tok_embd=base + o_emb, out_norm=base + o_onorm, output=base + o_out,
             attn_norm=[base + d["attn_norm"] for d in lay], wqkv=[base + d["wqkv"] for d in lay],
             wo=[base + d["wo"] for d in lay], ffn_norm=[base + d["ffn_norm"] for d in lay],
             w_router=[base + d["w_router"] for d in lay] if s.expert_count > 0 else None,
             w_gate_up=[base + off for d in lay for off in d["w_gate_up"]],
-            w_down=[base + off for d in lay for off in d["w_down"]], keepalive=self.buf)
+            w_down=[base + off for d in lay for off in d["w_down"]],
+            bqkv=[base + d["bqkv"] for d in lay] if s.qkv_bias else None, keepalive=self.buf)
         self.weight_bytes = ar.size
+
+    def _interleave_halves(self, d, H, Hkv, hd, row_bytes, bias):
+        """NeoX models: each head's Wq / Wk rows (and q / k bias entries) in the
+        order 0, hd/2, 1, hd/2 + 1, ... - the library's layout for them."""
+        import torch
+
+        perm = torch.empty(hd, dtype=torch.long)
+        perm[0::2] = torch.arange(hd // 2)
+        perm[1::2] = torch.arange(hd // 2) + hd // 2
+        perm = perm.to(self.buf.device)
+        torch.cuda.synchronize(self.buf.device)   # the fills ran on the generator's stream
+        heads = H + Hkv                       # Wq then Wk, one block of hd rows per head
+        w = self.buf[d["wqkv"]:d["wqkv"] + heads * hd * row_bytes].view(heads, hd, row_bytes)
+        w.copy_(w[:, perm, :].clone())
+        if bias:
+            b = self.buf[d["bqkv"]:d["bqkv"] + heads * hd * 4].view(torch.float32).view(heads, hd)
+            b.copy_(b[:, perm].clone())
 
     def new_state(self, start_pos: int = 0, slot: int = 0, stream=None):
         """A zeroed state; with start_pos > 0 the cache positions below it (the last
@@ -103,6 +132,9 @@ class SynthModel:
         return state
 
     def prefill(self, state, start_pos: int, slot: int = 0, stream=None):
+        """Generated cache contents for positions below start_pos.  They are in
+        the library's layout; for NeoX models that is the interleaved key order,
+        which is not the order an oracle cache of the same values uses."""
         import torch
 
         s = self.shape
