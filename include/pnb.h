@@ -210,11 +210,16 @@ int pnb_forward(pnb_model *m, pnb_state *s, int32_t token, pnb_stream stream, fl
    or NULL.  1 <= B <= 64.  Every weight is read once per step for all slots:
    the projections run on tcgen05 tensor cores with each activation split into
    a bf16 high and low part, so results equal B single-sequence steps to about
-   1e-5 relative (not bitwise).  Supported: bf16 dense models with n_embd,
-   n_head * head_dim and n_ff multiples of 64; MoE and fp32 models return
-   PNB_E_UNSUPPORTED (as the pages' batched decoder returns -1 for MoE and
-   F32).  B = 1 runs the single-sequence step (the faster path for one
-   slot).  PNB_E_CTX_FULL when any slot's pos already reached n_ctx; a token
+   1e-5 relative (not bitwise).  Supported: bf16 models with n_embd,
+   n_head * head_dim and n_ff multiples of 64, dense or MoE; fp32 and Q8
+   models return PNB_E_UNSUPPORTED (the pages' batched decoder returns -1
+   for F32, and for MoE, which this one covers).  MoE: a router kernel gives
+   every slot its top-k experts and their softmax weights (the
+   single-sequence router's arithmetic per slot); each expert's gate/up and
+   down projections then run over all slots, and the down projection adds
+   weight * output to the slots that chose the expert - every expert's
+   weights are streamed once per step.  B = 1 runs the single-sequence step
+   (the faster path for one slot).  PNB_E_CTX_FULL when any slot's pos already reached n_ctx; a token
    outside [0, n_vocab) sets PNB_DEV_ERR_TOKEN in that slot's state.  The
    first call allocates the model's batched workspace (make it before any
    stream capture). */
@@ -272,8 +277,8 @@ int pnb_model_fused_attention(const pnb_model *m);
    stored by the chunk's QKV kernel before its attention kernel reads them,
    and each token attends to the positions up to its own. A sliding-window
    ring must not wrap inside a chunk, so once the ring is full the remaining
-   tokens go one per step, as do models the batched step does not cover (MoE,
-   fp32); a chunk of one token is a single-sequence step.
+   tokens go one per step, as do models the batched step does not cover
+   (fp32, Q8); a chunk of one token is a single-sequence step.
    logits_dev: optional [T][n_vocab] fp32 (16-byte aligned); argmax_dev:
    optional [T]. After the call the state's device token is the last token's
    argmax (PNB_TOKEN_PREV continues from it). Stream-ordered; it uses the

@@ -37,6 +37,10 @@ SHAPE = wl.Shape(n_vocab=3001, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_f
 SHAPE_WIN = dataclasses.replace(SHAPE, sliding_window=48, n_ctx=200, n_vocab=2000, rope_theta=1e6)
 SHAPE_HD128 = wl.Shape(n_vocab=1500, n_embd=1024, n_head=8, n_kv_head=8, n_layer=1, n_ff=1536,
                        n_ctx=300, rope_theta=5e5, rms_norm_eps=1e-5, dtype=BF16)
+# MoE: 4 experts, top-2 (the router runs per slot, every expert's FFN over all slots)
+SHAPE_MOE = wl.Shape(n_vocab=3001, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_ff=1024,
+                     n_ctx=160, rope_theta=1e6, rms_norm_eps=1e-5, expert_count=4, expert_used=2,
+                     dtype=BF16)
 SEED = 31
 
 
@@ -95,13 +99,17 @@ def run(shape, B, steps=3):
     return near
 
 
-@pytest.mark.parametrize("shape", [SHAPE, SHAPE_WIN, SHAPE_HD128], ids=["gqa", "window", "mha_hd128"])
+@pytest.mark.parametrize("shape", [SHAPE, SHAPE_WIN, SHAPE_HD128, SHAPE_MOE],
+                         ids=["gqa", "window", "mha_hd128", "moe"])
 @pytest.mark.parametrize("B", [1, 5, 20, 40])
 def test_batched_step_matches_per_slot_oracle(shape, B):
-    assert run(shape, B) == 0
+    # argmax may differ only on near-ties (inside the logit tolerance); with
+    # these seeds the dense shapes have none, the MoE shape at most one
+    assert run(shape, B) <= (1 if shape.expert_count else 0)
 
 
-def test_batched_step_matches_single_sequence_steps():
+@pytest.mark.parametrize("SHAPE", [SHAPE, SHAPE_MOE], ids=["dense", "moe"])
+def test_batched_step_matches_single_sequence_steps(SHAPE):
     B = 12
     starts = starts_for(SHAPE, B, 7)
     sm = pnb.SynthModel(SHAPE, SEED, device=DEV)
@@ -157,12 +165,6 @@ def test_batched_errors():
     with pytest.raises(pnb.PnbError) as e:
         sm.model.forward_batch([s0] * 65)
     assert e.value.code == -1
-    moe = wl.Shape(n_vocab=777, n_embd=256, n_head=4, n_kv_head=2, n_layer=1, n_ff=512, n_ctx=64,
-                   expert_count=4, expert_used=2, dtype=BF16)
-    mm = pnb.SynthModel(moe, 3, device=DEV)
-    with pytest.raises(pnb.PnbError) as e:
-        mm.model.forward_batch([mm.new_state(3)])
-    assert e.value.code == -5
     f32 = dataclasses.replace(SHAPE, dtype=F32)
     fm = pnb.SynthModel(f32, 3, device=DEV)
     with pytest.raises(pnb.PnbError) as e:

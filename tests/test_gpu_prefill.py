@@ -37,7 +37,7 @@ SHAPE_HD128 = wl.Shape(n_vocab=1500, n_embd=1024, n_head=8, n_kv_head=8, n_layer
                        n_ctx=300, rope_theta=5e5, rms_norm_eps=1e-5, dtype=BF16)
 # a 48-slot ring: chunks stop where the ring would wrap, then one token per step
 SHAPE_WIN = dataclasses.replace(SHAPE, sliding_window=48, n_ctx=200, n_vocab=2000, rope_theta=1e6)
-# MoE: no batched step, every token is a single-sequence step
+# MoE: chunks through the batched step's router and per-expert FFNs
 SHAPE_MOE = wl.Shape(n_vocab=777, n_embd=256, n_head=4, n_kv_head=2, n_layer=2, n_ff=512,
                      n_ctx=128, rope_theta=1e6, rms_norm_eps=1e-5, expert_count=4, expert_used=2,
                      dtype=BF16)
@@ -88,7 +88,7 @@ def gpu_prefill(sm, start, tokens):
     ("mha_hd128_70", SHAPE_HD128, 150, 70),
     ("ring_fills_then_wraps", SHAPE_WIN, 0, 70),
     ("ring_partial_chunk", SHAPE_WIN, 30, 40),
-    ("moe_per_token", SHAPE_MOE, 5, 9),
+    ("moe", SHAPE_MOE, 5, 9),
 ])
 def test_prefill_matches_oracle(name, shape, start, T):
     rng = np.random.default_rng(T + start)

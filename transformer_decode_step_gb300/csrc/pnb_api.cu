@@ -133,6 +133,7 @@ struct BatchCtx {
   unsigned *acnt = nullptr, *tile_cnt = nullptr, *am_cnt = nullptr;
   int32_t *am_idx = nullptr, *pos = nullptr, *err = nullptr;
   StepIO *pio = nullptr;                 // prefill: the I/O words of a chunk's virtual slots
+  float *gates = nullptr;                // MoE: [slot][expert] router weights (0 = not chosen)
   __nv_bfloat16 *xop_e = nullptr, *xop_o = nullptr, *xop_f = nullptr;
   float2 *rope = nullptr;
   BSlot *slots = nullptr;
@@ -777,6 +778,7 @@ int batch_setup(pnb_model *m) {
   const size_t o_gp = take((size_t)std::max<int64_t>(gpart, 1) * 4), o_tc = take((size_t)tiles * 4);
   const size_t o_amv = take((size_t)MB * m->num_sms * 4), o_ami = take((size_t)MB * m->num_sms * 4);
   const size_t o_amc = take(4), o_err = take(4), o_pio = take((size_t)MB * sizeof(StepIO));
+  const size_t o_gates = take((size_t)MB * std::max(1, c.expert_count) * 4);
   if (cudaMalloc(&b->ws, off) != cudaSuccess) {
     delete b;
     return PNB_E_NOMEM;
@@ -802,16 +804,20 @@ int batch_setup(pnb_model *m) {
   b->am_cnt = reinterpret_cast<unsigned *>(b->ws + o_amc);
   b->err = reinterpret_cast<int32_t *>(b->ws + o_err);
   b->pio = reinterpret_cast<StepIO *>(b->ws + o_pio);
+  b->gates = reinterpret_cast<float *>(b->ws + o_gates);
   bool ok = true;
   b->w_qkv.resize(L);
   b->w_o.resize(L);
-  b->w_gu.resize(L);
-  b->w_dn.resize(L);
+  const int S = m->n_sets;                // experts (1 when dense): maps per layer and expert
+  b->w_gu.resize((size_t)L * S);
+  b->w_dn.resize((size_t)L * S);
   for (int l = 0; l < L && ok; ++l) {
     ok = encode_map(&b->w_qkv[l], m->wqkv[l], m->qkv_rows, E, 128) &&
-         encode_map(&b->w_o[l], m->wo[l], E, Hd, 128) &&
-         encode_map(&b->w_gu[l], m->w_gate_up[l], 2 * (int64_t)F, E, 128) &&
-         encode_map(&b->w_dn[l], m->w_down[l], E, F, 128);
+         encode_map(&b->w_o[l], m->wo[l], E, Hd, 128);
+    for (int e = 0; ok && e < S; ++e)
+      ok = encode_map(&b->w_gu[(size_t)l * S + e], m->w_gate_up[(size_t)l * S + e], 2 * (int64_t)F,
+                      E, 128) &&
+           encode_map(&b->w_dn[(size_t)l * S + e], m->w_down[(size_t)l * S + e], E, F, 128);
   }
   ok = ok && encode_map(&b->w_lm, m->output, c.n_vocab, E, 128);
   for (int i = 0; i < 3 && ok; ++i) {
@@ -960,18 +966,44 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
     na.norm_w = m->ffn_norm[l];
     na.tr = KTrace{trace, 7 * l + 4};
     if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
-    g = bgemm_args(m, b, b->p_gu, kEpiGateUp, B, bp);
-    g.tr = KTrace{trace, 7 * l + 5};
-    g.xop = b->xop_f;
-    g.xop_ld = F;
-    if ((e = launch_bgemm(&b->w_gu[l], &b->x_e[bi], g, b->p_gu.grid, smem, st, true)) != cudaSuccess)
-      return e;
-    if (g.ksplit > 1 && (e = launch_bmerge(g, st, true)) != cudaSuccess) return e;
-    g = bgemm_args(m, b, b->p_dn, kEpiResid, B, bp);
-    g.tr = KTrace{trace, 7 * l + 6};
-    g.x = b->xb;
-    if ((e = launch_bgemm(&b->w_dn[l], &b->x_f[bi], g, b->p_dn.grid, smem, st, true)) != cudaSuccess)
-      return e;
+    // dense: one SwiGLU FFN.  MoE: the router gives every slot its experts'
+    // weights; then each expert's FFN runs over all slots (the weights are
+    // streamed once either way, and at these slot counts that is the cost)
+    // and its down projection adds weight * output to the slots that chose it
+    const int S = m->n_sets;
+    if (c.expert_count > 0) {
+      BRouterArgs ra{};
+      ra.w = static_cast<const __nv_bfloat16 *>(m->w_router[l]);
+      ra.n_expert = c.expert_count;
+      ra.k = c.expert_used;
+      ra.E = E;
+      ra.x = b->xb;
+      ra.norm_w = m->ffn_norm[l];
+      ra.eps = (float)c.rms_norm_eps;
+      ra.gates = b->gates;
+      ra.tr = KTrace{trace, 7 * l + 4};
+      if ((e = launch_brouter(ra, B, st, true)) != cudaSuccess) return e;
+    }
+    for (int ex = 0; ex < S; ++ex) {
+      g = bgemm_args(m, b, b->p_gu, kEpiGateUp, B, bp);
+      g.tr = KTrace{trace, 7 * l + 5};
+      g.xop = b->xop_f;
+      g.xop_ld = F;
+      if ((e = launch_bgemm(&b->w_gu[(size_t)l * S + ex], &b->x_e[bi], g, b->p_gu.grid, smem, st,
+                            true)) != cudaSuccess)
+        return e;
+      if (g.ksplit > 1 && (e = launch_bmerge(g, st, true)) != cudaSuccess) return e;
+      g = bgemm_args(m, b, b->p_dn, kEpiResid, B, bp);
+      g.tr = KTrace{trace, 7 * l + 6};
+      g.x = b->xb;
+      if (c.expert_count > 0) {
+        g.gate = b->gates + ex;
+        g.gate_ld = c.expert_count;
+      }
+      if ((e = launch_bgemm(&b->w_dn[(size_t)l * S + ex], &b->x_f[bi], g, b->p_dn.grid, smem, st,
+                            true)) != cudaSuccess)
+        return e;
+    }
   }
   na.emb = nullptr;
   na.tokens = nullptr;
@@ -1364,7 +1396,7 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
   if (!m || !states) return PNB_E_NULL;
   if (B < 1 || B > kMaxBatch) return PNB_E_INVAL;
   const pnb_config &c = m->cfg;
-  if (c.expert_count > 0 || c.dtype != PNB_BF16) return PNB_E_UNSUPPORTED;
+  if (c.dtype != PNB_BF16) return PNB_E_UNSUPPORTED;
   if (c.n_embd % 64 || (c.n_head * m->hd) % 64 || c.n_ff % 64) return PNB_E_UNSUPPORTED;
   for (int i = 0; i < B; ++i) {
     if (!states[i]) return PNB_E_NULL;
@@ -1569,7 +1601,7 @@ int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T
   int rc = check_device(m);
   if (rc != PNB_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const bool batched = c.expert_count == 0 && c.dtype == PNB_BF16 && c.n_embd % 64 == 0 &&
+  const bool batched = c.dtype == PNB_BF16 && c.n_embd % 64 == 0 &&
                        (c.n_head * m->hd) % 64 == 0 && c.n_ff % 64 == 0;
   if (batched && (rc = batch_setup(m)) != PNB_OK) return rc;
   const bool ring = c.sliding_window > 0 && m->cap < c.n_ctx;
@@ -1649,9 +1681,11 @@ int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
   if (B > 1) {
     // batched: norm, QKV (+ merge of its K parts), attention, o, norm, gate/up
     // (+ merge), down per layer; final norm and LM head
-    const int merges = (plan_bgemm(m->qkv_rows, m->cfg.n_embd, m->num_sms).ksplit > 1) +
-                       (plan_bgemm(2 * (int64_t)m->cfg.n_ff, m->cfg.n_embd, m->num_sms).ksplit > 1);
-    return m->cfg.n_layer * (7 + merges) + 2;
+    // (MoE: the router, then gate/up (+ merge) and down per expert)
+    const int qmerge = plan_bgemm(m->qkv_rows, m->cfg.n_embd, m->num_sms).ksplit > 1;
+    const int fmerge = plan_bgemm(2 * (int64_t)m->cfg.n_ff, m->cfg.n_embd, m->num_sms).ksplit > 1;
+    const int ffn = m->n_sets * (2 + fmerge) + (m->cfg.expert_count > 0 ? 1 : 0);
+    return m->cfg.n_layer * (5 + qmerge + ffn) + 2;
   }
   if (m->persistent) return 1;
   const int attn = m->block == PNB_FUSED_BLOCK ? 1 : (m->block == PNB_FUSED_ATTN_OPROJ ? 2 : 3);

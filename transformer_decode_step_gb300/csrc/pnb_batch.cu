@@ -232,13 +232,17 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
   if constexpr (KIND == kEpiResid) {
 #pragma unroll
     for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
-      float xv[kEpiChunk];
+      float xv[kEpiChunk], gs[kEpiChunk];
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j) {
+        const bool live = in && c0 + j < a.B;
+        gs[j] = (live && a.gate) ? a.gate[(size_t)(c0 + j) * a.gate_ld] : 1.f;
+        xv[j] = (live && gs[j] != 0.f) ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
+      }
 #pragma unroll
       for (int j = 0; j < kEpiChunk; ++j)
-        xv[j] = (in && c0 + j < a.B) ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
-#pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j)
-        if (in && c0 + j < a.B) a.x[(size_t)(c0 + j) * a.rows + grow] = xv[j] + y[c0 + j];
+        if (in && c0 + j < a.B && gs[j] != 0.f)
+          a.x[(size_t)(c0 + j) * a.rows + grow] = a.gate ? xv[j] + gs[j] * y[c0 + j] : xv[j] + y[c0 + j];
     }
   } else if constexpr (KIND == kEpiQkv) {
     const int hd = a.hd, half = hd / 2;
@@ -470,7 +474,10 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         if (grow < a.rows) {
 #pragma unroll
           for (int b = 0; b < BP; ++b)
-            if (b < a.B) atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
+            if (b < a.B) {
+              const float gs = a.gate ? a.gate[(size_t)b * a.gate_ld] : 1.f;
+              if (gs != 0.f) atomicAdd(a.x + (size_t)b * a.rows + grow, a.gate ? gs * y[b] : y[b]);
+            }
         }
       } else if constexpr (KIND == kEpiQkv || KIND == kEpiGateUp) {
         // partial tile only: k_bmerge sums the K parts and applies the epilogue
@@ -706,6 +713,72 @@ cudaError_t launch_bmerge(const BGemmArgs &a, cudaStream_t st, bool pdl) {
   if (a.kind == kEpiQkv) return cudaLaunchKernelEx(&cfg, k_bmerge<kEpiQkv>, a);
   if (a.kind == kEpiGateUp) return cudaLaunchKernelEx(&cfg, k_bmerge<kEpiGateUp>, a);
   return cudaErrorInvalidValue;
+}
+
+namespace {
+// one CTA per slot; per slot the arithmetic of the single-sequence router
+__global__ void __launch_bounds__(256, 1) k_brouter(const BRouterArgs a) {
+  extern __shared__ float rsm[];
+  float *xs = rsm;
+  float *red = xs + a.E;
+  float *r = red + 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, b = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const float *x = a.x + (size_t)b * a.E;
+  for (int i = tid; i < a.E; i += 256) xs[i] = x[i];
+  float ss = 0.f;
+  for (int i = tid; i < a.E; i += 256) ss = fmaf(xs[i], xs[i], ss);
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int k = 0; k < 8; ++k) tot += red[k];
+  const float inv = 1.0f / sqrtf(tot / (float)a.E + a.eps);
+  for (int i = tid; i < a.E; i += 256) xs[i] = xs[i] * inv * a.norm_w[i];
+  __syncthreads();
+  for (int e = warp; e < a.n_expert; e += 8) {
+    const __nv_bfloat16 *row = a.w + (int64_t)e * a.E;
+    float acc = 0.f;
+    for (int i = lane; i < a.E; i += 32) acc = fmaf(__bfloat162float(row[i]), xs[i], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) r[e] = acc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int idx[kMaxSegments];
+    float mx = -FLT_MAX;
+    for (int i = 0; i < a.k; ++i) {
+      int best = -1;
+      for (int e = 0; e < a.n_expert; ++e) {
+        bool taken = false;
+        for (int j = 0; j < i; ++j) taken |= (idx[j] == e);
+        if (!taken && (best < 0 || r[e] > r[best])) best = e;
+      }
+      idx[i] = best;
+      mx = fmaxf(mx, r[best]);
+    }
+    float z = 0.f;
+    for (int i = 0; i < a.k; ++i) z += expf(r[idx[i]] - mx);
+    float *g = a.gates + (size_t)b * a.n_expert;
+    for (int e = 0; e < a.n_expert; ++e) g[e] = 0.f;
+    for (int i = 0; i < a.k; ++i) g[idx[i]] = expf(r[idx[i]] - mx) / z;
+  }
+}
+}  // namespace
+
+cudaError_t launch_brouter(const BRouterArgs &a, int B, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = (size_t)(a.E + 32 + a.n_expert) * 4;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_brouter, a);
 }
 
 cudaError_t prepare_bgemm_kernels(int smem_bytes) {

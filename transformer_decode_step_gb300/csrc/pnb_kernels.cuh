@@ -271,6 +271,8 @@ struct BGemmArgs {
   int n_head, n_kv, hd, cap;
   __nv_bfloat16 *xop;    // kEpiGateUp: next operand [2 * bp][xop_ld]
   int xop_ld;
+  const float *gate;     // kEpiResid: per-slot scale gate[b * gate_ld] (0 = no add), or null
+  int gate_ld;
   float *logits;         // kEpiLm: [B][rows] or null
   int32_t *argmax_out;   // kEpiLm: [B] or null
   float *am_val;         // kEpiLm: [B][gridDim.x]
@@ -279,6 +281,20 @@ struct BGemmArgs {
   int32_t *err;          // batch error word
   KTrace tr;
 };
+
+// MoE router of every slot of a batched step: RMSNorm of the slot's residual,
+// the router logits, top-k (ties to the lower index) and the softmax over the
+// chosen; gates[b][e] is expert e's weight for slot b, 0 when not chosen
+struct BRouterArgs {
+  const __nv_bfloat16 *w;  // [n_expert][E]
+  int n_expert, k, E;
+  const float *x;          // [B][E] residual streams
+  const float *norm_w;
+  float eps;
+  float *gates;            // [B][n_expert]
+  KTrace tr;
+};
+cudaError_t launch_brouter(const BRouterArgs &a, int B, cudaStream_t st, bool pdl);
 
 // RMSNorm of every slot into the bf16 hi / lo operand; on the first layer
 // also the embedding gather, the step's slot table and RoPE table
