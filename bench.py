@@ -422,11 +422,15 @@ def run_ours(args, w):
 
 
 def batch_step_bytes(shape, positions) -> int:
-    """Algorithmic HBM bytes of one batched step: the weights once, each slot's
-    attended KV entries and its new entry."""
+    """Algorithmic HBM bytes of one batched step: the weights once (for MoE,
+    every expert: the batched step streams each expert once for all slots), each
+    slot's attended KV entries and its new entry."""
     es = shape.elem_bytes
-    weights = int(shape.params_read_per_token() * shape.weight_bytes_per_param) + \
-        (2 * shape.n_layer + 1) * shape.n_embd * 4
+    params = shape.params_read_per_token()
+    if shape.expert_count > 0:
+        params += (shape.expert_count - shape.expert_used) * 3 * shape.n_ff * shape.n_embd * \
+            shape.n_layer
+    weights = int(params * shape.weight_bytes_per_param) + (2 * shape.n_layer + 1) * shape.n_embd * 4
     per_pos = shape.n_layer * 2 * shape.n_kv_head * shape.head_dim * es
     kv = 0
     for p in positions:
@@ -451,7 +455,7 @@ def run_batched(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     s = w.shape
     B = args.batch or w.batch
-    starts = wl.slot_positions(w)[:B]
+    starts = wl.slot_positions(w.with_(batch=max(B, w.batch)))[:B]
     budget = s.n_ctx - max(starts)
     sm = pnb.SynthModel(s, w.seed)
     # replica r serves its own slots (seeded by slot id r * B + b)
@@ -642,7 +646,7 @@ def main():
         return run_reference(args, w)
     if args.prefill:
         return run_prefill(args, w)
-    if w.batch > 1:
+    if w.batch > 1 or args.batch > 1:
         return run_batched(args, w)
     return run_ours(args, w)
 
