@@ -192,6 +192,16 @@ def dist_setup(n_gpus: int):
     return rank, world, local
 
 
+def max_over_ranks(ms: float, dist=None, device: str = "cuda") -> float:
+    """The slowest replica's time, on every rank (the job's time is the max)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0, start_pos=None):
@@ -332,11 +342,7 @@ def run_ours(args, w):
     clocks.stop()
     if dist:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist)
     err = st.device_error()
     clk = clocks.summary()
     passes = (args.steps + budget - 1) // budget
@@ -493,11 +499,7 @@ def run_batched(args, w):
     clocks.stop()
     if dist:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist)
     err = max(st.device_error() for st in states)
     clk = clocks.summary()
     passes = (args.steps + budget - 1) // budget
