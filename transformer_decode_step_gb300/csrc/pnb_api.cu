@@ -21,6 +21,10 @@ namespace {
 constexpr int kStageTarget = 36 * 1024;   // bytes of whole rows per GEMV ring slot
 constexpr int kRingBudget = 192 * 1024;   // bytes of GEMV ring per CTA
 constexpr int kMaxSmem = 227 * 1024;
+// prefill chunks whose positions stay below this run their attention as one
+// chunk kernel (CUDA cores, each tile of the prefix read once per 16 query
+// rows); past it the per-token tensor-core attention is faster
+constexpr int kChunkAttnMaxPos = 256;
 constexpr int kMaxBatch = 64;
 #ifndef PNB_INFLIGHT_KB
 #define PNB_INFLIGHT_KB 192
@@ -833,7 +837,7 @@ int batch_setup(pnb_model *m) {
     batch_free(b);
     return PNB_E_UNSUPPORTED;
   }
-  if (prepare_bgemm_kernels(kMaxSmem) != cudaSuccess) {
+  if (prepare_bgemm_kernels(kMaxSmem) != cudaSuccess || prepare_pattn_kernels() != cudaSuccess) {
     batch_free(b);
     return PNB_E_CUDA;
   }
@@ -871,8 +875,11 @@ BGemmArgs bgemm_args(const pnb_model *m, const BatchCtx *b, const BPlan &p, int 
 // down GEMM (residual); then the final norm and the LM-head GEMM (argmax,
 // position advance).  The first kernel waits for all earlier stream work;
 // every later one uses programmatic stream serialization.
+// shared_kv: the slots are one sequence's consecutive tokens sharing its
+// cache (a prefill chunk), whose attention runs as one chunk kernel
 cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t *tokens,
-                          unsigned long long *trace, cudaStream_t st, float *logits, int32_t *argmax) {
+                          unsigned long long *trace, cudaStream_t st, float *logits, int32_t *argmax,
+                          bool shared_kv = false) {
   BatchCtx *b = m->batch;
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, Hd = c.n_head * m->hd, F = c.n_ff;
@@ -913,7 +920,23 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
     if ((e = launch_bgemm(&b->w_qkv[l], &b->x_e[bi], g, b->p_qkv.grid, smem, st, true)) != cudaSuccess)
       return e;
     if (g.ksplit > 1 && (e = launch_bmerge(g, st, true)) != cudaSuccess) return e;
-    if (m->attn_tc) {
+    if (shared_kv) {
+      PAttnArgs pa{};
+      pa.q = b->qb;
+      pa.k = reinterpret_cast<const __nv_bfloat16 *>(slots[0].kv + (size_t)(2 * l) * layer_kv);
+      pa.v = reinterpret_cast<const __nv_bfloat16 *>(slots[0].kv + (size_t)(2 * l + 1) * layer_kv);
+      pa.pos = b->pos;
+      pa.n = B;
+      pa.n_head = c.n_head;
+      pa.n_kv = c.n_kv_head;
+      pa.cap = m->cap;
+      pa.window = c.sliding_window;
+      pa.qscale = (float)(1.4426950408889634 / std::sqrt((double)m->hd));
+      pa.xop = b->xop_o;
+      pa.xop_ld = Hd;
+      pa.bp = bp;
+      if ((e = launch_pattn(m->hd, pa, st, true)) != cudaSuccess) return e;
+    } else if (m->attn_tc) {
       AttnTcArgs ta{};
       ta.q = b->qb;
       ta.layer = l;
@@ -1624,7 +1647,8 @@ int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T
       BSlot slots[kMaxBatch];
       for (int j = 0; j < n; ++j) slots[j] = BSlot{s->kv, &b->pio[j], s->maps};
       if (launch_prefill_begin(b->pio, s->io, n, st) != cudaSuccess ||
-          enqueue_batch(m, slots, n, tokens_dev + i, nullptr, st, lg, am) != cudaSuccess ||
+          enqueue_batch(m, slots, n, tokens_dev + i, nullptr, st, lg, am,
+                        s->pos + n <= kChunkAttnMaxPos) != cudaSuccess ||
           launch_prefill_end(s->io, b->pio, n, st) != cudaSuccess)
         return PNB_E_CUDA;
     }

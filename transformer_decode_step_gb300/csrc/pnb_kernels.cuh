@@ -240,6 +240,21 @@ struct AttnTcArgs {
 };
 
 cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl);
+
+// attention of a prefill chunk: n consecutive tokens of one sequence whose
+// keys and values are already in its cache; one CTA per (KV head, 16 query
+// rows) walks the attended positions once for all its rows
+struct PAttnArgs {
+  const float *q;              // [n][n_head][hd] rotated queries
+  const __nv_bfloat16 *k, *v;  // this layer's cache [n_kv][cap][hd]
+  const int32_t *pos;          // [n] the tokens' positions (ascending)
+  int n, n_head, n_kv, cap, window;
+  float qscale;                // log2(e) / sqrt(hd)
+  __nv_bfloat16 *xop;          // o-proj operand: rows j (hi) and bp + j (lo)
+  int xop_ld, bp;
+};
+cudaError_t launch_pattn(int head_dim, const PAttnArgs &a, cudaStream_t st, bool pdl);
+cudaError_t prepare_pattn_kernels();
 int attn_tc_smem(int head_dim, int nstages);
 int attn_tc_stages(int head_dim);
 int attn_tc_max_split();
