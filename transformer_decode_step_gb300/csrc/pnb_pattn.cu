@@ -8,8 +8,9 @@
 // read the cached prefix once per token; here one CTA takes a block of query
 // rows - (token, query head) pairs of one KV head - and walks the positions
 // once in tiles of kPTile:
-//   * the tile's keys and values go to shared memory (fp32, rows padded by one
-//     word so that reading one dimension of many rows is conflict-free);
+//   * the tile's keys and values go to shared memory (fp32, rows padded by
+//     four words, so that rows start in different banks and stay 16-byte
+//     aligned for vector loads);
 //   * each row's scores (q . k scaled by log2(e) / sqrt(hd)) update a running
 //     max and sum in the log2 domain, as the decode kernels do, and the
 //     row's output is rescaled and accumulated in registers;
@@ -30,7 +31,8 @@ constexpr int kPTile = 64;     // positions per tile
 template <int HD>
 __global__ void __launch_bounds__(kPThreads) k_pattn(const PAttnArgs a) {
   extern __shared__ float psm[];
-  constexpr int LD = HD + 1;                   // padded row of a K / V tile
+  constexpr int LD = HD + 4;                   // padded row of a K / V tile
+  constexpr int CPT = HD / 16;                 // output columns per thread (contiguous)
   float *qs = psm;                             // [kPRows][HD]
   float *ks = qs + kPRows * HD;                // [kPTile][LD]
   float *vs = ks + kPTile * LD;                // [kPTile][LD]
@@ -65,9 +67,9 @@ __global__ void __launch_bounds__(kPThreads) k_pattn(const PAttnArgs a) {
     qs[i] = v;
   }
   float m = -INFINITY, l = 0.f;
-  float o[HD / 16];
+  float o[CPT];
 #pragma unroll
-  for (int c = 0; c < HD / 16; ++c) o[c] = 0.f;
+  for (int c = 0; c < CPT; ++c) o[c] = 0.f;
   const __nv_bfloat16 *kb = a.k + (size_t)g * a.cap * HD;
   const __nv_bfloat16 *vb = a.v + (size_t)g * a.cap * HD;
 
@@ -90,16 +92,30 @@ __global__ void __launch_bounds__(kPThreads) k_pattn(const PAttnArgs a) {
     __syncthreads();
     // scores of this row for positions sub, sub + 16, sub + 32, sub + 48
     float s[kPTile / 16];
+    {
+      // one q vector load serves the four positions
+      const float4 *q4 = reinterpret_cast<const float4 *>(qs + row * HD);
+      float acc[kPTile / 16];
+#pragma unroll
+      for (int c = 0; c < kPTile / 16; ++c) acc[c] = 0.f;
+#pragma unroll 8
+      for (int d4 = 0; d4 < HD / 4; ++d4) {
+        const float4 qv = q4[d4];
+#pragma unroll
+        for (int c = 0; c < kPTile / 16; ++c) {
+          const float4 kv = reinterpret_cast<const float4 *>(ks + (sub + 16 * c) * LD)[d4];
+          acc[c] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, acc[c]))));
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kPTile / 16; ++c) s[c] = acc[c];
+    }
     float tmax = -INFINITY;
 #pragma unroll
     for (int c = 0; c < kPTile / 16; ++c) {
       const int p = sub + 16 * c, pos = t0 + p;
-      float acc = 0.f;
-      const float *qr = qs + row * HD, *kr = ks + p * LD;
-#pragma unroll 16
-      for (int d = 0; d < HD; ++d) acc = fmaf(qr[d], kr[d], acc);
       const bool ok = live && p < nt && pos >= lo_j && pos <= pj;
-      s[c] = ok ? acc : -INFINITY;
+      s[c] = ok ? s[c] : -INFINITY;
       tmax = fmaxf(tmax, s[c]);
     }
     // the row's 16 threads are one half-warp
@@ -119,26 +135,37 @@ __global__ void __launch_bounds__(kPThreads) k_pattn(const PAttnArgs a) {
     l = l * f + tsum;
     m = mn;
     __syncwarp();
-    // output columns sub, sub + 16, ... of this row
+    // output columns CPT * sub .. CPT * sub + CPT - 1 of this row
 #pragma unroll
-    for (int c = 0; c < HD / 16; ++c) o[c] *= f;
+    for (int c = 0; c < CPT; ++c) o[c] *= f;
     const float *pr = ps + row * kPTile;
     for (int p = 0; p < nt; ++p) {
       const float w = pr[p];
-      const float *vr = vs + p * LD + sub;
+      const float *vr = vs + p * LD + CPT * sub;
+      if constexpr (CPT % 4 == 0) {
 #pragma unroll
-      for (int c = 0; c < HD / 16; ++c) o[c] = fmaf(w, vr[16 * c], o[c]);
+        for (int c = 0; c < CPT; c += 4) {
+          const float4 vv = *reinterpret_cast<const float4 *>(vr + c);
+          o[c] = fmaf(w, vv.x, o[c]);
+          o[c + 1] = fmaf(w, vv.y, o[c + 1]);
+          o[c + 2] = fmaf(w, vv.z, o[c + 2]);
+          o[c + 3] = fmaf(w, vv.w, o[c + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) o[c] = fmaf(w, vr[c], o[c]);
+      }
     }
   }
   if (!live) return;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const int h = g * G + hh;
 #pragma unroll
-  for (int c = 0; c < HD / 16; ++c) {
+  for (int c = 0; c < CPT; ++c) {
     const float v = o[c] * inv;
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
     const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-    const size_t col = (size_t)h * HD + sub + 16 * c;
+    const size_t col = (size_t)h * HD + CPT * sub + c;
     a.xop[(size_t)j * a.xop_ld + col] = hi;
     a.xop[(size_t)(a.bp + j) * a.xop_ld + col] = lo;
   }
@@ -146,7 +173,7 @@ __global__ void __launch_bounds__(kPThreads) k_pattn(const PAttnArgs a) {
 
 template <int HD>
 constexpr int pattn_smem() {
-  return (kPRows * HD + 2 * kPTile * (HD + 1) + kPRows * kPTile) * 4;
+  return (kPRows * HD + 2 * kPTile * (HD + 4) + kPRows * kPTile) * 4;
 }
 
 template <int HD>
