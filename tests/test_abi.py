@@ -62,7 +62,7 @@ def _create(cfg, w):
     dict(n_ff=690),                    # not a multiple of 8
     dict(n_vocab=0), dict(n_layer=0), dict(n_ctx=0),
     dict(sliding_window=-1), dict(rope_theta=0.0), dict(rms_norm_eps=-1.0),
-    dict(dtype=7),
+    dict(dtype=7), dict(rope_neox=2),
     dict(expert_count=8, expert_used=0), dict(expert_count=8, expert_used=9),
     dict(expert_count=65, expert_used=2), dict(expert_count=16, expert_used=9),
 ])
@@ -88,11 +88,30 @@ def test_null_and_misaligned_pointers():
     assert _create(_cfg(), w) == -2
     w, keep = _weights()                   # MoE without router pointers
     assert _create(_cfg(expert_count=4, expert_used=2), w) == -2
+    w, keep = _weights()                   # a bias array with a NULL layer entry
+    bias = (ctypes.c_void_p * 2)(4096, None)
+    w.bqkv = ctypes.cast(bias, ctypes.c_void_p)
+    assert _create(_cfg(), w) == -2
+    bias = (ctypes.c_void_p * 2)(4096, 4100)   # and one not 16-byte aligned
+    w.bqkv = ctypes.cast(bias, ctypes.c_void_p)
+    assert _create(_cfg(), w) == -3
 
 
 def test_null_handles():
     import transformer_decode_step_gb300 as pnb
     assert pnb.pnb_forward(None, None, 0, None, None, None) == -2
+    # sampler, draw counter and the begin / poll seam
+    p = pnb.sampling_params(0.8, 1.1, 40, 0.95, 7)
+    assert pnb.pnb_sample(None, None, None, ctypes.byref(p), None, 0, None, None) == -2
+    assert pnb.pnb_sample_batch(None, None, 1, None, None, None, None, None, None) == -2
+    assert pnb.pnb_state_set_draw(None, 3, None) == -2
+    assert pnb.pnb_forward_begin(None, None, 0, None, None) == -2
+    assert pnb.pnb_sample_begin(None, None, None, ctypes.byref(p), None, 0, None) == -2
+    assert pnb.pnb_forward_poll(None, None, None) == -2
+    assert pnb.pnb_state_stream(None, None) == -2
+    assert pnb.pnb_prefill(None, None, None, 4, None, None, None) == -2
+    assert pnb.pnb_strerror(-12).startswith(b"a begun step")
+    assert p.temperature == pytest.approx(0.8) and p.top_k == 40 and p.seed == 7
     assert pnb.pnb_state_new(None, None, 0, None) == -2
     assert pnb.pnb_state_kv_bytes(None) == 0
     assert pnb.pnb_strerror(-4) == b"position reached n_ctx"
