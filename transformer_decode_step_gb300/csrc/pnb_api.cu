@@ -1016,7 +1016,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
                             true)) != cudaSuccess)
         return e;
       if (g.ksplit > 1 && (e = launch_bmerge(g, st, true)) != cudaSuccess) return e;
-      g = bgemm_args(m, b, b->p_dn, kEpiResid, B, bp);
+      g = bgemm_args(m, b, b->p_dn, c.expert_count > 0 ? kEpiResidGate : kEpiResid, B, bp);
       g.tr = KTrace{trace, 7 * l + 6};
       g.x = b->xb;
       if (c.expert_count > 0) {

@@ -232,17 +232,27 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
   if constexpr (KIND == kEpiResid) {
 #pragma unroll
     for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
+      float xv[kEpiChunk];
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j)
+        xv[j] = (in && c0 + j < a.B) ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
+#pragma unroll
+      for (int j = 0; j < kEpiChunk; ++j)
+        if (in && c0 + j < a.B) a.x[(size_t)(c0 + j) * a.rows + grow] = xv[j] + y[c0 + j];
+    }
+  } else if constexpr (KIND == kEpiResidGate) {
+#pragma unroll
+    for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
       float xv[kEpiChunk], gs[kEpiChunk];
 #pragma unroll
       for (int j = 0; j < kEpiChunk; ++j) {
         const bool live = in && c0 + j < a.B;
-        gs[j] = (live && a.gate) ? a.gate[(size_t)(c0 + j) * a.gate_ld] : 1.f;
-        xv[j] = (live && gs[j] != 0.f) ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
+        gs[j] = live ? a.gate[(size_t)(c0 + j) * a.gate_ld] : 0.f;
+        xv[j] = gs[j] != 0.f ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
       }
 #pragma unroll
       for (int j = 0; j < kEpiChunk; ++j)
-        if (in && c0 + j < a.B && gs[j] != 0.f)
-          a.x[(size_t)(c0 + j) * a.rows + grow] = a.gate ? xv[j] + gs[j] * y[c0 + j] : xv[j] + y[c0 + j];
+        if (gs[j] != 0.f) a.x[(size_t)(c0 + j) * a.rows + grow] = xv[j] + gs[j] * y[c0 + j];
     }
   } else if constexpr (KIND == kEpiQkv) {
     const int hd = a.hd, half = hd / 2;
@@ -474,9 +484,16 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
         if (grow < a.rows) {
 #pragma unroll
           for (int b = 0; b < BP; ++b)
+            if (b < a.B) atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
+        }
+      } else if constexpr (KIND == kEpiResidGate) {
+        const int grow = tile * 128 + row;
+        if (grow < a.rows) {
+#pragma unroll
+          for (int b = 0; b < BP; ++b)
             if (b < a.B) {
-              const float gs = a.gate ? a.gate[(size_t)b * a.gate_ld] : 1.f;
-              if (gs != 0.f) atomicAdd(a.x + (size_t)b * a.rows + grow, a.gate ? gs * y[b] : y[b]);
+              const float gs = a.gate[(size_t)b * a.gate_ld];
+              if (gs != 0.f) atomicAdd(a.x + (size_t)b * a.rows + grow, gs * y[b]);
             }
         }
       } else if constexpr (KIND == kEpiQkv || KIND == kEpiGateUp) {
@@ -666,6 +683,7 @@ cudaError_t launch_bp(const void *tw, const void *tx, const BGemmArgs &a, int gr
     case kEpiResid: return launch_k<BP, kEpiResid>(tw, tx, a, grid, smem, st, pdl);
     case kEpiGateUp: return launch_k<BP, kEpiGateUp>(tw, tx, a, grid, smem, st, pdl);
     case kEpiLm: return launch_k<BP, kEpiLm>(tw, tx, a, grid, smem, st, pdl);
+    case kEpiResidGate: return launch_k<BP, kEpiResidGate>(tw, tx, a, grid, smem, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -681,6 +699,9 @@ cudaError_t prepare_bp(int smem) {
     return e;
   if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiResidGate>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(k_bgemm<BP, kEpiLm>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }

@@ -261,7 +261,9 @@ int attn_tc_max_split();
 cudaError_t prepare_attn_tc_kernels();
 
 // Epilogues of the batched tensor-core GEMM
-enum BEpi { kEpiQkv = 0, kEpiResid = 1, kEpiGateUp = 2, kEpiLm = 3 };
+// kEpiResidGate: the residual add scaled per slot by gate[b * gate_ld] (0 =
+// no add), for the MoE down projections of the batched step
+enum BEpi { kEpiQkv = 0, kEpiResid = 1, kEpiGateUp = 2, kEpiLm = 3, kEpiResidGate = 4 };
 
 // Y[b][r] = sum_k W[r][k] * X[b][k] for the B slots of a batched step, on
 // tcgen05 (tiles of 128 weight rows, slots as the MMA's N dimension with the
@@ -286,7 +288,7 @@ struct BGemmArgs {
   int n_head, n_kv, hd, cap;
   __nv_bfloat16 *xop;    // kEpiGateUp: next operand [2 * bp][xop_ld]
   int xop_ld;
-  const float *gate;     // kEpiResid: per-slot scale gate[b * gate_ld] (0 = no add), or null
+  const float *gate;     // kEpiResidGate: per-slot scale gate[b * gate_ld] (0 = no add)
   int gate_ld;
   float *logits;         // kEpiLm: [B][rows] or null
   int32_t *argmax_out;   // kEpiLm: [B] or null
