@@ -12,7 +12,8 @@ and KV cache are far larger than L2, so nothing stays cached between steps.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
-only reference this project has) on the same workload, per-layer units.
+only reference this project has) on the same workload: whole decode steps on
+the host cores, as many as --steps asks or as fit in 150 s.
 """
 from __future__ import annotations
 
@@ -204,41 +205,47 @@ def max_over_ranks(ms: float, dist=None, device: str = "cuda") -> float:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_units(w, seconds_budget: float, max_units: int, warmup: int = 0, start_pos=None):
-    """Time the oracle on the workload in per-token units (layer 0 with the
-    embedding, layers 1..L-1, final norm + LM head), rotating through them.
-    Returns (tokens/s, units run, seconds, threads)."""
+def oracle_steps(w, seconds_budget: float, max_steps: int, warmup: int = 0, start_pos=None,
+                 slot: int = 0):
+    """Time whole greedy decode steps of the oracle (embedding, every layer, final
+    norm, LM head and argmax), each step feeding the previous step's argmax from
+    the workload's start token and pre-filled cache, rewinding to the start
+    position when the cache is full (as the GPU arm does).  Stops after
+    max_steps or once seconds_budget has passed (at least one step).
+    Returns (tokens/s, steps timed, seconds, OpenMP threads used)."""
     import oracle
     import synth.workloads as wl
 
+    P = w.prefill if start_pos is None else start_pos
     m = oracle.Model(w.shape, seed=w.seed)
     st = m.new_state()
-    lo, hi = wl.kv_prefill_range(w.shape, w.prefill if start_pos is None else start_pos)
-    st.prefill_synth(w.seed, 0, lo, hi)
-    tok = wl.prompt_tokens(w)[0]
-    L = w.shape.n_layer
-    x = None
+    lo, hi = wl.kv_prefill_range(w.shape, P)
+    st.prefill_synth(w.seed, slot, lo, hi)
+    tok0 = wl.prompt_tokens(w, slot)[0]
+    tok = tok0
 
-    def run_unit(u):
-        nonlocal x
-        if u == 0:
-            x = st.embed(tok)
-        if u < L:
-            st.layer(u, x)
-        else:
-            st.head(x, want_logits=False)
+    def step():
+        nonlocal tok
+        if st.pos >= w.shape.n_ctx:
+            st.pos = P
+            tok = tok0
+        _, tok = st.forward(tok, want_logits=False)
 
-    for u in range(warmup):
-        run_unit(u % (L + 1))
+    for _ in range(warmup):
+        step()
     t0 = time.perf_counter()
     n = 0
-    while n < max_units:
-        run_unit(n % (L + 1))
+    while n < max(1, max_steps):
+        step()
         n += 1
-        if time.perf_counter() - t0 > seconds_budget and n % (L + 1) == 0:
+        if time.perf_counter() - t0 > seconds_budget:
             break
     dt = time.perf_counter() - t0
-    return (n / (L + 1)) / dt, n, dt, oracle.max_threads()
+    return n / dt, n, dt, oracle.max_threads()
+
+
+def host_cpus() -> int:
+    return os.cpu_count() or 0
 
 
 # ------------------------------------------------------------------ main arms
@@ -252,30 +259,84 @@ def workload_config(w, extra=None, batch=None):
                        + (f" experts{s.expert_count}top{s.expert_used}" if s.expert_count else "")
                        + f", KV pre-filled to {w.prefill}, greedy decode of {w.steps} tokens, batch {batch}",
            "batch": batch, "weights_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype],
-           "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)"}
+           "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)"
+                 if s.params_read_per_token() * s.weight_bytes_per_param > 129e6 else
+                 "weights fit in L2 and stay resident between steps, as in a real decode loop "
+                 "(no flush; this workload is latency-bound)"}
     if extra:
         cfg.update(extra)
     return cfg
 
 
+SAMPLED = ("sampled on the GPU: temperature 0.8, top-k 40, top-p 0.95, penalty 1.1 over 64 "
+           "tokens")
+
+
+def is_batched(args, w) -> bool:
+    return w.batch > 1 or args.batch > 1
+
+
+def batched_starts(w, B: int):
+    import synth.workloads as wl
+    return wl.slot_positions(w.with_(batch=max(B, w.batch)))[:B]
+
+
+def prefill_len(args, w) -> int:
+    return min(args.prefill, w.shape.n_ctx)
+
+
+def arm_config(args, w, world: int) -> dict:
+    """The workload description both arms print (so the two lines name the same
+    configuration)."""
+    par = {"parallelism": f"replicas x{world}"}
+    if args.prefill:
+        T = prefill_len(args, w)
+        return workload_config(w, {"prefill_tokens": T, "chunks_of_64": -(-T // 64), **par})
+    if is_batched(args, w):
+        B = args.batch or w.batch
+        starts = batched_starts(w, B)
+        return workload_config(w, {**par, "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"},
+                               batch=B)
+    P = w.prefill
+    return workload_config(w, {**par, "positions": f"{P}..{w.shape.n_ctx - 1}",
+                               "next_token": SAMPLED if args.sample else "greedy (argmax)"})
+
+
 def run_reference(args, w):
+    """The reference arm: the CPU oracle, as it stands, on the host cores, timing
+    whole decode steps of the same workload (rank 0 only under torchrun).  A
+    batched workload's step is one slot's token (the oracle runs slots one at a
+    time); a prefill's step is one prompt token fed from position 0."""
     rank, world, local = dist_setup(args.gpus)
     if rank != 0:
         return 0
-    budget = 200.0
     import synth.workloads as wl
-    start = wl.slot_positions(w)[0] if w.batch > 1 else None
-    tps, n, dt, threads = oracle_units(w, budget, max_units=args.steps, warmup=min(args.warmup, 2),
+    batched = is_batched(args, w) and not args.prefill
+    if args.prefill:
+        w_ref = w.with_(prefill=0, slot_pos_range=None)
+        start = 0
+    else:
+        w_ref = w
+        start = batched_starts(w, args.batch or w.batch)[0] if batched else None
+    warm = min(max(args.warmup, 0), 3)
+    tps, n, dt, threads = oracle_steps(w_ref, 150.0, max_steps=args.steps, warmup=warm,
                                        start_pos=start)
-    L = w.shape.n_layer
-    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 / tps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(w, batch=args.batch),
-            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n} per-token units ({L} layers + LM head, rotated) of the "
-                                       f"workload's first decode step, {dt:.1f} s"},
+    what = ("tokens of slot 0 from its seeded start position (the oracle runs slots one at a time)"
+            if batched else "tokens fed one per forward from position 0 (a prompt token's cost)" if args.prefill
+            else "greedy decode steps from the pre-filled cache")
+    line = {"impl": "reference", "metric": "prefill_tokens_per_s" if args.prefill else METRIC,
+            "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": n,
+            "steps_requested": args.steps, "warmup": warm, "ms_per_step": 1000.0 * dt / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generated weights and KV cache)",
+            "config": arm_config(args, w, args.gpus),
+            "step_is": "one whole token through the oracle: embedding, every layer, final norm, "
+                        "LM head and argmax",
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads,
+                             "host_cpus": host_cpus(), "kind": "oracle",
+                             "sample": f"{n} whole {what}, {dt:.1f} s on {threads} OpenMP "
+                                       f"threads (weights regenerated from the seed inside "
+                                       f"each step)"},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -389,22 +450,19 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, n, dt, threads = oracle_units(w, 15.0, max_units=10 * (L + 1))
-        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} per-token units ({L} layers + LM head) = {n / (L + 1):.2f} decode "
-                         f"steps of the workload at position {P}, {dt:.1f} s"}
+        tps, n, dt, threads = oracle_steps(w, 15.0, max_steps=16)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "host_cpus": host_cpus(),
+               "kind": "oracle",
+               "sample": f"{n} whole greedy decode steps of the workload from position {P} "
+                         f"(embedding, {L} layers, LM head), {dt:.1f} s on {threads} OpenMP "
+                         f"threads"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype], "data": "synthetic (seeded generated weights and KV cache)",
-                "config": workload_config(w, {"parallelism": f"replicas x{world}",
-                                              "positions": f"{P}..{P + budget - 1}",
-                                              "next_token": "sampled on the GPU: temperature 0.8, "
-                                                            "top-k 40, top-p 0.95, penalty 1.1 "
-                                                            "over 64 tokens" if args.sample
-                                                            else "greedy (argmax)"}),
+                "config": arm_config(args, w, world),
                 "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"],
                 "bytes_per_step": mean_bytes,
@@ -461,7 +519,7 @@ def run_batched(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     s = w.shape
     B = args.batch or w.batch
-    starts = wl.slot_positions(w.with_(batch=max(B, w.batch)))[:B]
+    starts = batched_starts(w, B)
     budget = s.n_ctx - max(starts)
     sm = pnb.SynthModel(s, w.seed)
     # replica r serves its own slots (seeded by slot id r * B + b)
@@ -533,18 +591,18 @@ def run_batched(args, w):
     cpu = None
     L = s.n_layer
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, n, dt, threads = oracle_units(w, 15.0, max_units=10 * (L + 1), start_pos=starts[0])
-        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} per-token units ({L} layers + LM head) = {n / (L + 1):.2f} decode "
-                         f"steps of slot 0 at position {starts[0]} (the oracle runs slots one "
-                         f"at a time), {dt:.1f} s"}
+        tps, n, dt, threads = oracle_steps(w, 15.0, max_steps=16, start_pos=starts[0])
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "host_cpus": host_cpus(),
+               "kind": "oracle",
+               "sample": f"{n} whole greedy decode steps of slot 0 from position {starts[0]} "
+                         f"(the oracle runs slots one at a time), {dt:.1f} s on {threads} "
+                         f"OpenMP threads"}
     if rank == 0:
         line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded generated weights and KV cache)",
-                "config": workload_config(w, {"parallelism": f"replicas x{world}",
-                                              "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"}, batch=B),
+                "config": arm_config(args, w, world),
                 "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"], "bytes_per_step": mean_bytes,
                 "roofline": {"bound": "hbm", "kernel": "whole batched step (weights once + every slot's KV)",
@@ -579,7 +637,7 @@ def run_prefill(args, w):
         return 0
     torch.cuda.set_device(local)
     s = w.shape
-    T = min(args.prefill, s.n_ctx)
+    T = prefill_len(args, w)
     sm = pnb.SynthModel(s, w.seed)
     st = sm.new_state()
     rng = __import__("numpy").random.default_rng(w.seed)
@@ -617,13 +675,11 @@ def run_prefill(args, w):
         stream.synchronize()
     e2e = T * args.steps / (time.perf_counter() - t0)
     tps = T * args.steps / (ms / 1000.0)
-    chunks = -(-T // 64)
     line = {"metric": "prefill_tokens_per_s", "value": tps, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded generated weights, seeded prompt)",
-            "config": workload_config(w, {"prefill_tokens": T, "chunks_of_64": chunks,
-                                          "parallelism": "replicas x1"}),
+            "config": arm_config(args, w, 1),
             "weight_bytes_per_chunk": int(s.params_read_per_token() * s.weight_bytes_per_param),
             "clocks": clocks.summary(), "device_error": err,
             "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * T,

@@ -424,12 +424,16 @@ int pnb_state_activations(const pnb_state *s, pnb_activations *out);
    any stream capture.  Every call uses the same array and leaves its
    contents behind: each call clears the counters and I/O word it needs, and
    calls whose work overlaps on the GPU (concurrent streams) race on the
-   array and must be serialised by the caller.  A bounded wait that expires
-   inside the kernel is not reported by this entry point. */
+   array and must be serialised by the caller.
+     err_dev optional device int32 (NULL: not written).  After the kernel, in
+             stream order, it receives the call's device error bits
+             (PNB_DEV_ERR_*, 0 = none): PNB_DEV_ERR_TIMEOUT means a bounded
+             wait inside the kernel gave up and out_dev is not valid.  It is
+             copied out of the static array before the next call clears it. */
 int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const void *v_dev,
                                 int32_t dtype, int32_t n_head, int32_t n_kv_head, int32_t head_dim,
                                 int32_t cap, int32_t window, int32_t pos, float *out_dev,
-                                pnb_stream stream);
+                                int32_t *err_dev, pnb_stream stream);
 
 /* Diagnostics: have the persistent kernel record globaltimer stamps (ns) into
    trace_dev, laid out [CTA][phase][6] with CTA < number of SMs, phase < 5 *

@@ -94,7 +94,7 @@ _SIGS = {
     "pnb_step_kernel": (_i32, [_p, _p, _i32, _i32, _p]),
     "pnb_state_set_trace": (_i32, [_p, _p, _sz]),
     "pnb_attention_decode_static": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-                                           _p, _p]),
+                                           _p, _p, _p]),
     "pnb_strerror": (ctypes.c_char_p, [_i32]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -107,11 +107,13 @@ EXPORTED = tuple(_SIGS)
 
 
 def attention_decode_static(q, k, v, dtype: int, n_head: int, n_kv_head: int, head_dim: int,
-                            cap: int, window: int, pos: int, out, stream=None):
+                            cap: int, window: int, pos: int, out, err=None, stream=None):
     """One layer's decode attention with no device allocation
-    (pnb_attention_decode_static): the library's static scratch array is used."""
+    (pnb_attention_decode_static): the library's static scratch array is used.
+    ``err`` (optional device int32) receives the call's device error bits."""
     check(pnb_attention_decode_static(_ptr(q), _ptr(k), _ptr(v), dtype, n_head, n_kv_head,
-                                      head_dim, cap, window, pos, _ptr(out), _stream(stream)),
+                                      head_dim, cap, window, pos, _ptr(out), _ptr(err),
+                                      _stream(stream)),
           "pnb_attention_decode_static")
 
 

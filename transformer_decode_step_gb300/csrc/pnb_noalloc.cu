@@ -55,9 +55,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const void *v_dev,
                                            int32_t dtype, int32_t n_head, int32_t n_kv_head,
                                            int32_t head_dim, int32_t cap, int32_t window,
-                                           int32_t pos, float *out_dev, pnb_stream stream) {
+                                           int32_t pos, float *out_dev, int32_t *err_dev,
+                                           pnb_stream stream) {
   if (!q_dev || !k_dev || !v_dev || !out_dev) return PNB_E_NULL;
-  if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev))
+  if (!aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) || !aligned16(out_dev) ||
+      (reinterpret_cast<uintptr_t>(err_dev) & 3u))
     return PNB_E_ALIGN;
   if (dtype != PNB_F32 && dtype != PNB_BF16) return PNB_E_INVAL;
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return PNB_E_UNSUPPORTED;
@@ -108,5 +110,10 @@ extern "C" int pnb_attention_decode_static(const float *q_dev, const void *k_dev
   a.nstages = ag.nstages;
   a.io = io;
   if (launch_attn(dtype, head_dim, a, ag, st, false) != cudaSuccess) return PNB_E_CUDA;
+  // the kernel's error bits leave the shared array before another call can
+  // clear them (a device-to-device copy: no allocation)
+  if (err_dev && cudaMemcpyAsync(err_dev, &io->error, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                 st) != cudaSuccess)
+    return PNB_E_CUDA;
   return PNB_OK;
 }
