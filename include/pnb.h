@@ -70,10 +70,7 @@ enum {
 /* device-side error bits (pnb_state_check) */
 enum {
   PNB_DEV_ERR_TOKEN = 1,   /* a token from device memory was out of range; id 0 was used */
-  PNB_DEV_ERR_TIMEOUT = 2, /* a bounded wait inside a kernel expired; results are invalid */
-  PNB_DEV_ERR_RANGE = 4    /* one head's output-projection value reached 2^30 in magnitude
-                              (the fused attention block's fixed-point accumulator range);
-                              it was clamped and results are invalid */
+  PNB_DEV_ERR_TIMEOUT = 2  /* a bounded wait inside a kernel expired; results are invalid */
 };
 
 /* Model dimensions: the config fields of the pages ("Engine Architecture",
@@ -120,8 +117,7 @@ typedef struct {
      w_down[l*S + e]     [E][n_ff]                             dtype
      bqkv[l]             [(n_head + 2 n_kv_head) hd]           fp32   q, k, v biases in wqkv's row order
                                                                       (Qwen2; NULL array: no biases)
-   A model with biases runs the per-phase and batched kernels (not the
-   persistent kernel or the fused attention block: PNB_E_UNSUPPORTED). */
+   A model with biases runs the single-sequence and batched steps alike. */
 typedef struct {
   const void *tok_embd;
   const float *out_norm;
@@ -147,9 +143,8 @@ typedef struct pnb_state pnb_state;
    n_ff multiples of 8, 0 < expert_used <= expert_count <= 64 when MoE,
    pointer non-NULL and 16-byte aligned.  PNB_Q8_0 needs n_embd and n_ff
    multiples of 256 (whole 16-byte vectors per row) and a dense FFN
-   (PNB_E_UNSUPPORTED otherwise); its models run the per-phase kernels only
-   (no persistent, fused-attention or batched form; pnb_prefill goes one
-   token per step).  *out is set on success. */
+   (PNB_E_UNSUPPORTED otherwise); its models run the single-sequence step
+   only (no batched form; pnb_prefill goes one token per step).  *out is set on success. */
 int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **out);
 void pnb_model_free(pnb_model *m);
 
@@ -230,15 +225,6 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
    the kernels one by one (0).  Results are identical either way. */
 int pnb_model_set_graphs(pnb_model *m, int enable);
 
-/* Run each single-sequence step as one persistent cooperative kernel
-   (enable = 1; possible when head_dim is in {32, 64, 128} and n_head /
-   n_kv_head in {1, 2, 4, 8} with (n_head / n_kv_head) * head_dim <= 512), or
-   as one kernel per phase (enable = 0, the default).  Results agree to fp32
-   rounding.  Returns PNB_E_UNSUPPORTED when enabling is not possible for this
-   model. */
-int pnb_model_set_persistent(pnb_model *m, int enable);
-int pnb_model_is_persistent(const pnb_model *m);
-
 /* Decode attention on tcgen05 tensor cores (enable = 1, the default where
    the model allows it: bf16 weights and KV, head_dim 64 or 128, n_head /
    n_kv_head in {1, 2, 4, 8}, and with a sliding window a cache of a multiple
@@ -249,24 +235,6 @@ int pnb_model_is_persistent(const pnb_model *m);
    Returns PNB_E_UNSUPPORTED when enabling is not possible for this model. */
 int pnb_model_set_tensor_attention(pnb_model *m, int enable);
 int pnb_model_is_tensor_attention(const pnb_model *m);
-
-/* How the attention half of each layer of the single-sequence step runs.
-   PNB_FUSED_OFF (the default): three kernels - QKV (with RMSNorm, RoPE and
-   the KV append), attention, output projection.  PNB_FUSED_ATTN_OPROJ: the
-   QKV kernel, then attention and the output projection as one kernel.
-   PNB_FUSED_BLOCK: all of it as one kernel.  The fused kernel runs one
-   thread-block cluster of up to 8 CTAs per query head (so n_head * cluster
-   size SMs); the heads' output-projection values meet in a 64-bit
-   fixed-point accumulator (units of 2^-32, |value| < 2^30 per head) that the
-   following kernels fold into the residual, so the step stays bitwise
-   reproducible.  Results agree with the default to fp32 rounding.  Possible
-   when head_dim is in {32, 64, 128}, n_head <= the SM count, n_embd is
-   divisible by the cluster size and an output-projection tile has at least
-   8 rows; else setting a fused mode returns PNB_E_UNSUPPORTED.  An unknown
-   mode returns PNB_E_INVAL. */
-enum { PNB_FUSED_OFF = 0, PNB_FUSED_ATTN_OPROJ = 1, PNB_FUSED_BLOCK = 2 };
-int pnb_model_set_fused_attention(pnb_model *m, int mode);
-int pnb_model_fused_attention(const pnb_model *m);
 
 /* Prefill: feed T >= 1 prompt tokens (tokens_dev [T], device int32) to a
    state, advancing its position by T, with every token's logits and greedy
@@ -370,23 +338,14 @@ enum {
   PNB_KERNEL_ROUTER = 3,  /* MoE only: router logits, top-k, softmax */
   PNB_KERNEL_GATE_UP = 4, /* RMSNorm, gate/up (chosen experts), SwiGLU */
   PNB_KERNEL_DOWN = 5,    /* down projection(s) + residual */
-  PNB_KERNEL_LM_HEAD = 6, /* final RMSNorm, LM head, argmax, pos += 1 */
-  PNB_KERNEL_ATTN_BLOCK = 7 /* fused attention block into the attention-output accumulator:
-                               QKV + attention + output projection, or, in mode
-                               PNB_FUSED_ATTN_OPROJ, attention + output projection after
-                               the QKV kernel (replaces kinds 0-2 / 1-2 in a fused step) */
+  PNB_KERNEL_LM_HEAD = 6  /* final RMSNorm, LM head, argmax, pos += 1 */
 };
 
 /* Launch one kernel of the single-sequence step for `layer` in isolation
    (stream-ordered, no overlap with the previous kernel), reading and writing
    the state's workspace and KV cache exactly as inside a step: meant for
    per-kernel timing and checks.  The host position is not changed (the LM
-   head kernel still advances the device position, as in a step).  The
-   fused attention block adds into the state's attention-output accumulator,
-   which the next router / gate-up kernel reads and the down-projection kernel
-   folds into the residual while the model is in a fused mode.
-   PNB_KERNEL_ATTN_BLOCK returns PNB_E_UNSUPPORTED unless the model is in a
-   fused mode. */
+   head kernel still advances the device position, as in a step). */
 int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb_stream stream);
 
 /* Device pointers of a state's fp32 activation buffers after its last step
@@ -435,29 +394,19 @@ int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const voi
                                 int32_t cap, int32_t window, int32_t pos, float *out_dev,
                                 int32_t *err_dev, pnb_stream stream);
 
-/* Diagnostics: have the persistent kernel record globaltimer stamps (ns) into
-   trace_dev, laid out [CTA][phase][6] with CTA < number of SMs, phase < 5 *
-   n_layer + 1 (per layer: QKV, attention, output projection, gate/up, down;
-   then the LM head) and slots 0 = compute finished the phase, 1 = passed the
-   phase's grid barrier (for the LM-head phase: kernel start), 2 = ns the first compute warp spent on staged GEMV slots after their data
-   arrived, 3 = ns it spent waiting for ring data (accumulated: zero the buffer
-   first), 4 / 5 = when its last GEMV slot loop of the phase started / ended.
-   In per-phase mode the same buffer is laid out [launch][256][8]: launch =
-   6 * layer + kernel kind (PNB_KERNEL_*), 6 * n_layer for the LM head; the
-   CTA's linear index (< 256) picks the row; slots 0 = CTA start, 1 = compute
-   warps past griddepcontrol.wait, 2 = activation prologue done, 3 = first
-   ring slot arrived, 4 = all slots consumed, 5 = epilogue done, 6 / 7 = the
-   producer reached / passed griddepcontrol.wait; the fused attention block
-   records as launch 6 * layer (6 * layer + 1 after the QKV kernel in mode
-   PNB_FUSED_ATTN_OPROJ) with 4 = the head's q / k / v exchanged,
-   5 = the cluster's softmax partials exchanged, 6 = its producer reached
-   griddepcontrol.wait and 7 = the CTA's end.  A batched step records into
+/* Diagnostics: have the step's kernels record globaltimer stamps (ns) into
+   trace_dev, laid out [launch][256][8]: launch = 6 * layer + kernel kind
+   (PNB_KERNEL_*), 6 * n_layer for the LM head; the CTA's linear index
+   (< 256) picks the row; slots 0 = CTA start, 1 = compute warps past
+   griddepcontrol.wait, 2 = activation prologue done, 3 = first ring slot
+   arrived, 4 = all slots consumed, 5 = epilogue done, 6 / 7 = the producer
+   reached / passed griddepcontrol.wait.  A batched step records into
    its first slot's buffer with launch = 7 * layer + (0 norm, 1 QKV,
    2 attention, 3 o-proj, 4 norm, 5 gate/up, 6 down), 7 * n_layer (+1) for the
    final norm (LM head); its GEMM slots are 0 start, 1 / 2 first / last MMA,
    3 first accumulator read, 4 epilogue done, 5 end, 6 / 7 producer done /
    past griddepcontrol.wait.  NULL turns it off.  bytes must cover
-   (7 * n_layer + 2) * 256 * 8 words and the persistent layout. */
+   (7 * n_layer + 2) * 256 * 8 words. */
 int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes);
 
 const char *pnb_strerror(int code);

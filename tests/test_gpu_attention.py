@@ -66,7 +66,6 @@ def close(ref, got, tol, what):
 def test_tensor_attention_matches_oracle_and_cuda_core_kernel(name):
     shape, start = SHAPES[name]
     sm = pnb.SynthModel(shape, SEED, device=DEV)
-    sm.model.set_fused_attention(pnb.PNB_FUSED_OFF)   # the attention kernels run unfused only
     assert sm.model.tensor_attention, "the tensor-core kernel should cover this shape"
     om = oracle.Model(shape, seed=SEED)
     os_ = om.new_state()

@@ -33,35 +33,21 @@ def tol(shape):
     return 1e-3 if shape.dtype == F32 else 2e-2
 
 
-FUSED = {"kernels": pnb.PNB_FUSED_OFF, "fused_ao": pnb.PNB_FUSED_ATTN_OPROJ, "fused": pnb.PNB_FUSED_BLOCK}
-
-
-def set_mode(sm, mode):
-    """'persistent': one cooperative kernel per step; 'kernels': one kernel per
-    phase; 'fused_ao': attention and output projection as one cluster kernel;
-    'fused': the whole attention half of each layer (QKV, attention, output
-    projection) as one cluster kernel."""
-    if mode == "persistent":
+def set_attention(sm, kind):
+    """'tensor': decode attention on tcgen05 tensor cores; 'cuda': the CUDA-core
+    kernel.  Both run inside the same per-phase step."""
+    if kind == "tensor" and not sm.model.tensor_attention:
         try:
-            sm.model.set_persistent(True)
+            sm.model.set_tensor_attention(True)
         except pnb.PnbError as e:
             if e.code == -5:
-                pytest.skip("the persistent kernel does not cover this shape")
+                pytest.skip("the tensor-core attention does not cover this shape")
             raise
-        assert sm.model.persistent and sm.model.step_kernel_count() == 1
-        return
-    sm.model.set_persistent(False)
-    assert not sm.model.persistent
-    try:
-        sm.model.set_fused_attention(FUSED[mode])
-    except pnb.PnbError as e:
-        if e.code == -5:
-            pytest.skip("the fused attention block does not cover this shape")
-        raise
-    assert sm.model.fused_attention == FUSED[mode]
+    if kind == "cuda":
+        sm.model.set_tensor_attention(False)
+    assert sm.model.tensor_attention == (kind == "tensor")
     moe = sm.shape.expert_count > 0
-    per_layer = {"kernels": 3, "fused_ao": 2, "fused": 1}[mode] + (3 if moe else 2)
-    assert sm.model.step_kernel_count() == sm.shape.n_layer * per_layer + 1
+    assert sm.model.step_kernel_count() == sm.shape.n_layer * (5 + (1 if moe else 0)) + 1
 
 
 def gpu_run(sm, state, tokens, graphs=True):
@@ -148,25 +134,21 @@ def _tiny_tokens():
     return prompt, gen
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
-def test_tiny_teacher_forced_matches_oracle(mode):
+def test_tiny_teacher_forced_matches_oracle():
     w = wl.TINY
     prompt, gen = _tiny_tokens()
     tokens = prompt + gen[:-1]
     sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
-    set_mode(sm, mode)
     got, gam = gpu_run(sm, sm.new_state(), tokens)
     ref, ram = oracle_run(w.shape, w.seed, tokens)
     assert compare(w.shape, got, gam, ref, ram, "tiny") == 0
     assert gam[len(prompt) - 1:] == gen
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
-def test_tiny_free_running_greedy_matches_stored_oracle_run(mode):
+def test_tiny_free_running_greedy_matches_stored_oracle_run():
     w = wl.TINY
     prompt, gen = _tiny_tokens()
     sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
-    set_mode(sm, mode)
     st = sm.new_state()
     a = torch.empty(len(gen), dtype=torch.int32, device=DEV)
     for t in prompt[:-1]:
@@ -179,13 +161,14 @@ def test_tiny_free_running_greedy_matches_stored_oracle_run(mode):
     assert st.pos == len(prompt) + len(gen) - 1
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
-def test_graph_replay_equals_eager_launches_bitwise(mode):
-    w = wl.TINY
-    prompt, gen = _tiny_tokens()
-    tokens = prompt + gen[:8]
-    sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
-    set_mode(sm, mode)
+@pytest.mark.parametrize("attention", ["cuda", "tensor"])
+def test_graph_replay_equals_eager_launches_bitwise(attention):
+    shape = SMALL_HD128 if attention == "tensor" else wl.TINY.shape
+    seed = 11
+    rng = np.random.default_rng(3)
+    tokens = [int(t) for t in rng.integers(0, shape.n_vocab, size=12)]
+    sm = pnb.SynthModel(shape, seed, device=DEV)
+    set_attention(sm, attention)
     a, _ = gpu_run(sm, sm.new_state(), tokens, graphs=True)
     b, _ = gpu_run(sm, sm.new_state(), tokens, graphs=False)
     for x, y in zip(a, b):
@@ -240,7 +223,7 @@ SMALL_HD128 = wl.Shape(n_vocab=1000, n_embd=1024, n_head=8, n_kv_head=2, n_layer
                        n_ctx=300, rope_theta=1e4, rms_norm_eps=1e-5, dtype=BF16)
 
 
-@pytest.mark.parametrize("mode", ["persistent", "kernels", "fused_ao", "fused"])
+@pytest.mark.parametrize("attention", ["tensor", "cuda"])
 @pytest.mark.parametrize("name,shape,start,steps", [
     ("window_ring", SMALL_WIN, 40, 24),       # ring of 24 slots, pre-fill wraps it
     ("window_short", SMALL_WIN, 0, 30),       # empty cache, window fills then slides
@@ -251,10 +234,10 @@ SMALL_HD128 = wl.Shape(n_vocab=1000, n_embd=1024, n_head=8, n_kv_head=2, n_layer
     ("mha32_cross", SMALL_MHA32, 300, 6),      # 32 KV heads: CTA ranges cross head boundaries
     ("kv5_window_cross", SMALL_KV5, 450, 6),   # 5 KV heads, window ring, crossing ranges
 ])
-def test_small_bf16_models_match_oracle(name, shape, start, steps, mode):
+def test_small_bf16_models_match_oracle(name, shape, start, steps, attention):
     seed = 77
     sm = pnb.SynthModel(shape, seed, device=DEV)
-    set_mode(sm, mode)
+    set_attention(sm, attention)
     st = sm.new_state(start_pos=start)
     rng = np.random.default_rng(5)
     tokens = [int(t) for t in rng.integers(0, shape.n_vocab, size=steps)]
@@ -264,72 +247,17 @@ def test_small_bf16_models_match_oracle(name, shape, start, steps, mode):
     assert ties <= 1
 
 
-def test_persistent_and_per_kernel_steps_agree():
-    """Same model and tokens through the three execution modes: logits agree to fp32 rounding."""
-    shape, seed = SMALL_WIN, 13
-    tokens = [5, 17, 400, 3000, 9, 9, 1]
+def test_tensor_and_cuda_core_attention_steps_agree():
+    """Same model and tokens with either attention kernel: logits agree to fp32 rounding."""
+    shape, seed = SMALL_HD128, 13
+    tokens = [5, 17, 400, 300, 9, 9, 1]
     outs = []
-    for mode in ("persistent", "kernels", "fused_ao", "fused"):
+    for attention in ("tensor", "cuda"):
         sm = pnb.SynthModel(shape, seed, device=DEV)
-        set_mode(sm, mode)
-        outs.append(gpu_run(sm, sm.new_state(start_pos=30), tokens))
-    for other in outs[1:]:
-        for a, b in zip(outs[0][0], other[0]):
-            assert np.max(np.abs(a - b)) <= 1e-4 * np.max(np.abs(a))
-
-
-@pytest.mark.parametrize("fused", ["fused_ao", "fused"])
-@pytest.mark.parametrize("name,shape,start", [
-    ("window_ring", SMALL_WIN, 40), ("mha", SMALL_MHA, 17), ("hd128_gqa8", SMALL_G8, 40),
-    ("kv5_window_cross", SMALL_KV5, 450), ("empty_cache", SMALL_HD128, 0)])
-def test_fused_block_activations_match_three_kernel_path(name, shape, start, fused):
-    """One layer's attention half run alone both ways from the same state: the
-    rotated queries, the KV slot of the position and the attention output agree
-    to fp32 rounding, and the residual after the down projection (which folds
-    the fused kernel's fixed-point accumulator) agrees too."""
-    seed = 29
-    sm = pnb.SynthModel(shape, seed, device=DEV)
-    L = shape.n_layer
-    acts = {}
-    for mode in ("kernels", fused):
-        sm.model.set_fused_attention(pnb.PNB_FUSED_OFF)
-        st = sm.new_state(start_pos=start)
-        st.forward(7)                      # one whole step: x is a real residual stream
-        st.set_pos(start + 1)
-        sm.model.set_fused_attention(FUSED[mode])   # the down kernel folds the accumulator
-        layer = L - 1
-        kinds = {"kernels": (pnb.PNB_KERNEL_QKV, pnb.PNB_KERNEL_ATTN, pnb.PNB_KERNEL_OPROJ),
-                 "fused_ao": (pnb.PNB_KERNEL_QKV, pnb.PNB_KERNEL_ATTN_BLOCK),
-                 "fused": (pnb.PNB_KERNEL_ATTN_BLOCK,)}[mode]
-        for k in kinds:
-            st.run_kernel(k, layer)
-        if shape.expert_count:
-            st.run_kernel(pnb.PNB_KERNEL_ROUTER, layer)
-        st.run_kernel(pnb.PNB_KERNEL_GATE_UP, layer)
-        st.run_kernel(pnb.PNB_KERNEL_DOWN, layer)
-        torch.cuda.synchronize()
-        assert st.device_error() == 0
-        a = st.activations()
-        n = shape.n_head * shape.head_dim
-        acts[mode] = {k: _dev(a[k], shape.n_embd if k == "x" else n).cpu().numpy()
-                      for k in ("x", "q", "attn")}
-        cap, hd = shape.kv_cap, shape.head_dim
-        blk = shape.n_kv_head * cap * hd
-        et = torch.bfloat16 if shape.dtype == BF16 else torch.float32
-        kv = st.kv.view(et)[:2 * L * blk].view(L, 2, shape.n_kv_head, cap, hd)
-        acts[mode]["kv"] = kv[layer, :, :, (start + 1) % cap].float().cpu().numpy()
-        del st
-    for k in ("q", "attn", "x", "kv"):
-        ref, got = acts["kernels"][k], acts[fused][k]
-        scale = float(np.max(np.abs(ref)))
-        assert scale > 0 and np.all(np.isfinite(got)), k
-        assert float(np.max(np.abs(got - ref))) <= 1e-5 * scale, f"{name} {k}"
-
-
-def _dev(ptr, n):
-    class _H:
-        __cuda_array_interface__ = {"shape": (n,), "typestr": "<f4", "data": (ptr, False), "version": 3}
-    return torch.as_tensor(_H(), device=DEV).clone()
+        set_attention(sm, attention)
+        outs.append(gpu_run(sm, sm.new_state(start_pos=200), tokens))
+    for a, b in zip(outs[0][0], outs[1][0]):
+        assert np.max(np.abs(a - b)) <= 1e-4 * np.max(np.abs(a))
 
 
 # ------------------------------------------------- full-size workloads, sampled steps

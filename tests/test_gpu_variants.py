@@ -161,24 +161,14 @@ def test_variant_prefill_matches_oracle(shape):
         check(r, ra, got[i], int(gam[i]), f"token {i}", tol(shape))
 
 
-def test_neox_runs_in_every_launch_mode_and_bias_models_refuse_the_fused_forms():
+def test_neox_with_either_attention_kernel_matches_oracle():
+    """Phi-3-style NeoX RoPE with the tensor-core and the CUDA-core attention."""
     rng = np.random.default_rng(21)
     tokens = [int(t) for t in rng.integers(0, PHI3.n_vocab, size=10)]
     ref = oracle_steps(PHI3, 0, tokens)
     sm = pnb.SynthModel(PHI3, SEED, device=DEV)
-    for mode in (pnb.PNB_FUSED_BLOCK, pnb.PNB_FUSED_ATTN_OPROJ):
-        sm.model.set_fused_attention(mode)
+    kinds = [False] + ([True] if sm.model.tensor_attention else [])
+    for tc in kinds:
+        sm.model.set_tensor_attention(tc)
         for i, ((g, ga), (r, ra)) in enumerate(zip(gpu_steps(sm, 0, tokens), ref)):
-            check(r, ra, g, ga, f"fused {mode} step {i}", tol(PHI3))
-    sm.model.set_fused_attention(pnb.PNB_FUSED_OFF)
-    sm.model.set_persistent(True)
-    for i, ((g, ga), (r, ra)) in enumerate(zip(gpu_steps(sm, 0, tokens), ref)):
-        check(r, ra, g, ga, f"persistent step {i}", tol(PHI3))
-    sm.model.set_persistent(False)
-    qm = pnb.SynthModel(QWEN2, SEED, device=DEV)
-    for fn, arg in ((qm.model.set_persistent, True),
-                    (qm.model.set_fused_attention, pnb.PNB_FUSED_BLOCK),
-                    (qm.model.set_fused_attention, pnb.PNB_FUSED_ATTN_OPROJ)):
-        with pytest.raises(pnb.PnbError) as e:
-            fn(arg)
-        assert e.value.code == -5
+            check(r, ra, g, ga, f"tensor attention {tc} step {i}", tol(PHI3))

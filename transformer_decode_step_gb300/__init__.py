@@ -21,10 +21,9 @@ _lib = ctypes.CDLL(LIB)
 
 PNB_F32, PNB_BF16, PNB_Q8_0 = 0, 1, 2
 PNB_TOKEN_PREV = -1
-PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT, PNB_DEV_ERR_RANGE = 1, 2, 4
-PNB_FUSED_OFF, PNB_FUSED_ATTN_OPROJ, PNB_FUSED_BLOCK = 0, 1, 2
+PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT = 1, 2
 (PNB_KERNEL_QKV, PNB_KERNEL_ATTN, PNB_KERNEL_OPROJ, PNB_KERNEL_ROUTER, PNB_KERNEL_GATE_UP,
- PNB_KERNEL_DOWN, PNB_KERNEL_LM_HEAD, PNB_KERNEL_ATTN_BLOCK) = range(8)
+ PNB_KERNEL_DOWN, PNB_KERNEL_LM_HEAD) = range(7)
 ERRORS = {0: "PNB_OK", -1: "PNB_E_INVAL", -2: "PNB_E_NULL", -3: "PNB_E_ALIGN",
           -4: "PNB_E_CTX_FULL", -5: "PNB_E_UNSUPPORTED", -6: "PNB_E_CUDA", -7: "PNB_E_TOKEN",
           -8: "PNB_E_DEVICE", -9: "PNB_E_NOMEM", -10: "PNB_E_WRONG_DEVICE", -11: "PNB_E_TOO_LARGE",
@@ -83,12 +82,8 @@ _SIGS = {
     "pnb_forward_poll": (_i32, [_p, _p, _p]),
     "pnb_state_stream": (_i32, [_p, _p]),
     "pnb_model_set_graphs": (_i32, [_p, _i32]),
-    "pnb_model_set_persistent": (_i32, [_p, _i32]),
-    "pnb_model_is_persistent": (_i32, [_p]),
     "pnb_model_set_tensor_attention": (_i32, [_p, _i32]),
     "pnb_model_is_tensor_attention": (_i32, [_p]),
-    "pnb_model_set_fused_attention": (_i32, [_p, _i32]),
-    "pnb_model_fused_attention": (_i32, [_p]),
     "pnb_step_kernel_count": (_i32, [_p, _i32]),
     "pnb_state_activations": (_i32, [_p, _p]),
     "pnb_step_kernel": (_i32, [_p, _p, _i32, _i32, _p]),
@@ -193,23 +188,6 @@ class Model:
     @property
     def tensor_attention(self) -> bool:
         return bool(pnb_model_is_tensor_attention(self._h))
-
-    def set_fused_attention(self, mode: int):
-        """PNB_FUSED_OFF, PNB_FUSED_ATTN_OPROJ or PNB_FUSED_BLOCK."""
-        if isinstance(mode, bool):
-            raise TypeError("pass a PNB_FUSED_* mode, not a bool")
-        check(pnb_model_set_fused_attention(self._h, int(mode)), "pnb_model_set_fused_attention")
-
-    @property
-    def fused_attention(self) -> int:
-        return int(pnb_model_fused_attention(self._h))
-
-    def set_persistent(self, enable: bool):
-        check(pnb_model_set_persistent(self._h, 1 if enable else 0), "pnb_model_set_persistent")
-
-    @property
-    def persistent(self) -> bool:
-        return bool(pnb_model_is_persistent(self._h))
 
     def step_kernel_count(self, batch: int = 0) -> int:
         return int(pnb_step_kernel_count(self._h, batch))

@@ -12,7 +12,6 @@
 
 #include "pnb.h"
 #include "pnb_kernels.cuh"
-#include "pnb_step.cuh"
 
 using namespace pnb;
 
@@ -109,17 +108,8 @@ struct pnb_model {
   // tensor-core attention (bf16 KV, head_dim 64 / 128, <= 8 query heads per KV head)
   bool attn_tc_ok = false, attn_tc = false;
   int n_split_tc = 1;
-  // fused attention block (one cluster per query head): geometry, per-layer Wo maps
-  bool block_ok = false;
   bool sample_ok = false;                // the sampler kernel fits this vocabulary
-  int block = 0;                         // PNB_FUSED_*: off, attention + o-proj, whole block
-  BlockGeom bgeom{};
-  int block_clusters = 0;                // clusters that fit on the GPU at once
-  std::vector<CUtensorMap> wo_maps;      // per layer: Wo boxes of one head's columns
   int mode_gen = 0;                      // bumped when a launch mode changes (graphs re-captured)
-  // persistent step kernel
-  bool persistent = false;
-  int st_nslots = 0, st_slot_bytes = 0, st_sp = 0, st_union = 0, st_smem = 0;
   cudaStream_t cap_stream = nullptr;     // stream used for graph capture
   struct BatchCtx *batch = nullptr;      // batched-slot step (made on first use)
 };
@@ -164,18 +154,11 @@ struct pnb_state {
   StepIO *io = nullptr;
   float *x = nullptr, *q = nullptr, *attn = nullptr, *h = nullptr, *part = nullptr;
   float *gate = nullptr, *lm_val = nullptr;
-  long long *acc = nullptr;              // [n_embd] attention-output accumulator (2^-32 units)
   int32_t *idx = nullptr, *lm_idx = nullptr;
   unsigned *attn_cnt = nullptr, *lm_cnt = nullptr;
   size_t counters_off = 0, counters_bytes = 0;
-  unsigned *bar_count = nullptr, *bar_gen = nullptr;
-  int32_t *abort_flag = nullptr;
   unsigned *work = nullptr;              // [launch][claim, done] item counters
-  float *step_part = nullptr;            // attention partials of the persistent kernel
-  float *ss_part = nullptr;              // per-CTA sums of squares [2][grid]
-  StepLayer *layers = nullptr;           // device [n_layer]
-  unsigned long long *trace = nullptr;   // optional phase timestamps (persistent kernel)
-  unsigned long long *ktrace = nullptr;  // optional per-CTA timestamps (per-phase kernels)
+  unsigned long long *ktrace = nullptr;  // optional per-CTA timestamps of the step's kernels
   void *maps = nullptr;                  // device [layer][K|V] tensor maps over kv (tensor-core attention)
   int g_gen = -1;                        // model mode generation the graph was captured in
   cudaGraphExec_t exec = nullptr;
@@ -243,45 +226,6 @@ void plan(pnb_model *m) {
   m->n_split_tc = std::max(1, std::min({attn_tc_max_split(), m->num_sms / c.n_kv_head, ceil_div(m->cap, 128)}));
 }
 
-bool geoms_supported(const pnb_model *m);
-
-// Persistent-kernel geometry: one ring slot holds the largest GEMV stage or a
-// 2 x sp x head_dim KV stage; the scratch union holds the largest per-CTA
-// partial array or the attention merge area.
-void plan_step(pnb_model *m) {
-  const pnb_config &c = m->cfg;
-  const int G = c.n_head / c.n_kv_head, hd = m->hd, es = m->kv_es;
-  m->persistent = false;
-  if (c.dtype == PNB_Q8_0) return;   // the persistent kernel streams fp32 / bf16 weights
-  if (!m->bqkv.empty()) return;      // nor does it add q / k / v biases
-  if (!(hd == 32 || hd == 64 || hd == 128) || !(G == 1 || G == 2 || G == 4 || G == 8) ||
-      G * hd > 512)
-    return;
-  int slot = 0, uni = 0;
-  for (const Geom *g : {&m->g_qkv, &m->g_o, &m->g_gateup, &m->g_down, &m->g_lm}) {
-    slot = std::max(slot, g->stage_bytes);
-    uni = std::max(uni, g->rows_cta_max * g->cw * g->nsum);
-  }
-  slot = std::max(slot, 2 * 32 * hd * es);
-  int sp = slot / (2 * hd * es);
-  sp = std::min(256, sp - sp % 32);
-  uni = std::max(uni, kGemvWarps * G * (hd + 2));
-  const int fixed = step_smem(1, slot, uni).total - slot;
-  int ns = std::min(kRingBudget / slot, (kMaxSmem - fixed - 1024) / slot);
-  if (ns < 2) return;
-  ns = std::min(ns, 8);
-  m->st_nslots = ns;
-  m->st_slot_bytes = slot;
-  m->st_sp = sp;
-  m->st_union = uni;
-  m->st_smem = step_smem(ns, slot, uni).total;
-  if (m->st_smem > kMaxSmem || !geoms_supported(m)) return;
-  StepArgs dummy{};
-  int bps = 0;
-  cudaError_t e = (c.dtype ? step_bf16 : step_f32)(hd, G, dummy, m->grid, m->st_smem, nullptr, true, &bps);
-  m->persistent = e == cudaSuccess && bps >= 1;
-}
-
 int max_smem(const pnb_model *m) {
   int s = std::max({smem_layout(m->g_qkv).total, smem_layout(m->g_o).total,
                     smem_layout(m->g_gateup).total, smem_layout(m->g_down).total,
@@ -306,12 +250,7 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
   const float eps = (float)c.rms_norm_eps;
   const bool moe = c.expert_count > 0;
   const int k = moe ? c.expert_used : 1;
-  // the fused block records in its layer's QKV slot, or in the attention
-  // slot when it follows the QKV kernel
-  const int block_slot = m->block == PNB_FUSED_ATTN_OPROJ ? PNB_KERNEL_ATTN : PNB_KERNEL_QKV;
-  const KTrace tr{s->ktrace, kind == PNB_KERNEL_LM_HEAD    ? 6 * c.n_layer
-                            : kind == PNB_KERNEL_ATTN_BLOCK ? 6 * l + block_slot
-                                                            : 6 * l + kind};
+  const KTrace tr{s->ktrace, kind == PNB_KERNEL_LM_HEAD ? 6 * c.n_layer : 6 * l + kind};
   unsigned *work = s->work + 2 * tr.phase;
   switch (kind) {
     case PNB_KERNEL_QKV: {
@@ -340,34 +279,6 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       qa.tr = tr;
       qa.work = work;
       return launch_qkv(c.dtype, qa, m->grid, st, pdl);
-    }
-    case PNB_KERNEL_ATTN_BLOCK: {
-      if (!m->block_ok) return cudaErrorInvalidValue;
-      BlockArgs ba{};
-      ba.b = m->bgeom;
-      ba.H = H;
-      ba.Hkv = Hkv;
-      ba.cap = m->cap;
-      ba.window = c.sliding_window;
-      ba.wqkv = m->wqkv[l];
-      ba.x = s->x;
-      ba.emb = l == 0 ? m->tok_embd : nullptr;
-      ba.x_out = s->x;
-      ba.n_vocab = c.n_vocab;
-      ba.norm_w = m->attn_norm[l];
-      ba.eps = eps;
-      ba.inv_freq = m->inv_freq;
-      ba.k_cache = kc;
-      ba.v_cache = vc;
-      ba.qscale = (float)(1.4426950408889634 / std::sqrt((double)hd));
-      ba.acc = s->acc;
-      ba.q_out = s->q;
-      ba.o_out = s->attn;
-      ba.q_in = m->block == PNB_FUSED_ATTN_OPROJ ? s->q : nullptr;
-      if (ba.q_in) ba.q_out = nullptr;   // the QKV kernel wrote them
-      ba.io = s->io;
-      ba.tr = tr;
-      return launch_attn_block(c.dtype, hd, &m->wo_maps[l], ba, st, pdl);
     }
     case PNB_KERNEL_ATTN: {
       if (m->attn_tc) {
@@ -427,7 +338,6 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ra.k = k;
       ra.E = E;
       ra.x = s->x;
-      ra.acc = m->block ? s->acc : nullptr;
       ra.norm_w = m->ffn_norm[l];
       ra.eps = eps;
       ra.idx = s->idx;
@@ -441,7 +351,6 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       ga.g = m->g_gateup;
       ga.s.rows = 2 * (int64_t)F;
       ga.x = s->x;
-      ga.acc = m->block ? s->acc : nullptr;
       ga.norm_w = m->ffn_norm[l];
       ga.eps = eps;
       ga.h = s->h;
@@ -467,7 +376,6 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
         da.s.w[0] = m->w_down[l];
         da.vec = s->h;
         da.x = s->x;
-        da.acc = m->block ? s->acc : nullptr;
         da.io = s->io;
         da.tr = tr;
         da.work = work;
@@ -483,7 +391,6 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
       da.n_ff = F;
       da.gate = s->gate;
       da.x = s->x;
-      da.acc = m->block ? s->acc : nullptr;
       da.io = s->io;
       da.tr = tr;
       return launch_down_moe(c.dtype, da, m->grid, st, pdl);
@@ -512,89 +419,20 @@ cudaError_t enqueue_kernel(pnb_model *m, pnb_state *s, int kind, int l, cudaStre
   }
 }
 
-// The persistent kernel's arguments for state s.
-StepArgs step_args(const pnb_model *m, const pnb_state *s, float *logits, int32_t *argmax) {
-  const pnb_config &c = m->cfg;
-  StepArgs a{};
-  a.E = c.n_embd;
-  a.H = c.n_head;
-  a.Hkv = c.n_kv_head;
-  a.hd = m->hd;
-  a.F = c.n_ff;
-  a.V = c.n_vocab;
-  a.L = c.n_layer;
-  a.X = c.expert_count;
-  a.k = c.expert_count > 0 ? c.expert_used : 1;
-  a.cap = m->cap;
-  a.window = c.sliding_window;
-  a.eps = (float)c.rms_norm_eps;
-  a.qscale = (float)(1.4426950408889634 / std::sqrt((double)m->hd));
-  a.g_qkv = m->g_qkv;
-  a.g_o = m->g_o;
-  a.g_gu = m->g_gateup;
-  a.g_dn = m->g_down;
-  a.g_lm = m->g_lm;
-  a.nslots = m->st_nslots;
-  a.slot_bytes = m->st_slot_bytes;
-  a.sp = m->st_sp;
-  a.union_floats = m->st_union;
-  a.tok_embd = m->tok_embd;
-  a.output = m->output;
-  a.out_norm = m->out_norm;
-  a.inv_freq = m->inv_freq;
-  a.layers = s->layers;
-  a.x = s->x;
-  a.q = s->q;
-  a.o = s->attn;
-  a.h = s->h;
-  a.attn_part = s->step_part;
-  a.lm_val = s->lm_val;
-  a.lm_idx = s->lm_idx;
-  a.attn_cnt = s->attn_cnt;
-  a.lm_cnt = s->lm_cnt;
-  a.bar_count = s->bar_count;
-  a.bar_gen = s->bar_gen;
-  a.abort_flag = s->abort_flag;
-  a.ss_part = s->ss_part;
-  a.logits = logits;
-  a.argmax_out = argmax;
-  a.io = s->io;
-  a.trace = s->trace;
-  return a;
-}
-
-// Enqueue one single-sequence step (everything after the token write): the
-// persistent kernel when the model supports it, else one kernel per phase
-// (the first waits for all earlier stream work; every later one is launched
-// with programmatic stream serialization).
+// Enqueue one single-sequence step (everything after the token write): one
+// kernel per phase; the first waits for all earlier stream work, every later
+// one is launched with programmatic stream serialization.
 cudaError_t enqueue_step(pnb_model *m, pnb_state *s, cudaStream_t st, float *logits,
                          int32_t *argmax) {
-  if (m->persistent) {
-    const StepArgs a = step_args(m, s, logits, argmax);
-    const int G = m->cfg.n_head / m->cfg.n_kv_head;
-    return (m->cfg.dtype ? step_bf16 : step_f32)(m->hd, G, a, m->grid, m->st_smem, st, false, nullptr);
-  }
   const bool moe = m->cfg.expert_count > 0;
   cudaError_t e;
   for (int l = 0; l < m->cfg.n_layer; ++l) {
-    if (m->block == PNB_FUSED_BLOCK) {
-      if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN_BLOCK, l, st, l > 0, nullptr, nullptr)) !=
-          cudaSuccess)
-        return e;
-    } else if (m->block == PNB_FUSED_ATTN_OPROJ) {
-      if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
-        return e;
-      if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN_BLOCK, l, st, true, nullptr, nullptr)) !=
-          cudaSuccess)
-        return e;
-    } else {
-      if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
-        return e;
-      if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN, l, st, true, nullptr, nullptr)) != cudaSuccess)
-        return e;
-      if ((e = enqueue_kernel(m, s, PNB_KERNEL_OPROJ, l, st, true, nullptr, nullptr)) != cudaSuccess)
-        return e;
-    }
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_QKV, l, st, l > 0, nullptr, nullptr)) != cudaSuccess)
+      return e;
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_ATTN, l, st, true, nullptr, nullptr)) != cudaSuccess)
+      return e;
+    if ((e = enqueue_kernel(m, s, PNB_KERNEL_OPROJ, l, st, true, nullptr, nullptr)) != cudaSuccess)
+      return e;
     if (moe && (e = enqueue_kernel(m, s, PNB_KERNEL_ROUTER, l, st, true, nullptr, nullptr)) !=
                    cudaSuccess)
       return e;
@@ -641,56 +479,6 @@ bool encode_map(CUtensorMap *map, const void *base, int64_t rows, int K, int box
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 2-D tensor map over one layer's Wo [n_embd rows][H * hd columns] (bf16 or
-// fp32), boxes of hd columns x o_item rows, no swizzle: a box is one head's
-// column block of o_item rows, stored row after row.
-bool encode_wo_map(CUtensorMap *map, const void *base, int dtype, int E, int HHD, int hd, int o_item) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const int es = dtype ? 2 : 4;
-  const cuuint64_t dims[2] = {(cuuint64_t)HHD, (cuuint64_t)E};
-  const cuuint64_t strides[1] = {(cuuint64_t)HHD * es};
-  const cuuint32_t box[2] = {(cuuint32_t)hd, (cuuint32_t)o_item};
-  const cuuint32_t el[2] = {1, 1};
-  return fn(map, dtype ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-            const_cast<void *>(base), dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Geometry of the fused attention block: the largest cluster (<= 8 CTAs, a
-// power of two) with one cluster per query head on at most one CTA per SM,
-// 32 KB ring items of whole Wqkv rows / K and V positions / Wo rows.
-bool plan_block(pnb_model *m) {
-  const pnb_config &c = m->cfg;
-  const int hd = m->hd, H = c.n_head, E = c.n_embd, es = m->kv_es;
-  if (!(hd == 32 || hd == 64 || hd == 128) || c.dtype == PNB_Q8_0 || !m->bqkv.empty()) return false;
-  int C = 8;
-  while (C > 1 && H * C > m->num_sms) C >>= 1;
-  if (H * C > m->num_sms || E % C) return false;
-  BlockGeom b{};
-  b.C = C;
-  b.rows_cta = 3 * hd / C;
-  b.g = plan_gemv(E, c.dtype, 3 * hd, 1, 1, H * C, 1);
-  if (b.g.nv > 4) return false;
-  int kv = 64;
-  while (kv > 4 && 2 * kv * hd * es > kStageTarget) kv >>= 1;
-  b.kv_item = kv;
-  int oi = 256;
-  while (oi > 1 && ((E / C) % oi || oi * hd * es > kStageTarget)) oi >>= 1;
-  if (oi < 8) return false;
-  b.o_item = oi;
-  b.stage_bytes = align_up(std::max({b.g.rows_per_stage * b.g.row_bytes, 2 * kv * hd * es, oi * hd * es}), 1024);
-  b.nstages = 0;
-  const int fixed = block_smem(b, hd).total;
-  b.nstages = std::min(8, std::min(kRingBudget, kMaxSmem - fixed) / b.stage_bytes);
-  if (b.nstages < 2) return false;
-  b.smem = block_smem(b, hd).total;
-  if (b.smem > kMaxSmem) return false;
-  m->bgeom = b;
-  return true;
 }
 
 // Split of a GEMM over K so that (tiles x ksplit) units fill whole waves of
@@ -1153,33 +941,11 @@ int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **ou
   // recent-token bitmap one bit per token in shared memory
   if (ok && c.n_vocab < (1 << 22) && sample_smem_bytes(c.n_vocab) <= (size_t)kMaxSmem)
     m->sample_ok = prepare_sample_kernel(c.n_vocab) == cudaSuccess;
-  // one kernel per phase is the default: on the 7B-class shapes it is the
-  // faster of the two; the persistent kernel is opt-in
+  // tensor-core attention where the shape allows it (bf16 KV, whole tiles)
   if (ok) {
-    plan_step(m);
-    m->persistent = false;
     if (m->attn_tc_ok) m->attn_tc_ok = encode_fn() != nullptr && prepare_attn_tc_kernels() == cudaSuccess;
     m->attn_tc = m->attn_tc_ok;
-    // the fused attention block (default where the model allows it)
-    if (plan_block(m) && encode_fn() != nullptr &&
-        prepare_attn_block_kernels(c.dtype, m->bgeom.smem) == cudaSuccess) {
-      m->block_clusters = attn_block_max_clusters(c.dtype, m->hd, m->bgeom, c.n_head);
-      bool maps_ok = m->block_clusters > 0;
-      try {
-        m->wo_maps.resize(c.n_layer);
-      } catch (...) {
-        maps_ok = false;
-      }
-      for (int l = 0; maps_ok && l < c.n_layer; ++l)
-        maps_ok = encode_wo_map(&m->wo_maps[l], m->wo[l], c.dtype, c.n_embd, c.n_head * m->hd, m->hd,
-                                m->bgeom.o_item);
-      m->block_ok = maps_ok;
-    }
     cudaGetLastError();   // a declined option leaves no sticky launch error behind
-    // opt-in: with one cluster per query head the block runs on n_head * C
-    // SMs (128 of 152 for 32 heads), and on the 7B-class shapes the three
-    // per-phase kernels on every SM are the faster of the two
-    m->block = PNB_FUSED_OFF;
   }
   if (!ok) {
     pnb_model_free(m);
@@ -1231,16 +997,12 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   const size_t o_attn = take((size_t)c.n_head * m->hd * 4);
   const size_t o_h = take((size_t)k * c.n_ff * 4);
   const size_t o_part = take((size_t)c.n_head * std::max(m->n_split, m->n_split_tc) * (m->hd + 2) * 4);
-  const size_t o_acc = take((size_t)c.n_embd * 8);
   const size_t o_gate = take((size_t)k * 4);
   const size_t o_idx = take((size_t)k * 4);
   const size_t o_lmv = take((size_t)m->grid * 4);
   const size_t o_lmi = take((size_t)m->grid * 4);
-  const size_t n_cnt = (size_t)(c.n_kv_head * m->zgroups + 1 + 3) + 2 * (6 * c.n_layer + 1);
+  const size_t n_cnt = (size_t)(c.n_kv_head * m->zgroups + 1) + 2 * (6 * c.n_layer + 1);
   const size_t o_cnt = take(n_cnt * 4);
-  const size_t o_spart = take((size_t)c.n_head * m->grid * (m->hd + 2) * 4);
-  const size_t o_layers = take((size_t)c.n_layer * sizeof(StepLayer));
-  const size_t o_ss = take((size_t)2 * m->grid * 4);
   const size_t o_maps = m->attn_tc_ok ? take((size_t)2 * c.n_layer * sizeof(CUtensorMap)) : 0;
   if (cudaMalloc(&s->ws, off) != cudaSuccess) {
     delete s;
@@ -1252,22 +1014,15 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
   s->attn = reinterpret_cast<float *>(s->ws + o_attn);
   s->h = reinterpret_cast<float *>(s->ws + o_h);
   s->part = reinterpret_cast<float *>(s->ws + o_part);
-  s->acc = reinterpret_cast<long long *>(s->ws + o_acc);
   s->gate = reinterpret_cast<float *>(s->ws + o_gate);
   s->idx = reinterpret_cast<int32_t *>(s->ws + o_idx);
   s->lm_val = reinterpret_cast<float *>(s->ws + o_lmv);
   s->lm_idx = reinterpret_cast<int32_t *>(s->ws + o_lmi);
   s->attn_cnt = reinterpret_cast<unsigned *>(s->ws + o_cnt);
   s->lm_cnt = s->attn_cnt + c.n_kv_head * m->zgroups;
-  s->bar_count = s->lm_cnt + 1;
-  s->bar_gen = s->lm_cnt + 2;
-  s->abort_flag = reinterpret_cast<int32_t *>(s->lm_cnt + 3);
-  s->work = s->lm_cnt + 4;
+  s->work = s->lm_cnt + 1;
   s->counters_off = o_cnt;
   s->counters_bytes = n_cnt * 4;
-  s->step_part = reinterpret_cast<float *>(s->ws + o_spart);
-  s->layers = reinterpret_cast<StepLayer *>(s->ws + o_layers);
-  s->ss_part = reinterpret_cast<float *>(s->ws + o_ss);
   std::vector<CUtensorMap> maps;
   if (m->attn_tc_ok) {
     // [layer][K|V] maps over this state's cache: rows = n_kv_head * cap positions, hd columns
@@ -1283,29 +1038,7 @@ int pnb_state_new(pnb_model *m, void *kv_dev, size_t kv_bytes, pnb_state **out) 
           return PNB_E_CUDA;
         }
   }
-  // per-layer table of the persistent kernel
-  std::vector<StepLayer> lt(c.n_layer);
-  const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->kv_es;
-  for (int l = 0; l < c.n_layer; ++l) {
-    StepLayer &L = lt[l];
-    L.wqkv = m->wqkv[l];
-    L.wo = m->wo[l];
-    L.attn_norm = m->attn_norm[l];
-    L.ffn_norm = m->ffn_norm[l];
-    if (c.expert_count > 0) {
-      L.w_router = m->w_router[l];
-      L.tab_gate_up = m->tab_gate_up + (size_t)l * c.expert_count;
-      L.tab_down = m->tab_down + (size_t)l * c.expert_count;
-    } else {
-      L.w_gate_up = m->w_gate_up[l];
-      L.w_down = m->w_down[l];
-    }
-    L.kc = s->kv + (size_t)(2 * l) * layer_kv;
-    L.vc = s->kv + (size_t)(2 * l + 1) * layer_kv;
-  }
   if (cudaMemset(s->ws, 0, off) != cudaSuccess ||
-      cudaMemcpy(s->layers, lt.data(), lt.size() * sizeof(StepLayer), cudaMemcpyHostToDevice) !=
-          cudaSuccess ||
       (s->maps && cudaMemcpy(s->maps, maps.data(), maps.size() * sizeof(CUtensorMap),
                              cudaMemcpyHostToDevice) != cudaSuccess)) {
     cudaFree(s->ws);
@@ -1333,7 +1066,6 @@ int pnb_state_reset(pnb_state *s, pnb_stream stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(s->kv, 0, pnb_state_kv_bytes(s->m), st) != cudaSuccess ||
       cudaMemsetAsync(s->io, 0, sizeof(StepIO), st) != cudaSuccess ||
-      cudaMemsetAsync(s->acc, 0, (size_t)s->m->cfg.n_embd * 8, st) != cudaSuccess ||
       cudaMemsetAsync(s->ws + s->counters_off, 0, s->counters_bytes, st) != cudaSuccess)
     return PNB_E_CUDA;
   s->pos = 0;
@@ -1658,17 +1390,6 @@ int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T
   return PNB_OK;
 }
 
-int pnb_model_set_persistent(pnb_model *m, int enable) {
-  if (!m) return PNB_E_NULL;
-  ++m->mode_gen;
-  if (!enable) {
-    m->persistent = false;
-    return PNB_OK;
-  }
-  plan_step(m);
-  return m->persistent ? PNB_OK : PNB_E_UNSUPPORTED;
-}
-
 int pnb_model_set_tensor_attention(pnb_model *m, int enable) {
   if (!m) return PNB_E_NULL;
   if (enable && !m->attn_tc_ok) return PNB_E_UNSUPPORTED;
@@ -1678,19 +1399,6 @@ int pnb_model_set_tensor_attention(pnb_model *m, int enable) {
 }
 
 int pnb_model_is_tensor_attention(const pnb_model *m) { return m && m->attn_tc ? 1 : 0; }
-
-int pnb_model_set_fused_attention(pnb_model *m, int mode) {
-  if (!m) return PNB_E_NULL;
-  if (mode < PNB_FUSED_OFF || mode > PNB_FUSED_BLOCK) return PNB_E_INVAL;
-  if (mode != PNB_FUSED_OFF && !m->block_ok) return PNB_E_UNSUPPORTED;
-  if (m->block != mode) ++m->mode_gen;
-  m->block = mode;
-  return PNB_OK;
-}
-
-int pnb_model_fused_attention(const pnb_model *m) { return m ? m->block : 0; }
-
-int pnb_model_is_persistent(const pnb_model *m) { return m && m->persistent ? 1 : 0; }
 
 int pnb_model_set_graphs(pnb_model *m, int enable) {
   if (!m) return PNB_E_NULL;
@@ -1711,18 +1419,14 @@ int pnb_step_kernel_count(const pnb_model *m, int32_t B) {
     const int ffn = m->n_sets * (2 + fmerge) + (m->cfg.expert_count > 0 ? 1 : 0);
     return m->cfg.n_layer * (5 + qmerge + ffn) + 2;
   }
-  if (m->persistent) return 1;
-  const int attn = m->block == PNB_FUSED_BLOCK ? 1 : (m->block == PNB_FUSED_ATTN_OPROJ ? 2 : 3);
-  const int per_layer = attn + (m->cfg.expert_count > 0 ? 3 : 2);
+  const int per_layer = 3 + (m->cfg.expert_count > 0 ? 3 : 2);
   return m->cfg.n_layer * per_layer + 1;
 }
 
 int pnb_step_kernel(pnb_model *m, pnb_state *s, int32_t kind, int32_t layer, pnb_stream stream) {
   if (!m || !s) return PNB_E_NULL;
   if (s->m != m) return PNB_E_INVAL;
-  if (kind < PNB_KERNEL_QKV || kind > PNB_KERNEL_ATTN_BLOCK) return PNB_E_INVAL;
-  if (kind == PNB_KERNEL_ATTN_BLOCK && (!m->block_ok || m->block == PNB_FUSED_OFF))
-    return PNB_E_UNSUPPORTED;
+  if (kind < PNB_KERNEL_QKV || kind > PNB_KERNEL_LM_HEAD) return PNB_E_INVAL;
   if (kind == PNB_KERNEL_ROUTER && m->cfg.expert_count == 0) return PNB_E_INVAL;
   if (layer < 0 || layer >= m->cfg.n_layer) return PNB_E_INVAL;
   int rc = check_device(m);
@@ -1737,13 +1441,11 @@ int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes) {
   if (!s) return PNB_E_NULL;
   if (trace_dev) {
     const int L = s->m->cfg.n_layer;
-    const size_t need = std::max((size_t)s->m->grid * (5 * L + 1) * 6 * 8,
-                                 (size_t)(7 * L + 2) * kTraceCtas * 8 * 8);
+    const size_t need = (size_t)(7 * L + 2) * kTraceCtas * 8 * 8;
     if (bytes < need) return PNB_E_INVAL;
     if (reinterpret_cast<uintptr_t>(trace_dev) & 7u) return PNB_E_ALIGN;
   }
-  s->trace = reinterpret_cast<unsigned long long *>(trace_dev);
-  s->ktrace = s->trace;
+  s->ktrace = reinterpret_cast<unsigned long long *>(trace_dev);
   if (s->exec) {   // the captured graph holds the old argument
     cudaGraphExecDestroy(s->exec);
     s->exec = nullptr;

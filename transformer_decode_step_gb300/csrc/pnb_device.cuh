@@ -24,7 +24,6 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 
 // device-side error bits (mirror of PNB_DEV_ERR_*)
 constexpr int kErrToken = 1;
 constexpr int kErrTimeout = 2;
-constexpr int kErrRange = 4;
 
 // -------------------------------------------------------------- shared mem
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -124,13 +124,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_resid(const ResidArgs a) {
   gemv_sync();
   if (tid == 0) ktrace(a.tr, 4);
   for_claimed_rows(a.g, c, a.s.rows, false, tid, [&](int k, int r, int, int64_t row) {
-    const float d = item_row_total(a.g, c, k, r);
-    if (a.acc) {   // fold the fused block's attention output in, then clear it
-      a.x[row] = (a.x[row] + fix_to_float(a.acc[row])) + d;
-      a.acc[row] = 0;
-    } else {
-      a.x[row] += d;
-    }
+    a.x[row] += item_row_total(a.g, c, k, r);
   });
   if (tid == 0) ktrace(a.tr, 5);
 }
@@ -142,12 +136,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gateup(const GateUpArgs a) 
   load_weight_slice(xs, a.norm_w, a.g, warp, lane);
   pdl_wait();
   if (tid == 0) ktrace(a.tr, 1);
-  if (a.acc) {
-    const XAcc xa{a.x, a.acc};
-    norm_slice(xs, &xa, a.g.K, a.eps, a.g, c.red, warp, lane);
-  } else {
-    norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
-  }
+  norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
   if (tid == 0) ktrace(a.tr, 2);
   consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
@@ -177,12 +166,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_down_moe(const DownMoeArgs 
     for (int s = 0; s < a.s.n; ++s)
       acc = fmaf(a.gate[s], row_total(c.part + s * a.g.rows_cta_max * a.g.cw, (int)(r - c.r0), a.g.cw),
                  acc);
-    if (a.acc) {   // fold the fused block's attention output in, then clear it
-      a.x[r] = (a.x[r] + fix_to_float(a.acc[r])) + acc;
-      a.acc[r] = 0;
-    } else {
-      a.x[r] += acc;
-    }
+    a.x[r] += acc;
   }
   if (tid == 0) ktrace(a.tr, 5);
 }
@@ -270,8 +254,7 @@ __global__ void __launch_bounds__(256, 1) k_router(const RouterArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
   pdl_trigger();
-  // the residual (with the fused block's pending attention output)
-  for (int i = tid; i < a.E; i += 256) xs[i] = a.acc ? a.x[i] + fix_to_float(a.acc[i]) : a.x[i];
+  for (int i = tid; i < a.E; i += 256) xs[i] = a.x[i];
   float ss = 0.f;
   for (int i = tid; i < a.E; i += 256) ss = fmaf(xs[i], xs[i], ss);
   ss = warp_sum(ss);

@@ -1,7 +1,6 @@
-// pnb_gemv_dev.cuh - device building blocks shared by the weight-streaming
-// kernels and the persistent decode-step kernel: ring item enumeration,
-// the producer loop, register slices of the activation vector, RMSNorm
-// factor, row dot products, RoPE angles.
+// pnb_gemv_dev.cuh - device building blocks of the weight-streaming kernels:
+// ring item enumeration, the producer loops, register slices of the
+// activation vector, RMSNorm factor, row dot products, RoPE angles.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -362,19 +361,6 @@ struct XSlice {
   float2 p[NV][Vec<T>::N / 2];
 };
 
-// The residual stream while an attention-output accumulator is pending:
-// element i is x[i] + acc[i] * 2^-32 (fp32, acc word rounded once).
-struct XAcc {
-  const float *x;
-  const long long *acc;
-};
-
-__device__ __forceinline__ float2 load2(const XAcc *src, int col) {
-  const float2 v = __ldcg(reinterpret_cast<const float2 *>(src->x + col));
-  const longlong2 f = __ldcg(reinterpret_cast<const longlong2 *>(src->acc + col));
-  return make_float2(v.x + fix_to_float(f.x), v.y + fix_to_float(f.y));
-}
-
 __device__ __forceinline__ float2 load2(const float *src, int col) {
   return __ldcg(reinterpret_cast<const float2 *>(src + col));
 }
@@ -394,6 +380,40 @@ __device__ __forceinline__ float2 load2(const Q8Row *src, int col) {
   return make_float2(d * (float)v[col], d * (float)v[col + 1]);
 }
 
+// The N consecutive source columns [col, col + N) of one weight vector as fp32
+// pairs.  An fp32 source comes in 16-byte loads: the lanes of a warp sit one
+// vector (4 or 8 columns) apart, so 8-byte loads would fetch every sector of
+// the vector from L2 two or four times over.  col is a multiple of N, and the
+// vectors are 16-byte aligned.
+template <int N, typename S>
+__device__ __forceinline__ void load_cols(const S *src, int col, float2 (&o)[N / 2]) {
+#pragma unroll
+  for (int e = 0; e < N / 2; ++e) o[e] = load2(src, col + 2 * e);
+}
+template <int N>
+__device__ __forceinline__ void load_cols(const float *src, int col, float2 (&o)[N / 2]) {
+  static_assert(N % 4 == 0, "whole 16-byte vectors");
+#pragma unroll
+  for (int j = 0; j < N / 4; ++j) {
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + col) + j);
+    o[2 * j] = make_float2(v.x, v.y);
+    o[2 * j + 1] = make_float2(v.z, v.w);
+  }
+}
+template <int N>
+__device__ __forceinline__ void load_cols(const __nv_bfloat16 *src, int col, float2 (&o)[N / 2]) {
+  if constexpr (N == 8) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(src + col);
+    o[0] = bf16x2_to_float2(u.x);
+    o[1] = bf16x2_to_float2(u.y);
+    o[2] = bf16x2_to_float2(u.z);
+    o[3] = bf16x2_to_float2(u.w);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N / 2; ++e) o[e] = load2(src, col + 2 * e);
+  }
+}
+
 // xs = src * scale * w (w optional), columns of this lane only.  Every load
 // is issued (from an always-valid address) before any is used, so the lane
 // pays one memory round trip, not one per vector.
@@ -407,10 +427,12 @@ __device__ __forceinline__ void load_slice(XSlice<T, NV> &xs, const S *src, floa
   for (int t = 0; t < NV; ++t) {
     const int v = c * 32 + lane + t * 32 * g.cw;
     const int vc = v < vpr ? v : 0;
+    load_cols<Vec<T>::N>(src, vc * Vec<T>::N, xv[t]);
+    if (w) {
+      load_cols<Vec<T>::N>(w, vc * Vec<T>::N, wv[t]);
+    } else {
 #pragma unroll
-    for (int e = 0; e < P; ++e) {
-      xv[t][e] = load2(src, vc * Vec<T>::N + 2 * e);
-      wv[t][e] = w ? load2(w, vc * Vec<T>::N + 2 * e) : make_float2(1.f, 1.f);
+      for (int e = 0; e < P; ++e) wv[t][e] = make_float2(1.f, 1.f);
     }
   }
 #pragma unroll
@@ -688,8 +710,12 @@ __device__ __forceinline__ void load_weight_slice(XSlice<T, NV> &ws, const float
   for (int t = 0; t < NV; ++t) {
     const int v = c * 32 + lane + t * 32 * g.cw;
     const int vc = v < vpr ? v : 0;
+    if (w) {
+      load_cols<Vec<T>::N>(w, vc * Vec<T>::N, ws.p[t]);
+    } else {
 #pragma unroll
-    for (int e = 0; e < P; ++e) ws.p[t][e] = w ? load2(w, vc * Vec<T>::N + 2 * e) : make_float2(1.f, 1.f);
+      for (int e = 0; e < P; ++e) ws.p[t][e] = make_float2(1.f, 1.f);
+    }
   }
 }
 
@@ -707,8 +733,7 @@ __device__ __forceinline__ void norm_slice(XSlice<T, NV> &xs, const S *src, int 
   for (int t = 0; t < NV; ++t) {
     const int v = c * 32 + lane + t * 32 * g.cw;
     const int vc = v < vpr ? v : 0;
-#pragma unroll
-    for (int e = 0; e < P; ++e) xv[t][e] = load2(src, vc * Vec<T>::N + 2 * e);
+    load_cols<Vec<T>::N>(src, vc * Vec<T>::N, xv[t]);
   }
   float ss = 0.f;
 #pragma unroll

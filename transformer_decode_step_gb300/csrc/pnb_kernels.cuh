@@ -118,7 +118,6 @@ struct ResidArgs {
   Segs s;
   const float *vec;
   float *x;
-  long long *acc;      // attention-output accumulator folded into x (and cleared), or null
   unsigned *work;      // [claim, done] item counters of this launch, zero between launches
   StepIO *io;
   KTrace tr;
@@ -130,7 +129,6 @@ struct GateUpArgs {
   Geom g;
   Segs s;
   const float *x;
-  const long long *acc;  // attention-output accumulator: the residual is x + acc, or null
   const float *norm_w;
   float eps;
   float *h;  // [nseg][n_ff]
@@ -148,7 +146,6 @@ struct DownMoeArgs {
   int n_ff;
   const float *gate;
   float *x;
-  long long *acc;  // attention-output accumulator folded into x (and cleared), or null
   StepIO *io;
   KTrace tr;
 };
@@ -175,7 +172,6 @@ struct RouterArgs {
   const void *w;  // [n_expert][E]
   int n_expert, k, E;
   const float *x;
-  const long long *acc;  // attention-output accumulator: the residual is x + acc, or null
   const float *norm_w;
   float eps;
   int32_t *idx;
@@ -334,83 +330,6 @@ struct BNormArgs {
   BSlot slots[64];         // first layer: the slots of this step
 };
 
-// ------------------------------------------------ fused attention block
-//
-// RMSNorm -> the q / k / v rows of one query head -> RoPE -> KV append ->
-// attention -> that head's column block of the output projection, in one
-// kernel: one thread-block cluster of C CTAs per query head, exchanging the
-// q / k / v results and the softmax partials through distributed shared
-// memory.  The heads' output-projection sums meet in a 64-bit fixed-point
-// accumulator (units of 2^-32) that the next kernels fold into the residual.
-
-constexpr float kFixScale = 4294967296.0f;   // 2^32 accumulator units per 1.0
-constexpr float kFixUnit = 2.3283064365386963e-10f;   // 2^-32
-constexpr float kFixLimit = 1073741824.0f;   // largest |value| one head may add (2^30)
-
-// fp32 value of an accumulator word (exact scaling after one rounding)
-__device__ __forceinline__ float fix_to_float(long long v) { return __ll2float_rn(v) * kFixUnit; }
-
-struct BlockGeom {
-  Geom g;          // the Wqkv rows (K = n_embd): activation slice and dot geometry;
-                   // g.rows_per_stage = rows per ring item
-  int C;           // CTAs per cluster (one cluster per query head)
-  int rows_cta;    // Wqkv rows per CTA: 3 * head_dim / C (q, then k, then v of the head)
-  int kv_item;     // cached positions per ring item (K and V rows)
-  int o_item;      // Wo rows per ring item (height of the 2-D tile)
-  int stage_bytes; // ring slot size (multiple of 1024)
-  int nstages;     // ring slots
-  int smem;        // dynamic shared memory bytes
-};
-
-struct BlockSmem {
-  int ring, part, qkv, wst, apart, ofin, rope, red, bars, total;
-};
-
-// offsets from the 1024-byte aligned base; total includes the alignment slack
-__host__ __device__ inline BlockSmem block_smem(const BlockGeom &b, int hd) {
-  BlockSmem L;
-  L.ring = 0;
-  L.part = b.nstages * b.stage_bytes;
-  L.qkv = align_up(L.part + b.rows_cta * b.g.cw * 4, 16);   // [3][hd] q, k, v of the head
-  L.wst = L.qkv + 3 * hd * 4;                               // [warps][hd + 4] softmax states
-  L.apart = L.wst + 16 * (hd + 4) * 4;                      // [C][hd + 4] the CTAs' partials
-  L.ofin = L.apart + b.C * (hd + 4) * 4;                    // [hd] attention output
-  L.rope = L.ofin + hd * 4;                                 // 64 (cos, sin) pairs
-  L.red = L.rope + 64 * 8;
-  L.bars = L.red + 64 * 4;
-  L.total = L.bars + (2 * b.nstages + 2) * 8 + 1024;
-  return L;
-}
-
-struct BlockArgs {
-  BlockGeom b;
-  int H, Hkv, cap, window;
-  const void *wqkv;        // this layer's [(H + 2 Hkv) hd][n_embd]
-  const float *x;          // residual stream (layers > 0)
-  const void *emb;         // first layer: token embedding table, else null
-  float *x_out;            // first layer: the embedding row is written here
-  int n_vocab;
-  const float *norm_w;
-  float eps;
-  const double *inv_freq;  // [hd / 2]
-  void *k_cache, *v_cache; // this layer's [Hkv][cap][hd]
-  float qscale;            // log2(e) / sqrt(hd)
-  long long *acc;          // [n_embd] attention-output accumulator
-  float *q_out, *o_out;    // [H][hd] rotated queries and attention output (diagnostics)
-  const float *q_in;       // attention + output projection only: [H][hd] rotated queries
-                           // of the QKV kernel, which also stored the current K / V;
-                           // null: the kernel computes q / k / v itself
-  StepIO *io;
-  KTrace tr;
-};
-
-// wo_map: CUtensorMap over this layer's Wo [n_embd][H hd], box {hd, o_item}, no swizzle
-cudaError_t launch_attn_block(int dtype, int head_dim, const void *wo_map, const BlockArgs &a,
-                              cudaStream_t st, bool pdl);
-cudaError_t prepare_attn_block_kernels(int dtype, int smem_bytes);
-// clusters of the block kernel that fit on the GPU at once (0 on error)
-int attn_block_max_clusters(int dtype, int head_dim, const BlockGeom &b, int n_clusters);
-
 struct AttnGeom {
   int stage_pos;  // positions per ring slot
   int nstages;
@@ -444,14 +363,6 @@ int bgemm_smem(int bp, int nstages);
 // sums the K parts of a split QKV / gate-up GEMM and applies its epilogue
 cudaError_t launch_bmerge(const BGemmArgs &a, cudaStream_t st, bool pdl);
 cudaError_t prepare_bgemm_kernels(int smem_bytes);
-
-// persistent step kernel (one cooperative launch per decode step); with
-// prepare = true only sets its shared-memory limit and reports occupancy
-struct StepArgs;
-cudaError_t step_bf16(int hd, int G, const StepArgs &a, int grid, int smem, cudaStream_t st,
-                      bool prepare, int *blocks_per_sm);
-cudaError_t step_f32(int hd, int G, const StepArgs &a, int grid, int smem, cudaStream_t st,
-                     bool prepare, int *blocks_per_sm);
 
 // raise the dynamic shared-memory limit of the kernels a model will launch
 // (outside any stream capture)
