@@ -198,12 +198,16 @@ __device__ __forceinline__ void produce(const Geom &g, const Segs &s, bool summe
 // have returned, each CTA counts itself in work[1]; the last one puts both
 // counters back to zero for the next launch.
 
+// (32-bit arithmetic: a segment has fewer than 2^31 rows; 64-bit divisions
+// are emulated and cost the epilogues, which run on the kernel's tail)
 __device__ __forceinline__ void item_rows(const Geom &g, int64_t rows, int item, int &seg,
                                           int64_t &row0, int &n) {
-  const int ips = (int)((rows + g.rows_per_stage - 1) / g.rows_per_stage);
+  const int rows32 = (int)rows, rps = g.rows_per_stage;
+  const int ips = (rows32 + rps - 1) / rps;
   seg = item / ips;
-  row0 = (int64_t)(item - seg * ips) * g.rows_per_stage;
-  n = (int)((int64_t)g.rows_per_stage < rows - row0 ? (int64_t)g.rows_per_stage : rows - row0);
+  const int r0 = (item - seg * ips) * rps;
+  row0 = r0;
+  n = rps < rows32 - r0 ? rps : rows32 - r0;
 }
 
 __device__ __forceinline__ void finish_claims(unsigned *work) {
@@ -690,11 +694,23 @@ __device__ __forceinline__ void for_claimed_rows(const Geom &g, const Ctx &c, in
   }
 }
 
-__device__ __forceinline__ float item_row_total(const Geom &g, const Ctx &c, int k, int r) {
-  const float *p = c.part + ((size_t)k * g.rows_per_stage + r) * g.cw;
+// The cw per-warp partial sums of one row (16-byte aligned), added in a fixed
+// pairwise order from 16-byte loads: the epilogues run on the kernel's tail,
+// where a serial chain of cw dependent shared-memory loads and adds cost
+// about 3% of a decode step.
+__device__ __forceinline__ float sum_partials(const float *p, int cw) {
+  const float4 *q = reinterpret_cast<const float4 *>(p);
+  auto s4 = [](float4 v) { return (v.x + v.y) + (v.z + v.w); };
+  if (cw == 16) return (s4(q[0]) + s4(q[1])) + (s4(q[2]) + s4(q[3]));
+  if (cw == 8) return s4(q[0]) + s4(q[1]);
+  if (cw == 4) return s4(q[0]);
   float v = 0.f;
-  for (int w = 0; w < g.cw; ++w) v += p[w];
+  for (int w = 0; w < cw; ++w) v += p[w];
   return v;
+}
+
+__device__ __forceinline__ float item_row_total(const Geom &g, const Ctx &c, int k, int r) {
+  return sum_partials(c.part + ((size_t)k * g.rows_per_stage + r) * g.cw, g.cw);
 }
 
 // The multiplier slice of an RMSNorm weight (1 without one): weights do not
@@ -760,9 +776,7 @@ __device__ __forceinline__ void norm_slice(XSlice<T, NV> &xs, const S *src, int 
 }
 
 __device__ __forceinline__ float row_total(const float *part, int local, int cw) {
-  float v = 0.f;
-  for (int w = 0; w < cw; ++w) v += part[local * cw + w];
-  return v;
+  return sum_partials(part + local * cw, cw);
 }
 
 // sin / cos of pos * inv_freq: the angle is formed and reduced to [-pi, pi]
