@@ -409,6 +409,17 @@ int pnb_attention_decode_static(const float *q_dev, const void *k_dev, const voi
    (7 * n_layer + 2) * 256 * 8 words. */
 int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes);
 
+/* Diagnostic: make a bounded device wait run out.  Enqueues one kernel that
+   copies part of the state's workspace into shared memory with a bulk copy,
+   then waits, with a limit of limit_ns (<= 1e9, else PNB_E_INVAL), on an
+   mbarrier that nothing arrives on - the same bounded wait every kernel of
+   the step uses, with a shorter limit.  When it gives up, the kernel sets
+   PNB_DEV_ERR_TIMEOUT in the state's error word (pnb_state_check; a later
+   pnb_forward_poll on the state answers PNB_E_DEVICE), waits for its copy to
+   land and returns, so the context stays usable; pnb_state_reset clears the
+   word.  The KV cache and activations are not touched. */
+int pnb_state_wait_probe(pnb_state *s, uint64_t limit_ns, pnb_stream stream);
+
 const char *pnb_strerror(int code);
 
 #ifdef __cplusplus

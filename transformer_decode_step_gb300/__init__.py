@@ -90,6 +90,7 @@ _SIGS = {
     "pnb_state_set_trace": (_i32, [_p, _p, _sz]),
     "pnb_attention_decode_static": (_i32, [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                            _p, _p, _p]),
+    "pnb_state_wait_probe": (_i32, [_p, ctypes.c_uint64, _p]),
     "pnb_strerror": (ctypes.c_char_p, [_i32]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -305,6 +306,10 @@ class State:
         if rc not in (0, -8):
             check(rc, "pnb_state_check")
         return e.value
+
+    def wait_probe(self, limit_ns: int, stream=None):
+        """Make one bounded device wait run out after limit_ns (pnb_state_wait_probe)."""
+        check(pnb_state_wait_probe(self._h, limit_ns, _stream(stream)), "pnb_state_wait_probe")
 
     def run_kernel(self, kind: int, layer: int, stream=None):
         """One kernel of the step in isolation (pnb_step_kernel)."""

@@ -1461,6 +1461,19 @@ int pnb_state_set_trace(pnb_state *s, uint64_t *trace_dev, size_t bytes) {
   return PNB_OK;
 }
 
+int pnb_state_wait_probe(pnb_state *s, uint64_t limit_ns, pnb_stream stream) {
+  if (!s) return PNB_E_NULL;
+  if (limit_ns > 1000000000ull) return PNB_E_INVAL;
+  int rc = check_device(s->m);
+  if (rc != PNB_OK) return rc;
+  // the copy reads the state's own residual buffer (n_embd fp32, a multiple of 32 bytes)
+  const uint32_t bytes = (uint32_t)std::min<size_t>((size_t)s->m->cfg.n_embd * 4, kWaitProbeBytes);
+  if (launch_wait_probe(s->x, bytes, limit_ns, s->io, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return PNB_E_CUDA;
+  return PNB_OK;
+}
+
 int pnb_state_activations(const pnb_state *s, pnb_activations *out) {
   if (!s || !out) return PNB_E_NULL;
   out->x = s->x;

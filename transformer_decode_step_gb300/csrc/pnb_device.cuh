@@ -84,16 +84,22 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity
 }
 
 // Wait for the phase with the given parity to complete; gives up after about
-// kWaitLimitNs (or 2^26 polls) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// limit_ns (or 2^26 polls) and returns false.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
-      if (global_ns() - t0 > kWaitLimitNs || it > (1u << 26)) return false;
+      if (global_ns() - t0 > limit_ns || it > (1u << 26)) return false;
     }
   }
+}
+
+// The kernels' bounded wait: gives up after about kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // 1-D bulk copy global -> shared, completion counted on an mbarrier (TMA).

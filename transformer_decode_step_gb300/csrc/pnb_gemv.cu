@@ -310,6 +310,26 @@ __global__ void k_prefill_end(StepIO *state, const StepIO *pio, int n) {
   if (e) set_error(&state->error, e);
 }
 
+// A bounded wait that runs out, the way any of the kernels' waits would: one
+// thread copies `bytes` of src into shared memory with a bulk copy, then waits
+// with a limit of limit_ns on an mbarrier that nothing arrives on.  When the
+// wait gives up it sets the timeout bit in the state's error word, waits (with
+// the normal limit) for its copy to land, and returns: the kernel ends with no
+// copy in flight and the context stays usable.
+__global__ void k_wait_probe(const uint8_t *src, uint32_t bytes, unsigned long long limit_ns,
+                             StepIO *io) {
+  __shared__ __align__(128) uint8_t buf[kWaitProbeBytes];
+  __shared__ uint64_t full, never;
+  if (threadIdx.x != 0) return;
+  mbar_init(&full, 1);
+  mbar_init(&never, 1);
+  fence_barrier_init();
+  mbar_arrive_expect_tx(&full, bytes);
+  bulk_g2s(buf, src, bytes, &full);
+  if (!mbar_wait_for(&never, 0u, limit_ns)) set_error(&io->error, kErrTimeout);
+  if (!mbar_wait(&full, 0u)) set_error(&io->error, kErrTimeout);
+}
+
 __global__ void k_set_token(StepIO *io, int32_t token) { io->token = token; }
 __global__ void k_copy_token(StepIO *io, const int32_t *token) { io->token = *token; }
 __global__ void k_set_pos(StepIO *io, int32_t pos) { io->pos = pos; }
@@ -415,6 +435,11 @@ cudaError_t launch_prefill_begin(StepIO *pio, const StepIO *state, int n, cudaSt
 }
 cudaError_t launch_prefill_end(StepIO *state, const StepIO *pio, int n, cudaStream_t st) {
   k_prefill_end<<<1, 32, 0, st>>>(state, pio, n);
+  return cudaGetLastError();
+}
+cudaError_t launch_wait_probe(const void *src, uint32_t bytes, unsigned long long limit_ns, StepIO *io,
+                              cudaStream_t st) {
+  k_wait_probe<<<1, 32, 0, st>>>(static_cast<const uint8_t *>(src), bytes, limit_ns, io);
   return cudaGetLastError();
 }
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st) {

@@ -348,6 +348,12 @@ cudaError_t launch_router(int dtype, const RouterArgs &a, cudaStream_t st, bool 
 cudaError_t launch_attn(int dtype, int head_dim, const AttnArgs &a, const AttnGeom &ag,
                         cudaStream_t st, bool pdl);
 cudaError_t launch_set_token(StepIO *io, int32_t token, cudaStream_t st);
+// diagnostic: a bounded wait on an mbarrier nothing arrives on, after a bulk
+// copy of bytes (multiple of 16, <= kWaitProbeBytes) from src; sets the
+// timeout bit in io->error when the wait gives up
+constexpr int kWaitProbeBytes = 4096;
+cudaError_t launch_wait_probe(const void *src, uint32_t bytes, unsigned long long limit_ns, StepIO *io,
+                              cudaStream_t st);
 cudaError_t launch_set_pos(StepIO *io, int32_t pos, cudaStream_t st);
 cudaError_t launch_copy_token(StepIO *io, const int32_t *token, cudaStream_t st);
 // prefill chunk of n <= 64 virtual slots: pio[b] = {pos: state->pos + b}; then
