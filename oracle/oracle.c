@@ -34,8 +34,10 @@
  * and rounded once to fp32.  Weights and the KV cache hold their storage type
  * (fp32, or bf16 values widened exactly to fp32; Q8 weights are their
  * block's fp16 scale times the int8 value, the dequantization of a GGUF
- * Q8_0 block: "Engine Architecture", "Weight Loading Modes", quantized mode,
- * per-block dequantization inside the matvec - exact in fp32).  New K/V
+ * Q8_0 block, and Q4 weights the scale times the 4-bit code less 8, that of
+ * a GGUF Q4_0 block: "Engine Architecture", "Weight Loading Modes",
+ * quantized mode, per-block dequantization inside the matvec - exact in
+ * fp32).  New K/V
  * entries are rounded fp32 -> bf16 (nearest even) before they are stored when the cache
  * is bf16; the argmax is taken over the fp32 logits, lowest id on ties.
  */
@@ -56,7 +58,8 @@ typedef struct {
   int32_t expert_count;   /* 0 = dense FFN */
   int32_t expert_used;    /* top-k */
   int32_t dtype;          /* storage of weights: 0 fp32, 1 bf16, 2 Q8 (blocks of 32: int8
-                             values times an fp16 scale); KV: fp32 for 0, bf16 otherwise */
+                             values times an fp16 scale), 3 Q4 (blocks of 32: 4-bit codes
+                             less 8 times an fp16 scale); KV: fp32 for 0, bf16 otherwise */
   int32_t qkv_bias;       /* 1: bias vectors added to q, k, v (Qwen2) */
   int32_t rope_neox;      /* 1: RoPE pairs dimension i with i + hd/2 (Phi-3) */
 } orc_config;
@@ -141,6 +144,17 @@ static void get_row(const orc_tensor *t, int64_t r, int64_t cols, int dtype, flo
       synth_q8_block(t->key, base + (uint64_t)b, t->sigma, q, &d);
       const float df = synth_f16_to_f32(d);
       for (int j = 0; j < SYNTH_Q8_BLOCK; ++j) out[b + j] = df * (float)q[j];
+    }
+  } else if (t->mode == ORC_SYNTH && dtype == SYNTH_Q4) {
+    /* Q4 weights: per block of 32, the weight is the block's fp16 scale
+       times the element's 4-bit code less 8 (GGUF Q4_0 dequantization) */
+    const uint64_t base = (uint64_t)(r * cols);
+    for (int64_t b = 0; b + SYNTH_Q4_BLOCK <= cols; b += SYNTH_Q4_BLOCK) {
+      uint8_t u[SYNTH_Q4_BLOCK];
+      uint16_t d;
+      synth_q4_block(t->key, base + (uint64_t)b, t->sigma, u, &d);
+      const float df = synth_f16_to_f32(d);
+      for (int j = 0; j < SYNTH_Q4_BLOCK; ++j) out[b + j] = df * (float)((int)u[j] - 8);
     }
   } else if (t->mode == ORC_SYNTH) {
     const uint64_t base = (uint64_t)(r * cols);

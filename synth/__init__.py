@@ -19,7 +19,7 @@ _DIR = os.path.dirname(os.path.abspath(__file__))
 HOST_LIB = os.path.join(_DIR, "libsynth_host.so")
 CUDA_LIB = os.path.join(_DIR, "libsynth_cuda.so")
 
-F32, BF16, Q8 = 0, 1, 2
+F32, BF16, Q8, Q4 = 0, 1, 2, 3
 
 TOK_EMBD, ATTN_NORM, WQ, WK, WV, WO, FFN_NORM = 1, 2, 3, 4, 5, 6, 7
 WGATE, WUP, WDOWN, WROUTER, OUT_NORM, OUTPUT = 8, 9, 10, 11, 12, 13
@@ -59,6 +59,7 @@ def _host():
         lib.synth_host_f32_to_bf16.restype = ctypes.c_uint16
         lib.synth_host_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.synth_host_fill_q8_rows.argtypes = [p, p, u64, i64, i64, i64, ctypes.c_float]
+        lib.synth_host_fill_q4_rows.argtypes = [p, p, u64, i64, i64, i64, ctypes.c_float]
         lib.synth_host_f32_to_f16.restype = ctypes.c_uint16
         lib.synth_host_f32_to_f16.argtypes = [ctypes.c_float]
         lib.synth_host_f16_to_f32.restype = ctypes.c_float
@@ -143,6 +144,16 @@ def q8_rows(k: int, row0: int, nrows: int, cols: int, sigma: float):
     raw = np.empty((nrows, cols + cols // 16), dtype=np.uint8)
     w = np.empty((nrows, cols), dtype=np.float32)
     _host().synth_host_fill_q8_rows(raw.ctypes.data, w.ctypes.data, k, row0, nrows, cols, sigma)
+    return raw, w
+
+
+def q4_rows(k: int, row0: int, nrows: int, cols: int, sigma: float):
+    """Q4 rows [row0, row0 + nrows) of a [.][cols] matrix: (the row bytes in the
+    library's layout, uint8 [nrows][cols / 2 + cols / 16]; the weights d * (u - 8),
+    fp32)."""
+    raw = np.empty((nrows, cols // 2 + cols // 16), dtype=np.uint8)
+    w = np.empty((nrows, cols), dtype=np.float32)
+    _host().synth_host_fill_q4_rows(raw.ctypes.data, w.ctypes.data, k, row0, nrows, cols, sigma)
     return raw, w
 
 

@@ -40,9 +40,9 @@
 
 #define SYNTH_GAMMA 0x9E3779B97F4A7C15ULL
 
-/* storage types of generated values (SYNTH_Q8: weight matrices only, in
-   blocks of 32 along a row; see synth_q8_block) */
-enum { SYNTH_F32 = 0, SYNTH_BF16 = 1, SYNTH_Q8 = 2 };
+/* storage types of generated values (SYNTH_Q8, SYNTH_Q4: weight matrices
+   only, in blocks of 32 along a row; see synth_q8_block, synth_q4_block) */
+enum { SYNTH_F32 = 0, SYNTH_BF16 = 1, SYNTH_Q8 = 2, SYNTH_Q4 = 3 };
 
 /* logical tensor kinds (part of a stream key) */
 enum {
@@ -189,6 +189,39 @@ SYNTH_FN void synth_q8_block(uint64_t key, uint64_t idx0, float sigma, int8_t *q
 /* bytes of one Q8 row of `cols` weights: the int8 values, then one fp16
    scale per 32 (the layout of the decode-step library's Q8 matrices) */
 SYNTH_FN int64_t synth_q8_row_bytes(int64_t cols) { return cols + cols / 16; }
+
+/* Q4 weights, in blocks of 32 consecutive elements of a row (element indices
+   idx0 .. idx0 + 31, idx0 a multiple of 32): w_i are the generated fp32
+   values; the block's scale is d = fp16(max_i |w_i| / 7) (one fp32 division,
+   one rounding to fp16, nearest even); the 4-bit code of element i is
+   u_i = clamp(rint(w_i / float(d)), -8, 7) + 8 in [0, 15] (ties to even; all
+   8 when d is 0).  The element's weight is float(d) * (u_i - 8), exact in
+   fp32 (the GGUF Q4_0 block: 32 codes and one fp16 scale). */
+#define SYNTH_Q4_BLOCK 32
+SYNTH_FN void synth_q4_block(uint64_t key, uint64_t idx0, float sigma, uint8_t *u, uint16_t *d_out) {
+  float w[SYNTH_Q4_BLOCK];
+  float amax = 0.0f;
+  for (int i = 0; i < SYNTH_Q4_BLOCK; ++i) {
+    w[i] = synth_normal_f32(key, idx0 + (uint64_t)i, sigma);
+    const float a = w[i] < 0.0f ? -w[i] : w[i];
+    if (a > amax) amax = a;
+  }
+  const uint16_t d = synth_f32_to_f16(amax / 7.0f);
+  const float df = synth_f16_to_f32(d);
+  for (int i = 0; i < SYNTH_Q4_BLOCK; ++i) {
+    float r = df > 0.0f ? rintf(w[i] / df) : 0.0f;
+    if (r > 7.0f) r = 7.0f;
+    if (r < -8.0f) r = -8.0f;
+    u[i] = (uint8_t)((int)r + 8);
+  }
+  *d_out = d;
+}
+
+/* bytes of one Q4 row of `cols` weights: the 4-bit codes, two per byte
+   (byte j holds element 2j in its low and element 2j + 1 in its high
+   nibble), then one fp16 scale per 32 (the layout of the decode-step
+   library's Q4 matrices) */
+SYNTH_FN int64_t synth_q4_row_bytes(int64_t cols) { return cols / 2 + cols / 16; }
 
 /* uniform integer in [lo, lo + n) for element idx (multiply-shift on 32 high bits) */
 SYNTH_FN int64_t synth_uniform_int(uint64_t key, uint64_t idx, int64_t lo, uint32_t n) {

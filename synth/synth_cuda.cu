@@ -50,6 +50,25 @@ __global__ void fill_q8_kernel(uint8_t *dst, int64_t dst_row0, int64_t dst_row_s
   }
 }
 
+/* Q4: one thread per 32-element block; logical row r goes to device row
+   dst_row0 + r*dst_row_step of synth_q4_row_bytes(cols) bytes */
+__global__ void fill_q4_kernel(uint8_t *dst, int64_t dst_row0, int64_t dst_row_step, int64_t rows,
+                               int64_t cols, uint64_t key, float sigma) {
+  const int64_t nb = cols / SYNTH_Q4_BLOCK, n = rows * nb;
+  const int64_t rb = synth_q4_row_bytes(cols);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / nb, b = i - r * nb;
+    uint8_t u[SYNTH_Q4_BLOCK];
+    uint16_t d;
+    synth_q4_block(key, (uint64_t)(r * cols + b * SYNTH_Q4_BLOCK), sigma, u, &d);
+    uint8_t *row = dst + (dst_row0 + r * dst_row_step) * rb;
+    for (int j = 0; j < SYNTH_Q4_BLOCK; j += 2)
+      row[(b * SYNTH_Q4_BLOCK + j) / 2] = (uint8_t)(u[j] | (u[j + 1] << 4));
+    reinterpret_cast<uint16_t *>(row + cols / 2)[b] = d;
+  }
+}
+
 __global__ void fill_const_kernel(void *dst, int dtype, int64_t n, float value) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -102,6 +121,12 @@ int synth_dev_fill_matrix(void *dst, int dtype, int64_t dst_row0, int64_t dst_ro
   if (dtype == SYNTH_Q8) {
     if (cols % SYNTH_Q8_BLOCK) return (int)cudaErrorInvalidValue;
     fill_q8_kernel<<<grid_for(rows * (cols / SYNTH_Q8_BLOCK)), 256, 0, stream>>>(
+        static_cast<uint8_t *>(dst), dst_row0, dst_row_step, rows, cols, key, sigma);
+    return (int)cudaGetLastError();
+  }
+  if (dtype == SYNTH_Q4) {
+    if (cols % SYNTH_Q4_BLOCK) return (int)cudaErrorInvalidValue;
+    fill_q4_kernel<<<grid_for(rows * (cols / SYNTH_Q4_BLOCK)), 256, 0, stream>>>(
         static_cast<uint8_t *>(dst), dst_row0, dst_row_step, rows, cols, key, sigma);
     return (int)cudaGetLastError();
   }

@@ -63,5 +63,31 @@ void synth_host_fill_q8_rows(uint8_t *out_rows, float *out_f32, uint64_t key, in
     }
 }
 
+/* Q4 rows [row0, row0 + nrows) of a [.][cols] matrix (cols a multiple of 32):
+   the library's row layout (cols / 2 bytes of 4-bit codes, two per byte,
+   then cols / 32 fp16 scales) into out_rows (nrows * synth_q4_row_bytes(cols)
+   bytes), and, if out_f32 is given, the weights float(d) * (u - 8) as fp32 */
+void synth_host_fill_q4_rows(uint8_t *out_rows, float *out_f32, uint64_t key, int64_t row0,
+                             int64_t nrows, int64_t cols, float sigma) {
+  const int64_t rb = synth_q4_row_bytes(cols), nb = cols / SYNTH_Q4_BLOCK;
+  for (int64_t r = 0; r < nrows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      uint8_t u[SYNTH_Q4_BLOCK];
+      uint16_t d;
+      synth_q4_block(key, (uint64_t)((row0 + r) * cols + b * SYNTH_Q4_BLOCK), sigma, u, &d);
+      if (out_rows) {
+        uint8_t *row = out_rows + r * rb;
+        for (int j = 0; j < SYNTH_Q4_BLOCK; j += 2)
+          row[(b * SYNTH_Q4_BLOCK + j) / 2] = (uint8_t)(u[j] | (u[j + 1] << 4));
+        memcpy(row + cols / 2 + 2 * b, &d, 2);
+      }
+      if (out_f32) {
+        const float df = synth_f16_to_f32(d);
+        for (int j = 0; j < SYNTH_Q4_BLOCK; ++j)
+          out_f32[r * cols + b * SYNTH_Q4_BLOCK + j] = df * (float)((int)u[j] - 8);
+      }
+    }
+}
+
 uint16_t synth_host_f32_to_f16(float f) { return synth_f32_to_f16(f); }
 float synth_host_f16_to_f32(uint16_t h) { return synth_f16_to_f32(h); }

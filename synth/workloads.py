@@ -6,7 +6,7 @@ decoder with a 4096-position sliding window, a Mixtral-shaped 8-expert top-2
 MoE decoder and a Llama-8B-shaped batched-slot decoder.  The recipe:
 
 * weights (embeddings, projections, router, LM head) ~ N(0, 0.02^2), stored in
-  the model's dtype (Q8: blocks of 32 quantized as the generator defines);
+  the model's dtype (Q8, Q4: blocks of 32 quantized as the generator defines);
   q / k / v biases (models with qkv_bias) ~ N(0, 0.5^2), fp32;
   every norm weight is 1.0 (fp32);
 * the KV cache of positions below the start position ~ N(0, 1) in the cache
@@ -20,7 +20,7 @@ from __future__ import annotations
 from dataclasses import dataclass, field, replace
 from typing import List, Optional
 
-from . import (ATTN_NORM, BF16, BK, BQ, BV, F32, FFN_NORM, OUT_NORM, OUTPUT, POSITIONS, Q8,
+from . import (ATTN_NORM, BF16, BK, BQ, BV, F32, FFN_NORM, OUT_NORM, OUTPUT, POSITIONS, Q4, Q8,
                TOK_EMBD, TOKENS, WDOWN, WGATE, WK, WO, WQ, WROUTER, WUP, WV, key, uniform_int)
 
 WEIGHT_SIGMA = 0.02
@@ -60,7 +60,7 @@ class Shape:
 
     @property
     def elem_bytes(self) -> int:
-        """Bytes of one KV-cache element (bf16 for bf16 and Q8 weights)."""
+        """Bytes of one KV-cache element (bf16 for bf16, Q8 and Q4 weights)."""
         return 4 if self.dtype == F32 else 2
 
     @property
@@ -72,11 +72,13 @@ class Shape:
         cols int8 values, then one fp16 scale per 32)."""
         if self.dtype == Q8:
             return rows * (cols + cols // 16)
+        if self.dtype == Q4:
+            return rows * (cols // 2 + cols // 16)
         return rows * cols * (4 if self.dtype == F32 else 2)
 
     @property
     def weight_bytes_per_param(self) -> float:
-        return {F32: 4.0, BF16: 2.0, Q8: 1.0625}[self.dtype]
+        return {F32: 4.0, BF16: 2.0, Q8: 1.0625, Q4: 0.5625}[self.dtype]
 
     def params_read_per_token(self) -> int:
         """Weight elements one decode step reads (top-k experts only for MoE)."""
@@ -139,7 +141,11 @@ LLAMA8B_BATCHED = Workload(
 LLAMA7B_Q8 = Workload("llama7b_q8_0", replace(LLAMA7B.shape, dtype=Q8), seed=2, prefill=2048,
                       steps=128)
 
-ALL = [TINY, LLAMA7B, MISTRAL7B, MIXTRAL, LLAMA8B_BATCHED, LLAMA7B_Q8]
+# the same with GGUF Q4_0-style weights (blocks of 32 4-bit codes and an fp16 scale)
+LLAMA7B_Q4 = Workload("llama7b_q4_0", replace(LLAMA7B.shape, dtype=Q4), seed=2, prefill=2048,
+                      steps=128)
+
+ALL = [TINY, LLAMA7B, MISTRAL7B, MIXTRAL, LLAMA8B_BATCHED, LLAMA7B_Q8, LLAMA7B_Q4]
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -623,6 +623,55 @@ def test_q8_model_is_the_model_of_its_dequantized_weights():
         assert np.array_equal(x, y)
 
 
+# ------------------------------------------------------------------ Q4 weights
+
+@pytest.mark.parametrize("cols,sigma", [(64, 0.02), (256, 1.0), (96, 3e-4)])
+def test_q4_blocks_follow_their_definition(cols, sigma):
+    """Each block of 32: d = fp16(max|w| / 7), code u = clip(rint(w / d), -8, 7) + 8, two
+    codes per byte (element 2j in the low nibble of byte j), the scales after the codes;
+    the weight is d * (u - 8), recomputed here with numpy; an unclamped weight is within
+    d / 2 of w (sigma 3e-4 gives subnormal fp16 scales)."""
+    k = synth.key(5, synth.WQ, 3, 0)
+    rows = 6
+    raw, deq = synth.q4_rows(k, 2, rows, cols, sigma)
+    assert raw.shape == (rows, cols // 2 + cols // 16)
+    for r in range(rows):
+        w = synth.values(k, (2 + r) * cols, cols, sigma, F32)
+        packed = raw[r, :cols // 2]
+        u = np.empty(cols, dtype=np.int32)
+        u[0::2] = packed & 0xF
+        u[1::2] = packed >> 4
+        d = raw[r, cols // 2:].view(np.uint16)
+        for b in range(cols // 32):
+            wb = w[32 * b:32 * b + 32]
+            dw = (np.float32(np.max(np.abs(wb))) / np.float32(7)).astype(np.float16)
+            assert d[b] == dw.view(np.uint16)
+            df = np.float32(dw)
+            qw = np.clip(np.rint(wb / df), -8, 7).astype(np.int32)
+            assert np.array_equal(u[32 * b:32 * b + 32], qw + 8)
+            assert np.array_equal(deq[r, 32 * b:32 * b + 32], df * qw.astype(np.float32))
+            inner = (qw > -8) & (qw < 7)
+            assert np.all(np.abs(wb - df * qw)[inner] <= 0.5 * df * (1 + 2.0 ** -9))
+            if df >= 2.0 ** -14:   # normal fp16 scale: the largest value uses the range
+                assert np.max(np.abs(qw)) >= 6
+
+
+def test_q4_model_is_the_model_of_its_dequantized_weights():
+    """A seeded Q4 oracle model equals the bf16-cache model given d * (u - 8) explicitly."""
+    shape = dataclasses.replace(TS, dtype=synth.Q4, n_embd=64, n_head=4, n_kv_head=2, n_ff=96)
+    arrays = {}
+    for spec in wl.weight_specs(shape):
+        k = spec.name if spec.name in ("tok_embd", "out_norm", "output") else (spec.name, spec.layer, spec.sub)
+        if spec.const is None:
+            arrays[k] = synth.q4_rows(spec.key(11), 0, spec.rows, spec.cols, wl.WEIGHT_SIGMA)[1]
+    a, _ = _oracle_run(dataclasses.replace(shape, dtype=BF16), arrays, [1, 2, 3])
+    m = oracle.Model(shape, seed=11)
+    s = m.new_state()
+    b = [s.forward(t)[0] for t in [1, 2, 3]]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
 # ------------------------------------------------------------------ sampling
 
 def test_sample_uniform_is_splitmix64_published_sequence():
