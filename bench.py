@@ -258,7 +258,7 @@ def workload_config(w, extra=None, batch=None):
                        + (f" window{s.sliding_window}" if s.sliding_window else "")
                        + (f" experts{s.expert_count}top{s.expert_used}" if s.expert_count else "")
                        + f", KV pre-filled to {w.prefill}, greedy decode of {w.steps} tokens, batch {batch}",
-           "batch": batch, "weights_dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype],
+           "batch": batch, "weights_dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_0"}[s.dtype],
            "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)"
                  if s.params_read_per_token() * s.weight_bytes_per_param > 129e6 else
                  "weights fit in L2 and stay resident between steps, as in a real decode loop "
@@ -461,7 +461,7 @@ def run_ours(args, w):
         line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": {0: "f32", 1: "bf16", 2: "q8_0"}[s.dtype], "data": "synthetic (seeded generated weights and KV cache)",
+                "dtype": {0: "f32", 1: "bf16", 2: "q8_0", 3: "q4_0"}[s.dtype], "data": "synthetic (seeded generated weights and KV cache)",
                 "config": arm_config(args, w, world),
                 "hbm_gbs_step": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                 "hbm_frac_of_measured": step_gbs / peaks["hbm_gbs"],

@@ -48,8 +48,12 @@ typedef struct CUstream_st *pnb_stream;
    Architecture", "Weight Loading Modes": weights stay in their GGUF blocks
    and are dequantized per block inside the matvec), with GGUF Q8_0 blocks of
    32 int8 values and one fp16 scale (weight = scale * value), stored per row
-   as all K values followed by the row's K / 32 scales (K + K / 16 bytes). */
-enum { PNB_F32 = 0, PNB_BF16 = 1, PNB_Q8_0 = 2 };
+   as all K values followed by the row's K / 32 scales (K + K / 16 bytes).
+   PNB_Q4_0: the same mode with GGUF Q4_0 blocks of 32 4-bit codes u and one
+   fp16 scale (weight = scale * (u - 8)), stored per row as K / 2 bytes of
+   codes (byte j holds code 2j in its low and code 2j + 1 in its high nibble)
+   followed by the row's K / 32 scales (K / 2 + K / 16 bytes). */
+enum { PNB_F32 = 0, PNB_BF16 = 1, PNB_Q8_0 = 2, PNB_Q4_0 = 3 };
 
 enum {
   PNB_OK = 0,
@@ -96,7 +100,7 @@ typedef struct {
   int32_t sliding_window; /* 0 = attend to every position */
   int32_t expert_count;   /* 0 = dense SwiGLU FFN */
   int32_t expert_used;    /* top-k experts per token when expert_count > 0 */
-  int32_t dtype;          /* PNB_F32, PNB_BF16 or PNB_Q8_0: weights (KV: fp32 / bf16 / bf16) */
+  int32_t dtype;          /* PNB_F32, PNB_BF16, PNB_Q8_0 or PNB_Q4_0: weights (KV: fp32, else bf16) */
   int32_t rope_neox;      /* 0 Llama-style RoPE, 1 NeoX-style (see above) */
 } pnb_config;
 
@@ -141,7 +145,7 @@ typedef struct pnb_state pnb_state;
    forward, "Architecture registry").  Checks: n_embd = n_head * head_dim,
    head_dim even and in {32, 64, 128}, n_head % n_kv_head == 0, n_embd and
    n_ff multiples of 8, 0 < expert_used <= expert_count <= 64 when MoE,
-   pointer non-NULL and 16-byte aligned.  PNB_Q8_0 needs n_embd and n_ff
+   pointer non-NULL and 16-byte aligned.  PNB_Q8_0 and PNB_Q4_0 need n_embd and n_ff
    multiples of 256 (whole 16-byte vectors per row) and a dense FFN
    (PNB_E_UNSUPPORTED otherwise); its models run the single-sequence step
    only (no batched form; pnb_prefill goes one token per step).  *out is set on success. */

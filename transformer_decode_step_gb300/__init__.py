@@ -19,7 +19,7 @@ if not os.path.exists(LIB):
 
 _lib = ctypes.CDLL(LIB)
 
-PNB_F32, PNB_BF16, PNB_Q8_0 = 0, 1, 2
+PNB_F32, PNB_BF16, PNB_Q8_0, PNB_Q4_0 = 0, 1, 2, 3
 PNB_TOKEN_PREV = -1
 PNB_DEV_ERR_TOKEN, PNB_DEV_ERR_TIMEOUT = 1, 2
 (PNB_KERNEL_QKV, PNB_KERNEL_ATTN, PNB_KERNEL_OPROJ, PNB_KERNEL_ROUTER, PNB_KERNEL_GATE_UP,

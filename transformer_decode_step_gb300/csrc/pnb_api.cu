@@ -45,13 +45,15 @@ int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // rows_total: rows over all segments; nseg: segments concatenated in it (0 when
 // the launch sums its segments into the same rows: static row ranges).
-// wt: weight storage type (PNB_F32, PNB_BF16 or PNB_Q8_0)
+// wt: weight storage type (PNB_F32, PNB_BF16, PNB_Q8_0 or PNB_Q4_0)
 Geom plan_gemv(int K, int wt, int64_t rows_total, int row_align, int nsum, int grid, int nseg) {
   Geom g{};
   g.K = K;
-  g.es = wt == PNB_Q8_0 ? 1 : (wt == PNB_BF16 ? 2 : 4);
-  g.row_bytes = wt == PNB_Q8_0 ? K + K / 16 : K * g.es;   // Q8: the values, then fp16 scales
-  g.vpr = wt == PNB_Q8_0 ? K / 8 : g.row_bytes / 16;   // Q8: 8-byte vectors of values
+  const bool q = wt == PNB_Q8_0 || wt == PNB_Q4_0;
+  g.es = q ? 1 : (wt == PNB_BF16 ? 2 : 4);
+  // Q8: the values, then fp16 scales; Q4: the codes, two per byte, then the scales
+  g.row_bytes = wt == PNB_Q8_0 ? K + K / 16 : (wt == PNB_Q4_0 ? K / 2 + K / 16 : K * g.es);
+  g.vpr = q ? K / 8 : g.row_bytes / 16;   // Q8: 8-byte, Q4: 4-byte vectors of 8 values
   int rps = 1;
   const int target = g.row_bytes > kLongRowBytes ? kLongRowStage : kStageTarget;
   while (rps * 2 <= 64 && rps * 2 * g.row_bytes <= target) rps *= 2;
@@ -98,7 +100,7 @@ struct pnb_model {
   pnb_config cfg;
   int device = 0, num_sms = 0, grid = 0;
   int hd = 0, n_sets = 0, qkv_rows = 0, cap = 0;
-  int kv_es = 0;                         // KV-cache element bytes (bf16 for bf16 and Q8 weights)
+  int kv_es = 0;                         // KV-cache element bytes (bf16 for bf16, Q8 and Q4 weights)
   int kv_dt = 0;                         // KV-cache element type (PNB_F32 or PNB_BF16)
   const void *tok_embd = nullptr;
   const float *out_norm = nullptr;
@@ -199,10 +201,12 @@ int validate_config(const pnb_config *c) {
   if (hd != 32 && hd != 64 && hd != 128) return PNB_E_UNSUPPORTED;
   if (c->n_embd % 8 || c->n_ff % 8) return PNB_E_INVAL;
   if (c->sliding_window < 0 || !(c->rope_theta > 0.0) || !(c->rms_norm_eps >= 0.0)) return PNB_E_INVAL;
-  if (c->dtype != PNB_F32 && c->dtype != PNB_BF16 && c->dtype != PNB_Q8_0) return PNB_E_INVAL;
-  // Q8 rows (K values, then K / 32 fp16 scales) are whole 16-byte vectors;
+  if (c->dtype != PNB_F32 && c->dtype != PNB_BF16 && c->dtype != PNB_Q8_0 && c->dtype != PNB_Q4_0)
+    return PNB_E_INVAL;
+  // Q8 / Q4 rows (the values, then K / 32 fp16 scales) are whole 16-byte vectors;
   // MoE models keep fp32 / bf16 weights
-  if (c->dtype == PNB_Q8_0 && (c->n_embd % 256 || c->n_ff % 256 || c->expert_count > 0))
+  if ((c->dtype == PNB_Q8_0 || c->dtype == PNB_Q4_0) &&
+      (c->n_embd % 256 || c->n_ff % 256 || c->expert_count > 0))
     return PNB_E_UNSUPPORTED;
   if (c->expert_count < 0 || c->expert_count > 64) return PNB_E_INVAL;
   if (c->expert_count > 0 &&

@@ -225,13 +225,22 @@ __device__ __forceinline__ float round_to(float v) {
 // block of 32 consecutive values); weight k = scale[k / 32] * value[k].
 struct Q8 {};
 
-// KV-cache element type of a model with weights of type T (bf16 for Q8)
+// Tag type of Q4 weight rows: K / 2 bytes of 4-bit codes (byte j holds code
+// 2j in its low and code 2j + 1 in its high nibble), then K / 32 fp16 scales;
+// weight k = scale[k / 32] * (code[k] - 8).
+struct Q4 {};
+
+// KV-cache element type of a model with weights of type T (bf16 for Q8, Q4)
 template <typename T>
 struct KvOf {
   using type = T;
 };
 template <>
 struct KvOf<Q8> {
+  using type = __nv_bfloat16;
+};
+template <>
+struct KvOf<Q4> {
   using type = __nv_bfloat16;
 };
 

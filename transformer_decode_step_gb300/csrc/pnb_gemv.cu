@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
     if constexpr (std::is_same<T, Q8>::value) {
       const Q8Row row{static_cast<const uint8_t *>(a.emb) + (int64_t)tok * a.g.row_bytes, a.g.K};
       embed(&row);
+    } else if constexpr (std::is_same<T, Q4>::value) {
+      const Q4Row row{static_cast<const uint8_t *>(a.emb) + (int64_t)tok * a.g.row_bytes, a.g.K};
+      embed(&row);
     } else {
       embed(static_cast<const T *>(a.emb) + (int64_t)tok * a.g.K);
     }
@@ -371,7 +374,7 @@ cudaError_t prepare_nv(int bytes) {
   if ((e = ensure_smem(k_qkv<T, NV>, bytes)) != cudaSuccess) return e;
   if ((e = ensure_smem(k_resid<T, NV>, bytes)) != cudaSuccess) return e;
   if ((e = ensure_smem(k_gateup<T, NV>, bytes)) != cudaSuccess) return e;
-  if constexpr (!std::is_same<T, Q8>::value)   // MoE: fp32 / bf16 weights
+  if constexpr (!std::is_same<T, Q8>::value && !std::is_same<T, Q4>::value)   // MoE: fp32 / bf16
     if ((e = ensure_smem(k_down_moe<T, NV>, bytes)) != cudaSuccess) return e;
   return ensure_smem(k_lmhead<T, NV>, bytes);
 }
@@ -382,14 +385,15 @@ cudaError_t prepare_t(int bytes) {
   if ((e = prepare_nv<T, 1>(bytes)) != cudaSuccess) return e;
   if ((e = prepare_nv<T, 2>(bytes)) != cudaSuccess) return e;
   if ((e = prepare_nv<T, 4>(bytes)) != cudaSuccess) return e;
-  if constexpr (std::is_same<T, Q8>::value) return cudaSuccess;
+  if constexpr (std::is_same<T, Q8>::value || std::is_same<T, Q4>::value) return cudaSuccess;
   else return ensure_smem(k_router<T>, bytes);
 }
 
 }  // namespace
 
-// weight storage type: 0 fp32, 1 bf16, 2 Q8
+// weight storage type: 0 fp32, 1 bf16, 2 Q8, 3 Q4
 #define GEMV_DTYPES(KERNEL, ARGS, GRID, ST, PDL)                       \
+  if (dtype == 3) { GEMV_LAUNCH(KERNEL, Q4, ARGS, GRID, ST, PDL) }      \
   if (dtype == 2) { GEMV_LAUNCH(KERNEL, Q8, ARGS, GRID, ST, PDL) }      \
   if (dtype == 1) { GEMV_LAUNCH(KERNEL, __nv_bfloat16, ARGS, GRID, ST, PDL) } \
   GEMV_LAUNCH(KERNEL, float, ARGS, GRID, ST, PDL)
@@ -404,7 +408,7 @@ cudaError_t launch_gateup(int dtype, const GateUpArgs &a, int grid, cudaStream_t
   GEMV_DTYPES(k_gateup, a, grid, st, pdl)
 }
 cudaError_t launch_down_moe(int dtype, const DownMoeArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype == 2) return cudaErrorInvalidValue;   // MoE: fp32 / bf16 weights
+  if (dtype == 2 || dtype == 3) return cudaErrorInvalidValue;   // MoE: fp32 / bf16 weights
   if (dtype == 1) { GEMV_LAUNCH(k_down_moe, __nv_bfloat16, a, grid, st, pdl) }
   GEMV_LAUNCH(k_down_moe, float, a, grid, st, pdl)
 }
@@ -413,11 +417,12 @@ cudaError_t launch_lmhead(int dtype, const LmArgs &a, int grid, cudaStream_t st,
 }
 cudaError_t launch_router(int dtype, const RouterArgs &a, cudaStream_t st, bool pdl) {
   const int smem = (a.E + 32 + a.n_expert) * 4;
-  if (dtype == 2) return cudaErrorInvalidValue;
+  if (dtype == 2 || dtype == 3) return cudaErrorInvalidValue;
   if (dtype == 1) return launch(k_router<__nv_bfloat16>, a, dim3(1), dim3(256), smem, st, pdl);
   return launch(k_router<float>, a, dim3(1), dim3(256), smem, st, pdl);
 }
 cudaError_t prepare_gemv_kernels(int dtype, int smem_bytes) {
+  if (dtype == 3) return prepare_t<Q4>(smem_bytes);
   if (dtype == 2) return prepare_t<Q8>(smem_bytes);
   return dtype ? prepare_t<__nv_bfloat16>(smem_bytes) : prepare_t<float>(smem_bytes);
 }

@@ -356,6 +356,10 @@ template <>
 struct Vec<Q8> {
   static constexpr int N = 8;   // 8-byte vectors of int8 values (the row's fp16 scales follow)
 };
+template <>
+struct Vec<Q4> {
+  static constexpr int N = 8;   // 4-byte vectors of 4-bit codes (the row's fp16 scales follow)
+};
 
 // A lane's slice of the activation vector: for t < NV, the Vec<T>::N columns
 // of 16-byte vector v(t) = c*32 + lane + t*32*cw (c = the warp's column slot),
@@ -382,6 +386,18 @@ __device__ __forceinline__ float2 load2(const Q8Row *src, int col) {
   const int8_t *v = reinterpret_cast<const int8_t *>(src->p);
   const float d = __half2float(reinterpret_cast<const __half *>(src->p + src->K)[col / 32]);
   return make_float2(d * (float)v[col], d * (float)v[col + 1]);
+}
+
+// One Q4 row (the embedding row of a token): codes at p, scales at p + K / 2.
+struct Q4Row {
+  const uint8_t *p;
+  int K;
+};
+
+__device__ __forceinline__ float2 load2(const Q4Row *src, int col) {
+  const uint32_t b = src->p[col >> 1];   // col even: codes col (low nibble) and col + 1
+  const float d = __half2float(reinterpret_cast<const __half *>(src->p + src->K / 2)[col / 32]);
+  return make_float2(d * (float)((int)(b & 15u) - 8), d * (float)((int)(b >> 4) - 8));
 }
 
 // The N consecutive source columns [col, col + N) of one weight vector as fp32
@@ -482,12 +498,17 @@ __device__ __forceinline__ float rms_inv(const S *src, int E, float eps, float *
 template <int NV>
 __device__ __forceinline__ float dot_row_q8(const uint8_t *row, const XSlice<Q8, NV> &xs, int vpr,
                                             int c, int cw, int lane);
+template <int NV>
+__device__ __forceinline__ float dot_row_q4(const uint8_t *row, const XSlice<Q4, NV> &xs, int vpr,
+                                            int c, int cw, int lane);
 
 template <typename T, int NV>
 __device__ __forceinline__ float dot_row(const uint8_t *row, const XSlice<T, NV> &xs, int vpr,
                                          int c, int cw, int lane) {
   if constexpr (std::is_same<T, Q8>::value) {
     return dot_row_q8<NV>(row, xs, vpr, c, cw, lane);
+  } else if constexpr (std::is_same<T, Q4>::value) {
+    return dot_row_q4<NV>(row, xs, vpr, c, cw, lane);
   } else {
   constexpr int P = Vec<T>::N / 2;
   uint4 wv[NV];
@@ -555,6 +576,44 @@ __device__ __forceinline__ float dot_row_q8(const uint8_t *row, const XSlice<Q8,
                                 one, off);
         acc = ffma2(q0, xs.p[t][2 * k], acc);
         acc = ffma2(q1, xs.p[t][2 * k + 1], acc);
+      }
+      s = fmaf(acc.x + acc.y, dv[t], s);
+    }
+  }
+  return s;
+}
+
+// Q4 rows: each 4-byte vector is 8 codes of one quarter of a block of 32.
+// The low and the high nibbles are masked into two words of four bytes, a
+// byte permute makes the float 2^23 + u of each code (the code in the low
+// mantissa bits) and one packed FMA removes 2^23 + 8 exactly, so each u - 8
+// is exact before it multiplies the fp32 activation pair it belongs to; each
+// vector is scaled once by its block's fp16 scale.
+template <int NV>
+__device__ __forceinline__ float dot_row_q4(const uint8_t *row, const XSlice<Q4, NV> &xs, int vpr,
+                                            int c, int cw, int lane) {
+  uint32_t wv[NV];
+  float dv[NV];
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    const int v = c * 32 + lane + t * 32 * cw;
+    const int vc = v < vpr ? v : 0;
+    wv[t] = *reinterpret_cast<const uint32_t *>(row + 4 * vc);
+    dv[t] = __half2float(reinterpret_cast<const __half *>(row + 4 * vpr)[vc >> 2]);
+  }
+  const float2 off = make_float2(-8388616.0f, -8388616.0f), one = make_float2(1.f, 1.f);
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < NV; ++t) {
+    if (c * 32 + lane + t * 32 * cw < vpr) {
+      const uint32_t lo = wv[t] & 0x0F0F0F0Fu, hi = (wv[t] >> 4) & 0x0F0F0F0Fu;
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 q = ffma2(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + k)),
+                                           __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + k))),
+                               one, off);
+        acc = ffma2(q, xs.p[t][k], acc);
       }
       s = fmaf(acc.x + acc.y, dv[t], s);
     }
