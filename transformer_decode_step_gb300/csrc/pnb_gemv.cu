@@ -45,10 +45,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
   XSlice<T, NV> xs;
   load_weight_slice(xs, a.norm_w, a.g, warp, lane);
   const int hd = a.head_dim;
+  // The position was written by the previous step's last kernel (or before
+  // the step), which has completed when any layer's QKV kernel starts: the
+  // RoPE angles are tabulated before the dependency wait.
+  const int pos = a.io->pos;
+  if (tid < hd / 2) {
+    float sn, cs;
+    rope_sincos(pos, a.inv_freq[tid], &sn, &cs);
+    c.rope[tid] = make_float2(cs, sn);
+  }
   pdl_wait();
   if (tid == 0) ktrace(a.tr, 1);
-  const double inv_freq = tid < hd / 2 ? a.inv_freq[tid] : 0.0;
-  const int pos = a.io->pos;
   if (a.emb) {
     int tok = a.io->token;
     if (tok < 0 || tok >= a.n_vocab) {
@@ -74,12 +81,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
     norm_slice(xs, a.x, a.g.K, a.eps, a.g, c.red, warp, lane);
   }
   if (tid == 0) ktrace(a.tr, 2);
-  // RoPE angles of this position, one per dimension pair
-  if (tid < hd / 2) {
-    float sn, cs;
-    rope_sincos(pos, inv_freq, &sn, &cs);
-    c.rope[tid] = make_float2(cs, sn);
-  }
   consume_dyn<T, NV>(a.g, c, xs, warp, lane, &a.io->error, a.tr);
   gemv_sync();
   if (tid == 0) ktrace(a.tr, 4);
@@ -118,6 +119,27 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_qkv(const QkvArgs a) {
 template <typename T, int NV>
 __global__ void __launch_bounds__(kGemvThreads, 1) k_resid(const ResidArgs a) {
   GEMV_ROLES_DYN(a, true)
+  // The residual rows this thread adds to in the epilogue, loaded before the
+  // dependency wait: x was last written two (down projection) or three
+  // (output projection) kernels back, and those have completed when this
+  // kernel's CTAs start.  Rows follow the static split of the items (the
+  // rows of the CTA's k-th item are the epilogue's indices k * rps + r).
+  int64_t xrow = -1;
+  float xpre = 0.f;
+  if (a.g.n_static_total == a.g.n_items) {
+    const int rps = a.g.rows_per_stage;
+    const int s0 = (int)((int64_t)a.g.n_items * blockIdx.x / gridDim.x);
+    const int n_own = (int)((int64_t)a.g.n_items * (blockIdx.x + 1) / gridDim.x) - s0;
+    if (tid < n_own * rps) {
+      int seg, n;
+      int64_t row0;
+      item_rows(a.g, a.s.rows, s0 + tid / rps, seg, row0, n);
+      if (tid % rps < n) {
+        xrow = row0 + tid % rps;
+        xpre = __ldcg(a.x + xrow);
+      }
+    }
+  }
   pdl_wait();
   if (tid == 0) ktrace(a.tr, 1);
   XSlice<T, NV> xs;
@@ -127,7 +149,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_resid(const ResidArgs a) {
   gemv_sync();
   if (tid == 0) ktrace(a.tr, 4);
   for_claimed_rows(a.g, c, a.s.rows, false, tid, [&](int k, int r, int, int64_t row) {
-    a.x[row] += item_row_total(a.g, c, k, r);
+    a.x[row] = (row == xrow ? xpre : a.x[row]) + item_row_total(a.g, c, k, r);
   });
   if (tid == 0) ktrace(a.tr, 5);
 }
