@@ -37,6 +37,10 @@ SHAPE_HD128 = wl.Shape(n_vocab=1500, n_embd=1024, n_head=8, n_kv_head=8, n_layer
                        n_ctx=300, rope_theta=5e5, rms_norm_eps=1e-5, dtype=BF16)
 # a 48-slot ring: chunks stop where the ring would wrap, then one token per step
 SHAPE_WIN = dataclasses.replace(SHAPE, sliding_window=48, n_ctx=200, n_vocab=2000, rope_theta=1e6)
+# long prompts: chunks past position 256 run the tensor-core attention with
+# token groups (2 tokens per KV-head pass at 4 query heads per KV head, 8 at MHA)
+SHAPE_LONG = dataclasses.replace(SHAPE, n_ctx=600)
+SHAPE_HD128_LONG = dataclasses.replace(SHAPE_HD128, n_ctx=600)
 # MoE: chunks through the batched step's router and per-expert FFNs
 SHAPE_MOE = wl.Shape(n_vocab=777, n_embd=256, n_head=4, n_kv_head=2, n_layer=2, n_ff=512,
                      n_ctx=128, rope_theta=1e6, rms_norm_eps=1e-5, expert_count=4, expert_used=2,
@@ -89,6 +93,12 @@ def gpu_prefill(sm, start, tokens):
     ("ring_fills_then_wraps", SHAPE_WIN, 0, 70),
     ("ring_partial_chunk", SHAPE_WIN, 30, 40),
     ("moe", SHAPE_MOE, 5, 9),
+    ("gqa_512", SHAPE_LONG, 0, 512),
+    ("mha_hd128_512", SHAPE_HD128_LONG, 0, 512),
+    # a chunk that starts off the 64-token grid and crosses position 256: its
+    # new K / V span two cache tiles, loaded only after the QKV kernel ends
+    ("mha_hd128_unaligned", SHAPE_HD128, 150, 140),
+    ("gqa_unaligned_from_cache", SHAPE_LONG, 230, 90),
 ])
 def test_prefill_matches_oracle(name, shape, start, T):
     rng = np.random.default_rng(T + start)
@@ -102,7 +112,8 @@ def test_prefill_matches_oracle(name, shape, start, T):
         check(rl1, ra1, lg1, am1, f"{name} next step")
 
 
-@pytest.mark.parametrize("shape,start,T", [(SHAPE, 11, 100), (SHAPE_HD128, 40, 64)])
+@pytest.mark.parametrize("shape,start,T", [(SHAPE, 11, 100), (SHAPE_HD128, 40, 64),
+                                           (SHAPE_HD128_LONG, 200, 130)])
 def test_prefill_equals_single_sequence_steps(shape, start, T):
     rng = np.random.default_rng(3)
     tokens = [int(t) for t in rng.integers(0, shape.n_vocab, size=T)]

@@ -675,11 +675,16 @@ BGemmArgs bgemm_args(const pnb_model *m, const BatchCtx *b, const BPlan &p, int 
 // down GEMM (residual); then the final norm and the LM-head GEMM (argmax,
 // position advance).  The first kernel waits for all earlier stream work;
 // every later one uses programmatic stream serialization.
-// shared_kv: the slots are one sequence's consecutive tokens sharing its
-// cache (a prefill chunk), whose attention runs as one chunk kernel
+// chunk: the slots are one sequence's consecutive tokens sharing its cache
+// (a prefill chunk).  kChunkKernel: the attention runs as one CUDA-core chunk
+// kernel; kChunkGroups: on the tensor cores, consecutive tokens sharing each
+// pass over the cached positions (token groups); kChunkSlots: the per-slot
+// attention kernel, each token a slot.
+enum { kSlots = 0, kChunkKernel = 1, kChunkGroups = 2, kChunkSlots = 3 };
 cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t *tokens,
                           unsigned long long *trace, cudaStream_t st, float *logits, int32_t *argmax,
-                          bool shared_kv = false) {
+                          int chunk = kSlots) {
+  const bool shared_kv = chunk == kChunkKernel;
   BatchCtx *b = m->batch;
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, Hd = c.n_head * m->hd, F = c.n_ff;
@@ -754,7 +759,19 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
       ta.pos = b->pos;
       ta.nstages = attn_tc_stages(m->hd);
       ta.tr = KTrace{trace, 7 * l + 2};
-      if ((e = launch_attn_tc(m->hd, c.n_head / c.n_kv_head, ta, st, true)) != cudaSuccess) return e;
+      ta.shared_cache = chunk != kSlots;
+      int cols = c.n_head / c.n_kv_head;
+      if (chunk == kChunkGroups) {
+        // a chunk's tokens share the cache: T consecutive tokens per CTA
+        // column block (all 8 columns of the MMA) read the cached positions
+        // once for all of them instead of once each
+        ta.tok_group = std::max(1, 8 / cols);
+        cols *= ta.tok_group;
+        const int groups = (B + ta.tok_group - 1) / ta.tok_group;
+        ta.n_split = std::max(1, std::min({attn_tc_max_split(), m->num_sms / (c.n_kv_head * groups),
+                                           ceil_div(m->cap, 128)}));
+      }
+      if ((e = launch_attn_tc(m->hd, cols, ta, st, true)) != cudaSuccess) return e;
     } else {
     AttnArgs aa{};
     aa.q = b->qb;
@@ -776,6 +793,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
     aa.xop_ld = Hd;
     aa.bp = bp;
     aa.nb = B;
+    aa.shared_cache = chunk != kSlots;
     aa.tr = KTrace{trace, 7 * l + 2};
     if ((e = launch_attn(m->kv_dt, m->hd, aa, m->ag, st, true)) != cudaSuccess) return e;
     }
@@ -1392,7 +1410,9 @@ int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T
       for (int j = 0; j < n; ++j) slots[j] = BSlot{s->kv, &b->pio[j], s->maps};
       if (launch_prefill_begin(b->pio, s->io, n, st) != cudaSuccess ||
           enqueue_batch(m, slots, n, tokens_dev + i, nullptr, st, lg, am,
-                        s->pos + n <= kChunkAttnMaxPos) != cudaSuccess ||
+                        s->pos + n <= kChunkAttnMaxPos ? kChunkKernel
+                                                       : (m->attn_tc ? kChunkGroups : kChunkSlots)) !=
+              cudaSuccess ||
           launch_prefill_end(s->io, b->pio, n, st) != cudaSuccess)
         return PNB_E_CUDA;
     }

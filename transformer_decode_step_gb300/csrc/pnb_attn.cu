@@ -64,6 +64,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
 
   // positions of this CTA (pos was written by an earlier step: readable before the wait)
   const int pos = batched ? a.pos[b] : a.io->pos;
+  // the first position whose K / V the preceding kernel wrote: this one, or
+  // a prefill chunk's first (its tokens share the cache); stages reaching it
+  // are loaded after the dependency wait
+  const int p_new = batched && a.shared_cache ? a.pos[0] : pos;
   const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
   const int n = pos - lo + 1;
   const int chunk = (n + a.n_split - 1) / a.n_split;
@@ -99,7 +103,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(const AttnArgs a) {
       for (; st < nst; ++st) {
         const int a0 = c0 + st * SP, np = min(SP, npos - st * SP);
         const int slot = st % NS, round = st / NS;
-        if (!waited && (a0 + np > pos || st == NS)) {
+        if (!waited && (a0 + np > p_new || st == NS)) {
           ktrace(a.tr, 6);
           pdl_wait();
           pdl_trigger();

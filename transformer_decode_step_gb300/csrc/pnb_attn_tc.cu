@@ -22,6 +22,7 @@
 // order and write the output.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <limits.h>
 #include <math.h>
 
 #include "pnb_kernels.cuh"
@@ -141,20 +142,35 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
   const int NS = a.nstages;
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const bool batched = a.slots != nullptr;
-  const BSlot bs = batched ? a.slots[b] : BSlot{nullptr, a.io, a.maps};
+  // column h: query head h0 + h % GH of virtual slot b * T + h / GH (T = 1:
+  // the CTA's slot, every column one of its query heads)
+  const int T = batched && a.tok_group > 1 ? a.tok_group : 1;
+  const int GH = G / T;
+  const int h0 = g * GH;
+  auto col_slot = [&](int h) { return b * T + h / GH; };
+  auto col_head = [&](int h) { return h0 + h % GH; };
+  const BSlot bs = batched ? a.slots[b * T] : BSlot{nullptr, a.io, a.maps};
   int32_t *err = &bs.io->error;
   const CUtensorMap *maps = static_cast<const CUtensorMap *>(bs.maps) + 2 * a.layer;
   const CUtensorMap *kmap = maps, *vmap = maps + 1;
-  const float *qb = a.q + (size_t)b * a.n_head * HD;
-  const int h0 = g * G;
   const int ns = a.n_split;         // splits = CTAs of this KV head's cluster
   const bool clustered = ns > 1;
   // query heads this CTA merges: h = split + j * ns < G
   const int nloc = split < G ? (G - 1 - split) / ns + 1 : 0;
 
-  // positions: [lo, pos]; tiles of 128 aligned positions, split evenly
-  const int pos = batched ? a.pos[b] : a.io->pos;
-  const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
+  // positions: [lo_h, pos_h] per column (a dead column, past the last slot,
+  // attends to nothing); the CTA's tiles cover the union [lo, pos], 128
+  // aligned positions each, split evenly
+  int posc[G], loc[G];
+  int pos = -1, lo = INT_MAX;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const bool live = !batched || col_slot(h) < a.nb;
+    posc[h] = live ? (batched ? a.pos[col_slot(h)] : a.io->pos) : -1;
+    loc[h] = live ? (a.window > 0 ? max(0, posc[h] - a.window + 1) : 0) : INT_MAX;
+    pos = max(pos, posc[h]);
+    lo = min(lo, loc[h]);
+  }
   const int t_first = lo / kTile, t_last = pos / kTile;
   const int nt_all = t_last - t_first + 1;
   const int tb = t_first + (int)((int64_t)nt_all * split / ns);
@@ -216,12 +232,14 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
 
   if (warp == 0) {
     if (lane == 0) {
-      // tiles before the current position were written by earlier steps; the
-      // tile holding pos waits for the kernel that wrote this step's K / V
+      // tiles before the first new position were written by earlier steps;
+      // a tile holding a new position (pos, or from a prefill chunk's first
+      // token on) waits for the kernel that wrote this step's K / V
+      const int p_new = batched && a.shared_cache ? a.pos[0] : pos;
       bool waited = false, ok = true;
       for (int i = 0; i < ntiles; ++i) {
         const int T = tb + i, s = i % NS, r = i / NS;
-        if (!waited && ((T + 1) * kTile > pos || i == NS)) {
+        if (!waited && ((T + 1) * kTile > p_new || i == NS)) {
           ktrace(a.tr, 6);
           pdl_wait();
           pdl_trigger();
@@ -310,7 +328,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
     epi_sync_t();
     for (int i = tid; i < G * HD; i += 128) {
       const int h = i / HD, d = i - h * HD;
-      const float v = qb[(size_t)(h0 + h) * HD + d] * a.qscale;
+      const float v = (col_slot(h) < (batched ? a.nb : 1))
+                          ? a.q[((size_t)col_slot(h) * a.n_head + col_head(h)) * HD + d] * a.qscale
+                          : 0.f;
       const __nv_bfloat16 hi = __float2bfloat16_rn(v);
       const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
       uint8_t *tile = Q + (d >> 6) * 2048;
@@ -355,12 +375,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.s_empty);
       const int p = (tb + t) * kTile + 32 * q + lane;
-      const bool valid = p >= lo && p <= pos;
+      bool valid[G];
       float sc[G];
       float *rm = red + (t & 1) * 32;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        sc[h] = valid ? v[h] + v[8 + h] : -INFINITY;
+        valid[h] = p >= loc[h] && p <= posc[h];
+        sc[h] = valid[h] ? v[h] + v[8 + h] : -INFINITY;
         const float mx = warp_max(sc[h]);
         if (lane == 0) rm[q * 8 + h] = mx;
       }
@@ -419,7 +440,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
       float pp[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        pp[h] = (valid && m[h] != -INFINITY) ? exp2f(sc[h] - m[h]) : 0.f;
+        pp[h] = (valid[h] && m[h] != -INFINITY) ? exp2f(sc[h] - m[h]) : 0.f;
         l[h] += pp[h];
       }
       // P of this tile into buffer t & 1, once the P V product of tile t - 2 is done
@@ -473,12 +494,15 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
       if (!clustered) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const size_t col = (size_t)(h0 + h) * HD + d;
+          const size_t col = (size_t)col_head(h) * HD + d;
           const float x = l[h] > 0.f ? oh[h] / l[h] : 0.f;
           if (a.xop) {
-            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-            a.xop[(size_t)b * a.xop_ld + col] = hi;
-            a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+            const int r = col_slot(h);
+            if (r < a.nb) {
+              const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+              a.xop[(size_t)r * a.xop_ld + col] = hi;
+              a.xop[(size_t)(a.bp + r) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+            }
           } else {
             a.out[col] = x;
           }
@@ -534,14 +558,17 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
             }
           if (a.n_split == 1) {
             const float inv = lh > 0.f ? 1.f / lh : 0.f;
-            const size_t row = (size_t)(h0 + lane) * HD;
+            const size_t row = (size_t)col_head(lane) * HD;
             if (a.xop) {
+              const int r = col_slot(lane);
+              if (r < a.nb) {
   #pragma unroll
-              for (int d = 0; d < HD; ++d) {
-                const float x = o[d] * inv;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-                a.xop[(size_t)b * a.xop_ld + row + d] = hi;
-                a.xop[(size_t)(a.bp + b) * a.xop_ld + row + d] = __float2bfloat16_rn(x - __bfloat162float(hi));
+                for (int d = 0; d < HD; ++d) {
+                  const float x = o[d] * inv;
+                  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+                  a.xop[(size_t)r * a.xop_ld + row + d] = hi;
+                  a.xop[(size_t)(a.bp + r) * a.xop_ld + row + d] = __float2bfloat16_rn(x - __bfloat162float(hi));
+                }
               }
             } else {
   #pragma unroll
@@ -579,11 +606,15 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
           Os = fmaf(Rs[d], f, Os);
         }
         const float x = Ls > 0.f ? Os / Ls : 0.f;
-        const size_t col = (size_t)(h0 + split + j * ns) * HD + d;
+        const int hc = split + j * ns;
+        const size_t col = (size_t)col_head(hc) * HD + d;
         if (a.xop) {
-          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-          a.xop[(size_t)b * a.xop_ld + col] = hi;
-          a.xop[(size_t)(a.bp + b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+          const int r = col_slot(hc);
+          if (r < a.nb) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+            a.xop[(size_t)r * a.xop_ld + col] = hi;
+            a.xop[(size_t)(a.bp + r) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+          }
         } else {
           a.out[col] = x;
         }
@@ -604,7 +635,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
 template <int HD, int G>
 cudaError_t launch_g(const AttnTcArgs &a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_split, a.n_kv, a.slots ? a.nb : 1);
+  const int T = a.slots && a.tok_group > 1 ? a.tok_group : 1;
+  cfg.gridDim = dim3(a.n_split, a.n_kv, a.slots ? (a.nb + T - 1) / T : 1);
   cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = attn_tc_smem(HD, a.nstages);
   cfg.stream = st;

@@ -206,6 +206,9 @@ struct AttnArgs {
   size_t kv_off, layer_kv_bytes;
   __nv_bfloat16 *xop;
   int xop_ld, bp, nb;    // operand row pitch, padded slots, slots
+  // prefill chunk (slots share one cache): the K / V of every position from
+  // pos[0] on are new, and their stages are loaded after the dependency wait
+  int shared_cache;
 };
 
 // One slot of a batched step (device table, written at the start of the step).
@@ -232,9 +235,21 @@ struct AttnTcArgs {
   const int32_t *pos;      // batched positions
   StepIO *io;              // one sequence
   int nstages;
+  // Prefill chunk: the slots are one sequence's consecutive tokens sharing
+  // one cache, so the preceding kernel wrote the K / V of every position from
+  // pos[0] on; the tiles holding them are loaded after the dependency wait.
+  // 0: each slot's own position is the only new one.
+  int shared_cache;
+  // Token groups (prefill chunks, whose virtual slots share one cache): one
+  // CTA column block serves tok_group consecutive virtual slots, column
+  // t * (n_head / n_kv) + j being query head j of slot group * tok_group + t,
+  // each masked to its own positions; the grid's z is the group.  0 or 1:
+  // one slot per z.
+  int tok_group;
   KTrace tr;
 };
 
+// group: columns per KV head (query heads per KV head, times tok_group)
 cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl);
 
 // attention of a prefill chunk: n consecutive tokens of one sequence whose
