@@ -146,9 +146,11 @@ typedef struct pnb_state pnb_state;
    head_dim even and in {32, 64, 128}, n_head % n_kv_head == 0, n_embd and
    n_ff multiples of 8, 0 < expert_used <= expert_count <= 64 when MoE,
    pointer non-NULL and 16-byte aligned.  PNB_Q8_0 and PNB_Q4_0 need n_embd and n_ff
-   multiples of 256 (whole 16-byte vectors per row) and a dense FFN
-   (PNB_E_UNSUPPORTED otherwise); its models run the single-sequence step
-   only (no batched form; pnb_prefill goes one token per step).  *out is set on success. */
+   multiples of 256 (whole 16-byte vectors per row; PNB_E_UNSUPPORTED
+   otherwise).  Every matrix of such a model is in the blocks, the MoE router
+   and experts included (the pages dequantize only the embeddings and norms at
+   load, "Weight Loading Modes"); its models run the single-sequence step only
+   (no batched form; pnb_prefill goes one token per step).  *out is set on success. */
 int pnb_model_create(const pnb_config *cfg, const pnb_weights *w, pnb_model **out);
 void pnb_model_free(pnb_model *m);
 

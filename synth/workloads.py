@@ -145,7 +145,15 @@ LLAMA7B_Q8 = Workload("llama7b_q8_0", replace(LLAMA7B.shape, dtype=Q8), seed=2, 
 LLAMA7B_Q4 = Workload("llama7b_q4_0", replace(LLAMA7B.shape, dtype=Q4), seed=2, prefill=2048,
                       steps=128)
 
-ALL = [TINY, LLAMA7B, MISTRAL7B, MIXTRAL, LLAMA8B_BATCHED, LLAMA7B_Q8, LLAMA7B_Q4]
+# Mixtral's decode step with every matrix in Q8_0 / Q4_0 blocks (router and
+# experts included; embeddings and norms as the dense quantized models)
+MIXTRAL_Q8 = Workload("mixtral8x_top2_q8_0", replace(MIXTRAL.shape, dtype=Q8), seed=4,
+                      prefill=4096, steps=128)
+MIXTRAL_Q4 = Workload("mixtral8x_top2_q4_0", replace(MIXTRAL.shape, dtype=Q4), seed=4,
+                      prefill=4096, steps=128)
+
+ALL = [TINY, LLAMA7B, MISTRAL7B, MIXTRAL, LLAMA8B_BATCHED, LLAMA7B_Q8, LLAMA7B_Q4, MIXTRAL_Q8,
+       MIXTRAL_Q4]
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -2,7 +2,8 @@
 
 The oracle multiplies by exactly the weights the GPU holds (each block's fp16
 scale times its int8 values, from the same seeded generator), so the only
-difference is the GPU's fp32 accumulation and bf16 KV cache: the bf16 bar
+difference is the GPU's fp32 accumulation and bf16 KV cache (MoE models: the
+router and the experts in the same blocks): the bf16 bar
 applies (argmax identical unless the oracle's top-2 margin is inside the
 logit tolerance; max|d logit| <= 2e-2 * max|logit|).
 """
@@ -33,6 +34,11 @@ Q8_GQA = wl.Shape(n_vocab=3001, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_
 Q8_WIN = dataclasses.replace(Q8_GQA, sliding_window=24, n_vocab=2000, rope_theta=1e6)
 Q8_MHA128 = wl.Shape(n_vocab=1500, n_embd=1024, n_head=8, n_kv_head=8, n_layer=2, n_ff=1536,
                      n_ctx=300, rope_theta=5e5, rms_norm_eps=1e-5, dtype=Q8)
+# MoE: router and experts in Q8 blocks too (top-2 of 4; top-2 of 8 with a window ring)
+Q8_MOE = wl.Shape(n_vocab=1200, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_ff=768,
+                  n_ctx=96, rope_theta=1e6, rms_norm_eps=1e-5, expert_count=4, expert_used=2,
+                  dtype=Q8)
+Q8_MOE8_WIN = dataclasses.replace(Q8_MOE, expert_count=8, sliding_window=32, n_vocab=900)
 # rows of 11008 values (the Llama-7B down projection): one row per ring slot
 Q8_WIDE_FF = wl.Shape(n_vocab=1000, n_embd=512, n_head=4, n_kv_head=4, n_layer=1, n_ff=11008,
                       n_ctx=64, rope_theta=1e4, rms_norm_eps=1e-5, dtype=Q8)
@@ -91,6 +97,8 @@ def compare(got, gam, ref, ram, what):
     ("window_ring", Q8_WIN, 40, 16),       # ring of 24 slots, already wrapped
     ("mha_hd128", Q8_MHA128, 250, 8),
     ("wide_ff", Q8_WIDE_FF, 9, 6),
+    ("moe", Q8_MOE, 30, 10),
+    ("moe8_window_ring", Q8_MOE8_WIN, 40, 12),   # ring of 32 slots, already wrapped
 ])
 def test_small_q8_models_match_oracle(name, shape, start, steps):
     rng = np.random.default_rng(17)
@@ -130,6 +138,29 @@ def test_llama7b_q8_first_steps_match_oracle():
     torch.cuda.empty_cache()
 
 
+def test_mixtral_q8_first_step_matches_oracle():
+    """Mixtral with every matrix in Q8 blocks (router and experts included): the
+    first greedy step from the pre-filled cache, teacher-forced."""
+    w = wl.MIXTRAL_Q8
+    m = oracle.Model(w.shape, seed=w.seed)
+    s = m.new_state()
+    lo, hi = wl.kv_prefill_range(w.shape, w.prefill)
+    s.prefill_synth(w.seed, 0, lo, hi)
+    tok = wl.prompt_tokens(w)[0]
+    ref, ram = s.forward(tok)
+    del s, m
+    sm = pnb.SynthModel(w.shape, w.seed, device=DEV)
+    st = sm.new_state(w.prefill)
+    lg = torch.empty(w.shape.n_vocab, dtype=torch.float32, device=DEV)
+    a = torch.empty(1, dtype=torch.int32, device=DEV)
+    st.forward(int(tok), logits=lg, argmax=a)
+    got = lg.cpu().numpy().copy()
+    assert st.device_error() == 0
+    assert compare([got], [int(a.item())], [ref], [ram], w.name) == 0
+    del st, sm
+    torch.cuda.empty_cache()
+
+
 def test_q8_forms_and_limits():
     sm = pnb.SynthModel(Q8_GQA, 5, device=DEV)
     states = [sm.new_state(3), sm.new_state(4)]
@@ -146,8 +177,20 @@ def test_q8_forms_and_limits():
     for i, t in enumerate(toks):
         st2.forward(t, logits=one)
         assert torch.equal(one, lg[i])
-    for bad in (dataclasses.replace(Q8_GQA, n_ff=1056),   # rows not whole 16-byte vectors
-                dataclasses.replace(Q8_GQA, expert_count=4, expert_used=2)):
-        with pytest.raises(pnb.PnbError) as e:
-            pnb.SynthModel(bad, 5, device=DEV)
-        assert e.value.code == -5
+    with pytest.raises(pnb.PnbError) as e:   # rows not whole 16-byte vectors
+        pnb.SynthModel(dataclasses.replace(Q8_GQA, n_ff=1056), 5, device=DEV)
+    assert e.value.code == -5
+    # MoE: no batched form either; prefill one token per step, equal to the steps
+    sm = pnb.SynthModel(Q8_MOE, 5, device=DEV)
+    with pytest.raises(pnb.PnbError) as e:
+        sm.model.forward_batch([sm.new_state(3), sm.new_state(4)])
+    assert e.value.code == -5
+    st = sm.new_state(10)
+    lg = torch.empty(len(toks), Q8_MOE.n_vocab, dtype=torch.float32, device=DEV)
+    tk = [t % Q8_MOE.n_vocab for t in toks]
+    st.prefill(torch.tensor(tk, dtype=torch.int32, device=DEV), logits=lg)
+    st2 = sm.new_state(10)
+    one = torch.empty(Q8_MOE.n_vocab, dtype=torch.float32, device=DEV)
+    for i, t in enumerate(tk):
+        st2.forward(t, logits=one)
+        assert torch.equal(one, lg[i])

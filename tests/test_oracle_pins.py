@@ -607,9 +607,12 @@ def test_q8_blocks_follow_their_definition(cols, sigma):
                 assert np.max(np.abs(qw)) >= 126
 
 
-def test_q8_model_is_the_model_of_its_dequantized_weights():
-    """A seeded Q8 oracle model equals the bf16-cache model given d * q explicitly."""
-    shape = dataclasses.replace(TS, dtype=synth.Q8, n_embd=64, n_head=4, n_kv_head=2, n_ff=96)
+@pytest.mark.parametrize("experts", [0, 4])
+def test_q8_model_is_the_model_of_its_dequantized_weights(experts):
+    """A seeded Q8 oracle model (with experts: router and experts in blocks too)
+    equals the bf16-cache model given d * q explicitly."""
+    shape = dataclasses.replace(TS, dtype=synth.Q8, n_embd=64, n_head=4, n_kv_head=2, n_ff=96,
+                                expert_count=experts, expert_used=2 if experts else 0)
     arrays = {}
     for spec in wl.weight_specs(shape):
         k = spec.name if spec.name in ("tok_embd", "out_norm", "output") else (spec.name, spec.layer, spec.sub)
@@ -656,9 +659,12 @@ def test_q4_blocks_follow_their_definition(cols, sigma):
                 assert np.max(np.abs(qw)) >= 6
 
 
-def test_q4_model_is_the_model_of_its_dequantized_weights():
-    """A seeded Q4 oracle model equals the bf16-cache model given d * (u - 8) explicitly."""
-    shape = dataclasses.replace(TS, dtype=synth.Q4, n_embd=64, n_head=4, n_kv_head=2, n_ff=96)
+@pytest.mark.parametrize("experts", [0, 4])
+def test_q4_model_is_the_model_of_its_dequantized_weights(experts):
+    """A seeded Q4 oracle model (with experts: router and experts in blocks too)
+    equals the bf16-cache model given d * (u - 8) explicitly."""
+    shape = dataclasses.replace(TS, dtype=synth.Q4, n_embd=64, n_head=4, n_kv_head=2, n_ff=96,
+                                expert_count=experts, expert_used=2 if experts else 0)
     arrays = {}
     for spec in wl.weight_specs(shape):
         k = spec.name if spec.name in ("tok_embd", "out_norm", "output") else (spec.name, spec.layer, spec.sub)

@@ -203,10 +203,8 @@ int validate_config(const pnb_config *c) {
   if (c->sliding_window < 0 || !(c->rope_theta > 0.0) || !(c->rms_norm_eps >= 0.0)) return PNB_E_INVAL;
   if (c->dtype != PNB_F32 && c->dtype != PNB_BF16 && c->dtype != PNB_Q8_0 && c->dtype != PNB_Q4_0)
     return PNB_E_INVAL;
-  // Q8 / Q4 rows (the values, then K / 32 fp16 scales) are whole 16-byte vectors;
-  // MoE models keep fp32 / bf16 weights
-  if ((c->dtype == PNB_Q8_0 || c->dtype == PNB_Q4_0) &&
-      (c->n_embd % 256 || c->n_ff % 256 || c->expert_count > 0))
+  // Q8 / Q4 rows (the values, then K / 32 fp16 scales) are whole 16-byte vectors
+  if ((c->dtype == PNB_Q8_0 || c->dtype == PNB_Q4_0) && (c->n_embd % 256 || c->n_ff % 256))
     return PNB_E_UNSUPPORTED;
   if (c->expert_count < 0 || c->expert_count > 64) return PNB_E_INVAL;
   if (c->expert_count > 0 &&

@@ -291,9 +291,21 @@ __global__ void __launch_bounds__(256, 1) k_router(const RouterArgs a) {
   for (int i = tid; i < a.E; i += 256) xs[i] = xs[i] * inv * a.norm_w[i];
   __syncthreads();
   for (int e = warp; e < a.n_expert; e += 8) {
-    const T *row = static_cast<const T *>(a.w) + (int64_t)e * a.E;
     float acc = 0.f;
-    for (int i = lane; i < a.E; i += 32) acc = fmaf(Elem<T>::load(row, i), xs[i], acc);
+    if constexpr (std::is_same<T, Q8>::value || std::is_same<T, Q4>::value) {
+      // a quantized router row (values, then the blocks' fp16 scales), in pairs
+      using Row = typename std::conditional<std::is_same<T, Q8>::value, Q8Row, Q4Row>::type;
+      const int64_t rb = std::is_same<T, Q8>::value ? a.E + a.E / 16 : a.E / 2 + a.E / 16;
+      const Row row{static_cast<const uint8_t *>(a.w) + (int64_t)e * rb, a.E};
+      for (int i = 2 * lane; i < a.E; i += 64) {
+        const float2 w = load2(&row, i);
+        acc = fmaf(w.x, xs[i], acc);
+        acc = fmaf(w.y, xs[i + 1], acc);
+      }
+    } else {
+      const T *row = static_cast<const T *>(a.w) + (int64_t)e * a.E;
+      for (int i = lane; i < a.E; i += 32) acc = fmaf(Elem<T>::load(row, i), xs[i], acc);
+    }
     acc = warp_sum(acc);
     if (lane == 0) r[e] = acc;
   }
@@ -396,8 +408,7 @@ cudaError_t prepare_nv(int bytes) {
   if ((e = ensure_smem(k_qkv<T, NV>, bytes)) != cudaSuccess) return e;
   if ((e = ensure_smem(k_resid<T, NV>, bytes)) != cudaSuccess) return e;
   if ((e = ensure_smem(k_gateup<T, NV>, bytes)) != cudaSuccess) return e;
-  if constexpr (!std::is_same<T, Q8>::value && !std::is_same<T, Q4>::value)   // MoE: fp32 / bf16
-    if ((e = ensure_smem(k_down_moe<T, NV>, bytes)) != cudaSuccess) return e;
+  if ((e = ensure_smem(k_down_moe<T, NV>, bytes)) != cudaSuccess) return e;
   return ensure_smem(k_lmhead<T, NV>, bytes);
 }
 
@@ -407,8 +418,7 @@ cudaError_t prepare_t(int bytes) {
   if ((e = prepare_nv<T, 1>(bytes)) != cudaSuccess) return e;
   if ((e = prepare_nv<T, 2>(bytes)) != cudaSuccess) return e;
   if ((e = prepare_nv<T, 4>(bytes)) != cudaSuccess) return e;
-  if constexpr (std::is_same<T, Q8>::value || std::is_same<T, Q4>::value) return cudaSuccess;
-  else return ensure_smem(k_router<T>, bytes);
+  return ensure_smem(k_router<T>, bytes);
 }
 
 }  // namespace
@@ -430,16 +440,15 @@ cudaError_t launch_gateup(int dtype, const GateUpArgs &a, int grid, cudaStream_t
   GEMV_DTYPES(k_gateup, a, grid, st, pdl)
 }
 cudaError_t launch_down_moe(int dtype, const DownMoeArgs &a, int grid, cudaStream_t st, bool pdl) {
-  if (dtype == 2 || dtype == 3) return cudaErrorInvalidValue;   // MoE: fp32 / bf16 weights
-  if (dtype == 1) { GEMV_LAUNCH(k_down_moe, __nv_bfloat16, a, grid, st, pdl) }
-  GEMV_LAUNCH(k_down_moe, float, a, grid, st, pdl)
+  GEMV_DTYPES(k_down_moe, a, grid, st, pdl)
 }
 cudaError_t launch_lmhead(int dtype, const LmArgs &a, int grid, cudaStream_t st, bool pdl) {
   GEMV_DTYPES(k_lmhead, a, grid, st, pdl)
 }
 cudaError_t launch_router(int dtype, const RouterArgs &a, cudaStream_t st, bool pdl) {
   const int smem = (a.E + 32 + a.n_expert) * 4;
-  if (dtype == 2 || dtype == 3) return cudaErrorInvalidValue;
+  if (dtype == 3) return launch(k_router<Q4>, a, dim3(1), dim3(256), smem, st, pdl);
+  if (dtype == 2) return launch(k_router<Q8>, a, dim3(1), dim3(256), smem, st, pdl);
   if (dtype == 1) return launch(k_router<__nv_bfloat16>, a, dim3(1), dim3(256), smem, st, pdl);
   return launch(k_router<float>, a, dim3(1), dim3(256), smem, st, pdl);
 }
