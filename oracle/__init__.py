@@ -85,6 +85,8 @@ def lib():
         L.orc_state_pos.restype = i64
         L.orc_state_pos.argtypes = [p]
         L.orc_state_set_pos.argtypes = [p, i64]
+        L.orc_state_route_margin.restype = d
+        L.orc_state_route_margin.argtypes = [p]
         L.orc_state_kv.restype = p
         L.orc_state_kv.argtypes = [p, i32, i32]
         L.orc_state_prefill_synth.restype = i32
@@ -294,6 +296,13 @@ class State:
 
     def reset(self):
         lib().orc_state_reset(self._h)
+
+    @property
+    def route_margin(self) -> float:
+        """After a forward of a MoE model: over its layers, the smallest gap between
+        the k-th chosen router logit and the best unchosen one, relative to the
+        layer's largest |logit| (a routing near-tie when small); inf for dense."""
+        return float(lib().orc_state_route_margin(self._h))
 
     def kv(self, layer: int, kind: int) -> np.ndarray:
         """Writable view [n_ctx][n_kv_head][head_dim] of one layer's K (0) or V (1)."""

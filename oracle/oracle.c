@@ -103,6 +103,10 @@ typedef struct {
   int64_t pos;
   float *k; /* [n_layer][n_ctx][n_kv_head][head_dim] */
   float *v;
+  /* diagnostic, not arithmetic: over the MoE layers of the last forward, the
+     smallest gap between the k-th chosen router logit and the best unchosen
+     one, relative to the layer's largest |logit| (INFINITY for dense models) */
+  double route_margin;
 } orc_state;
 
 /* ------------------------------------------------------------- helpers */
@@ -461,6 +465,7 @@ orc_state *orc_state_new(const orc_model *m) {
   orc_state *s = (orc_state *)calloc(1, sizeof(orc_state));
   const size_t n = (size_t)(kv_layer_elems(m) * m->cfg.n_layer);
   s->m = m;
+  s->route_margin = INFINITY;
   s->k = (float *)calloc(n, sizeof(float));
   s->v = (float *)calloc(n, sizeof(float));
   if (!s->k || !s->v) {
@@ -488,6 +493,7 @@ void orc_state_reset(orc_state *s) {
 }
 
 int64_t orc_state_pos(const orc_state *s) { return s->pos; }
+double orc_state_route_margin(const orc_state *s) { return s->route_margin; }
 void orc_state_set_pos(orc_state *s, int64_t pos) { s->pos = pos; }
 
 /* [n_ctx][n_kv][hd] cache of one layer; kind 0 = K, 1 = V */
@@ -593,6 +599,19 @@ int orc_layer(const orc_model *m, orc_state *s, int l, float *x) {
     double g[256];
     orc_matvec(ltensor(m, l, ORC_L_WROUTER), X, E, dt, xn, r);
     orc_topk_softmax(r, X, k, idx, g);
+    if (k < X) {
+      /* how close the top-k choice came to a tie: the k-th chosen logit
+         against the best unchosen one */
+      float best_out = -INFINITY, amax = 0.f;
+      for (int e = 0; e < X; ++e) {
+        int chosen = 0;
+        for (int i = 0; i < k; ++i) chosen |= (idx[i] == e);
+        if (!chosen && r[e] > best_out) best_out = r[e];
+        if (fabsf(r[e]) > amax) amax = fabsf(r[e]);
+      }
+      const double gap = ((double)r[idx[k - 1]] - (double)best_out) / (amax > 0.f ? (double)amax : 1.0);
+      if (gap < s->route_margin) s->route_margin = gap;
+    }
     double *acc = (double *)calloc((size_t)E, sizeof(double));
     for (int i = 0; i < k; ++i) {
       const int base = ORC_L_EXPERT0 + 3 * idx[i];
@@ -640,6 +659,7 @@ int orc_forward(const orc_model *m, orc_state *s, int32_t token, float *logits, 
   if (token < 0 || token >= m->cfg.n_vocab) return -1;
   if (s->pos >= m->cfg.n_ctx) return -2;
   float *x = (float *)malloc((size_t)m->cfg.n_embd * sizeof(float));
+  s->route_margin = INFINITY;
   orc_embed(m, token, x);
   for (int l = 0; l < m->cfg.n_layer; ++l) orc_layer(m, s, l, x);
   orc_head(m, x, logits, argmax);

@@ -11,6 +11,7 @@ a tie broken upwards - fails at least one of them.
 """
 import dataclasses
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -24,6 +25,14 @@ from synth import BF16, F32
 from synth.workloads import Shape
 
 RNG = np.random.default_rng(20261202)
+
+
+@pytest.fixture(autouse=True)
+def _rng_per_test(request):
+    """Each test draws from its own generator, seeded by its name, so its inputs do
+    not depend on which other tests ran before it."""
+    global RNG
+    RNG = np.random.default_rng(zlib.crc32(request.node.name.encode()))
 
 
 def f32(a):
@@ -325,7 +334,7 @@ def _rand_arrays(shape: Shape, scale=0.3):
     return arrays
 
 
-def _library_forward(shape: Shape, arrays, tokens):
+def _library_forward(shape: Shape, arrays, tokens, margins=None):
     """Brute force: the decode steps composed of library routines (numpy norm, complex
     exponentials, scipy softmax / expit, matmul), fp64 throughout; the cache stores
     torch-rounded bf16 values when the model is bf16."""
@@ -354,6 +363,7 @@ def _library_forward(shape: Shape, arrays, tokens):
     out = []
     for p, tok in enumerate(tokens):
         x = d(arrays["tok_embd"])[tok].copy()
+        step_margin = math.inf
         for l in range(shape.n_layer):
             xn = norm(x, arrays[("attn_norm", l, 0)])
             q = d(arrays[("wq", l, 0)]) @ xn
@@ -379,11 +389,16 @@ def _library_forward(shape: Shape, arrays, tokens):
             if shape.expert_count > 0:
                 r = d(arrays[("wrouter", l, 0)]) @ xn
                 top = np.argsort(-r, kind="stable")[: shape.expert_used]
+                if shape.expert_used < shape.expert_count:
+                    rest = np.argsort(-r, kind="stable")[shape.expert_used]
+                    step_margin = min(step_margin, (r[top[-1]] - r[rest]) / np.max(np.abs(r)))
                 gate = sp.softmax(r[top])
                 x = x + sum(gi * swiglu("", l, int(e), xn) for gi, e in zip(gate, top))
             else:
                 x = x + swiglu("", l, 0, xn)
         out.append(d(arrays["output"]) @ norm(x, arrays["out_norm"]))
+        if margins is not None:
+            margins.append(step_margin)
     return out
 
 
@@ -419,6 +434,37 @@ def test_whole_step_matches_library_composition(variant):
         if srt[-1] - srt[-2] > 1e-4 * scale:
             assert am[p] == int(np.argmax(want[p]))
 
+
+
+def test_route_margin_is_the_top_k_gap_of_the_router_logits():
+    """The oracle's routing near-tie diagnostic: after each forward, the smallest
+    gap between the k-th chosen router logit and the best unchosen one, over the
+    layers, relative to the layer's largest |logit|, as the brute-force
+    composition's fp64 router logits give it; an exact tie gives 0 and a dense
+    model infinity."""
+    shape = dataclasses.replace(TS, expert_count=4, expert_used=2)
+    arrays = _rand_arrays(shape)
+    tokens = [int(t) for t in RNG.integers(0, shape.n_vocab, size=shape.n_ctx)]
+    want = []
+    _library_forward(shape, arrays, tokens, margins=want)
+    m = oracle.Model(shape, arrays=arrays)
+    st = m.new_state()
+    for t, w in zip(tokens, want):
+        st.forward(t)
+        assert w > 0 and abs(st.route_margin - w) <= 1e-5, (st.route_margin, w)
+    # three identical router rows, top-2: the unchosen expert ties the second
+    shape3 = dataclasses.replace(TS, expert_count=3, expert_used=2)
+    arrays3 = _rand_arrays(shape3)
+    for l in range(shape3.n_layer):
+        wr = arrays3[("wrouter", l, 0)]
+        wr[1] = wr[0]
+        wr[2] = wr[0]
+    st3 = oracle.Model(shape3, arrays=arrays3).new_state()
+    st3.forward(3)
+    assert st3.route_margin == 0.0
+    st_dense = oracle.Model(TS, arrays=_rand_arrays(TS)).new_state()
+    st_dense.forward(3)
+    assert st_dense.route_margin == math.inf
 
 def test_residual_only_model_gives_closed_form_logits():
     arrays = _rand_arrays(TS)
