@@ -54,6 +54,11 @@ def parse():
                     help="each step also draws the next token on the GPU (pnb_sample: "
                          "temperature 0.8, top-k 40, top-p 0.95, repetition penalty 1.1 "
                          "over 64 recent tokens) instead of taking the greedy one")
+    ap.add_argument("--kernel-trace", action="store_true",
+                    help="single-sequence workloads: after the timed steps, one traced step "
+                         "(per-CTA globaltimer stamps) gives each kernel's in-graph time, from the "
+                         "previous launch's last CTA to its own, against its bytes at the measured "
+                         "HBM peak (key kernel_trace of the JSON line)")
     ap.add_argument("--prefill", type=int, default=0,
                     help="instead of decode steps, time pnb_prefill of this many prompt tokens "
                          "from position 0 (one step = one prefill)")
@@ -447,6 +452,8 @@ def run_ours(args, w):
         tok = int(pinned[0])
     e2e_s = time.perf_counter() - t0
     e2e_tps = world * e2e_steps / e2e_s   # every rank runs the same loop
+    # (after the e2e loop: turning the trace on and off re-captures the step's graph)
+    ktrace = kernel_trace(st, s, P, tok0, peaks["hbm_gbs"]) if args.kernel_trace else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -479,10 +486,67 @@ def run_ours(args, w):
                         "how": "pnb_forward with the token passed by value from the host, "
                                "argmax copied to pinned host memory and synchronised every step"},
                 "cpu_baseline": cpu}
+        if ktrace is not None:
+            line["kernel_trace"] = ktrace
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+KERNEL_KINDS = ["qkv", "attention", "o-proj", "router", "gate/up", "down"]
+
+
+def kernel_trace(st, s, P, tok0, peak_gbs):
+    """In-graph time of each kernel of one decode step at position P + 3 (the
+    library's per-CTA timestamps, launch order 6 * layer + kind, then the LM
+    head): from the previous launch's last CTA end to this launch's last CTA
+    end, averaged over the layers, beside the kernel's algorithmic bytes at the
+    measured HBM peak."""
+    import numpy as np
+    import torch
+
+    import transformer_decode_step_gb300 as pnb
+    L = s.n_layer
+    buf = torch.zeros((7 * L + 2) * 256 * 8, dtype=torch.int64, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    st.set_pos(P)
+    st.forward(tok0, argmax=am)
+    st.set_trace(buf)
+    for _ in range(3):
+        st.forward(pnb.PNB_TOKEN_PREV, argmax=am)
+    torch.cuda.synchronize()
+    st.set_trace(None)
+    pos = P + 3
+    t = buf.cpu().numpy().reshape(7 * L + 2, 256, 8)[:6 * L + 1].astype(np.float64)
+    k = s.expert_used if s.expert_count > 0 else 1
+    n_att = pos + 1 if s.sliding_window <= 0 else min(pos + 1, s.sliding_window)
+    mb = s.matrix_bytes
+    Hd = s.n_head * s.head_dim
+    bytes_of = {"qkv": mb((s.n_head + 2 * s.n_kv_head) * s.head_dim, s.n_embd),
+                "attention": n_att * 2 * s.n_kv_head * s.head_dim * s.elem_bytes,
+                "o-proj": mb(s.n_embd, Hd), "router": mb(max(1, s.expert_count), s.n_embd),
+                "gate/up": k * mb(2 * s.n_ff, s.n_embd), "down": k * mb(s.n_embd, s.n_ff),
+                "lm head": mb(s.n_vocab, s.n_embd)}
+    per = {}
+    prev_end = None
+    for ph in range(6 * L + 1):
+        rows = t[ph][t[ph][:, 0] > 0]
+        if rows.shape[0] == 0:
+            continue
+        end = rows[:, 5].max()
+        kind = "lm head" if ph == 6 * L else KERNEL_KINDS[ph % 6]
+        if prev_end is not None:
+            per.setdefault(kind, []).append((end - prev_end) / 1000.0)
+        prev_end = end
+    out = {"unit": "us", "position": pos, "peak_gbs": peak_gbs, "kernels": {}}
+    for kind, us in per.items():
+        bound = bytes_of[kind] / (peak_gbs * 1e9) * 1e6
+        m = float(np.mean(us))
+        out["kernels"][kind] = {"launches": len(us), "us": m, "bound_us": bound,
+                                "bound_frac": bound / m, "bytes": bytes_of[kind]}
+    out["step_us_traced"] = float(sum(np.sum(v) for v in per.values()))
+    return out
 
 
 def batch_step_bytes(shape, positions) -> int:
