@@ -7,6 +7,8 @@ Loop": forward, then argmax at temperature 0, lowest id on ties):
 
 * Llama-7B, Mistral-7B (sliding window 4096) and Mixtral (8 experts, top-2):
   128 steps from the pre-filled positions 2048 / 8192 / 4096;
+* Llama-7B with Q8_0 and with Q4_0 weights (64 steps) and Mixtral with Q8_0
+  weights, router and experts included (32 steps), from the same positions;
 * the batched Llama-8B workload: 64 steps of slots 0, 7, 15, 31 and 63, each
   from its own seeded start position and token (a slot's sequence does not
   depend on which other slots share the batch, so one run per slot serves
@@ -14,12 +16,15 @@ Loop": forward, then argmax at temperature 0, lowest id on ties):
 
 Stored per step (arrays [slot][step] for the batched workload): the token fed,
 the oracle's argmax, its top-1 and top-2 logit values and max|logit|, the 8
-largest logits with their ids, and the logits at 512 fixed ids (seeded); the
+largest logits with their ids, the logits at 512 fixed ids (seeded), the
+smallest relative gap between chosen and unchosen router logits over the MoE
+layers (inf for dense models; a routing near-tie when small); the
 full logit vector of a few steps (``full_steps``).  The GPU test feeds the
 stored tokens (teacher forcing) and compares every step.
 
 Dense weights are handed to the oracle as explicit fp32 arrays generated once
-from the same seeded recipe (the values the oracle would otherwise generate on
+from the same seeded recipe (for the quantized forms: the blocks' dequantized
+weights, which the oracle's own block decoding equals bit for bit) (the values the oracle would otherwise generate on
 every step), so a step costs one pass over memory; Mixtral's experts, too
 large for host memory in fp32, stay seed-generated inside the oracle.  The
 arithmetic is the oracle's either way.
@@ -64,9 +69,18 @@ def explicit_arrays(shape, seed, skip_experts):
     out = {}
 
     def gen(spec):
+        k = spec.key(seed)
+        if shape.dtype in (synth.Q8, synth.Q4):
+            # the dequantized block weights d * q (Q8) or d * (u - 8) (Q4)
+            rows_fn = synth.q8_rows if shape.dtype == synth.Q8 else synth.q4_rows
+            a = np.empty((spec.rows, spec.cols), dtype=np.float32)
+            step = max(1, (1 << 22) // spec.cols)
+            for r in range(0, spec.rows, step):
+                n = min(step, spec.rows - r)
+                a[r:r + n] = rows_fn(k, r, n, spec.cols, spec.sigma)[1]
+            return spec, a
         a = np.empty(spec.rows * spec.cols, dtype=np.float32)
         step = 1 << 22
-        k = spec.key(seed)
         for i in range(0, a.size, step):
             n = min(step, a.size - i)
             a[i:i + n] = synth.values(k, i, n, spec.sigma, shape.dtype)
@@ -89,7 +103,7 @@ def decode(model, w, slot, start_pos, steps, full_at):
     s.prefill_synth(w.seed, slot, lo, hi)
     tok = wl.prompt_tokens(w, slot)[0]
     rec = {k: [] for k in ("tokens", "argmax", "top1", "top2", "maxabs", "top_idx", "top_val",
-                           "sample_val")}
+                           "sample_val", "route_margin")}
     full = []
     t0 = time.time()
     for i in range(steps):
@@ -104,13 +118,14 @@ def decode(model, w, slot, start_pos, steps, full_at):
         rec["top_idx"].append(order.astype(np.int32))
         rec["top_val"].append(logits[order])
         rec["sample_val"].append(logits[ids])
+        rec["route_margin"].append(s.route_margin)
         if i in full_at:
             full.append(logits.copy())
         tok = am
         if i % 16 == 15:
             print(f"  {w.name} slot {slot}: step {i + 1}/{steps} ({time.time() - t0:.0f} s)",
                   flush=True)
-    dt = {"tokens": np.int32, "argmax": np.int32, "top_idx": np.int32}
+    dt = {"tokens": np.int32, "argmax": np.int32, "top_idx": np.int32, "route_margin": np.float64}
     out = {k: np.asarray(v, dtype=dt.get(k, np.float32)) for k, v in rec.items()}
     out["full_logits"] = np.asarray(full, dtype=np.float32).reshape(len(full), V)
     return out
@@ -143,7 +158,12 @@ def run(w):
     print(f"{w.name}: done in {time.time() - t0:.0f} s -> {path_for(w)}", flush=True)
 
 
-WORKLOADS = [wl.LLAMA7B, wl.MISTRAL7B, wl.LLAMA8B_BATCHED, wl.MIXTRAL]
+# the quantized forms (every matrix in Q8_0 / Q4_0 blocks) over shorter decodes
+QUANT_STEPS = {wl.LLAMA7B_Q8.name: 64, wl.LLAMA7B_Q4.name: 64, wl.MIXTRAL_Q8.name: 32}
+WORKLOADS = [wl.LLAMA7B, wl.MISTRAL7B, wl.LLAMA8B_BATCHED, wl.MIXTRAL,
+             wl.LLAMA7B_Q8.with_(steps=QUANT_STEPS[wl.LLAMA7B_Q8.name]),
+             wl.LLAMA7B_Q4.with_(steps=QUANT_STEPS[wl.LLAMA7B_Q4.name]),
+             wl.MIXTRAL_Q8.with_(steps=QUANT_STEPS[wl.MIXTRAL_Q8.name])]
 
 if __name__ == "__main__":
     names = sys.argv[1:] or [w.name for w in WORKLOADS]

@@ -5,6 +5,8 @@ The oracle's greedy decodes are stored by ``tests/golden/make_decode_golden.py``
 
 * Llama-7B, Mistral-7B (4096-position window ring) and Mixtral (8 experts,
   top-2): 128 steps from the pre-filled positions 2048 / 8192 / 4096;
+* Llama-7B with Q8_0 and Q4_0 weights (64 steps) and Mixtral with Q8_0
+  weights (32 steps), every matrix in blocks;
 * the batched Llama-8B workload: 64 steps of slots 0, 7, 15, 31 and 63.
 
 The GPU decodes the same workload through the C ABI (``pnb_forward``, or
@@ -38,6 +40,14 @@ import transformer_decode_step_gb300 as pnb  # noqa: E402
 
 DEV = torch.device("cuda:0")
 TOL = 2e-2
+# A MoE step whose top-k routing came within this relative gap of a tie in the
+# oracle (the smallest gap between a chosen and an unchosen router logit over the
+# layers, relative to the layer's largest |logit|) may route one layer through
+# another expert on the GPU: the residual streams of the two sides differ by
+# about 1e-4 of their size (bf16 cache, summation order), and the router logits
+# with them.  Such a step is a routing near-tie: reported, its logits not
+# compared (the same rule as an argmax near-tie, for the router's decision).
+ROUTE_TOL = 1e-3
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
@@ -74,7 +84,11 @@ class Recorder:
         samp, topv = self.samp.cpu().numpy(), self.topv.cpu().numpy()
         amax, am = self.amax.cpu().numpy(), self.am.cpu().numpy()
         near, worst = [], 0.0
+        route = g["route_margin"][gi] if "route_margin" in g else np.full(samp.shape[0], np.inf)
+        routing_ties = [i for i in range(samp.shape[0]) if route[i] < ROUTE_TOL]
         for i in range(samp.shape[0]):
+            if i in routing_ties:
+                continue
             scale = float(g["maxabs"][gi][i])
             tol = TOL * scale
             err = max(float(np.max(np.abs(samp[i] - g["sample_val"][gi][i]))),
@@ -91,6 +105,8 @@ class Recorder:
         for k, (sl, st) in enumerate(zip(g["full_slot"], g["full_step"])):
             if sl != slot:
                 continue
+            if int(st) in routing_ties:
+                continue
             ref = g["full_logits"][k]
             got = self.full[int(st)].cpu().numpy()
             scale = float(np.max(np.abs(ref)))
@@ -98,11 +114,19 @@ class Recorder:
             worst = max(worst, err / scale)
             assert err <= TOL * scale, f"{what} full logits of step {st}: {err:.3e}"
         print(f"\n{what}: {samp.shape[0]} steps, worst max|d|/max|logit| {worst:.2e}, "
-              f"near-ties {len(near)} {near}")
+              f"near-ties {len(near)} {near}, routing near-ties {len(routing_ties)} "
+              f"{[(i, float(route[i])) for i in routing_ties]}")
+        assert len(routing_ties) <= samp.shape[0] // 4, f"{what}: too many routing near-ties"
         return near
 
 
-@pytest.mark.parametrize("w", [wl.LLAMA7B, wl.MISTRAL7B, wl.MIXTRAL], ids=lambda w: w.name)
+# the quantized forms: shorter stored decodes (Q8_0 / Q4_0 blocks, MoE router and
+# experts included)
+QUANT = [wl.LLAMA7B_Q8.with_(steps=64), wl.LLAMA7B_Q4.with_(steps=64),
+         wl.MIXTRAL_Q8.with_(steps=32)]
+
+
+@pytest.mark.parametrize("w", [wl.LLAMA7B, wl.MISTRAL7B, wl.MIXTRAL] + QUANT, ids=lambda w: w.name)
 def test_full_size_greedy_decode_matches_oracle(w):
     g = golden(w)
     tokens = g["tokens"][0]
