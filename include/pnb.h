@@ -231,6 +231,18 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
    the kernels one by one (0).  Results are identical either way. */
 int pnb_model_set_graphs(pnb_model *m, int enable);
 
+/* Bitwise reproducible batched steps (enable = 1) or the faster default (0).
+   The batched step splits the output and down projections over K; by default
+   each K part adds into the fp32 residual with an atomic add, so the last bits
+   of the residual, and of the logits, can change from run to run.  Enabled,
+   each part adds into a 64-bit fixed-point sum (units of 2^-32, exact and
+   independent of the order), which the next norm folds into the residual
+   once: the same steps from the same states then give the same bits, at
+   about 3.5 % of step time (Llama-8B shapes, B = 8 and 64; the 64-bit adds
+   and the fold).  The single-sequence step is reproducible either way.  Takes effect at the next
+   batched step (its graph is re-captured). */
+int pnb_model_set_deterministic_batch(pnb_model *m, int enable);
+
 /* Decode attention on tcgen05 tensor cores (enable = 1, the default where
    the model allows it: bf16 weights and KV, head_dim 64 or 128, n_head /
    n_kv_head in {1, 2, 4, 8}, and with a sliding window a cache of a multiple

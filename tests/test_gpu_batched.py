@@ -133,6 +133,36 @@ def test_batched_step_matches_single_sequence_steps(SHAPE):
     assert all(s.device_error() == 0 for s in bstates + sstates)
 
 
+@pytest.mark.parametrize("shape", [SHAPE, SHAPE_MOE], ids=["dense", "moe"])
+@pytest.mark.parametrize("B", [5, 40])
+def test_batched_step_is_bitwise_reproducible(shape, B):
+    """With pnb_model_set_deterministic_batch the K parts of the residual
+    projections add into a fixed-point sum, which does not depend on the order
+    of the adds: the same steps from the same states give the same logits, bit
+    for bit, and they agree with the default (fp32 atomic) step to rounding."""
+    starts = starts_for(shape, B, 77)
+    sm = pnb.SynthModel(shape, SEED, device=DEV)
+    states = [sm.new_state(p, slot=b) for b, p in enumerate(starts)]
+    tokens = [int(t) for t in np.random.default_rng(9).integers(0, shape.n_vocab, size=B)]
+    tk = torch.tensor(tokens, dtype=torch.int32, device=DEV)
+    lg = torch.empty(B, shape.n_vocab, dtype=torch.float32, device=DEV)
+    runs = []
+    for det in (True, True, False):
+        sm.model.set_deterministic_batch(det)
+        for b, st in enumerate(states):
+            st.set_pos(starts[b])
+        out = []
+        for i in range(3):
+            sm.model.forward_batch(states, tokens=tk if i == 0 else None, logits=lg)
+            out.append(lg.clone())
+        runs.append(torch.stack(out))
+    sm.model.set_deterministic_batch(False)
+    assert all(st.device_error() == 0 for st in states)
+    assert torch.equal(runs[0], runs[1])
+    scale = runs[0].abs().max().item()
+    assert (runs[0] - runs[2]).abs().max().item() <= 1e-3 * scale
+
+
 def test_batched_step_continues_from_each_slots_own_argmax():
     """tokens=None: every slot feeds back its previous greedy token on the device."""
     B = 6

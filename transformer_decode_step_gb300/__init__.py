@@ -82,6 +82,7 @@ _SIGS = {
     "pnb_forward_poll": (_i32, [_p, _p, _p]),
     "pnb_state_stream": (_i32, [_p, _p]),
     "pnb_model_set_graphs": (_i32, [_p, _i32]),
+    "pnb_model_set_deterministic_batch": (_i32, [_p, _i32]),
     "pnb_model_set_tensor_attention": (_i32, [_p, _i32]),
     "pnb_model_is_tensor_attention": (_i32, [_p]),
     "pnb_step_kernel_count": (_i32, [_p, _i32]),
@@ -181,6 +182,10 @@ class Model:
 
     def set_graphs(self, enable: bool):
         check(pnb_model_set_graphs(self._h, 1 if enable else 0), "pnb_model_set_graphs")
+
+    def set_deterministic_batch(self, enable: bool):
+        check(pnb_model_set_deterministic_batch(self._h, 1 if enable else 0),
+              "pnb_model_set_deterministic_batch")
 
     def set_tensor_attention(self, enable: bool):
         check(pnb_model_set_tensor_attention(self._h, 1 if enable else 0),

@@ -120,6 +120,7 @@ struct pnb_model {
   int n_split_tc = 1;
   bool sample_ok = false;                // the sampler kernel fits this vocabulary
   int mode_gen = 0;                      // bumped when a launch mode changes (graphs re-captured)
+  bool det_batch = false;                // batched residual K parts in fixed point
   cudaStream_t cap_stream = nullptr;     // stream used for graph capture
   struct BatchCtx *batch = nullptr;      // batched-slot step (made on first use)
 };
@@ -138,6 +139,7 @@ struct BatchCtx {
   int32_t *am_idx = nullptr, *pos = nullptr, *err = nullptr;
   StepIO *pio = nullptr;                 // prefill: the I/O words of a chunk's virtual slots
   float *gates = nullptr;                // MoE: [slot][expert] router weights (0 = not chosen)
+  long long *acc = nullptr;              // [slot][n_embd] residual K-part sums, fixed point 2^-32
   __nv_bfloat16 *xop_e = nullptr, *xop_o = nullptr, *xop_f = nullptr;
   float2 *rope = nullptr;
   BSlot *slots = nullptr;
@@ -581,6 +583,7 @@ int batch_setup(pnb_model *m) {
   const size_t o_amv = take((size_t)MB * m->num_sms * 4), o_ami = take((size_t)MB * m->num_sms * 4);
   const size_t o_amc = take(4), o_err = take(4), o_pio = take((size_t)MB * sizeof(StepIO));
   const size_t o_gates = take((size_t)MB * std::max(1, c.expert_count) * 4);
+  const size_t o_acc = take((size_t)MB * E * 8);
   if (cudaMalloc(&b->ws, off) != cudaSuccess) {
     delete b;
     return PNB_E_NOMEM;
@@ -607,6 +610,7 @@ int batch_setup(pnb_model *m) {
   b->err = reinterpret_cast<int32_t *>(b->ws + o_err);
   b->pio = reinterpret_cast<StepIO *>(b->ws + o_pio);
   b->gates = reinterpret_cast<float *>(b->ws + o_gates);
+  b->acc = reinterpret_cast<long long *>(b->ws + o_acc);
   bool ok = true;
   b->w_qkv.resize(L);
   b->w_o.resize(L);
@@ -665,6 +669,9 @@ BGemmArgs bgemm_args(const pnb_model *m, const BatchCtx *b, const BPlan &p, int 
   g.hd = m->hd;
   g.cap = m->cap;
   g.err = b->err;
+  g.acc = b->acc;
+  if (m->det_batch && kind == kEpiResid) g.kind = kEpiResidFix;
+  if (m->det_batch && kind == kEpiResidGate) g.kind = kEpiResidGateFix;
   return g;
 }
 
@@ -711,6 +718,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
   for (int l = 0; l < c.n_layer; ++l) {
     na.emb = l == 0 ? m->tok_embd : nullptr;
     na.tokens = l == 0 ? tokens : nullptr;
+    na.acc = l == 0 || !m->det_batch ? nullptr : b->acc;
     na.norm_w = m->attn_norm[l];
     na.tr = KTrace{trace, 7 * l};
     if ((e = launch_bnorm(na, st, l > 0)) != cudaSuccess) return e;
@@ -802,6 +810,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
       return e;
     na.emb = nullptr;
     na.tokens = nullptr;
+    na.acc = m->det_batch ? b->acc : nullptr;
     na.norm_w = m->ffn_norm[l];
     na.tr = KTrace{trace, 7 * l + 4};
     if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
@@ -846,6 +855,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
   }
   na.emb = nullptr;
   na.tokens = nullptr;
+  na.acc = m->det_batch ? b->acc : nullptr;
   na.norm_w = m->out_norm;
   na.tr = KTrace{trace, 7 * c.n_layer};
   if ((e = launch_bnorm(na, st, true)) != cudaSuccess) return e;
@@ -1434,6 +1444,13 @@ int pnb_model_set_graphs(pnb_model *m, int enable) {
   if (!m) return PNB_E_NULL;
   ++m->mode_gen;
   m->graphs = enable != 0;
+  return PNB_OK;
+}
+
+int pnb_model_set_deterministic_batch(pnb_model *m, int enable) {
+  if (!m) return PNB_E_NULL;
+  ++m->mode_gen;
+  m->det_batch = enable != 0;
   return PNB_OK;
 }
 

@@ -35,6 +35,25 @@ __device__ __forceinline__ float silu_b(float z) { return z / (1.0f + expf(-z));
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Fixed point of the residual K-part sums: units of 2^-32, 64-bit integers.
+// Scaling an fp32 value by 2^32 is exact, so each part converts to the
+// nearest unit directly (no fp64: its rate on this part is a small fraction
+// of fp32's).
+constexpr float kFixScale = 4294967296.0f, kFixUnit = 1.0f / 4294967296.0f;
+__device__ __forceinline__ void fix_add(long long *p, float v) {
+  atomicAdd(reinterpret_cast<unsigned long long *>(p),
+            static_cast<unsigned long long>(__float2ll_rn(v * kFixScale)));
+}
+// x plus its pending fixed-point sum (the sum rounded to fp32, then the add)
+__device__ __forceinline__ float fix_fold(float x, long long a) {
+  return x + __ll2float_rn(a) * kFixUnit;
+}
+__device__ __forceinline__ float4 fold4(float4 f, const long long *acc) {
+  const longlong2 a0 = __ldcg(reinterpret_cast<const longlong2 *>(acc));
+  const longlong2 a1 = __ldcg(reinterpret_cast<const longlong2 *>(acc) + 1);
+  return make_float4(fix_fold(f.x, a0.x), fix_fold(f.y, a0.y), fix_fold(f.z, a1.x), fix_fold(f.w, a1.y));
+}
+
 __device__ __forceinline__ void am_merge(float &v, int &i, float ov, int oi) {
   if (ov > v || (ov == v && oi < i)) {
     v = ov;
@@ -47,6 +66,7 @@ __device__ __forceinline__ void am_merge(float &v, int &i, float ov, int oi) {
 // value) and bp + b (bf16 of what the first rounding left).  On the first
 // layer x_b is the embedding row of the slot's token, and the CTA also
 // publishes the slot table, the slot's position and its RoPE angles.
+template <bool FOLD>   // FOLD: fold the fixed-point K-part sums into x first
 __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
   __shared__ float red[8];
   __shared__ int tok_s, pos_s;
@@ -105,6 +125,7 @@ __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
           f = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
         } else {
           f = __ldcg(reinterpret_cast<const float4 *>(xr + i));
+          if constexpr (FOLD) f = fold4(f, a.acc + (size_t)b * a.E + i);
         }
       }
       v[4 * j] = f.x;
@@ -134,6 +155,7 @@ __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
             f = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
           } else {
             f = __ldcg(reinterpret_cast<const float4 *>(xr + i));
+            if constexpr (FOLD) f = fold4(f, a.acc + (size_t)b * a.E + i);
           }
         }
         v[4 * j] = f.x;
@@ -147,8 +169,13 @@ __global__ void __launch_bounds__(256) k_bnorm(const BNormArgs a) {
       const int i = base + (j * 256 + tid) * 4;
       if (i >= a.E) continue;
       const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + i);
-      if (row) *reinterpret_cast<float4 *>(a.x_out + (size_t)b * a.E + i) =
+      if (row || FOLD) *reinterpret_cast<float4 *>(a.x_out + (size_t)b * a.E + i) =
           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      if constexpr (FOLD) {
+        longlong2 *z = reinterpret_cast<longlong2 *>(a.acc + (size_t)b * a.E + i);
+        z[0] = make_longlong2(0, 0);
+        z[1] = make_longlong2(0, 0);
+      }
       const float n[4] = {v[4 * j] * inv * w.x, v[4 * j + 1] * inv * w.y, v[4 * j + 2] * inv * w.z,
                           v[4 * j + 3] * inv * w.w};
       __nv_bfloat16 h[4], l[4];
@@ -329,6 +356,9 @@ template <int BP, int KIND>
 __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ CUtensorMap tw,
                                                         const __grid_constant__ CUtensorMap tx,
                                                         const BGemmArgs a) {
+  // the epilogue kind, and whether residual K parts go into the fixed-point sum
+  constexpr int EK = KIND == kEpiResidFix ? kEpiResid : (KIND == kEpiResidGateFix ? kEpiResidGate : KIND);
+  constexpr bool FIX = KIND != EK;
   constexpr int N = 2 * BP;
   constexpr int XB = N * 128, SB = kWTile + XB;
   constexpr uint32_t ACOLS = N < 32 ? 32u : (uint32_t)N;
@@ -476,24 +506,31 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
       if (lane == 0) mbar_arrive(&m.acce[acc]);
       const int tile = u / a.ksplit;
       if (a.ksplit == 1) {
-        epilogue<BP, KIND>(a, tile, row, y, bv, bi);
-      } else if constexpr (KIND == kEpiResid) {
+        epilogue<BP, EK>(a, tile, row, y, bv, bi);
+      } else if constexpr (EK == kEpiResid) {
         // a residual update is a sum: each K part adds its share with a
-        // fire-and-forget fp32 reduction (summation order not fixed)
+        // fire-and-forget reduction, in fp32 (order not fixed) or, for the
+        // deterministic step, in 64-bit fixed point (the next norm folds it in)
         const int grow = tile * 128 + row;
         if (grow < a.rows) {
 #pragma unroll
           for (int b = 0; b < BP; ++b)
-            if (b < a.B) atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
+            if (b < a.B) {
+              if constexpr (FIX) fix_add(a.acc + (size_t)b * a.rows + grow, y[b]);
+              else atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
+            }
         }
-      } else if constexpr (KIND == kEpiResidGate) {
+      } else if constexpr (EK == kEpiResidGate) {
         const int grow = tile * 128 + row;
         if (grow < a.rows) {
 #pragma unroll
           for (int b = 0; b < BP; ++b)
             if (b < a.B) {
               const float gs = a.gate[(size_t)b * a.gate_ld];
-              if (gs != 0.f) atomicAdd(a.x + (size_t)b * a.rows + grow, gs * y[b]);
+              if (gs != 0.f) {
+                if constexpr (FIX) fix_add(a.acc + (size_t)b * a.rows + grow, gs * y[b]);
+                else atomicAdd(a.x + (size_t)b * a.rows + grow, gs * y[b]);
+              }
             }
         }
       } else if constexpr (KIND == kEpiQkv || KIND == kEpiGateUp) {
@@ -525,7 +562,7 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
 #pragma unroll
             for (int b = 0; b < BP; ++b) y[b] += t[b];
           }
-          epilogue<BP, KIND>(a, tile, row, y, bv, bi);
+          epilogue<BP, EK>(a, tile, row, y, bv, bi);
           if (row == 0) a.tile_cnt[tile] = 0u;
         }
         epi_sync();
@@ -684,6 +721,8 @@ cudaError_t launch_bp(const void *tw, const void *tx, const BGemmArgs &a, int gr
     case kEpiGateUp: return launch_k<BP, kEpiGateUp>(tw, tx, a, grid, smem, st, pdl);
     case kEpiLm: return launch_k<BP, kEpiLm>(tw, tx, a, grid, smem, st, pdl);
     case kEpiResidGate: return launch_k<BP, kEpiResidGate>(tw, tx, a, grid, smem, st, pdl);
+    case kEpiResidFix: return launch_k<BP, kEpiResidFix>(tw, tx, a, grid, smem, st, pdl);
+    case kEpiResidGateFix: return launch_k<BP, kEpiResidGateFix>(tw, tx, a, grid, smem, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -699,6 +738,12 @@ cudaError_t prepare_bp(int smem) {
     return e;
   if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiResidFix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiResidGateFix>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(k_bgemm<BP, kEpiResidGate>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
@@ -820,7 +865,8 @@ cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_bnorm, a);
+  if (a.acc && !a.emb) return cudaLaunchKernelEx(&cfg, k_bnorm<true>, a);
+  return cudaLaunchKernelEx(&cfg, k_bnorm<false>, a);
 }
 
 }  // namespace pnb

@@ -274,7 +274,10 @@ cudaError_t prepare_attn_tc_kernels();
 // Epilogues of the batched tensor-core GEMM
 // kEpiResidGate: the residual add scaled per slot by gate[b * gate_ld] (0 =
 // no add), for the MoE down projections of the batched step
-enum BEpi { kEpiQkv = 0, kEpiResid = 1, kEpiGateUp = 2, kEpiLm = 3, kEpiResidGate = 4 };
+// kEpiResidFix / kEpiResidGateFix: the same, K parts added in fixed point
+// (the deterministic batched step; see acc below)
+enum BEpi { kEpiQkv = 0, kEpiResid = 1, kEpiGateUp = 2, kEpiLm = 3, kEpiResidGate = 4,
+            kEpiResidFix = 5, kEpiResidGateFix = 6 };
 
 // Y[b][r] = sum_k W[r][k] * X[b][k] for the B slots of a batched step, on
 // tcgen05 (tiles of 128 weight rows, slots as the MMA's N dimension with the
@@ -307,6 +310,11 @@ struct BGemmArgs {
   int32_t *am_idx;
   unsigned *am_cnt;
   int32_t *err;          // batch error word
+  // residual kinds with ksplit > 1: each K part adds its share into x with
+  // an fp32 atomic add (order not fixed), or (kEpiResidFix / kEpiResidGateFix)
+  // into acc in 64-bit fixed point (units of 2^-32): an integer sum, the same
+  // in any order, which the next k_bnorm folds into x and clears
+  long long *acc;        // [B][rows]
   KTrace tr;
 };
 
@@ -341,6 +349,9 @@ struct BNormArgs {
   const double *inv_freq;  // [hd / 2]
   int hd, n_ctx;
   int32_t *err;
+  // layers > 0 and the final norm: the residual GEMMs' fixed-point K-part
+  // sums [B][E] (units of 2^-32), folded into x (written back) and cleared
+  long long *acc;
   KTrace tr;
   BSlot slots[64];         // first layer: the slots of this step
 };
