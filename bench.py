@@ -54,6 +54,9 @@ def parse():
                     help="each step also draws the next token on the GPU (pnb_sample: "
                          "temperature 0.8, top-k 40, top-p 0.95, repetition penalty 1.1 "
                          "over 64 recent tokens) instead of taking the greedy one")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="batched workloads: bitwise reproducible steps "
+                         "(pnb_model_set_deterministic_batch: residual K parts in fixed point)")
     ap.add_argument("--kernel-trace", action="store_true",
                     help="single-sequence workloads: after the timed steps, one traced step "
                          "(per-CTA globaltimer stamps) gives each kernel's in-graph time, from the "
@@ -300,8 +303,10 @@ def arm_config(args, w, world: int) -> dict:
     if is_batched(args, w):
         B = args.batch or w.batch
         starts = batched_starts(w, B)
-        return workload_config(w, {**par, "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"},
-                               batch=B)
+        extra = {**par, "slot_positions": f"U[{min(starts)}, {max(starts)}] + step"}
+        if args.deterministic:
+            extra["residual_k_parts"] = "64-bit fixed point (bitwise reproducible steps)"
+        return workload_config(w, extra, batch=B)
     P = w.prefill
     return workload_config(w, {**par, "positions": f"{P}..{w.shape.n_ctx - 1}",
                                "next_token": SAMPLED if args.sample else "greedy (argmax)"})
@@ -586,6 +591,7 @@ def run_batched(args, w):
     starts = batched_starts(w, B)
     budget = s.n_ctx - max(starts)
     sm = pnb.SynthModel(s, w.seed)
+    sm.model.set_deterministic_batch(args.deterministic)
     # replica r serves its own slots (seeded by slot id r * B + b)
     states = [sm.new_state(p, slot=rank * B + b) for b, p in enumerate(starts)]
     tok0 = torch.tensor([wl.prompt_tokens(w, rank * B + b)[0] for b in range(B)],
