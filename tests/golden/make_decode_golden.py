@@ -8,7 +8,8 @@ Loop": forward, then argmax at temperature 0, lowest id on ties):
 * Llama-7B, Mistral-7B (sliding window 4096) and Mixtral (8 experts, top-2):
   128 steps from the pre-filled positions 2048 / 8192 / 4096;
 * Llama-7B with Q8_0 and with Q4_0 weights (64 steps) and Mixtral with Q8_0
-  weights, router and experts included (32 steps), from the same positions;
+  and with Q4_0 weights, router and experts included (32 steps), from the
+  same positions;
 * the batched Llama-8B workload: 64 steps of slots 0, 7, 15, 31 and 63, each
   from its own seeded start position and token (a slot's sequence does not
   depend on which other slots share the batch, so one run per slot serves
@@ -159,11 +160,11 @@ def run(w):
 
 
 # the quantized forms (every matrix in Q8_0 / Q4_0 blocks) over shorter decodes
-QUANT_STEPS = {wl.LLAMA7B_Q8.name: 64, wl.LLAMA7B_Q4.name: 64, wl.MIXTRAL_Q8.name: 32}
-WORKLOADS = [wl.LLAMA7B, wl.MISTRAL7B, wl.LLAMA8B_BATCHED, wl.MIXTRAL,
-             wl.LLAMA7B_Q8.with_(steps=QUANT_STEPS[wl.LLAMA7B_Q8.name]),
-             wl.LLAMA7B_Q4.with_(steps=QUANT_STEPS[wl.LLAMA7B_Q4.name]),
-             wl.MIXTRAL_Q8.with_(steps=QUANT_STEPS[wl.MIXTRAL_Q8.name])]
+QUANT_STEPS = {wl.LLAMA7B_Q8.name: 64, wl.LLAMA7B_Q4.name: 64, wl.MIXTRAL_Q8.name: 32,
+               wl.MIXTRAL_Q4.name: 32}
+WORKLOADS = [wl.LLAMA7B, wl.MISTRAL7B, wl.LLAMA8B_BATCHED, wl.MIXTRAL] + \
+    [w.with_(steps=QUANT_STEPS[w.name]) for w in (wl.LLAMA7B_Q8, wl.LLAMA7B_Q4, wl.MIXTRAL_Q8,
+                                                  wl.MIXTRAL_Q4)]
 
 if __name__ == "__main__":
     names = sys.argv[1:] or [w.name for w in WORKLOADS]

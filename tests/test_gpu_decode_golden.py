@@ -5,8 +5,8 @@ The oracle's greedy decodes are stored by ``tests/golden/make_decode_golden.py``
 
 * Llama-7B, Mistral-7B (4096-position window ring) and Mixtral (8 experts,
   top-2): 128 steps from the pre-filled positions 2048 / 8192 / 4096;
-* Llama-7B with Q8_0 and Q4_0 weights (64 steps) and Mixtral with Q8_0
-  weights (32 steps), every matrix in blocks;
+* Llama-7B with Q8_0 and Q4_0 weights (64 steps) and Mixtral with Q8_0 and
+  Q4_0 weights (32 steps), every matrix in blocks;
 * the batched Llama-8B workload: 64 steps of slots 0, 7, 15, 31 and 63.
 
 The GPU decodes the same workload through the C ABI (``pnb_forward``, or
@@ -123,7 +123,7 @@ class Recorder:
 # the quantized forms: shorter stored decodes (Q8_0 / Q4_0 blocks, MoE router and
 # experts included)
 QUANT = [wl.LLAMA7B_Q8.with_(steps=64), wl.LLAMA7B_Q4.with_(steps=64),
-         wl.MIXTRAL_Q8.with_(steps=32)]
+         wl.MIXTRAL_Q8.with_(steps=32), wl.MIXTRAL_Q4.with_(steps=32)]
 
 
 @pytest.mark.parametrize("w", [wl.LLAMA7B, wl.MISTRAL7B, wl.MIXTRAL] + QUANT, ids=lambda w: w.name)
