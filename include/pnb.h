@@ -238,8 +238,8 @@ int pnb_model_set_graphs(pnb_model *m, int enable);
    each part adds into a 64-bit fixed-point sum (units of 2^-32, exact and
    independent of the order), which the next norm folds into the residual
    once: the same steps from the same states then give the same bits, at
-   about 3.5 % of step time (Llama-8B shapes, B = 8 and 64; the 64-bit adds
-   and the fold).  The single-sequence step is reproducible either way.  Takes effect at the next
+   3-4 % of step time (Llama-8B shapes: 4.2 % at B = 8, 3.2 % at B = 64; the
+   64-bit adds and the fold).  The single-sequence step is reproducible either way.  Takes effect at the next
    batched step (its graph is re-captured). */
 int pnb_model_set_deterministic_batch(pnb_model *m, int enable);
 
