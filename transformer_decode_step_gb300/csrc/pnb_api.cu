@@ -688,7 +688,7 @@ BGemmArgs bgemm_args(const pnb_model *m, const BatchCtx *b, const BPlan &p, int 
 enum { kSlots = 0, kChunkKernel = 1, kChunkGroups = 2, kChunkSlots = 3 };
 cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t *tokens,
                           unsigned long long *trace, cudaStream_t st, float *logits, int32_t *argmax,
-                          int chunk = kSlots) {
+                          int chunk = kSlots, const uint8_t *order = nullptr) {
   const bool shared_kv = chunk == kChunkKernel;
   BatchCtx *b = m->batch;
   const pnb_config &c = m->cfg;
@@ -766,6 +766,10 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
       ta.nstages = attn_tc_stages(m->hd);
       ta.tr = KTrace{trace, 7 * l + 2};
       ta.shared_cache = chunk != kSlots;
+      if (chunk == kSlots && order) {
+        ta.use_order = 1;
+        for (int i = 0; i < B; ++i) ta.order[i] = order[i];
+      }
       int cols = c.n_head / c.n_kv_head;
       if (chunk == kChunkGroups) {
         // a chunk's tokens share the cache: T consecutive tokens per CTA
@@ -1217,9 +1221,23 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   BSlot slots[kMaxBatch];
   for (int i = 0; i < B; ++i) slots[i] = BSlot{states[i]->kv, states[i]->io, states[i]->maps};
+  // the attention's slot order: longest attended range first (ties: lower
+  // slot), from the positions at capture; all slots advance together, so the
+  // ranking holds while the graph is replayed
+  uint8_t order[kMaxBatch];
+  {
+    int len[kMaxBatch];
+    for (int i = 0; i < B; ++i) {
+      const int64_t n = states[i]->pos + 1;
+      len[i] = (int)(c.sliding_window > 0 ? std::min<int64_t>(n, c.sliding_window) : n);
+      order[i] = (uint8_t)i;
+    }
+    std::stable_sort(order, order + B, [&](uint8_t x, uint8_t y) { return len[x] > len[y]; });
+  }
   unsigned long long *trace = states[0]->ktrace;   // optional, the first slot's buffer
   if (!m->graphs) {
-    if (enqueue_batch(m, slots, B, tokens_dev, trace, st, logits_dev, argmax_dev) != cudaSuccess)
+    if (enqueue_batch(m, slots, B, tokens_dev, trace, st, logits_dev, argmax_dev, kSlots, order) !=
+        cudaSuccess)
       return PNB_E_CUDA;
   } else {
     const bool same = b->exec && b->g_B == B && b->g_gen == m->mode_gen && b->g_tokens == tokens_dev &&
@@ -1234,7 +1252,8 @@ int pnb_forward_batch(pnb_model *m, pnb_state *const *states, int32_t B, const i
       cudaGraph_t graph = nullptr;
       if (cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
         return PNB_E_CUDA;
-      cudaError_t le = enqueue_batch(m, slots, B, tokens_dev, trace, m->cap_stream, logits_dev, argmax_dev);
+      cudaError_t le = enqueue_batch(m, slots, B, tokens_dev, trace, m->cap_stream, logits_dev, argmax_dev,
+                                     kSlots, order);
       cudaError_t ce = cudaStreamEndCapture(m->cap_stream, &graph);
       if (le != cudaSuccess || ce != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);

@@ -140,8 +140,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
   constexpr int PCH = TL<HD>::PCH;
   constexpr uint32_t TCOLS = TL<HD>::TCOLS;
   const int NS = a.nstages;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const bool batched = a.slots != nullptr;
+  const int split = blockIdx.x, g = blockIdx.y;
+  const int b = batched && a.use_order ? (int)a.order[blockIdx.z] : (int)blockIdx.z;
   // column h: query head h0 + h % GH of virtual slot b * T + h / GH (T = 1:
   // the CTA's slot, every column one of its query heads)
   const int T = batched && a.tok_group > 1 ? a.tok_group : 1;

@@ -246,6 +246,11 @@ struct AttnTcArgs {
   // each masked to its own positions; the grid's z is the group.  0 or 1:
   // one slot per z.
   int tok_group;
+  // batched slots with their own caches (tok_group <= 1): grid z = rank, slot
+  // order[rank]; ranked longest attended range first, so that in a grid of
+  // several waves the long CTAs start first (any permutation is correct)
+  uint8_t order[64];
+  int use_order;
   KTrace tr;
 };
 
