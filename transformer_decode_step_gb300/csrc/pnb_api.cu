@@ -523,9 +523,15 @@ BPlan plan_bgemm(int64_t rows, int K, int num_sms) {
 int bp_index(int bp) { return bp == 16 ? 0 : (bp == 32 ? 1 : 2); }
 
 int attn_split_b(const pnb_model *m, int B) {
-  if (m->attn_tc)
-    return std::max(1, std::min({attn_tc_max_split(), m->num_sms / (m->cfg.n_kv_head * B),
-                                 ceil_div(m->cap, 128)}));
+  if (m->attn_tc) {
+    // one wave of CTAs split evenly; when one CTA per (slot, KV head) would
+    // leave part of the wave idle, two per slot (the long slots' CTAs start
+    // first, so the second partial wave fills in behind them)
+    const int per = m->cfg.n_kv_head * B;
+    int split = m->num_sms / per;
+    if (split == 1 && per < m->num_sms) split = 2;
+    return std::max(1, std::min({attn_tc_max_split(), split, ceil_div(m->cap, 128)}));
+  }
   const int per = m->cfg.n_kv_head * m->zgroups * B;
   return std::max(1, std::min(m->num_sms / std::max(1, per), std::max(1, m->cap / 16)));
 }
