@@ -32,6 +32,8 @@ constexpr int kMaxSmem = 227 * 1024;
 // rows); past it the per-token tensor-core attention is faster
 constexpr int kChunkAttnMaxPos = 256;
 constexpr int kMaxBatch = 64;
+// prefill chunk: up to 128 virtual slots (the pages' default chunk length)
+constexpr int kMaxChunk = 128;
 #ifndef PNB_INFLIGHT_KB
 #define PNB_INFLIGHT_KB 192
 #endif
@@ -145,9 +147,10 @@ struct BatchCtx {
   BSlot *slots = nullptr;
   std::vector<CUtensorMap> w_qkv, w_o, w_gu, w_dn;
   CUtensorMap w_lm;
-  CUtensorMap x_e[3], x_o[3], x_f[3];   // per padded slot count 16, 32, 64
+  CUtensorMap x_e[4], x_o[4], x_f[4];   // per padded slot count 16, 32, 64, 128
   BPlan p_qkv, p_o, p_gu, p_dn, p_lm;
-  int nstages[3] = {0, 0, 0}, smem[3] = {0, 0, 0};
+  int nstages[4] = {0, 0, 0, 0}, smem[4] = {0, 0, 0, 0};
+  float *lgs = nullptr;                  // 128-slot LM head: logits when the caller wants none
   // captured step and what it was captured for
   cudaGraphExec_t exec = nullptr;
   int g_B = 0, g_gen = -1;
@@ -520,7 +523,7 @@ BPlan plan_bgemm(int64_t rows, int K, int num_sms) {
   return p;
 }
 
-int bp_index(int bp) { return bp == 16 ? 0 : (bp == 32 ? 1 : 2); }
+int bp_index(int bp) { return bp == 16 ? 0 : (bp == 32 ? 1 : (bp == 64 ? 2 : 3)); }
 
 int attn_split_b(const pnb_model *m, int B) {
   if (m->attn_tc) {
@@ -557,7 +560,7 @@ int batch_setup(pnb_model *m) {
   if (m->batch) return PNB_OK;
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, F = c.n_ff, Hd = c.n_head * m->hd, L = c.n_layer;
-  const int MB = kMaxBatch, BPmax = 64;
+  const int MB = kMaxChunk, BPmax = 128;
   BatchCtx *b = new (std::nothrow) BatchCtx();
   if (!b) return PNB_E_NOMEM;
   b->p_qkv = plan_bgemm(m->qkv_rows, E, m->num_sms);
@@ -590,6 +593,7 @@ int batch_setup(pnb_model *m) {
   const size_t o_amc = take(4), o_err = take(4), o_pio = take((size_t)MB * sizeof(StepIO));
   const size_t o_gates = take((size_t)MB * std::max(1, c.expert_count) * 4);
   const size_t o_acc = take((size_t)MB * E * 8);
+  const size_t o_lgs = take((size_t)MB * c.n_vocab * 4);
   if (cudaMalloc(&b->ws, off) != cudaSuccess) {
     delete b;
     return PNB_E_NOMEM;
@@ -617,6 +621,7 @@ int batch_setup(pnb_model *m) {
   b->pio = reinterpret_cast<StepIO *>(b->ws + o_pio);
   b->gates = reinterpret_cast<float *>(b->ws + o_gates);
   b->acc = reinterpret_cast<long long *>(b->ws + o_acc);
+  b->lgs = reinterpret_cast<float *>(b->ws + o_lgs);
   bool ok = true;
   b->w_qkv.resize(L);
   b->w_o.resize(L);
@@ -632,7 +637,7 @@ int batch_setup(pnb_model *m) {
            encode_map(&b->w_dn[(size_t)l * S + e], m->w_down[(size_t)l * S + e], E, F, 128);
   }
   ok = ok && encode_map(&b->w_lm, m->output, c.n_vocab, E, 128);
-  for (int i = 0; i < 3 && ok; ++i) {
+  for (int i = 0; i < 4 && ok; ++i) {
     const int bp = 16 << i;
     ok = encode_map(&b->x_e[i], b->xop_e, 2 * bp, E, 2 * bp) &&
          encode_map(&b->x_o[i], b->xop_o, 2 * bp, Hd, 2 * bp) &&
@@ -699,7 +704,7 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
   BatchCtx *b = m->batch;
   const pnb_config &c = m->cfg;
   const int E = c.n_embd, Hd = c.n_head * m->hd, F = c.n_ff;
-  const int bp = B <= 16 ? 16 : (B <= 32 ? 32 : 64), bi = bp_index(bp);
+  const int bp = B <= 16 ? 16 : (B <= 32 ? 32 : (B <= 64 ? 64 : 128)), bi = bp_index(bp);
   const int smem = b->smem[bi];
   const size_t layer_kv = (size_t)c.n_kv_head * m->cap * m->hd * m->kv_es;
   const float eps = (float)c.rms_norm_eps;
@@ -876,7 +881,19 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
   g.am_val = b->am_val;
   g.am_idx = b->am_idx;
   g.am_cnt = b->am_cnt;
-  return launch_bgemm(&b->w_lm, &b->x_e[bi], g, b->p_lm.grid, smem, st, true);
+  if (bp <= 64) return launch_bgemm(&b->w_lm, &b->x_e[bi], g, b->p_lm.grid, smem, st, true);
+  // 128 slots: the LM head writes logits only; the greedy pick follows
+  if (!logits) g.logits = b->lgs;
+  if ((e = launch_bgemm(&b->w_lm, &b->x_e[bi], g, b->p_lm.grid, smem, st, true)) != cudaSuccess) return e;
+  BArgmaxArgs ma{};
+  ma.logits = g.logits;
+  ma.V = c.n_vocab;
+  ma.B = B;
+  ma.slots = b->slots;
+  ma.pos = b->pos;
+  ma.argmax_out = argmax;
+  ma.err = b->err;
+  return launch_bargmax(ma, st, true);
 }
 
 }  // namespace
@@ -1425,7 +1442,7 @@ int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T
   const bool ring = c.sliding_window > 0 && m->cap < c.n_ctx;
   const size_t V = (size_t)c.n_vocab;
   for (int i = 0; i < T;) {
-    int n = std::min(kMaxBatch, T - i);
+    int n = std::min(kMaxChunk, T - i);
     // a ring cache must not wrap inside a chunk: a later chunk position would
     // overwrite a slot inside an earlier chunk token's window
     if (ring) n = s->pos >= m->cap ? 1 : std::min(n, m->cap - s->pos);
@@ -1439,7 +1456,7 @@ int pnb_prefill(pnb_model *m, pnb_state *s, const int32_t *tokens_dev, int32_t T
         return PNB_E_CUDA;
     } else {
       BatchCtx *b = m->batch;
-      BSlot slots[kMaxBatch];
+      BSlot slots[kMaxChunk];
       for (int j = 0; j < n; ++j) slots[j] = BSlot{s->kv, &b->pio[j], s->maps};
       if (launch_prefill_begin(b->pio, s->io, n, st) != cudaSuccess ||
           enqueue_batch(m, slots, n, tokens_dev + i, nullptr, st, lg, am,

@@ -251,35 +251,44 @@ struct UnitChunks {
 // compiler would otherwise keep one round trip per slot).
 constexpr int kEpiChunk = 16;
 
-template <int BP, int KIND>
-__device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, const float (&y)[BP],
-                                         float (&bv)[BP], int (&bi)[BP]) {
+// Slots b0 .. b0 + C - 1 of the epilogue (all BP slots at once up to 64
+// padded slots; 32 at a time above).  ARG: the LM head also keeps each slot's
+// best row (else it writes logits only).
+template <int C, int KIND, bool ARG = true>
+__device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, const float (&y)[C],
+                                         int b0, float (&bv)[C], int (&bi)[C]) {
   const int grow = tile * 128 + row;
   const bool in = grow < a.rows;
+  constexpr int CH = C < kEpiChunk ? C : kEpiChunk;
   if constexpr (KIND == kEpiResid) {
 #pragma unroll
-    for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
-      float xv[kEpiChunk];
+    for (int c0 = 0; c0 < C; c0 += CH) {
+      float xv[CH];
 #pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j)
-        xv[j] = (in && c0 + j < a.B) ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
+      for (int j = 0; j < CH; ++j) {
+        const int b = b0 + c0 + j;
+        xv[j] = (in && b < a.B) ? __ldcg(a.x + (size_t)b * a.rows + grow) : 0.f;
+      }
 #pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j)
-        if (in && c0 + j < a.B) a.x[(size_t)(c0 + j) * a.rows + grow] = xv[j] + y[c0 + j];
+      for (int j = 0; j < CH; ++j) {
+        const int b = b0 + c0 + j;
+        if (in && b < a.B) a.x[(size_t)b * a.rows + grow] = xv[j] + y[c0 + j];
+      }
     }
   } else if constexpr (KIND == kEpiResidGate) {
 #pragma unroll
-    for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
-      float xv[kEpiChunk], gs[kEpiChunk];
+    for (int c0 = 0; c0 < C; c0 += CH) {
+      float xv[CH], gs[CH];
 #pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j) {
-        const bool live = in && c0 + j < a.B;
-        gs[j] = live ? a.gate[(size_t)(c0 + j) * a.gate_ld] : 0.f;
-        xv[j] = gs[j] != 0.f ? __ldcg(a.x + (size_t)(c0 + j) * a.rows + grow) : 0.f;
+      for (int j = 0; j < CH; ++j) {
+        const int b = b0 + c0 + j;
+        const bool live = in && b < a.B;
+        gs[j] = live ? a.gate[(size_t)b * a.gate_ld] : 0.f;
+        xv[j] = gs[j] != 0.f ? __ldcg(a.x + (size_t)b * a.rows + grow) : 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j)
-        if (gs[j] != 0.f) a.x[(size_t)(c0 + j) * a.rows + grow] = xv[j] + gs[j] * y[c0 + j];
+      for (int j = 0; j < CH; ++j)
+        if (gs[j] != 0.f) a.x[(size_t)(b0 + c0 + j) * a.rows + grow] = xv[j] + gs[j] * y[c0 + j];
     }
   } else if constexpr (KIND == kEpiQkv) {
     const int hd = a.hd, half = hd / 2;
@@ -292,15 +301,15 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
     const int pair = (grow % hd) >> 1;
     const float bias = (a.bias && in) ? a.bias[grow] : 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < BP; c0 += kEpiChunk) {
-      float yv[kEpiChunk], par[kEpiChunk];
-      float2 cs[kEpiChunk];
-      int slot[kEpiChunk];
-      uint8_t *base[kEpiChunk];
+    for (int c0 = 0; c0 < C; c0 += CH) {
+      float yv[CH], par[CH];
+      float2 cs[CH];
+      int slot[CH];
+      uint8_t *base[CH];
 #pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j) {
-        const int b = c0 + j;
-        yv[j] = y[b] + bias;
+      for (int j = 0; j < CH; ++j) {
+        const int b = b0 + c0 + j;
+        yv[j] = y[c0 + j] + bias;
         par[j] = __shfl_xor_sync(0xffffffffu, yv[j], 1);
         const bool live = in && b < a.B;
         cs[j] = (live && rope) ? a.rope[(size_t)b * half + pair] : make_float2(1.f, 0.f);
@@ -308,8 +317,8 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
         base[j] = (live && !is_q) ? a.slots[b].kv : nullptr;
       }
 #pragma unroll
-      for (int j = 0; j < kEpiChunk; ++j) {
-        const int b = c0 + j;
+      for (int j = 0; j < CH; ++j) {
+        const int b = b0 + c0 + j;
         if (!(in && b < a.B)) continue;
         float v = yv[j];
         if (rope) {
@@ -328,10 +337,11 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
   } else if constexpr (KIND == kEpiGateUp) {
     const bool even = (grow & 1) == 0;
 #pragma unroll
-    for (int b = 0; b < BP; ++b) {
-      const float par = __shfl_xor_sync(0xffffffffu, y[b], 1);
+    for (int j = 0; j < C; ++j) {
+      const int b = b0 + j;
+      const float par = __shfl_xor_sync(0xffffffffu, y[j], 1);
       if (b < a.B && in && even) {
-        const float h = silu_b(y[b]) * par;
+        const float h = silu_b(y[j]) * par;
         const __nv_bfloat16 hi = __float2bfloat16_rn(h);
         const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
         const int i = grow >> 1;
@@ -342,10 +352,11 @@ __device__ __forceinline__ void epilogue(const BGemmArgs &a, int tile, int row, 
   } else {  // kEpiLm
     if (in) {
 #pragma unroll
-      for (int b = 0; b < BP; ++b) {
+      for (int j = 0; j < C; ++j) {
+        const int b = b0 + j;
         if (b < a.B) {
-          if (a.logits) a.logits[(size_t)b * a.rows + grow] = y[b];
-          am_merge(bv[b], bi[b], y[b], grow);
+          if (a.logits) a.logits[(size_t)b * a.rows + grow] = y[j];
+          if constexpr (ARG) am_merge(bv[j], bi[j], y[j], grow);
         }
       }
     }
@@ -461,170 +472,267 @@ __global__ void __launch_bounds__(kBThreads, 1) k_bgemm(const __grid_constant__ 
     // earlier kernels
     pdl_wait();
     const int q = warp & 3, row = 32 * q + lane;
-    float bv[BP];
-    int bi[BP];
-#pragma unroll
-    for (int b = 0; b < BP; ++b) {
-      bv[b] = -FLT_MAX;
-      bi[b] = INT_MAX;
-    }
-    bool ok = true;
-    int j = 0;
-    for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++j) {
-      const int acc = j & 1;
-      if (ok && !mbar_wait(&m.accf[acc], (j >> 1) & 1)) {
-        ok = false;
-        if (lane == 0) set_error(a.err, kErrTimeout);
-      }
-      if (j == 0 && row == 0) ktrace(a.tr, 3);
-      float y[BP];
-#pragma unroll
-      for (int b = 0; b < BP; ++b) y[b] = 0.f;
-      if (ok) {
-        tc_fence_after();
+    if constexpr (BP > 64) {
+      // 128 padded slots: each accumulator row is read and applied 32 slots
+      // at a time (a row's 128 values would not fit in registers); the LM
+      // head writes logits only, and a per-slot argmax kernel follows
+      float dv[32];
+      int di[32];
+      bool ok = true;
+      int j = 0;
+      for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++j) {
+        const int acc = j & 1;
+        if (ok && !mbar_wait(&m.accf[acc], (j >> 1) & 1)) {
+          ok = false;
+          if (lane == 0) set_error(a.err, kErrTimeout);
+        }
+        if (j == 0 && row == 0) ktrace(a.tr, 3);
+        const int tile = u / a.ksplit;
+        const int grow = tile * 128 + row;
         const uint32_t t0 = taddr + ((uint32_t)(32 * q) << 16) + (uint32_t)acc * ACOLS;
-        if constexpr (BP == 16) {
-          float v[32];
-          tmem_ld32(t0, v);
+        if (ok) tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < BP; c0 += 32) {
+          float y[32];
+          if (ok) {
+            float h[32], l[32];
+            tmem_ld32(t0 + c0, h);
+            tmem_ld32(t0 + BP + c0, l);
 #pragma unroll
-          for (int b = 0; b < 16; ++b) y[b] = v[b] + v[16 + b];
-        } else {
+            for (int i = 0; i < 32; ++i) y[i] = h[i] + l[i];
+          } else {
 #pragma unroll
-          for (int cb = 0; cb < N / 32; ++cb) {
-            float v[32];
-            tmem_ld32(t0 + 32 * cb, v);
+            for (int i = 0; i < 32; ++i) y[i] = 0.f;
+          }
+          if (a.ksplit == 1) {
+            epilogue<32, EK, false>(a, tile, row, y, c0, dv, di);
+          } else if constexpr (EK == kEpiResid) {
+            if (grow < a.rows) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (32 * cb < BP) y[32 * cb + i] = v[i];
-              else y[32 * cb - BP + i] += v[i];
+              for (int i = 0; i < 32; ++i)
+                if (c0 + i < a.B) {
+                  if constexpr (FIX) fix_add(a.acc + (size_t)(c0 + i) * a.rows + grow, y[i]);
+                  else atomicAdd(a.x + (size_t)(c0 + i) * a.rows + grow, y[i]);
+                }
             }
+          } else if constexpr (EK == kEpiResidGate) {
+            if (grow < a.rows) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (c0 + i < a.B) {
+                  const float gs = a.gate[(size_t)(c0 + i) * a.gate_ld];
+                  if (gs != 0.f) {
+                    if constexpr (FIX) fix_add(a.acc + (size_t)(c0 + i) * a.rows + grow, gs * y[i]);
+                    else atomicAdd(a.x + (size_t)(c0 + i) * a.rows + grow, gs * y[i]);
+                  }
+                }
+            }
+          } else {
+            // a partial tile: k_bmerge (QKV, gate/up) or the tile's last CTA
+            // (LM head) sums the K parts
+            float *P = a.part + (size_t)u * a.B * 128;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c0 + i < a.B) P[(size_t)(c0 + i) * 128 + row] = y[i];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.acce[acc]);
+        if constexpr (EK == kEpiLm) {
+          if (a.ksplit > 1) {
+            __threadfence();
+            epi_sync();
+            if (row == 0) *m.flag = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)a.ksplit - 1u;
+            epi_sync();
+            if (*m.flag) {
+              __threadfence();
+              const float *P0 = a.part + (size_t)tile * a.ksplit * a.B * 128;
+#pragma unroll 1
+              for (int c0 = 0; c0 < BP; c0 += 32) {
+                float y[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) y[i] = 0.f;
+                for (int k = 0; k < a.ksplit; ++k) {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (c0 + i < a.B) y[i] += __ldcg(P0 + ((size_t)k * a.B + c0 + i) * 128 + row);
+                }
+                epilogue<32, kEpiLm, false>(a, tile, row, y, c0, dv, di);
+              }
+              if (row == 0) a.tile_cnt[tile] = 0u;
+            }
+            epi_sync();
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&m.acce[acc]);
-      const int tile = u / a.ksplit;
-      if (a.ksplit == 1) {
-        epilogue<BP, EK>(a, tile, row, y, bv, bi);
-      } else if constexpr (EK == kEpiResid) {
-        // a residual update is a sum: each K part adds its share with a
-        // fire-and-forget reduction, in fp32 (order not fixed) or, for the
-        // deterministic step, in 64-bit fixed point (the next norm folds it in)
-        const int grow = tile * 128 + row;
-        if (grow < a.rows) {
-#pragma unroll
-          for (int b = 0; b < BP; ++b)
-            if (b < a.B) {
-              if constexpr (FIX) fix_add(a.acc + (size_t)b * a.rows + grow, y[b]);
-              else atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
-            }
+      if (row == 0) ktrace(a.tr, 4);
+    } else {
+      float bv[BP];
+      int bi[BP];
+  #pragma unroll
+      for (int b = 0; b < BP; ++b) {
+        bv[b] = -FLT_MAX;
+        bi[b] = INT_MAX;
+      }
+      bool ok = true;
+      int j = 0;
+      for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++j) {
+        const int acc = j & 1;
+        if (ok && !mbar_wait(&m.accf[acc], (j >> 1) & 1)) {
+          ok = false;
+          if (lane == 0) set_error(a.err, kErrTimeout);
         }
-      } else if constexpr (EK == kEpiResidGate) {
-        const int grow = tile * 128 + row;
-        if (grow < a.rows) {
-#pragma unroll
-          for (int b = 0; b < BP; ++b)
-            if (b < a.B) {
-              const float gs = a.gate[(size_t)b * a.gate_ld];
-              if (gs != 0.f) {
-                if constexpr (FIX) fix_add(a.acc + (size_t)b * a.rows + grow, gs * y[b]);
-                else atomicAdd(a.x + (size_t)b * a.rows + grow, gs * y[b]);
+        if (j == 0 && row == 0) ktrace(a.tr, 3);
+        float y[BP];
+  #pragma unroll
+        for (int b = 0; b < BP; ++b) y[b] = 0.f;
+        if (ok) {
+          tc_fence_after();
+          const uint32_t t0 = taddr + ((uint32_t)(32 * q) << 16) + (uint32_t)acc * ACOLS;
+          if constexpr (BP == 16) {
+            float v[32];
+            tmem_ld32(t0, v);
+  #pragma unroll
+            for (int b = 0; b < 16; ++b) y[b] = v[b] + v[16 + b];
+          } else {
+  #pragma unroll
+            for (int cb = 0; cb < N / 32; ++cb) {
+              float v[32];
+              tmem_ld32(t0 + 32 * cb, v);
+  #pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                if (32 * cb < BP) y[32 * cb + i] = v[i];
+                else y[32 * cb - BP + i] += v[i];
               }
             }
+          }
         }
-      } else if constexpr (KIND == kEpiQkv || KIND == kEpiGateUp) {
-        // partial tile only: k_bmerge sums the K parts and applies the epilogue
-        float *P = a.part + (size_t)u * a.B * 128;
-#pragma unroll
-        for (int b = 0; b < BP; ++b)
-          if (b < a.B) P[(size_t)b * 128 + row] = y[b];
-      } else {
-        float *P = a.part + (size_t)u * a.B * 128;
-#pragma unroll
-        for (int b = 0; b < BP; ++b)
-          if (b < a.B) P[(size_t)b * 128 + row] = y[b];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.acce[acc]);
+        const int tile = u / a.ksplit;
+        if (a.ksplit == 1) {
+          epilogue<BP, EK>(a, tile, row, y, 0, bv, bi);
+        } else if constexpr (EK == kEpiResid) {
+          // a residual update is a sum: each K part adds its share with a
+          // fire-and-forget reduction, in fp32 (order not fixed) or, for the
+          // deterministic step, in 64-bit fixed point (the next norm folds it in)
+          const int grow = tile * 128 + row;
+          if (grow < a.rows) {
+  #pragma unroll
+            for (int b = 0; b < BP; ++b)
+              if (b < a.B) {
+                if constexpr (FIX) fix_add(a.acc + (size_t)b * a.rows + grow, y[b]);
+                else atomicAdd(a.x + (size_t)b * a.rows + grow, y[b]);
+              }
+          }
+        } else if constexpr (EK == kEpiResidGate) {
+          const int grow = tile * 128 + row;
+          if (grow < a.rows) {
+  #pragma unroll
+            for (int b = 0; b < BP; ++b)
+              if (b < a.B) {
+                const float gs = a.gate[(size_t)b * a.gate_ld];
+                if (gs != 0.f) {
+                  if constexpr (FIX) fix_add(a.acc + (size_t)b * a.rows + grow, gs * y[b]);
+                  else atomicAdd(a.x + (size_t)b * a.rows + grow, gs * y[b]);
+                }
+              }
+          }
+        } else if constexpr (KIND == kEpiQkv || KIND == kEpiGateUp) {
+          // partial tile only: k_bmerge sums the K parts and applies the epilogue
+          float *P = a.part + (size_t)u * a.B * 128;
+  #pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < a.B) P[(size_t)b * 128 + row] = y[b];
+        } else {
+          float *P = a.part + (size_t)u * a.B * 128;
+  #pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < a.B) P[(size_t)b * 128 + row] = y[b];
+          __threadfence();
+          epi_sync();
+          if (row == 0) *m.flag = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)a.ksplit - 1u;
+          epi_sync();
+          if (*m.flag) {
+            __threadfence();
+            const float *P0 = a.part + (size_t)tile * a.ksplit * a.B * 128;
+            // fixed order over the K parts; each part's loads are independent
+  #pragma unroll
+            for (int b = 0; b < BP; ++b) y[b] = 0.f;
+            for (int k = 0; k < a.ksplit; ++k) {
+              float t[BP];
+  #pragma unroll
+              for (int b = 0; b < BP; ++b)
+                t[b] = b < a.B ? __ldcg(P0 + ((size_t)k * a.B + b) * 128 + row) : 0.f;
+  #pragma unroll
+              for (int b = 0; b < BP; ++b) y[b] += t[b];
+            }
+            epilogue<BP, EK>(a, tile, row, y, 0, bv, bi);
+            if (row == 0) a.tile_cnt[tile] = 0u;
+          }
+          epi_sync();
+        }
+      }
+      if (row == 0) ktrace(a.tr, 4);
+      if constexpr (KIND == kEpiLm) {
+        // each slot's best row of this CTA, then of the launch (last CTA)
+  #pragma unroll
+        for (int b = 0; b < BP; ++b) {
+          float v = bv[b];
+          int i = bi[b];
+  #pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+            am_merge(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+          if (lane == 0) {
+            m.amv[(warp - 2) * 64 + b] = v;
+            m.ami[(warp - 2) * 64 + b] = i;
+          }
+        }
+        epi_sync();
+        if (row < a.B) {
+          float v = m.amv[row];
+          int i = m.ami[row];
+          for (int w = 1; w < 4; ++w) am_merge(v, i, m.amv[w * 64 + row], m.ami[w * 64 + row]);
+          a.am_val[(size_t)row * gridDim.x + blockIdx.x] = v;
+          a.am_idx[(size_t)row * gridDim.x + blockIdx.x] = i;
+        }
         __threadfence();
         epi_sync();
-        if (row == 0) *m.flag = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)a.ksplit - 1u;
+        if (row == 0) *m.flag = atomicAdd(a.am_cnt, 1u) == gridDim.x - 1u;
         epi_sync();
         if (*m.flag) {
           __threadfence();
-          const float *P0 = a.part + (size_t)tile * a.ksplit * a.B * 128;
-          // fixed order over the K parts; each part's loads are independent
-#pragma unroll
-          for (int b = 0; b < BP; ++b) y[b] = 0.f;
-          for (int k = 0; k < a.ksplit; ++k) {
-            float t[BP];
-#pragma unroll
-            for (int b = 0; b < BP; ++b)
-              t[b] = b < a.B ? __ldcg(P0 + ((size_t)k * a.B + b) * 128 + row) : 0.f;
-#pragma unroll
-            for (int b = 0; b < BP; ++b) y[b] += t[b];
-          }
-          epilogue<BP, EK>(a, tile, row, y, bv, bi);
-          if (row == 0) a.tile_cnt[tile] = 0u;
-        }
-        epi_sync();
-      }
-    }
-    if (row == 0) ktrace(a.tr, 4);
-    if constexpr (KIND == kEpiLm) {
-      // each slot's best row of this CTA, then of the launch (last CTA)
-#pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        float v = bv[b];
-        int i = bi[b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-          am_merge(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
-        if (lane == 0) {
-          m.amv[(warp - 2) * 64 + b] = v;
-          m.ami[(warp - 2) * 64 + b] = i;
-        }
-      }
-      epi_sync();
-      if (row < a.B) {
-        float v = m.amv[row];
-        int i = m.ami[row];
-        for (int w = 1; w < 4; ++w) am_merge(v, i, m.amv[w * 64 + row], m.ami[w * 64 + row]);
-        a.am_val[(size_t)row * gridDim.x + blockIdx.x] = v;
-        a.am_idx[(size_t)row * gridDim.x + blockIdx.x] = i;
-      }
-      __threadfence();
-      epi_sync();
-      if (row == 0) *m.flag = atomicAdd(a.am_cnt, 1u) == gridDim.x - 1u;
-      epi_sync();
-      if (*m.flag) {
-        __threadfence();
-        if (row < a.B) {
-          float v = -FLT_MAX;
-          int i = INT_MAX;
-          for (int c0 = 0; c0 < (int)gridDim.x; c0 += 16) {
-            float cv[16];
-            int ci[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int c = c0 + j < (int)gridDim.x ? c0 + j : c0;
-              cv[j] = __ldcg(a.am_val + (size_t)row * gridDim.x + c);
-              ci[j] = __ldcg(a.am_idx + (size_t)row * gridDim.x + c);
+          if (row < a.B) {
+            float v = -FLT_MAX;
+            int i = INT_MAX;
+            for (int c0 = 0; c0 < (int)gridDim.x; c0 += 16) {
+              float cv[16];
+              int ci[16];
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int c = c0 + j < (int)gridDim.x ? c0 + j : c0;
+                cv[j] = __ldcg(a.am_val + (size_t)row * gridDim.x + c);
+                ci[j] = __ldcg(a.am_idx + (size_t)row * gridDim.x + c);
+              }
+  #pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < (int)gridDim.x) am_merge(v, i, cv[j], ci[j]);
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < (int)gridDim.x) am_merge(v, i, cv[j], ci[j]);
+            StepIO *io = a.slots[row].io;
+            if (i < 0 || i >= a.rows) {
+              set_error(&io->error, kErrToken);
+              i = 0;
+            }
+            if (a.argmax_out) a.argmax_out[row] = i;
+            io->token = i;
+            io->pos = a.pos[row] + 1;
+            const int e = *reinterpret_cast<volatile int32_t *>(a.err);
+            if (e) set_error(&io->error, e);
           }
-          StepIO *io = a.slots[row].io;
-          if (i < 0 || i >= a.rows) {
-            set_error(&io->error, kErrToken);
-            i = 0;
-          }
-          if (a.argmax_out) a.argmax_out[row] = i;
-          io->token = i;
-          io->pos = a.pos[row] + 1;
-          const int e = *reinterpret_cast<volatile int32_t *>(a.err);
-          if (e) set_error(&io->error, e);
+          if (row == 0) *a.am_cnt = 0u;
         }
-        if (row == 0) *a.am_cnt = 0u;
       }
     }
   }
@@ -761,6 +869,7 @@ cudaError_t launch_bgemm(const void *tmap_w, const void *tmap_x, const BGemmArgs
     case 16: return launch_bp<16>(tmap_w, tmap_x, a, grid, smem, st, pdl);
     case 32: return launch_bp<32>(tmap_w, tmap_x, a, grid, smem, st, pdl);
     case 64: return launch_bp<64>(tmap_w, tmap_x, a, grid, smem, st, pdl);
+    case 128: return launch_bp<128>(tmap_w, tmap_x, a, grid, smem, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -851,7 +960,60 @@ cudaError_t prepare_bgemm_kernels(int smem_bytes) {
   cudaError_t e;
   if ((e = prepare_bp<16>(smem_bytes)) != cudaSuccess) return e;
   if ((e = prepare_bp<32>(smem_bytes)) != cudaSuccess) return e;
-  return prepare_bp<64>(smem_bytes);
+  if ((e = prepare_bp<64>(smem_bytes)) != cudaSuccess) return e;
+  return prepare_bp<128>(smem_bytes);
+}
+
+namespace {
+// Greedy pick of each slot after an LM head that wrote logits only (128
+// padded slots): one CTA per slot, lowest id on ties; then the slot's next
+// token and position, and the batch's error bits, as the LM head's own merge
+// does at up to 64 slots.
+__global__ void __launch_bounds__(256) k_bargmax(const BArgmaxArgs a) {
+  __shared__ float sv[8];
+  __shared__ int si[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  const float *lg = a.logits + (size_t)b * a.V;
+  float v = -FLT_MAX;
+  int i = INT_MAX;
+  for (int r = tid; r < a.V; r += 256) am_merge(v, i, __ldcg(lg + r), r);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    am_merge(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+  if ((tid & 31) == 0) {
+    sv[tid >> 5] = v;
+    si[tid >> 5] = i;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < 8; ++w) am_merge(v, i, sv[w], si[w]);
+    StepIO *io = a.slots[b].io;
+    if (i < 0 || i >= a.V) {
+      set_error(&io->error, kErrToken);
+      i = 0;
+    }
+    if (a.argmax_out) a.argmax_out[b] = i;
+    io->token = i;
+    io->pos = a.pos[b] + 1;
+    const int e = *reinterpret_cast<volatile int32_t *>(a.err);
+    if (e) set_error(&io->error, e);
+  }
+}
+}  // namespace
+
+cudaError_t launch_bargmax(const BArgmaxArgs &a, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_bargmax, a);
 }
 
 cudaError_t launch_bnorm(const BNormArgs &a, cudaStream_t st, bool pdl) {

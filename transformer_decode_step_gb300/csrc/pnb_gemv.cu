@@ -466,7 +466,7 @@ cudaError_t launch_copy_token(StepIO *io, const int32_t *token, cudaStream_t st)
   return cudaGetLastError();
 }
 cudaError_t launch_prefill_begin(StepIO *pio, const StepIO *state, int n, cudaStream_t st) {
-  k_prefill_begin<<<1, 64, 0, st>>>(pio, state, n);
+  k_prefill_begin<<<1, 128, 0, st>>>(pio, state, n);
   return cudaGetLastError();
 }
 cudaError_t launch_prefill_end(StepIO *state, const StepIO *pio, int n, cudaStream_t st) {

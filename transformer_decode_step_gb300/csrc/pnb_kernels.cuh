@@ -358,7 +358,7 @@ struct BNormArgs {
   // sums [B][E] (units of 2^-32), folded into x (written back) and cleared
   long long *acc;
   KTrace tr;
-  BSlot slots[64];         // first layer: the slots of this step
+  BSlot slots[128];        // first layer: the slots of this step (prefill chunks: up to 128)
 };
 
 struct AttnGeom {
@@ -400,6 +400,17 @@ int bgemm_smem(int bp, int nstages);
 // sums the K parts of a split QKV / gate-up GEMM and applies its epilogue
 cudaError_t launch_bmerge(const BGemmArgs &a, cudaStream_t st, bool pdl);
 cudaError_t prepare_bgemm_kernels(int smem_bytes);
+
+// the greedy pick after a 128-slot LM head (logits [B][V] written by it)
+struct BArgmaxArgs {
+  const float *logits;
+  int V, B;
+  const BSlot *slots;
+  const int32_t *pos;
+  int32_t *argmax_out;   // [B] or null
+  int32_t *err;          // batch error word
+};
+cudaError_t launch_bargmax(const BArgmaxArgs &a, cudaStream_t st, bool pdl);
 
 // raise the dynamic shared-memory limit of the kernels a model will launch
 // (outside any stream capture)
