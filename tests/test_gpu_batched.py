@@ -37,6 +37,11 @@ SHAPE = wl.Shape(n_vocab=3001, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_f
 SHAPE_WIN = dataclasses.replace(SHAPE, sliding_window=48, n_ctx=200, n_vocab=2000, rope_theta=1e6)
 SHAPE_HD128 = wl.Shape(n_vocab=1500, n_embd=1024, n_head=8, n_kv_head=8, n_layer=1, n_ff=1536,
                        n_ctx=300, rope_theta=5e5, rms_norm_eps=1e-5, dtype=BF16)
+# head_dim 128 with 8 KV heads: from B = 20 on there are more (slot, KV head)
+# items than SMs and the attention runs persistent CTAs that take several
+# items each; the window variant reads a 128-slot ring (whole tiles, so the
+# tensor-core attention takes it), wrapped for most slots
+SHAPE_HD128_WIN = dataclasses.replace(SHAPE_HD128, sliding_window=128, n_ctx=320, rope_theta=1e6)
 # MoE: 4 experts, top-2 (the router runs per slot, every expert's FFN over all slots)
 SHAPE_MOE = wl.Shape(n_vocab=3001, n_embd=512, n_head=8, n_kv_head=2, n_layer=2, n_ff=1024,
                      n_ctx=160, rope_theta=1e6, rms_norm_eps=1e-5, expert_count=4, expert_used=2,
@@ -99,8 +104,8 @@ def run(shape, B, steps=3):
     return near
 
 
-@pytest.mark.parametrize("shape", [SHAPE, SHAPE_WIN, SHAPE_HD128, SHAPE_MOE],
-                         ids=["gqa", "window", "mha_hd128", "moe"])
+@pytest.mark.parametrize("shape", [SHAPE, SHAPE_WIN, SHAPE_HD128, SHAPE_HD128_WIN, SHAPE_MOE],
+                         ids=["gqa", "window", "mha_hd128", "window_hd128", "moe"])
 @pytest.mark.parametrize("B", [1, 5, 20, 40])
 def test_batched_step_matches_per_slot_oracle(shape, B):
     # argmax may differ only on near-ties (inside the logit tolerance); with

@@ -781,6 +781,10 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
         ta.use_order = 1;
         for (int i = 0; i < B; ++i) ta.order[i] = order[i];
       }
+      // more (slot, KV head) items than SMs, one split each: one persistent
+      // CTA per SM walks its items with the ring running on between them
+      if (chunk == kSlots && ta.n_split == 1 && m->hd == 128 && B * c.n_kv_head > m->num_sms)
+        ta.persist = m->num_sms;
       int cols = c.n_head / c.n_kv_head;
       if (chunk == kChunkGroups) {
         // a chunk's tokens share the cache: T consecutive tokens per CTA

@@ -21,6 +21,7 @@
 // receiver's mbarrier), and the receiving CTAs merge by log-sum-exp in split
 // order and write the output.
 #include <cuda.h>
+#include <algorithm>
 #include <cuda_bf16.h>
 #include <limits.h>
 #include <math.h>
@@ -633,6 +634,376 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
   if (warp == 1) tmem_dealloc(taddr, TCOLS);
 }
 
+// ------------------------------------------------------------------ persistent
+// Batched slots with one CTA's worth of work per (slot, KV head) item and more
+// items than SMs (head_dim 128, no splits): one CTA per SM walks a list of
+// items, and its TMA ring runs on across them, so the next item's first tiles
+// are in flight while the current one finishes (a grid of short CTAs pays each
+// CTA's start and drain instead).  Items are ranked longest first (slot order,
+// then KV head); CTA c takes the ranked items in snake order: its k-th item is
+// k * grid + c for even k and k * grid + grid - 1 - c for odd k.  Q (shared
+// memory) and O (TMEM) are double-buffered by item parity; the roles and the
+// per-tile protocol are those of k_attn_tc.
+struct TpItem {
+  int j;       // ranked item, or -1 past the CTA's last
+  int b, g;    // slot and KV head
+  int pos, lo; // attended positions [lo, pos]
+  int tb, nt;  // first tile and tile count
+};
+
+__device__ __forceinline__ TpItem tp_item(const AttnTcArgs &a, int k) {
+  TpItem it;
+  const int grid = (int)gridDim.x, c = (int)blockIdx.x;
+  const int j = k * grid + ((k & 1) ? grid - 1 - c : c);
+  it.j = j < a.nb * a.n_kv ? j : -1;
+  if (it.j < 0) {
+    it.b = it.g = it.pos = it.lo = it.tb = it.nt = 0;
+    return it;
+  }
+  const int z = j / a.n_kv;
+  it.g = j - z * a.n_kv;
+  it.b = a.use_order ? (int)a.order[z] : z;
+  it.pos = a.pos[it.b];
+  it.lo = a.window > 0 ? max(0, it.pos - a.window + 1) : 0;
+  it.tb = it.lo / kTile;
+  it.nt = it.pos / kTile - it.tb + 1;
+  return it;
+}
+
+constexpr int kTpHd = 128;
+constexpr uint32_t kTpCols = 128;   // S at column 0, O of even / odd items at 32 / 64
+
+__host__ __device__ constexpr int tp_smem(int nstages) {
+  return 1024 + nstages * TL<kTpHd>::STAGE + 2 * TL<kTpHd>::PT + 2 * TL<kTpHd>::QT + 1024;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
+  constexpr int HD = kTpHd;
+  constexpr int KT = TL<HD>::KT, STAGE = TL<HD>::STAGE, PT = TL<HD>::PT, QT = TL<HD>::QT;
+  constexpr int PCH = TL<HD>::PCH;
+  const int NS = a.nstages;
+
+  const uint32_t base = smem_addr(t_smem);
+  uint8_t *sm = t_smem + ((1024u - (base & 1023u)) & 1023u);
+  uint8_t *ring = sm;
+  uint8_t *P = ring + (size_t)NS * STAGE;
+  uint8_t *Qb = P + 2 * PT;   // two Q tiles
+  uint64_t *full = reinterpret_cast<uint64_t *>(Qb + 2 * QT);
+  uint64_t *empty = full + NS;
+  uint64_t *s_full = empty + NS, *s_empty = s_full + 1;
+  uint64_t *p_full = s_empty + 1, *p_empty = p_full + 2;
+  uint64_t *o_full = p_empty + 2, *q_ready = o_full + 1, *o_free = q_ready + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(o_free + 2);
+  float *red = reinterpret_cast<float *>(tslot + 4);   // [2][4][8] maxima, then [4][8] sums
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ktrace(a.tr, 0);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_empty[i], 1);
+      mbar_init(&q_ready[i], 4);
+      mbar_init(&o_free[i], 4);
+    }
+    mbar_init(o_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, kTpCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = *tslot;
+  const uint32_t t_s = taddr;
+  auto t_o = [&](int k) { return taddr + 32u + 32u * (uint32_t)(k & 1); };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // a tile holding an item's own position waits for the kernel that wrote
+      // this step's K / V; earlier tiles were written by earlier steps
+      bool waited = false, ok = true;
+      int i = 0;
+      for (int k = 0; ok; ++k) {
+        const TpItem it = tp_item(a, k);
+        if (it.j < 0) break;
+        const CUtensorMap *maps = static_cast<const CUtensorMap *>(a.slots[it.b].maps) + 2 * a.layer;
+        for (int t = 0; t < it.nt; ++t, ++i) {
+          const int T = it.tb + t, s = i % NS, r = i / NS;
+          if (!waited && ((T + 1) * kTile > it.pos || i == NS)) {
+            ktrace(a.tr, 6);
+            pdl_wait();
+            pdl_trigger();
+            ktrace(a.tr, 7);
+            waited = true;
+          }
+          if (i >= NS && !mbar_wait(&empty[s], (r - 1) & 1)) {
+            set_error(&a.slots[it.b].io->error, kErrTimeout);
+            ok = false;
+            break;
+          }
+          const int y = it.g * a.cap + (T * kTile) % a.cap;
+          uint8_t *kt = ring + (size_t)s * STAGE, *vt = kt + KT;
+          mbar_arrive_expect_tx(&full[s], STAGE);
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c) {
+            tma_load_2d(kt + c * kBox, maps, c * 64, y, &full[s]);
+            tma_load_2d(vt + c * kBox, maps + 1, c * 64, y, &full[s]);
+          }
+        }
+      }
+      if (!waited) {
+        pdl_wait();
+        pdl_trigger();
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, 16) | (1u << 15);   // V^T MN-major as A
+      // the CTA's tiles in order: item k, its tile t, ring index i; S of the
+      // next tile is issued before P V of this one
+      bool ok = true;
+      TpItem cur = tp_item(a, 0);
+      int k = 0, t = 0;
+      int32_t *merr = cur.j >= 0 ? &a.slots[cur.b].io->error : nullptr;
+      auto issue_s = [&](int i, int kk) {
+        const uint8_t *kt = ring + (size_t)(i % NS) * STAGE;
+        const uint8_t *Q = Qb + (size_t)(kk & 1) * QT;
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+#pragma unroll
+          for (int kq = 0; kq < 4; ++kq)
+            mma_bf16(t_s, desc_k_sw128(kt + c * kBox, kq * 32), desc_k_sw128(Q + c * 2048, kq * 32), idesc_s,
+                     c > 0 || kq > 0);
+        mma_commit(s_full);
+      };
+      if (cur.j >= 0) {
+        ok = mbar_wait(&q_ready[0], 0) && mbar_wait(&full[0], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+        }
+      }
+      for (int i = 0; cur.j >= 0 && ok; ++i) {
+        // the tile after i: the next of this item, or the first of the next item
+        int nk = k, ntt = t + 1;
+        TpItem nxt = cur;
+        if (ntt == cur.nt) {
+          nk = k + 1;
+          ntt = 0;
+          nxt = tp_item(a, nk);
+        }
+        if (nxt.j >= 0) {
+          ok = mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1) && mbar_wait(s_empty, i & 1);
+          if (ok && nk != k) ok = mbar_wait(&q_ready[nk & 1], (nk >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1, nk);
+        }
+        ok = mbar_wait(&p_full[i & 1], (i >> 1) & 1);
+        // O buffer k & 1 was read out after item k - 2
+        if (ok && t == 0 && k >= 2) ok = mbar_wait(&o_free[k & 1], ((k >> 1) - 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint8_t *pt = P + (size_t)(i & 1) * PT;
+        const uint8_t *vt = ring + (size_t)(i % NS) * STAGE + KT;
+#pragma unroll
+        for (int pc = 0; pc < kTile / 16; ++pc) {
+          const uint64_t dp = desc_k_sw128(pt + (pc >> 2) * PCH, (pc & 3) * 32);
+          const uint64_t dv = desc_mn_sw128(vt + pc * 2048, kBox);
+          mma_bf16(t_o(k), dv, dp, idesc_o, t > 0 || pc > 0);
+        }
+        mma_commit(o_full);
+        mma_commit(&p_empty[i & 1]);
+        mma_commit(&empty[i % NS]);
+        k = nk;
+        t = ntt;
+        cur = nxt;
+        if (cur.j >= 0) merr = &a.slots[cur.b].io->error;
+      }
+      if (!ok && merr) set_error(merr, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax warps 2-5
+    const int q = warp & 3, tid = threadIdx.x - 64;   // position 32 q + lane of each tile
+    auto stage_q = [&](const TpItem &it, int kk) {
+      uint8_t *Q = Qb + (size_t)(kk & 1) * QT;
+      for (int i = tid; i < G * HD; i += 128) {
+        const int h = i / HD, d = i - h * HD;
+        const float v = a.q[((size_t)it.b * a.n_head + it.g * G + h) * HD + d] * a.qscale;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        uint8_t *tile = Q + (d >> 6) * 2048;
+        *reinterpret_cast<__nv_bfloat16 *>(tile + sw128(h, (d & 63) * 2)) = hi;
+        *reinterpret_cast<__nv_bfloat16 *>(tile + sw128(8 + h, (d & 63) * 2)) = lo;
+      }
+      fence_async_smem();
+      epi_sync_t();
+      if (lane == 0) mbar_arrive(&q_ready[kk & 1]);
+    };
+    // Q and P: only rows h and 8 + h are ever written; the rest must be zero
+    for (int i = tid * 16; i < 2 * QT; i += 128 * 16) *reinterpret_cast<uint4 *>(Qb + i) = make_uint4(0, 0, 0, 0);
+    for (int i = tid * 16; i < 2 * PT; i += 128 * 16) *reinterpret_cast<uint4 *>(P + i) = make_uint4(0, 0, 0, 0);
+    pdl_wait();   // q comes from the QKV kernel
+    epi_sync_t();
+    TpItem cur = tp_item(a, 0);
+    if (cur.j >= 0) stage_q(cur, 0);
+    if (tid == 0) ktrace(a.tr, 1);
+
+    constexpr float kTau = 8.f;
+    bool ok = true;
+    int i = 0;
+    for (int k = 0; cur.j >= 0; ++k) {
+      const TpItem nxt = tp_item(a, k + 1);
+      // the next item's Q, into the buffer item k - 1 used (its S products
+      // are all done: this warp group consumed them)
+      if (nxt.j >= 0) stage_q(nxt, k + 1);
+      int32_t *err = &a.slots[cur.b].io->error;
+      float m[G], l[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+      }
+      for (int t = 0; t < cur.nt; ++t, ++i) {
+        if (ok && !mbar_wait(s_full, i & 1)) {
+          ok = false;
+          if (lane == 0) set_error(err, kErrTimeout);
+        }
+        float v[32];
+        if (ok) {
+          tc_fence_after();
+          tmem_ld32(t_s + ((uint32_t)(32 * q) << 16), v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty);
+        const int p = (cur.tb + t) * kTile + 32 * q + lane;
+        const bool valid = p >= cur.lo && p <= cur.pos;
+        float sc[G];
+        float *rm = red + (i & 1) * 32;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          sc[h] = valid ? v[h] + v[8 + h] : -INFINITY;
+          const float mx = warp_max(sc[h]);
+          if (lane == 0) rm[q * 8 + h] = mx;
+        }
+        epi_sync_t();
+        bool move = false;
+        float scale[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float mt = fmaxf(fmaxf(rm[h], rm[8 + h]), fmaxf(rm[16 + h], rm[24 + h]));
+          scale[h] = 1.f;
+          if (mt > m[h] + kTau) {
+            scale[h] = m[h] == -INFINITY ? 0.f : exp2f(m[h] - mt);
+            m[h] = mt;
+            l[h] *= scale[h];
+            move = true;
+          }
+        }
+        if (t > 0) {
+          // the previous tile's P V product is done; rescale O if the reference max moved
+          if (ok && !mbar_wait(o_full, (i - 1) & 1)) {
+            ok = false;
+            if (lane == 0) set_error(err, kErrTimeout);
+          }
+          if (ok && move) {
+            tc_fence_after();
+            float w[32];
+            tmem_ld32(t_o(k) + ((uint32_t)(32 * q) << 16), w);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              w[h] *= scale[h];
+              w[8 + h] *= scale[h];
+            }
+            tmem_st32(t_o(k) + ((uint32_t)(32 * q) << 16), w);
+            tc_fence_before();
+          }
+        }
+        float pp[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          pp[h] = (valid && m[h] != -INFINITY) ? exp2f(sc[h] - m[h]) : 0.f;
+          l[h] += pp[h];
+        }
+        // P into buffer i & 1, once the P V product of tile i - 2 is done
+        if (i >= 2 && ok && !mbar_wait(&p_empty[i & 1], ((i >> 1) - 1) & 1)) {
+          ok = false;
+          if (lane == 0) set_error(err, kErrTimeout);
+        }
+        uint8_t *pt = P + (size_t)(i & 1) * PT + ((32 * q + lane) >> 6) * PCH;
+        const int cb = ((32 * q + lane) & 63) * 2;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(pp[h]);
+          const __nv_bfloat16 lo2 = __float2bfloat16_rn(pp[h] - __bfloat162float(hi));
+          *reinterpret_cast<__nv_bfloat16 *>(pt + sw128(h, cb)) = hi;
+          *reinterpret_cast<__nv_bfloat16 *>(pt + sw128(8 + h, cb)) = lo2;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      }
+      // row sums over the item's positions (fixed order: lanes, then warps)
+      float *rs = red + 64;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sw = warp_sum(l[h]);
+        if (lane == 0) rs[q * 8 + h] = sw;
+      }
+      epi_sync_t();
+#pragma unroll
+      for (int h = 0; h < G; ++h) l[h] = rs[h] + rs[8 + h] + rs[16 + h] + rs[24 + h];
+      // O^T of the item: thread = dim d, columns h / 8 + h = high / low parts of head h
+      float oh[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) oh[h] = 0.f;
+      if (ok && !mbar_wait(o_full, (i - 1) & 1)) {
+        ok = false;
+        if (lane == 0) set_error(err, kErrTimeout);
+      }
+      if (ok) {
+        tc_fence_after();
+        float w[32];
+        tmem_ld32(t_o(k) + ((uint32_t)(32 * q) << 16), w);
+#pragma unroll
+        for (int h = 0; h < G; ++h) oh[h] = w[h] + w[8 + h];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[k & 1]);
+      const int d = 32 * q + lane;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const size_t col = (size_t)(cur.g * G + h) * HD + d;
+        const float x = l[h] > 0.f ? oh[h] / l[h] : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        a.xop[(size_t)cur.b * a.xop_ld + col] = hi;
+        a.xop[(size_t)(a.bp + cur.b) * a.xop_ld + col] = __float2bfloat16_rn(x - __bfloat162float(hi));
+      }
+      cur = nxt;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) ktrace(a.tr, 5);
+  if (warp == 1) tmem_dealloc(taddr, kTpCols);
+}
+
 template <int HD, int G>
 cudaError_t launch_g(const AttnTcArgs &a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
@@ -657,6 +1028,25 @@ cudaError_t launch_g(const AttnTcArgs &a, cudaStream_t st, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, k_attn_tc<HD, G>, a);
+}
+
+template <int G>
+cudaError_t launch_tp(const AttnTcArgs &a, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::min(a.nb * a.n_kv, a.persist));
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = tp_smem(a.nstages);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, k_attn_tp<G>, a);
 }
 
 template <int HD>
@@ -693,6 +1083,17 @@ int attn_tc_smem(int head_dim, int nstages) {
 }
 
 cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStream_t st, bool pdl) {
+  if (a.persist > 0) {
+    if (head_dim != kTpHd || !a.slots || a.n_split != 1 || a.tok_group > 1 || a.shared_cache || !a.xop)
+      return cudaErrorInvalidValue;
+    switch (group) {
+      case 1: return launch_tp<1>(a, st, pdl);
+      case 2: return launch_tp<2>(a, st, pdl);
+      case 4: return launch_tp<4>(a, st, pdl);
+      case 8: return launch_tp<8>(a, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (head_dim == 128) return launch_hd_tc<128>(group, a, st, pdl);
   if (head_dim == 64) return launch_hd_tc<64>(group, a, st, pdl);
   return cudaErrorInvalidValue;
@@ -701,6 +1102,11 @@ cudaError_t launch_attn_tc(int head_dim, int group, const AttnTcArgs &a, cudaStr
 cudaError_t prepare_attn_tc_kernels() {
   cudaError_t e = prepare_hd_tc<128>();
   if (e != cudaSuccess) return e;
+  const int tps = tp_smem(attn_tc_stages(kTpHd));
+  if ((e = cudaFuncSetAttribute(k_attn_tp<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, tps)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_attn_tp<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, tps)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_attn_tp<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, tps)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_attn_tp<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, tps)) != cudaSuccess) return e;
   return prepare_hd_tc<64>();
 }
 

@@ -251,6 +251,9 @@ struct AttnTcArgs {
   // several waves the long CTAs start first (any permutation is correct)
   uint8_t order[64];
   int use_order;
+  // > 0: the persistent form (batched slots with their own caches, one split,
+  // head_dim 128): min(items, persist) CTAs walk the (slot, KV head) items
+  int persist;
   KTrace tr;
 };
 
