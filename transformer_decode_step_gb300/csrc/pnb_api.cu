@@ -142,6 +142,7 @@ struct BatchCtx {
   StepIO *pio = nullptr;                 // prefill: the I/O words of a chunk's virtual slots
   float *gates = nullptr;                // MoE: [slot][expert] router weights (0 = not chosen)
   long long *acc = nullptr;              // [slot][n_embd] residual K-part sums, fixed point 2^-32
+  unsigned *tp_cnt = nullptr;            // persistent attention: [claim, done], zero between launches
   __nv_bfloat16 *xop_e = nullptr, *xop_o = nullptr, *xop_f = nullptr;
   float2 *rope = nullptr;
   BSlot *slots = nullptr;
@@ -594,6 +595,7 @@ int batch_setup(pnb_model *m) {
   const size_t o_gates = take((size_t)MB * std::max(1, c.expert_count) * 4);
   const size_t o_acc = take((size_t)MB * E * 8);
   const size_t o_lgs = take((size_t)MB * c.n_vocab * 4);
+  const size_t o_tpc = take(2 * sizeof(unsigned));
   if (cudaMalloc(&b->ws, off) != cudaSuccess) {
     delete b;
     return PNB_E_NOMEM;
@@ -622,6 +624,7 @@ int batch_setup(pnb_model *m) {
   b->gates = reinterpret_cast<float *>(b->ws + o_gates);
   b->acc = reinterpret_cast<long long *>(b->ws + o_acc);
   b->lgs = reinterpret_cast<float *>(b->ws + o_lgs);
+  b->tp_cnt = reinterpret_cast<unsigned *>(b->ws + o_tpc);
   bool ok = true;
   b->w_qkv.resize(L);
   b->w_o.resize(L);
@@ -783,8 +786,10 @@ cudaError_t enqueue_batch(pnb_model *m, const BSlot *slots, int B, const int32_t
       }
       // more (slot, KV head) items than SMs, one split each: one persistent
       // CTA per SM walks its items with the ring running on between them
-      if (chunk == kSlots && ta.n_split == 1 && m->hd == 128 && B * c.n_kv_head > m->num_sms)
+      if (chunk == kSlots && ta.n_split == 1 && m->hd == 128 && B * c.n_kv_head > m->num_sms) {
         ta.persist = m->num_sms;
+        ta.tp_claim = b->tp_cnt;
+      }
       int cols = c.n_head / c.n_kv_head;
       if (chunk == kChunkGroups) {
         // a chunk's tokens share the cache: T consecutive tokens per CTA

@@ -640,10 +640,15 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tc(const AttnTcArgs a) {
 // items, and its TMA ring runs on across them, so the next item's first tiles
 // are in flight while the current one finishes (a grid of short CTAs pays each
 // CTA's start and drain instead).  Items are ranked longest first (slot order,
-// then KV head); CTA c takes the ranked items in snake order: its k-th item is
-// k * grid + c for even k and k * grid + grid - 1 - c for odd k.  Q (shared
-// memory) and O (TMEM) are double-buffered by item parity; the roles and the
-// per-tile protocol are those of k_attn_tc.
+// then KV head).  With a claim counter the producer takes the next ranked
+// item with one atomic add when it reaches the last tile of the current one
+// (list scheduling in rank order: a CTA whose SM streams faster takes more;
+// the ring ahead of the consumers hides the round trip); without
+// one, CTA c takes its k-th item at k * grid + c for even k and
+// k * grid + grid - 1 - c for odd k.  The producer publishes each item through
+// a small queue in shared memory that the MMA and softmax warps read in order.
+// Q (shared memory) and O (TMEM) are double-buffered by item parity; the roles
+// and the per-tile protocol are those of k_attn_tc.
 struct TpItem {
   int j;       // ranked item, or -1 past the CTA's last
   int b, g;    // slot and KV head
@@ -651,11 +656,9 @@ struct TpItem {
   int tb, nt;  // first tile and tile count
 };
 
-__device__ __forceinline__ TpItem tp_item(const AttnTcArgs &a, int k) {
+__device__ __forceinline__ TpItem tp_item(const AttnTcArgs &a, int j) {
   TpItem it;
-  const int grid = (int)gridDim.x, c = (int)blockIdx.x;
-  const int j = k * grid + ((k & 1) ? grid - 1 - c : c);
-  it.j = j < a.nb * a.n_kv ? j : -1;
+  it.j = j >= 0 && j < a.nb * a.n_kv ? j : -1;
   if (it.j < 0) {
     it.b = it.g = it.pos = it.lo = it.tb = it.nt = 0;
     return it;
@@ -671,6 +674,7 @@ __device__ __forceinline__ TpItem tp_item(const AttnTcArgs &a, int k) {
 }
 
 constexpr int kTpHd = 128;
+constexpr int kTpQueue = 8;         // item queue entries (the producer runs at most a ring ahead)
 constexpr uint32_t kTpCols = 128;   // S at column 0, O of even / odd items at 32 / 64
 
 __host__ __device__ constexpr int tp_smem(int nstages) {
@@ -694,8 +698,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
   uint64_t *s_full = empty + NS, *s_empty = s_full + 1;
   uint64_t *p_full = s_empty + 1, *p_empty = p_full + 2;
   uint64_t *o_full = p_empty + 2, *q_ready = o_full + 1, *o_free = q_ready + 2;
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(o_free + 2);
+  uint64_t *it_full = o_free + 2, *it_empty = it_full + kTpQueue;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(it_empty + kTpQueue);
   float *red = reinterpret_cast<float *>(tslot + 4);   // [2][4][8] maxima, then [4][8] sums
+  int *itq = reinterpret_cast<int *>(red + 96);        // [kTpQueue] ranked items (-1: no more)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -711,6 +717,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
       mbar_init(&p_empty[i], 1);
       mbar_init(&q_ready[i], 4);
       mbar_init(&o_free[i], 4);
+    }
+    for (int i = 0; i < kTpQueue; ++i) {
+      mbar_init(&it_full[i], 1);
+      mbar_init(&it_empty[i], 5);   // the MMA thread and the four softmax warps
     }
     mbar_init(o_full, 1);
     fence_barrier_init();
@@ -728,16 +738,44 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
 
   if (warp == 0) {
     if (lane == 0) {
+      const int items = a.nb * a.n_kv, grid = (int)gridDim.x, c = (int)blockIdx.x;
+      auto claim = [&](int k) -> int {
+        if (a.tp_claim) {
+          const unsigned v = atomicAdd(a.tp_claim, 1u);
+          return v < (unsigned)items ? (int)v : -1;
+        }
+        const int j = k * grid + ((k & 1) ? grid - 1 - c : c);
+        return j < items ? j : -1;
+      };
+      // queue entry k: item k of this CTA (-1: no more)
+      auto publish = [&](int k, int j) -> bool {
+        const int e = k % kTpQueue;
+        if (k >= kTpQueue && !mbar_wait(&it_empty[e], ((k / kTpQueue) - 1) & 1)) return false;
+        itq[e] = j;
+        mbar_arrive(&it_full[e]);
+        return true;
+      };
       // a tile holding an item's own position waits for the kernel that wrote
       // this step's K / V; earlier tiles were written by earlier steps
       bool waited = false, ok = true;
       int i = 0;
-      for (int k = 0; ok; ++k) {
-        const TpItem it = tp_item(a, k);
-        if (it.j < 0) break;
+      int j = claim(0);
+      ok = publish(0, j);
+      for (int k = 0; ok && j >= 0; ++k) {
+        // the next item is claimed at this one's last tile (earlier claims
+        // would let the first CTAs to start take two items each) and
+        // published once that tile is issued
+        int jn = -1;
+        bool claimed = false;
+        const TpItem it = tp_item(a, j);
+        int32_t *err = &a.slots[it.b].io->error;
         const CUtensorMap *maps = static_cast<const CUtensorMap *>(a.slots[it.b].maps) + 2 * a.layer;
         for (int t = 0; t < it.nt; ++t, ++i) {
           const int T = it.tb + t, s = i % NS, r = i / NS;
+          if (t == it.nt - 1) {
+            jn = claim(k + 1);
+            claimed = true;
+          }
           if (!waited && ((T + 1) * kTile > it.pos || i == NS)) {
             ktrace(a.tr, 6);
             pdl_wait();
@@ -746,7 +784,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
             waited = true;
           }
           if (i >= NS && !mbar_wait(&empty[s], (r - 1) & 1)) {
-            set_error(&a.slots[it.b].io->error, kErrTimeout);
+            set_error(err, kErrTimeout);
             ok = false;
             break;
           }
@@ -754,38 +792,63 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
           uint8_t *kt = ring + (size_t)s * STAGE, *vt = kt + KT;
           mbar_arrive_expect_tx(&full[s], STAGE);
 #pragma unroll
-          for (int c = 0; c < HD / 64; ++c) {
-            tma_load_2d(kt + c * kBox, maps, c * 64, y, &full[s]);
-            tma_load_2d(vt + c * kBox, maps + 1, c * 64, y, &full[s]);
+          for (int cc = 0; cc < HD / 64; ++cc) {
+            tma_load_2d(kt + cc * kBox, maps, cc * 64, y, &full[s]);
+            tma_load_2d(vt + cc * kBox, maps + 1, cc * 64, y, &full[s]);
           }
         }
+        if (ok && !claimed) jn = claim(k + 1);
+        if (ok && !publish(k + 1, jn)) {
+          set_error(err, kErrTimeout);
+          ok = false;
+        }
+        j = jn;
       }
       if (!waited) {
         pdl_wait();
         pdl_trigger();
+      }
+      if (a.tp_claim) {
+        // every CTA is past its last claim once all have counted themselves
+        // done: the last one resets the counters for the next launch
+        __threadfence();
+        if (atomicAdd(a.tp_claim + 1, 1u) == (unsigned)grid - 1u) {
+          atomicExch(a.tp_claim, 0u);
+          atomicExch(a.tp_claim + 1, 0u);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, 16) | (1u << 15);   // V^T MN-major as A
-      // the CTA's tiles in order: item k, its tile t, ring index i; S of the
-      // next tile is issued before P V of this one
       bool ok = true;
-      TpItem cur = tp_item(a, 0);
-      int k = 0, t = 0;
-      int32_t *merr = cur.j >= 0 ? &a.slots[cur.b].io->error : nullptr;
+      int kq = 0;   // queue entries read
+      auto next_item = [&]() -> TpItem {
+        const int e = kq % kTpQueue;
+        if (!mbar_wait(&it_full[e], (kq / kTpQueue) & 1)) {
+          ok = false;
+          return tp_item(a, -1);
+        }
+        const int jj = itq[e];
+        mbar_arrive(&it_empty[e]);
+        ++kq;
+        return tp_item(a, jj);
+      };
+      // S of ring tile i for item kk
       auto issue_s = [&](int i, int kk) {
         const uint8_t *kt = ring + (size_t)(i % NS) * STAGE;
         const uint8_t *Q = Qb + (size_t)(kk & 1) * QT;
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
+        for (int cc = 0; cc < HD / 64; ++cc)
 #pragma unroll
-          for (int kq = 0; kq < 4; ++kq)
-            mma_bf16(t_s, desc_k_sw128(kt + c * kBox, kq * 32), desc_k_sw128(Q + c * 2048, kq * 32), idesc_s,
-                     c > 0 || kq > 0);
+          for (int kc = 0; kc < 4; ++kc)
+            mma_bf16(t_s, desc_k_sw128(kt + cc * kBox, kc * 32), desc_k_sw128(Q + cc * 2048, kc * 32),
+                     idesc_s, cc > 0 || kc > 0);
         mma_commit(s_full);
       };
+      TpItem cur = next_item();
+      int32_t *merr = cur.j >= 0 ? &a.slots[cur.b].io->error : nullptr;
       if (cur.j >= 0) {
         ok = mbar_wait(&q_ready[0], 0) && mbar_wait(&full[0], 0);
         if (ok) {
@@ -793,18 +856,23 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
           issue_s(0, 0);
         }
       }
+      // the CTA's tiles in order: item k, its tile t, ring index i.  Within an
+      // item, S of tile i + 1 goes out before P V of tile i; at an item's end,
+      // P V first (the next item's Q is staged after the softmax warps have
+      // published this item's last P)
+      int k = 0, t = 0;
       for (int i = 0; cur.j >= 0 && ok; ++i) {
-        // the tile after i: the next of this item, or the first of the next item
         int nk = k, ntt = t + 1;
         TpItem nxt = cur;
         if (ntt == cur.nt) {
           nk = k + 1;
           ntt = 0;
-          nxt = tp_item(a, nk);
+          nxt = next_item();
+          if (!ok) break;
         }
-        if (nxt.j >= 0) {
+        const bool boundary = nk != k;
+        if (!boundary) {
           ok = mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1) && mbar_wait(s_empty, i & 1);
-          if (ok && nk != k) ok = mbar_wait(&q_ready[nk & 1], (nk >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_s(i + 1, nk);
@@ -825,6 +893,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
         mma_commit(o_full);
         mma_commit(&p_empty[i & 1]);
         mma_commit(&empty[i % NS]);
+        if (boundary && nxt.j >= 0) {
+          ok = mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1) && mbar_wait(s_empty, i & 1) &&
+               mbar_wait(&q_ready[nk & 1], (nk >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1, nk);
+        }
         k = nk;
         t = ntt;
         cur = nxt;
@@ -836,6 +911,18 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
   } else {
     // ------------------------------------------------ softmax warps 2-5
     const int q = warp & 3, tid = threadIdx.x - 64;   // position 32 q + lane of each tile
+    bool ok = true;
+    int kq = 0;   // queue entries read
+    auto next_item = [&]() -> TpItem {
+      const int e = kq % kTpQueue;
+      int jj = -1;
+      if (ok && mbar_wait(&it_full[e], (kq / kTpQueue) & 1)) jj = itq[e];
+      else ok = false;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&it_empty[e]);
+      ++kq;
+      return tp_item(a, jj);
+    };
     auto stage_q = [&](const TpItem &it, int kk) {
       uint8_t *Q = Qb + (size_t)(kk & 1) * QT;
       for (int i = tid; i < G * HD; i += 128) {
@@ -856,18 +943,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
     for (int i = tid * 16; i < 2 * PT; i += 128 * 16) *reinterpret_cast<uint4 *>(P + i) = make_uint4(0, 0, 0, 0);
     pdl_wait();   // q comes from the QKV kernel
     epi_sync_t();
-    TpItem cur = tp_item(a, 0);
+    TpItem cur = next_item();
     if (cur.j >= 0) stage_q(cur, 0);
     if (tid == 0) ktrace(a.tr, 1);
 
     constexpr float kTau = 8.f;
-    bool ok = true;
     int i = 0;
     for (int k = 0; cur.j >= 0; ++k) {
-      const TpItem nxt = tp_item(a, k + 1);
-      // the next item's Q, into the buffer item k - 1 used (its S products
-      // are all done: this warp group consumed them)
-      if (nxt.j >= 0) stage_q(nxt, k + 1);
       int32_t *err = &a.slots[cur.b].io->error;
       float m[G], l[G];
 #pragma unroll
@@ -958,6 +1040,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_attn_tp(const AttnTcArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[i & 1]);
       }
+      // the next item and its Q (into the buffer of item k - 1, whose S
+      // products this warp group has consumed)
+      const TpItem nxt = next_item();
+      if (nxt.j >= 0) stage_q(nxt, k + 1);
       // row sums over the item's positions (fixed order: lanes, then warps)
       float *rs = red + 64;
 #pragma unroll

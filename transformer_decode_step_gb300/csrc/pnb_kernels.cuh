@@ -254,6 +254,9 @@ struct AttnTcArgs {
   // > 0: the persistent form (batched slots with their own caches, one split,
   // head_dim 128): min(items, persist) CTAs walk the (slot, KV head) items
   int persist;
+  // persistent form: [claim, done] counters, zero before the launch and left
+  // zero after it; null: a static item order
+  unsigned *tp_claim;
   KTrace tr;
 };
 
